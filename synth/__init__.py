@@ -1,0 +1,163 @@
+"""Seeded synthetic inputs for the fine-grained MoE layer.
+
+This module is the only code shared by the CUDA path's tests/benchmark and the
+CPU oracle.  It draws random tensors and nothing else: no step of the layer's
+arithmetic lives here.
+
+Shapes follow the pages' statement of the layer:
+  * Kimi K2 (d_model 7168, 384 routed experts, top-8, 1 shared expert) --
+    "Kimi K2 MoE", section 2 (Derivation); "Kimi K2" (visual-learn), "Many
+    experts, few used at a time"; "Kimi K2 · Router", parameter table
+    (gate weight 7168 x 384 plus a 384-entry bias).
+  * Kimi K3 (896 routed, top-16, 2 shared at 7168, latent 3584, intermediate
+    3072) -- "Kimi K3's router picks 16 of 896 experts", K3 table.
+
+Distributions: router weight kaiming-uniform with a = sqrt(5) (the pages'
+``reset_parameters``), i.e. U(-1/sqrt(d), 1/sqrt(d)); selection bias uniform;
+expert weights N(0, 0.02); activations N(0, 1) or a 32-cluster Gaussian
+mixture (centres N(0, I), unit noise) so that routing is skewed.
+
+Weight layouts (row-major, ``nn.Linear`` convention out x in):
+  W_r         [E, d]            fp32
+  bias        [E]               fp32
+  W_gate_up   [E, 2F, d]        rows 0..F-1 gate, rows F..2F-1 up
+  W_down      [E, d_out, F]
+  Ws_gate_up  [S, 2Fs, d]       shared experts, same convention
+  Ws_down     [S, d, Fs]
+  W_lat_down  [L, d]            K3 latent down-projection (d -> L)
+  W_lat_up    [d, L]            K3 latent up-projection (L -> d)
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Dict, Optional
+
+import torch
+
+__all__ = ["LayerShape", "CONFIGS", "SEEDS", "shape", "generate", "custom"]
+
+
+@dataclasses.dataclass(frozen=True)
+class LayerShape:
+    name: str
+    T: int
+    d_model: int
+    E_routed: int
+    K: int
+    E_shared: int = 0
+    d_ff: int = 0
+    d_ff_shared: int = 0
+    n_group: int = 1
+    topk_group: int = 1
+    routed_scaling_factor: float = 2.827
+    norm_topk_prob: bool = True
+    d_latent: int = 0
+    dtype: str = "bf16"          # "f32" or "bf16": activations and expert weights
+    x_dist: str = "normal"       # "normal" or "clusters32"
+    bias_range: float = 0.1
+    router_only: bool = False
+
+    @property
+    def d_expert(self) -> int:
+        """Width the routed experts work on (the latent width for K3)."""
+        return self.d_latent if self.d_latent else self.d_model
+
+
+CONFIGS: Dict[str, LayerShape] = {
+    "tiny": LayerShape("tiny", T=64, d_model=256, E_routed=16, K=4, E_shared=1,
+                       d_ff=64, d_ff_shared=64, dtype="f32", bias_range=0.1),
+    "k2_router": LayerShape("k2_router", T=4096, d_model=7168, E_routed=384, K=8,
+                            dtype="bf16", bias_range=0.05, router_only=True),
+    "k2_decode": LayerShape("k2_decode", T=128, d_model=7168, E_routed=384, K=8,
+                            E_shared=1, d_ff=2048, d_ff_shared=2048,
+                            x_dist="clusters32", bias_range=0.1),
+    "k2_prefill": LayerShape("k2_prefill", T=8192, d_model=7168, E_routed=384, K=8,
+                             E_shared=1, d_ff=2048, d_ff_shared=2048, n_group=8,
+                             topk_group=4, x_dist="clusters32", bias_range=0.1),
+    "k3_latent": LayerShape("k3_latent", T=4096, d_model=7168, E_routed=896, K=16,
+                            E_shared=2, d_ff=3072, d_ff_shared=3072, d_latent=3584,
+                            bias_range=0.1),
+}
+
+SEEDS = {"tiny": 0, "k2_router": 1, "k2_decode": 2, "k2_prefill": 3, "k3_latent": 4}
+
+
+def shape(name: str) -> LayerShape:
+    return CONFIGS[name]
+
+
+def custom(**kw) -> LayerShape:
+    kw.setdefault("name", "custom")
+    return LayerShape(**kw)
+
+
+def _wdtype(cfg: LayerShape) -> torch.dtype:
+    return torch.float32 if cfg.dtype == "f32" else torch.bfloat16
+
+
+def _normal(gen, shp, std, device, dtype):
+    t = torch.randn(shp, generator=gen, device=device, dtype=torch.float32)
+    if std != 1.0:
+        t.mul_(std)
+    return t.to(dtype)
+
+
+def _uniform(gen, shp, lo, hi, device):
+    t = torch.rand(shp, generator=gen, device=device, dtype=torch.float32)
+    return t.mul_(hi - lo).add_(lo)
+
+
+def _x(cfg: LayerShape, gen, device, T):
+    dt = _wdtype(cfg)
+    if cfg.x_dist == "normal":
+        return _normal(gen, (T, cfg.d_model), 1.0, device, dt)
+    if cfg.x_dist == "clusters32":
+        centres = torch.randn((32, cfg.d_model), generator=gen, device=device)
+        which = torch.randint(0, 32, (T,), generator=gen, device=device)
+        noise = torch.randn((T, cfg.d_model), generator=gen, device=device)
+        return (centres[which] + noise).to(dt)
+    raise ValueError(cfg.x_dist)
+
+
+def generate(cfg: LayerShape, device="cpu", seed: Optional[int] = None,
+             T: Optional[int] = None, weights: bool = True) -> Dict[str, torch.Tensor]:
+    """Draw every input of one layer call.  Deterministic for (seed, device).
+
+    Tensors are drawn in a fixed order, one expert at a time so that the peak
+    temporary stays at one expert's worth of fp32.
+    """
+    if seed is None:
+        seed = SEEDS.get(cfg.name, 12345)
+    T = cfg.T if T is None else T
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    out: Dict[str, torch.Tensor] = {}
+    d, E = cfg.d_model, cfg.E_routed
+    out["x"] = _x(cfg, gen, device, T)
+    bound = 1.0 / math.sqrt(d)  # kaiming_uniform(a=sqrt(5)): gain*sqrt(3/fan_in)
+    out["W_r"] = _uniform(gen, (E, d), -bound, bound, device)
+    out["bias"] = _uniform(gen, (E,), -cfg.bias_range, cfg.bias_range, device)
+    if cfg.router_only or not weights:
+        return out
+    dt = _wdtype(cfg)
+    de, F = cfg.d_expert, cfg.d_ff
+    W_gate_up = torch.empty((E, 2 * F, de), device=device, dtype=dt)
+    W_down = torch.empty((E, de, F), device=device, dtype=dt)
+    for e in range(E):
+        W_gate_up[e] = _normal(gen, (2 * F, de), 0.02, device, dt)
+        W_down[e] = _normal(gen, (de, F), 0.02, device, dt)
+    out["W_gate_up"], out["W_down"] = W_gate_up, W_down
+    S, Fs = cfg.E_shared, cfg.d_ff_shared
+    if S:
+        Ws_gate_up = torch.empty((S, 2 * Fs, d), device=device, dtype=dt)
+        Ws_down = torch.empty((S, d, Fs), device=device, dtype=dt)
+        for s in range(S):
+            Ws_gate_up[s] = _normal(gen, (2 * Fs, d), 0.02, device, dt)
+            Ws_down[s] = _normal(gen, (d, Fs), 0.02, device, dt)
+        out["Ws_gate_up"], out["Ws_down"] = Ws_gate_up, Ws_down
+    if cfg.d_latent:
+        L = cfg.d_latent
+        out["W_lat_down"] = _normal(gen, (L, d), 0.02, device, dt)
+        out["W_lat_up"] = _normal(gen, (d, L), 0.02, device, dt)
+    return out
