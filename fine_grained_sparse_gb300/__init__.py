@@ -1,0 +1,212 @@
+"""Fine-grained MoE layer forward (Kimi-K2 / Kimi-K3 shapes) on GB300.
+
+A thin ctypes binding over the C ABI declared in ``include/moe.h``: every
+function here has the C name, marshals tensors to pointers and raises
+``MoeError`` on a non-zero status.  All arithmetic runs in the library's
+CUDA kernels; there is no other implementation behind these names, and
+importing the package fails when the library has not been built
+(``python -m fine_grained_sparse_gb300.build``).
+
+Tensors are torch tensors on the current CUDA device (PyTorch provides the
+device memory and the stream); plain integers are accepted as raw pointers.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+from .build import lib_path
+
+__all__ = [
+    "MoeError", "MoeConfig", "MOE_F32", "MOE_BF16", "MOE_STAGE_COUNT", "STATUS", "lib",
+    "config", "moe_version", "moe_status_string", "moe_validate_config", "moe_workspace_size",
+    "moe_get_device_status", "moe_router", "moe_router_from_logits", "moe_permute",
+    "moe_grouped_swiglu", "moe_combine", "moe_linear", "moe_layer_forward",
+    "moe_layer_forward_host", "moe_last_error_detail",
+]
+
+MOE_F32, MOE_BF16 = 0, 1
+MOE_STAGE_COUNT = 5
+STAGE_NAMES = ("router", "dispatch", "expert_gate_up", "expert_down", "combine")
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
+          3: "MOE_ERR_ALIGNMENT", 4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA",
+          6: "MOE_ERR_TIMEOUT", 7: "MOE_ERR_DEVICE_INDEX"}
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, func: str, detail: str):
+        self.status = status
+        super().__init__(f"{func}: {STATUS.get(status, status)} ({detail})")
+
+
+class MoeConfig(ctypes.Structure):
+    _fields_ = [
+        ("d_model", ctypes.c_int32), ("d_ff", ctypes.c_int32), ("E_routed", ctypes.c_int32),
+        ("E_shared", ctypes.c_int32), ("d_ff_shared", ctypes.c_int32), ("K", ctypes.c_int32),
+        ("n_group", ctypes.c_int32), ("topk_group", ctypes.c_int32),
+        ("routed_scaling_factor", ctypes.c_float), ("norm_topk_prob", ctypes.c_int32),
+        ("d_latent", ctypes.c_int32), ("dtype", ctypes.c_int32),
+    ]
+
+
+def _load():
+    path = lib_path()
+    if not os.path.exists(path):
+        raise ImportError(
+            f"fine_grained_sparse_gb300: CUDA library {path} is missing; build it with "
+            "`python -m fine_grained_sparse_gb300.build`")
+    return ctypes.CDLL(path)
+
+
+lib = _load()
+
+_P, _I32, _I64, _SZ, _F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+_CFG = ctypes.POINTER(MoeConfig)
+_SIGS = {
+    "moe_version": ([], _I32),
+    "moe_status_string": ([_I32], ctypes.c_char_p),
+    "moe_last_error_detail": ([], ctypes.c_char_p),
+    "moe_validate_config": ([_CFG, _I64], _I32),
+    "moe_workspace_size": ([_CFG, _I64], _SZ),
+    "moe_get_device_status": ([_P, _P], _I32),
+    "moe_router": ([_CFG, _I64, _P, _P, _P, _P, _P, _P], _I32),
+    "moe_router_from_logits": ([_CFG, _I64, _P, _P, _P, _P, _P], _I32),
+    "moe_permute": ([_CFG, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P], _I32),
+    "moe_grouped_swiglu": ([_CFG, _I64] + [_P] * 12 + [_SZ, _P], _I32),
+    "moe_combine": ([_CFG, _I64, _P, _P, _P, _P, _P], _I32),
+    "moe_linear": ([_I64, _I32, _I32, _P, _P, _P, _P, _P, _SZ, _P], _I32),
+    "moe_layer_forward": ([_CFG, _I64] + [_P] * 14 + [_SZ, _P, _P], _I32),
+    "moe_layer_forward_host": ([_CFG, _I64] + [_P] * 11 + [_SZ, _P], _I32),
+}
+for _name, (_args, _res) in _SIGS.items():
+    _fn = getattr(lib, _name)
+    _fn.argtypes = _args
+    _fn.restype = _res
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, func: str):
+    if status != 0:
+        raise MoeError(status, func, lib.moe_last_error_detail().decode())
+
+
+def config(shape=None, **kw) -> MoeConfig:
+    """MoeConfig from a ``synth.LayerShape``-like object and/or keywords."""
+    vals = dict(d_model=0, d_ff=0, E_routed=0, E_shared=0, d_ff_shared=0, K=1, n_group=1,
+                topk_group=1, routed_scaling_factor=2.827, norm_topk_prob=1, d_latent=0,
+                dtype=MOE_BF16)
+    if shape is not None:
+        for k in vals:
+            if hasattr(shape, k):
+                vals[k] = getattr(shape, k)
+        if hasattr(shape, "dtype") and isinstance(shape.dtype, str):
+            vals["dtype"] = MOE_F32 if shape.dtype == "f32" else MOE_BF16
+        if getattr(shape, "router_only", False):
+            vals["d_ff"] = 0
+    vals.update(kw)
+    vals["norm_topk_prob"] = int(bool(vals["norm_topk_prob"]))
+    return MoeConfig(**vals)
+
+
+def moe_version() -> int:
+    return lib.moe_version()
+
+
+def moe_status_string(status: int) -> str:
+    return lib.moe_status_string(status).decode()
+
+
+def moe_last_error_detail() -> str:
+    return lib.moe_last_error_detail().decode()
+
+
+def moe_validate_config(cfg: MoeConfig, T: int) -> int:
+    return lib.moe_validate_config(ctypes.byref(cfg), T)
+
+
+def moe_workspace_size(cfg: MoeConfig, T: int) -> int:
+    return lib.moe_workspace_size(ctypes.byref(cfg), T)
+
+
+def moe_get_device_status(workspace, stream=None) -> int:
+    return lib.moe_get_device_status(_ptr(workspace), _stream(stream))
+
+
+def moe_router(cfg, T, x, W_r, bias, topk_idx, topk_w, stream=None):
+    _check(lib.moe_router(ctypes.byref(cfg), T, _ptr(x), _ptr(W_r), _ptr(bias), _ptr(topk_idx),
+                          _ptr(topk_w), _stream(stream)), "moe_router")
+
+
+def moe_router_from_logits(cfg, T, logits, bias, topk_idx, topk_w, stream=None):
+    _check(lib.moe_router_from_logits(ctypes.byref(cfg), T, _ptr(logits), _ptr(bias),
+                                      _ptr(topk_idx), _ptr(topk_w), _stream(stream)),
+           "moe_router_from_logits")
+
+
+def moe_permute(cfg, T, topk_idx, counts, offsets, perm, inv, workspace, ws_bytes, stream=None):
+    _check(lib.moe_permute(ctypes.byref(cfg), T, _ptr(topk_idx), _ptr(counts), _ptr(offsets),
+                           _ptr(perm), _ptr(inv), _ptr(workspace), ws_bytes, _stream(stream)),
+           "moe_permute")
+
+
+def moe_grouped_swiglu(cfg, T, x_e, offsets, perm, topk_w, W_gate_up, W_down, x_shared,
+                       Ws_gate_up, Ws_down, Y, Y_shared, workspace, ws_bytes, stream=None):
+    _check(lib.moe_grouped_swiglu(ctypes.byref(cfg), T, _ptr(x_e), _ptr(offsets), _ptr(perm),
+                                  _ptr(topk_w), _ptr(W_gate_up), _ptr(W_down), _ptr(x_shared),
+                                  _ptr(Ws_gate_up), _ptr(Ws_down), _ptr(Y), _ptr(Y_shared),
+                                  _ptr(workspace), ws_bytes, _stream(stream)),
+           "moe_grouped_swiglu")
+
+
+def moe_combine(cfg, T, Y, inv, Y_shared, y, stream=None):
+    _check(lib.moe_combine(ctypes.byref(cfg), T, _ptr(Y), _ptr(inv), _ptr(Y_shared), _ptr(y),
+                           _stream(stream)), "moe_combine")
+
+
+def moe_linear(T, in_features, out_features, x, W, add, y, workspace, ws_bytes, stream=None):
+    _check(lib.moe_linear(T, in_features, out_features, _ptr(x), _ptr(W), _ptr(add), _ptr(y),
+                          _ptr(workspace), ws_bytes, _stream(stream)), "moe_linear")
+
+
+def moe_layer_forward(cfg, T, x, W_r, bias, W_gate_up, W_down, Ws_gate_up, Ws_down, W_lat_down,
+                      W_lat_up, y, topk_idx_out=None, topk_w_out=None, counts_out=None,
+                      workspace=None, ws_bytes=0, stage_events: Optional[Sequence] = None,
+                      stream=None):
+    ev_array = None
+    if stage_events is not None:
+        handles = [e.cuda_event if hasattr(e, "cuda_event") else int(e) for e in stage_events]
+        if len(handles) != MOE_STAGE_COUNT + 1:
+            raise ValueError("stage_events needs MOE_STAGE_COUNT + 1 events")
+        ev_array = (ctypes.c_void_p * len(handles))(*handles)
+    _check(lib.moe_layer_forward(ctypes.byref(cfg), T, _ptr(x), _ptr(W_r), _ptr(bias),
+                                 _ptr(W_gate_up), _ptr(W_down), _ptr(Ws_gate_up), _ptr(Ws_down),
+                                 _ptr(W_lat_down), _ptr(W_lat_up), _ptr(y), _ptr(topk_idx_out),
+                                 _ptr(topk_w_out), _ptr(counts_out), _ptr(workspace), ws_bytes,
+                                 ctypes.cast(ev_array, ctypes.c_void_p) if ev_array is not None else None,
+                                 _stream(stream)), "moe_layer_forward")
+
+
+def moe_layer_forward_host(cfg, T, x_host, W_r, bias, W_gate_up, W_down, Ws_gate_up, Ws_down,
+                           W_lat_down, W_lat_up, y_host, workspace, ws_bytes, stream=None):
+    _check(lib.moe_layer_forward_host(ctypes.byref(cfg), T, _ptr(x_host), _ptr(W_r), _ptr(bias),
+                                      _ptr(W_gate_up), _ptr(W_down), _ptr(Ws_gate_up),
+                                      _ptr(Ws_down), _ptr(W_lat_down), _ptr(W_lat_up),
+                                      _ptr(y_host), _ptr(workspace), ws_bytes, _stream(stream)),
+           "moe_layer_forward_host")

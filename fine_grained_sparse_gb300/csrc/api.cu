@@ -1,0 +1,624 @@
+// C ABI of the fine-grained MoE layer: argument checks, workspace layout and
+// the order of kernel launches.  No call allocates; no exception escapes.
+//
+// The layer ("Kimi K2 MoE", sections 2-3; "Kimi K2 · Router", "All 4 steps";
+// "Kimi K3's router picks 16 of 896 experts", Stable LatentMoE):
+//   router -> dispatch -> grouped SwiGLU experts (+ shared experts)
+//          -> weighted combine (+ K3 latent projections)
+#include <stdio.h>
+#include <string.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+using namespace fgs;
+
+namespace {
+
+thread_local char g_detail[256] = "";
+
+int32_t fail(int32_t code, const char* what) {
+  snprintf(g_detail, sizeof(g_detail), "%s", what);
+  return code;
+}
+
+int32_t cuda_fail(cudaError_t e, const char* where) {
+  snprintf(g_detail, sizeof(g_detail), "%s: %s", where, cudaGetErrorString(e));
+  return MOE_ERR_CUDA;
+}
+
+#define MOE_CUDA(call)                                      \
+  do {                                                      \
+    cudaError_t e_ = (call);                                \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call);     \
+  } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+int elem_bytes(const moe_config* c) { return c->dtype == MOE_BF16 ? 2 : 4; }
+
+int d_expert(const moe_config* c) { return c->d_latent ? c->d_latent : c->d_model; }
+
+// token tile of the tensor-core GEMMs: no expert holds more than T rows
+int token_tile(int64_t T) {
+  if (T <= 32) return 32;
+  if (T <= 64) return 64;
+  if (T <= 128) return 128;
+  return 256;
+}
+
+int32_t check_router_cfg(const moe_config* c, int64_t T) {
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "cfg is null");
+  if (T < 1 || T > (1ll << 30)) return fail(MOE_ERR_INVALID_ARG, "T out of range");
+  if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return fail(MOE_ERR_INVALID_ARG, "dtype");
+  if (c->E_routed < 1 || c->E_routed > 1024) return fail(MOE_ERR_INVALID_ARG, "E_routed not in [1, 1024]");
+  if (c->K < 1 || c->K > c->E_routed) return fail(MOE_ERR_INVALID_ARG, "K not in [1, E]");
+  if (c->K > 32) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "K > 32");
+  if (T * c->K >= (1ll << 31)) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "T*K too large");
+  if (c->n_group < 1 || c->n_group > 32) return fail(MOE_ERR_INVALID_ARG, "n_group not in [1, 32]");
+  if (c->E_routed % c->n_group) return fail(MOE_ERR_INVALID_ARG, "E % n_group != 0");
+  if (c->n_group > 1 && c->E_routed / c->n_group < 2)
+    return fail(MOE_ERR_INVALID_ARG, "group-limited selection needs >= 2 experts per group");
+  if (c->topk_group < 1 || c->topk_group > c->n_group)
+    return fail(MOE_ERR_INVALID_ARG, "topk_group not in [1, n_group]");
+  if (static_cast<int64_t>(c->K) > static_cast<int64_t>(c->topk_group) * (c->E_routed / c->n_group) &&
+      c->n_group > 1)
+    return fail(MOE_ERR_INVALID_ARG, "K > topk_group * E / n_group");
+  if (!std::isfinite(c->routed_scaling_factor)) return fail(MOE_ERR_INVALID_ARG, "scale not finite");
+  if (c->d_model < 32 || c->d_model % 32) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "d_model % 32 != 0");
+  return MOE_OK;
+}
+
+int32_t check_layer_cfg(const moe_config* c, int64_t T) {
+  int32_t st = check_router_cfg(c, T);
+  if (st != MOE_OK) return st;
+  if (c->d_ff < 1) return fail(MOE_ERR_INVALID_ARG, "d_ff < 1");
+  if (c->E_shared < 0 || c->E_shared > 8) return fail(MOE_ERR_INVALID_ARG, "E_shared not in [0, 8]");
+  if (c->E_shared > 0 && c->d_ff_shared < 1) return fail(MOE_ERR_INVALID_ARG, "d_ff_shared < 1");
+  if (c->d_latent < 0) return fail(MOE_ERR_INVALID_ARG, "d_latent < 0");
+  if (c->dtype == MOE_BF16) {
+    if (c->d_model % 128) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "bf16 path: d_model % 128 != 0");
+    if (c->d_ff % 64) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "bf16 path: d_ff % 64 != 0");
+    if (c->E_shared > 0 && c->d_ff_shared % 64)
+      return fail(MOE_ERR_UNSUPPORTED_SHAPE, "bf16 path: d_ff_shared % 64 != 0");
+    if (c->d_latent % 128) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "bf16 path: d_latent % 128 != 0");
+  } else {
+    if (c->d_latent) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "fp32 path has no latent projection");
+  }
+  return MOE_OK;
+}
+
+// Workspace regions, each 256-byte aligned, in this order.
+struct Layout {
+  size_t status, topk_idx, topk_w, counts, offsets, perm, inv, tiles, ntiles, w_perm, Xp, H, Hs,
+      Y, U, Ysh, x_lat, r_lat, x_stage, y_stage, total;
+};
+
+Layout layout(const moe_config* c, int64_t T) {
+  Layout L;
+  const int64_t TK = T * c->K;
+  const int eb = elem_bytes(c);
+  const int de = d_expert(c);
+  const int S = c->d_ff > 0 ? c->E_shared : 0;
+  const int64_t tiles = TK / kSimtTile + c->E_routed + 1;  // bound for every tile height used
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o += round256(bytes);
+    return at;
+  };
+  L.status = take(kWsHeader);
+  L.topk_idx = take(4 * TK);
+  L.topk_w = take(4 * TK);
+  L.counts = take(4 * static_cast<size_t>(c->E_routed));
+  L.offsets = take(4 * static_cast<size_t>(c->E_routed + 1));
+  L.perm = take(4 * TK);
+  L.inv = take(4 * TK);
+  L.tiles = take(16 * tiles);
+  L.ntiles = take(16);
+  L.w_perm = take(4 * TK);
+  L.Xp = take(static_cast<size_t>(TK) * de * eb);
+  L.H = take(static_cast<size_t>(TK) * c->d_ff * eb);
+  L.Hs = take(static_cast<size_t>(S) * T * c->d_ff_shared * eb);
+  L.Y = take(static_cast<size_t>(TK) * de * eb);
+  // U and Ysh are adjacent (no padding: both are whole rows of d) so that
+  // the final combine reads them as one strided list of addends
+  const size_t U_bytes = c->d_latent ? static_cast<size_t>(T) * c->d_model * eb : 0;
+  L.U = o;
+  L.Ysh = o + U_bytes;
+  o = round256(o + U_bytes + static_cast<size_t>(S) * T * c->d_model * eb);
+  L.x_lat = take(c->d_latent ? static_cast<size_t>(T) * c->d_latent * eb : 0);
+  L.r_lat = take(c->d_latent ? static_cast<size_t>(T) * c->d_latent * eb : 0);
+  L.x_stage = take(static_cast<size_t>(T) * c->d_model * eb);
+  L.y_stage = take(static_cast<size_t>(T) * c->d_model * eb);
+  L.total = o;
+  return L;
+}
+
+template <typename P>
+P* at(void* ws, size_t off) {
+  return reinterpret_cast<P*>(static_cast<char*>(ws) + off);
+}
+
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 148;
+  }
+  return cached[dev];
+}
+
+// 5-D gate/up tensor map when the driver accepts it, else eight 16-row boxes
+int32_t set_gate_up_A(GemmSegment& s, const void* W, int groups, int F, int Kd) {
+  if (encode_tmap_gate_up_5d(&s.tmA, W, groups, F, Kd) == CUDA_SUCCESS) {
+    s.a_boxes = 1;
+  } else if (encode_tmap_weights_3d(&s.tmA, W, groups, 2 * static_cast<int64_t>(F), Kd, 16) ==
+             CUDA_SUCCESS) {
+    s.a_boxes = 8;
+  } else {
+    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for W_gate_up");
+  }
+  s.a_rows = F;
+  return MOE_OK;
+}
+
+int32_t set_B(GemmSegment& s, const void* B, int64_t rows, int Kd) {
+  if (encode_tmap_2d_rows(&s.tmB, B, rows, Kd, 32) != CUDA_SUCCESS)
+    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for activations");
+  s.k_steps = Kd / 64;
+  return MOE_OK;
+}
+
+int32_t set_store_A(GemmSegment& s, const void* W, int groups, int O, int Kd) {
+  if (encode_tmap_weights_3d(&s.tmA, W, groups, O, Kd, 128) != CUDA_SUCCESS)
+    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for weights");
+  s.a_boxes = 1;
+  s.a_rows = 0;
+  return MOE_OK;
+}
+
+void clear(GemmSegment& s) { memset(&s, 0, sizeof(s)); }
+
+// Expert passes shared by moe_grouped_swiglu and moe_layer_forward.
+struct ExpertIO {
+  const void* x_e;       // [T, d_e]
+  const int32_t* offsets;
+  const int32_t* perm;
+  const float* topk_w;   // may be null
+  const void* W_gate_up;
+  const void* W_down;
+  const void* x_shared;  // [T, d] or null
+  const void* Ws_gate_up;
+  const void* Ws_down;
+  void* Y;               // [T*K, d_e]
+  void* Y_shared;        // [S, T, d] or null
+};
+
+int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws,
+                    cudaEvent_t ev_up, cudaEvent_t ev_down, cudaStream_t st) {
+  const Layout L = layout(c, T);
+  const int E = c->E_routed, K = c->K, F = c->d_ff, de = d_expert(c);
+  const int S = io.x_shared ? c->E_shared : 0;
+  const int Fs = c->d_ff_shared, d = c->d_model;
+  const int64_t TK = T * K;
+  int* status = at<int>(ws, L.status);
+  int4* tiles = at<int4>(ws, L.tiles);
+  int* ntiles = at<int>(ws, L.ntiles);
+  float* w_perm = at<float>(ws, L.w_perm);
+  void* Xp = at<void>(ws, L.Xp);
+  void* H = at<void>(ws, L.H);
+  void* Hs = at<void>(ws, L.Hs);
+  const bool bf16 = c->dtype == MOE_BF16;
+  const int nt = bf16 ? token_tile(T) : kSimtTile;
+
+  MOE_CUDA(launch_build_tiles(io.offsets, E, nt, tiles, ntiles, st));
+  MOE_CUDA(launch_gather(io.x_e, T, K, de, elem_bytes(c), io.perm, io.offsets, E, io.topk_w, Xp,
+                         w_perm, st));
+  if (ev_up) MOE_CUDA(cudaEventRecord(ev_up, st));
+
+  if (bf16) {
+    GemmParams p;
+    memset(&p, 0, sizeof(p));
+    p.mode = kModeSwiGLU;
+    p.nt = nt;
+    p.status = status;
+    p.nseg = S ? 2 : 1;
+    // gate/up: routed experts over the gathered rows
+    GemmSegment& r = p.seg[0];
+    clear(r);
+    int32_t e;
+    if ((e = set_gate_up_A(r, io.W_gate_up, E, F, de)) != MOE_OK) return e;
+    if ((e = set_B(r, Xp, TK, de)) != MOE_OK) return e;
+    r.o_blocks = F / 64;
+    r.tiles = tiles;
+    r.ntiles = ntiles;
+    r.out = static_cast<__nv_bfloat16*>(H);
+    r.out_ld = F;
+    if (S) {
+      GemmSegment& s = p.seg[1];
+      clear(s);
+      if ((e = set_gate_up_A(s, io.Ws_gate_up, S, Fs, d)) != MOE_OK) return e;
+      if ((e = set_B(s, io.x_shared, T, d)) != MOE_OK) return e;
+      s.o_blocks = Fs / 64;
+      s.groups = S;
+      s.rows = static_cast<int>(T);
+      s.b_group_stride = 0;
+      s.out_group_stride = T;
+      s.out = static_cast<__nv_bfloat16*>(Hs);
+      s.out_ld = Fs;
+    }
+    MOE_CUDA(launch_tc_gemm(p, num_sms(), st));
+    if (ev_down) MOE_CUDA(cudaEventRecord(ev_down, st));
+
+    // down: routed rows scaled by their gate weight, shared rows unscaled
+    p.mode = kModeStore;
+    GemmSegment& r2 = p.seg[0];
+    clear(r2);
+    if ((e = set_store_A(r2, io.W_down, E, de, F)) != MOE_OK) return e;
+    if ((e = set_B(r2, H, TK, F)) != MOE_OK) return e;
+    r2.o_blocks = de / 128;
+    r2.tiles = tiles;
+    r2.ntiles = ntiles;
+    r2.out = static_cast<__nv_bfloat16*>(io.Y);
+    r2.out_ld = de;
+    r2.row_scale = io.topk_w ? w_perm : nullptr;
+    if (S) {
+      GemmSegment& s2 = p.seg[1];
+      clear(s2);
+      if ((e = set_store_A(s2, io.Ws_down, S, d, Fs)) != MOE_OK) return e;
+      if ((e = set_B(s2, Hs, S * T, Fs)) != MOE_OK) return e;
+      s2.o_blocks = d / 128;
+      s2.groups = S;
+      s2.rows = static_cast<int>(T);
+      s2.b_group_stride = T;
+      s2.out_group_stride = T;
+      s2.out = static_cast<__nv_bfloat16*>(io.Y_shared);
+      s2.out_ld = d;
+    }
+    MOE_CUDA(launch_tc_gemm(p, num_sms(), st));
+    return MOE_OK;
+  }
+
+  // fp32 CUDA-core path
+  const int64_t bound_r = TK / kSimtTile + E;
+  SimtGemm g;
+  g.B = static_cast<const float*>(Xp);
+  g.W = static_cast<const float*>(io.W_gate_up);
+  g.w_group_stride = 2ll * F * de;
+  g.Kdim = de;
+  g.O = F;
+  g.swiglu = true;
+  g.tiles = tiles;
+  g.ntiles = ntiles;
+  g.out = static_cast<float*>(H);
+  MOE_CUDA(launch_simt_gemm(g, bound_r, st));
+  SimtGemm gs;
+  const int64_t bound_s = S * ((T + kSimtTile - 1) / kSimtTile);
+  if (S) {
+    gs.B = static_cast<const float*>(io.x_shared);
+    gs.W = static_cast<const float*>(io.Ws_gate_up);
+    gs.w_group_stride = 2ll * Fs * d;
+    gs.Kdim = d;
+    gs.O = Fs;
+    gs.swiglu = true;
+    gs.groups = S;
+    gs.rows = static_cast<int>(T);
+    gs.b_group_stride = 0;
+    gs.out_group_stride = T;
+    gs.out = static_cast<float*>(Hs);
+    MOE_CUDA(launch_simt_gemm(gs, bound_s, st));
+  }
+  if (ev_down) MOE_CUDA(cudaEventRecord(ev_down, st));
+  SimtGemm g2;
+  g2.B = static_cast<const float*>(H);
+  g2.W = static_cast<const float*>(io.W_down);
+  g2.w_group_stride = static_cast<int64_t>(de) * F;
+  g2.Kdim = F;
+  g2.O = de;
+  g2.tiles = tiles;
+  g2.ntiles = ntiles;
+  g2.out = static_cast<float*>(io.Y);
+  g2.row_scale = io.topk_w ? w_perm : nullptr;
+  MOE_CUDA(launch_simt_gemm(g2, bound_r, st));
+  if (S) {
+    SimtGemm g3;
+    g3.B = static_cast<const float*>(Hs);
+    g3.W = static_cast<const float*>(io.Ws_down);
+    g3.w_group_stride = static_cast<int64_t>(d) * Fs;
+    g3.Kdim = Fs;
+    g3.O = d;
+    g3.groups = S;
+    g3.rows = static_cast<int>(T);
+    g3.b_group_stride = T;
+    g3.out_group_stride = T;
+    g3.out = static_cast<float*>(io.Y_shared);
+    MOE_CUDA(launch_simt_gemm(g3, bound_s, st));
+  }
+  (void)status;
+  return MOE_OK;
+}
+
+int32_t run_linear(int64_t T, int in_f, int out_f, const void* x, const void* W, const void* add,
+                   void* y, int* status, cudaStream_t st) {
+  GemmParams p;
+  memset(&p, 0, sizeof(p));
+  p.mode = kModeStore;
+  p.nt = token_tile(T);
+  p.status = status;
+  p.nseg = 1;
+  GemmSegment& s = p.seg[0];
+  clear(s);
+  int32_t e;
+  if ((e = set_store_A(s, W, 1, out_f, in_f)) != MOE_OK) return e;
+  if ((e = set_B(s, x, T, in_f)) != MOE_OK) return e;
+  s.o_blocks = out_f / 128;
+  s.groups = 1;
+  s.rows = static_cast<int>(T);
+  s.out = static_cast<__nv_bfloat16*>(y);
+  s.out_ld = out_f;
+  s.add = static_cast<const __nv_bfloat16*>(add);
+  s.add_ld = out_f;
+  MOE_CUDA(launch_tc_gemm(p, num_sms(), st));
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t moe_version(void) { return 100; }
+
+const char* moe_status_string(int32_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case MOE_ERR_CUDA: return "CUDA call failed";
+    case MOE_ERR_TIMEOUT: return "bounded device wait expired";
+    case MOE_ERR_DEVICE_INDEX: return "expert index out of range";
+    default: return "unknown status";
+  }
+}
+
+const char* moe_last_error_detail(void) { return g_detail; }
+
+int32_t moe_validate_config(const moe_config* cfg, int64_t T) {
+  if (cfg && cfg->d_ff > 0) return check_layer_cfg(cfg, T);
+  return check_router_cfg(cfg, T);
+}
+
+size_t moe_workspace_size(const moe_config* cfg, int64_t T) {
+  if (moe_validate_config(cfg, T) != MOE_OK) return 0;
+  return layout(cfg, T).total;
+}
+
+int32_t moe_get_device_status(void* workspace, void* stream) {
+  if (!workspace) return fail(MOE_ERR_WORKSPACE, "workspace is null");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MOE_CUDA(cudaStreamSynchronize(st));
+  int v = 0;
+  MOE_CUDA(cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost));
+  MOE_CUDA(cudaMemset(workspace, 0, sizeof(int)));
+  return v;
+}
+
+int32_t moe_router(const moe_config* cfg, int64_t T, const void* x, const float* W_r,
+                   const float* bias, int32_t* topk_idx, float* topk_w, void* stream) {
+  int32_t st = check_router_cfg(cfg, T);
+  if (st != MOE_OK) return st;
+  if (!x || !W_r || !bias || !topk_idx || !topk_w) return fail(MOE_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(x) || !aligned16(W_r) || !aligned16(bias) || !aligned16(topk_idx) ||
+      !aligned16(topk_w))
+    return fail(MOE_ERR_ALIGNMENT, "pointer not 16-byte aligned");
+  RouterArgs a;
+  a.x = x;
+  a.W_r = W_r;
+  a.bias = bias;
+  a.T = T;
+  a.d = cfg->d_model;
+  a.E = cfg->E_routed;
+  a.K = cfg->K;
+  a.G = cfg->n_group;
+  a.Gk = cfg->topk_group;
+  a.scale = cfg->routed_scaling_factor;
+  a.norm = cfg->norm_topk_prob;
+  a.x_bf16 = cfg->dtype == MOE_BF16;
+  a.topk_idx = topk_idx;
+  a.topk_w = topk_w;
+  MOE_CUDA(launch_router(a, static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int32_t moe_router_from_logits(const moe_config* cfg, int64_t T, const float* logits,
+                               const float* bias, int32_t* topk_idx, float* topk_w,
+                               void* stream) {
+  int32_t st = check_router_cfg(cfg, T);
+  if (st != MOE_OK) return st;
+  if (!logits || !bias || !topk_idx || !topk_w) return fail(MOE_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(logits) || !aligned16(bias) || !aligned16(topk_idx) || !aligned16(topk_w))
+    return fail(MOE_ERR_ALIGNMENT, "pointer not 16-byte aligned");
+  RouterArgs a;
+  a.logits = logits;
+  a.bias = bias;
+  a.T = T;
+  a.E = cfg->E_routed;
+  a.K = cfg->K;
+  a.G = cfg->n_group;
+  a.Gk = cfg->topk_group;
+  a.scale = cfg->routed_scaling_factor;
+  a.norm = cfg->norm_topk_prob;
+  a.topk_idx = topk_idx;
+  a.topk_w = topk_w;
+  MOE_CUDA(launch_router(a, static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int32_t moe_permute(const moe_config* cfg, int64_t T, const int32_t* topk_idx, int32_t* counts,
+                    int32_t* offsets, int32_t* perm, int32_t* inv, void* workspace,
+                    size_t ws_bytes, void* stream) {
+  int32_t st = check_router_cfg(cfg, T);
+  if (st != MOE_OK) return st;
+  if (!topk_idx || !counts || !offsets || !perm || !inv) return fail(MOE_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(topk_idx) || !aligned16(counts) || !aligned16(offsets) || !aligned16(perm) ||
+      !aligned16(inv))
+    return fail(MOE_ERR_ALIGNMENT, "pointer not 16-byte aligned");
+  if (!workspace || ws_bytes < kWsHeader) return fail(MOE_ERR_WORKSPACE, "workspace too small");
+  if (!aligned16(workspace)) return fail(MOE_ERR_ALIGNMENT, "workspace not aligned");
+  MOE_CUDA(launch_permute(topk_idx, T, cfg->K, cfg->E_routed, counts, offsets, perm, inv,
+                          static_cast<int*>(workspace), static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int32_t moe_grouped_swiglu(const moe_config* cfg, int64_t T, const void* x_e,
+                           const int32_t* offsets, const int32_t* perm, const float* topk_w,
+                           const void* W_gate_up, const void* W_down, const void* x_shared,
+                           const void* Ws_gate_up, const void* Ws_down, void* Y, void* Y_shared,
+                           void* workspace, size_t ws_bytes, void* stream) {
+  int32_t st = check_layer_cfg(cfg, T);
+  if (st != MOE_OK) return st;
+  if (!x_e || !offsets || !perm || !W_gate_up || !W_down || !Y)
+    return fail(MOE_ERR_INVALID_ARG, "null pointer");
+  const bool shared = x_shared != nullptr && cfg->E_shared > 0;
+  if (shared && (!Ws_gate_up || !Ws_down || !Y_shared))
+    return fail(MOE_ERR_INVALID_ARG, "shared expert pointers missing");
+  const void* ptrs[] = {x_e, offsets, perm, topk_w, W_gate_up, W_down, x_shared, Ws_gate_up,
+                        Ws_down, Y, Y_shared, workspace};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return fail(MOE_ERR_ALIGNMENT, "pointer not 16-byte aligned");
+  if (!workspace || ws_bytes < layout(cfg, T).total) return fail(MOE_ERR_WORKSPACE, "workspace too small");
+  ExpertIO io = {x_e, offsets, perm, topk_w, W_gate_up, W_down, shared ? x_shared : nullptr,
+                 Ws_gate_up, Ws_down, Y, Y_shared};
+  return run_experts(cfg, T, io, workspace, nullptr, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+int32_t moe_combine(const moe_config* cfg, int64_t T, const void* Y, const int32_t* inv,
+                    const void* Y_shared, void* y, void* stream) {
+  int32_t st = check_layer_cfg(cfg, T);
+  if (st != MOE_OK) return st;
+  if (!Y || !inv || !y) return fail(MOE_ERR_INVALID_ARG, "null pointer");
+  if (Y_shared && cfg->d_latent) return fail(MOE_ERR_INVALID_ARG, "Y_shared with d_latent");
+  if (!aligned16(Y) || !aligned16(inv) || !aligned16(y) || (Y_shared && !aligned16(Y_shared)))
+    return fail(MOE_ERR_ALIGNMENT, "pointer not 16-byte aligned");
+  const int D = d_expert(cfg);
+  if (D % 8) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "width % 8 != 0");
+  MOE_CUDA(launch_combine(Y, inv, T, cfg->K, D, Y_shared, Y_shared ? cfg->E_shared : 0, T, y,
+                          cfg->dtype == MOE_BF16, static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int32_t moe_linear(int64_t T, int32_t in_features, int32_t out_features, const void* x,
+                   const void* W, const void* add, void* y, void* workspace, size_t ws_bytes,
+                   void* stream) {
+  if (T < 1 || T > (1ll << 30)) return fail(MOE_ERR_INVALID_ARG, "T out of range");
+  if (in_features < 128 || out_features < 128 || in_features % 128 || out_features % 128)
+    return fail(MOE_ERR_UNSUPPORTED_SHAPE, "in/out features must be multiples of 128");
+  if (!x || !W || !y) return fail(MOE_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(x) || !aligned16(W) || !aligned16(y) || (add && !aligned16(add)))
+    return fail(MOE_ERR_ALIGNMENT, "pointer not 16-byte aligned");
+  if (!workspace || ws_bytes < kWsHeader) return fail(MOE_ERR_WORKSPACE, "workspace too small");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return run_linear(T, in_features, out_features, x, W, add, y, static_cast<int*>(workspace), st);
+}
+
+int32_t moe_layer_forward(const moe_config* cfg, int64_t T, const void* x, const float* W_r,
+                          const float* bias, const void* W_gate_up, const void* W_down,
+                          const void* Ws_gate_up, const void* Ws_down, const void* W_lat_down,
+                          const void* W_lat_up, void* y, int32_t* topk_idx_out,
+                          float* topk_w_out, int32_t* counts_out, void* workspace,
+                          size_t ws_bytes, void* const* stage_events, void* stream) {
+  int32_t st = check_layer_cfg(cfg, T);
+  if (st != MOE_OK) return st;
+  const int S = cfg->E_shared;
+  if (!x || !W_r || !bias || !W_gate_up || !W_down || !y) return fail(MOE_ERR_INVALID_ARG, "null pointer");
+  if (S && (!Ws_gate_up || !Ws_down)) return fail(MOE_ERR_INVALID_ARG, "shared expert weights missing");
+  if (cfg->d_latent && (!W_lat_down || !W_lat_up)) return fail(MOE_ERR_INVALID_ARG, "latent projections missing");
+  const void* ptrs[] = {x, W_r, bias, W_gate_up, W_down, Ws_gate_up, Ws_down, W_lat_down,
+                        W_lat_up, y, topk_idx_out, topk_w_out, counts_out, workspace};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return fail(MOE_ERR_ALIGNMENT, "pointer not 16-byte aligned");
+  const Layout L = layout(cfg, T);
+  if (!workspace || ws_bytes < L.total) return fail(MOE_ERR_WORKSPACE, "workspace too small");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto ev = [&](int i) -> cudaEvent_t {
+    return stage_events ? static_cast<cudaEvent_t>(stage_events[i]) : nullptr;
+  };
+  void* ws = workspace;
+  int* status = at<int>(ws, L.status);
+  int32_t* idx = topk_idx_out ? topk_idx_out : at<int32_t>(ws, L.topk_idx);
+  float* w = topk_w_out ? topk_w_out : at<float>(ws, L.topk_w);
+  int32_t* counts = counts_out ? counts_out : at<int32_t>(ws, L.counts);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* perm = at<int32_t>(ws, L.perm);
+  int32_t* inv = at<int32_t>(ws, L.inv);
+  const bool bf16 = cfg->dtype == MOE_BF16;
+
+  if (ev(0)) MOE_CUDA(cudaEventRecord(ev(0), s));
+  st = moe_router(cfg, T, x, W_r, bias, idx, w, s);
+  if (st != MOE_OK) return st;
+  if (ev(1)) MOE_CUDA(cudaEventRecord(ev(1), s));
+  MOE_CUDA(launch_permute(idx, T, cfg->K, cfg->E_routed, counts, offsets, perm, inv, status, s));
+  const void* x_e = x;
+  if (cfg->d_latent) {
+    st = run_linear(T, cfg->d_model, cfg->d_latent, x, W_lat_down, nullptr, at<void>(ws, L.x_lat),
+                    status, s);
+    if (st != MOE_OK) return st;
+    x_e = at<void>(ws, L.x_lat);
+  }
+  ExpertIO io = {x_e, offsets, perm, w, W_gate_up, W_down, S ? x : nullptr, Ws_gate_up, Ws_down,
+                 at<void>(ws, L.Y), S ? at<void>(ws, L.Ysh) : nullptr};
+  st = run_experts(cfg, T, io, ws, ev(2), ev(3), s);
+  if (st != MOE_OK) return st;
+  if (ev(4)) MOE_CUDA(cudaEventRecord(ev(4), s));
+  if (!cfg->d_latent) {
+    MOE_CUDA(launch_combine(at<void>(ws, L.Y), inv, T, cfg->K, cfg->d_model, at<void>(ws, L.Ysh),
+                            S, T, y, bf16, s));
+  } else {
+    // routed sum in latent space, project back, add the shared experts
+    MOE_CUDA(launch_combine(at<void>(ws, L.Y), inv, T, cfg->K, cfg->d_latent, nullptr, 0, 0,
+                            at<void>(ws, L.r_lat), bf16, s));
+    st = run_linear(T, cfg->d_latent, cfg->d_model, at<void>(ws, L.r_lat), W_lat_up, nullptr,
+                    at<void>(ws, L.U), status, s);
+    if (st != MOE_OK) return st;
+    MOE_CUDA(launch_combine(nullptr, nullptr, T, 0, cfg->d_model, at<void>(ws, L.U), 1 + S, T, y,
+                            bf16, s));
+  }
+  if (ev(5)) MOE_CUDA(cudaEventRecord(ev(5), s));
+  return MOE_OK;
+}
+
+int32_t moe_layer_forward_host(const moe_config* cfg, int64_t T, const void* x_host,
+                               const float* W_r, const float* bias, const void* W_gate_up,
+                               const void* W_down, const void* Ws_gate_up, const void* Ws_down,
+                               const void* W_lat_down, const void* W_lat_up, void* y_host,
+                               void* workspace, size_t ws_bytes, void* stream) {
+  int32_t st = check_layer_cfg(cfg, T);
+  if (st != MOE_OK) return st;
+  if (!x_host || !y_host) return fail(MOE_ERR_INVALID_ARG, "null host pointer");
+  const Layout L = layout(cfg, T);
+  if (!workspace || ws_bytes < L.total) return fail(MOE_ERR_WORKSPACE, "workspace too small");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t bytes = static_cast<size_t>(T) * cfg->d_model * elem_bytes(cfg);
+  void* xd = at<void>(workspace, L.x_stage);
+  void* yd = at<void>(workspace, L.y_stage);
+  MOE_CUDA(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s));
+  st = moe_layer_forward(cfg, T, xd, W_r, bias, W_gate_up, W_down, Ws_gate_up, Ws_down,
+                         W_lat_down, W_lat_up, yd, nullptr, nullptr, nullptr, workspace, ws_bytes,
+                         nullptr, stream);
+  if (st != MOE_OK) return st;
+  MOE_CUDA(cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s));
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,389 @@
+// Router of the fine-grained MoE layer.
+//
+// "Kimi K2 · Router · OpenModelAtlas", "All 4 steps":
+//   z = x_ffn W_r, s = sigmoid(z), E_sel = [i in top_K(s + b)],
+//   G_i = 2.827 s_i E_sel_i / sum_j s_j E_sel_j;
+// the page's MoEGate listing adds the fp32 cast of x and W_r, the group
+// limiting of noaux_tc (keep the topk_group groups whose two best biased
+// scores sum highest, fill the other experts' scores with 0.0), the
+// renormalisation with + 1e-20 (only when K > 1 and norm_topk_prob) and the
+// final routed_scaling_factor.
+//
+// Design (GB300): one thread-block cluster per 64 tokens, one CTA per 128
+// experts (K2: 3 CTAs, K3: 7).  Each CTA runs the fp32 FFMA GEMM for its
+// 64 x 128 logit tile, keeps the tile in shared memory, and after a cluster
+// barrier every CTA selects for a share of the 64 tokens by reading the
+// whole 64 x E logit row set through distributed shared memory -- the logits
+// never touch HBM.  Selection is one warp per token: sigmoid + bias per lane,
+// group top-2 sums by warp shuffles, then K rounds of a warp arg-max.
+#include <cooperative_groups.h>
+#include <math_constants.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace fgs {
+
+namespace {
+
+constexpr int kTM = 64;   // tokens per cluster
+constexpr int kEC = 128;  // experts per CTA
+constexpr int kBK = 32;   // reduction chunk
+constexpr int kThreads = 256;
+
+// s rounded once from the fp64 sigmoid of the fp32 logit: the correctly
+// rounded fp32 sigmoid except when the fp64 value lies within one fp64 ulp
+// of an fp32 rounding boundary.
+__device__ __forceinline__ double sigmoid_f64(float z) {
+  return 1.0 / (1.0 + exp(-static_cast<double>(z)));
+}
+
+// Order used for every discrete choice: larger value first, then the
+// smaller index.
+__device__ __forceinline__ bool before(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+// Selection for one token by one warp.  Lane `lane` holds the logits of
+// experts e = lane + 32 j, j < PM.  Writes topk_idx[0..K) and topk_w[0..K).
+template <int PM>
+__device__ __forceinline__ void select_token(const float (&z)[PM], int lane, int E,
+                                             const float* __restrict__ bias, int K, int G,
+                                             int Gk, float scale, int norm,
+                                             int32_t* __restrict__ out_idx,
+                                             float* __restrict__ out_w) {
+  const unsigned full = 0xffffffffu;
+  float c[PM];
+#pragma unroll
+  for (int j = 0; j < PM; ++j) {
+    const int e = lane + 32 * j;
+    if (e < E) {
+      const float s = static_cast<float>(sigmoid_f64(z[j]));
+      c[j] = __fadd_rn(s, __ldg(bias + e));  // c = s + b, one fp32 rounding
+    } else {
+      c[j] = -CUDART_INF_F;  // no such expert
+    }
+  }
+
+  if (G > 1) {
+    // group score = sum of the two largest biased scores in the group
+    const int gsize = E / G;
+    float my_gscore = -CUDART_INF_F;
+    for (int g = 0; g < G; ++g) {
+      float m1 = -CUDART_INF_F, m2 = -CUDART_INF_F;
+#pragma unroll
+      for (int j = 0; j < PM; ++j) {
+        const int e = lane + 32 * j;
+        if (e < E && e / gsize == g) {
+          const float v = c[j];
+          if (v > m1) {
+            m2 = m1;
+            m1 = v;
+          } else if (v > m2) {
+            m2 = v;
+          }
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float o1 = __shfl_xor_sync(full, m1, off);
+        const float o2 = __shfl_xor_sync(full, m2, off);
+        if (m1 >= o1) {
+          m2 = fmaxf(m2, o1);
+        } else {
+          m2 = fmaxf(m1, o2);
+          m1 = o1;
+        }
+      }
+      if (lane == g) my_gscore = __fadd_rn(m1, m2);
+    }
+    // keep the Gk best groups (ties: smaller group index)
+    bool kept = false;
+    for (int r = 0; r < Gk; ++r) {
+      float bv = (lane < G && !kept) ? my_gscore : -CUDART_INF_F;
+      int bi = (lane < G && !kept) ? lane : 0x7fffffff;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(full, bv, off);
+        const int oi = __shfl_xor_sync(full, bi, off);
+        if (before(ov, oi, bv, bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if (lane == bi) kept = true;
+    }
+    const unsigned kept_mask = __ballot_sync(full, kept);
+#pragma unroll
+    for (int j = 0; j < PM; ++j) {
+      const int e = lane + 32 * j;
+      if (e < E && !((kept_mask >> (e / gsize)) & 1u)) c[j] = 0.0f;  // literal 0.0 fill
+    }
+  }
+
+  // K rounds of warp arg-max over the (masked) biased scores
+  unsigned taken = 0u;
+  int my_idx = 0;
+  double my_s = 0.0;
+  for (int k = 0; k < K; ++k) {
+    float bv = -CUDART_INF_F;
+    int bi = 0x7fffffff;
+    float bz = 0.0f;
+#pragma unroll
+    for (int j = 0; j < PM; ++j) {
+      const int e = lane + 32 * j;
+      if (e < E && !((taken >> j) & 1u) && before(c[j], e, bv, bi)) {
+        bv = c[j];
+        bi = e;
+        bz = z[j];
+      }
+    }
+    const int mine = bi;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(full, bv, off);
+      const int oi = __shfl_xor_sync(full, bi, off);
+      if (before(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    const int owner = bi & 31;
+    double s = 0.0;
+    if (lane == owner && mine == bi) {
+      taken |= 1u << (bi >> 5);
+      s = sigmoid_f64(bz);  // unbiased score of the winner
+    }
+    s = __shfl_sync(full, s, owner);
+    if (lane == k) {
+      my_idx = bi;
+      my_s = s;
+    }
+  }
+  double sum = (lane < K) ? my_s : 0.0;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(full, sum, off);
+  if (lane < K) {
+    const double w = (K > 1 && norm) ? my_s / (sum + 1e-20) : my_s;
+    out_idx[lane] = my_idx;
+    out_w[lane] = static_cast<float>(w * static_cast<double>(scale));
+  }
+}
+
+template <typename XT>
+struct XLoad;
+
+template <>
+struct XLoad<__nv_bfloat16> {
+  // 8 consecutive bf16 as fp32
+  static __device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      v[2 * i] = f.x;
+      v[2 * i + 1] = f.y;
+    }
+  }
+};
+
+template <>
+struct XLoad<float> {
+  static __device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+};
+
+struct RouterSmem {
+  union {
+    struct {
+      float xs[2][kBK][kTM];  // x chunk, transposed: [k][token]
+      float ws[2][kBK][kEC];  // W_r chunk, transposed: [k][expert]
+    } pipe;
+    float zs[kTM][kEC];  // the CTA's logit tile
+  };
+};
+
+template <typename XT, int PM>
+__global__ void __launch_bounds__(kThreads) router_fused_kernel(
+    const XT* __restrict__ x, const float* __restrict__ W_r, const float* __restrict__ bias,
+    int T, int d, int E, int K, int G, int Gk, float scale, int norm,
+    int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+  __shared__ __align__(16) RouterSmem sm;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int CS = static_cast<int>(cluster.num_blocks());
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int tid = threadIdx.x;
+  const int tok0 = blockIdx.y * kTM;
+  const int e0 = rank * kEC;
+
+  // loader roles
+  const int lx_tok = tid % kTM, lx_k = (tid / kTM) * 8;     // 8 x values
+  const int lw_e = tid % kEC, lw_k = (tid / kEC) * 16;      // 16 W values
+  const bool x_ok = tok0 + lx_tok < T;
+  const bool w_ok = e0 + lw_e < E;
+  const XT* xrow = x + static_cast<int64_t>(x_ok ? tok0 + lx_tok : 0) * d + lx_k;
+  const float* wrow = W_r + static_cast<int64_t>(w_ok ? e0 + lw_e : 0) * d + lw_k;
+
+  // compute roles: 4 tokens x (4 + 4) experts per thread
+  const int tx = tid % 16, ty = tid / 16;
+
+  float acc[4][8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+
+  float xv[8];
+  float4 wv[4];
+  auto load_chunk = [&](int k0) {
+    if (x_ok) {
+      XLoad<XT>::load8(xrow + k0, xv);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) xv[i] = 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      wv[i] = w_ok ? __ldg(reinterpret_cast<const float4*>(wrow + k0) + i)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+  };
+  auto store_chunk = [&](int buf) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sm.pipe.xs[buf][lx_k + i][lx_tok] = xv[i];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      sm.pipe.ws[buf][lw_k + 4 * i + 0][lw_e] = wv[i].x;
+      sm.pipe.ws[buf][lw_k + 4 * i + 1][lw_e] = wv[i].y;
+      sm.pipe.ws[buf][lw_k + 4 * i + 2][lw_e] = wv[i].z;
+      sm.pipe.ws[buf][lw_k + 4 * i + 3][lw_e] = wv[i].w;
+    }
+  };
+
+  const int nchunks = d / kBK;
+  load_chunk(0);
+  store_chunk(0);
+  __syncthreads();
+  for (int c = 0; c < nchunks; ++c) {
+    const int buf = c & 1;
+    if (c + 1 < nchunks) load_chunk((c + 1) * kBK);
+#pragma unroll 8
+    for (int k = 0; k < kBK; ++k) {
+      const float4 a = *reinterpret_cast<const float4*>(&sm.pipe.xs[buf][k][ty * 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&sm.pipe.ws[buf][k][tx * 4]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&sm.pipe.ws[buf][k][64 + tx * 4]);
+      const float av[4] = {a.x, a.y, a.z, a.w};
+      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    if (c + 1 < nchunks) store_chunk(buf ^ 1);
+    __syncthreads();
+  }
+
+  // logit tile to shared memory (the pipeline buffers are dead now)
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      sm.zs[ty * 4 + i][tx * 4 + j] = acc[i][j];
+      sm.zs[ty * 4 + i][64 + tx * 4 + j] = acc[i][4 + j];
+    }
+  }
+  cluster.sync();
+
+  // selection: this CTA takes tokens tt = rank, rank + CS, ...; one warp each
+  const int warp = tid / 32, lane = tid % 32;
+  for (int tt = rank + CS * warp; tt < kTM; tt += CS * (kThreads / 32)) {
+    const int t = tok0 + tt;
+    if (t >= T) break;
+    float z[PM];
+#pragma unroll
+    for (int j = 0; j < PM; ++j) {
+      const int e = lane + 32 * j;
+      if (e < E) {
+        const float* peer = cluster.map_shared_rank(&sm.zs[0][0], e / kEC);
+        z[j] = peer[tt * kEC + (e % kEC)];
+      } else {
+        z[j] = 0.0f;
+      }
+    }
+    select_token<PM>(z, lane, E, bias, K, G, Gk, scale, norm,
+                     topk_idx + static_cast<int64_t>(t) * K, topk_w + static_cast<int64_t>(t) * K);
+  }
+  cluster.sync();  // peers may still read this CTA's tile
+}
+
+template <int PM>
+__global__ void __launch_bounds__(256) router_logits_kernel(
+    const float* __restrict__ logits, const float* __restrict__ bias, int T, int E, int K, int G,
+    int Gk, float scale, int norm, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+  const int lane = threadIdx.x % 32;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
+  if (t >= T) return;
+  float z[PM];
+#pragma unroll
+  for (int j = 0; j < PM; ++j) {
+    const int e = lane + 32 * j;
+    z[j] = e < E ? __ldg(logits + t * E + e) : 0.0f;
+  }
+  select_token<PM>(z, lane, E, bias, K, G, Gk, scale, norm, topk_idx + t * K, topk_w + t * K);
+}
+
+template <typename XT, int PM>
+cudaError_t launch_fused(const RouterArgs& a, cudaStream_t stream) {
+  const int CS = (a.E + kEC - 1) / kEC;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(CS, static_cast<unsigned>((a.T + kTM - 1) / kTM), 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, router_fused_kernel<XT, PM>, static_cast<const XT*>(a.x), a.W_r,
+                            a.bias, static_cast<int>(a.T), a.d, a.E, a.K, a.G, a.Gk, a.scale,
+                            a.norm, a.topk_idx, a.topk_w);
+}
+
+template <int PM>
+cudaError_t launch_logits(const RouterArgs& a, cudaStream_t stream) {
+  const int warps = 8;
+  const unsigned blocks = static_cast<unsigned>((a.T + warps - 1) / warps);
+  router_logits_kernel<PM><<<blocks, warps * 32, 0, stream>>>(
+      a.logits, a.bias, static_cast<int>(a.T), a.E, a.K, a.G, a.Gk, a.scale, a.norm, a.topk_idx,
+      a.topk_w);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream) {
+  if (a.logits) {
+    if (a.E <= 128) return launch_logits<4>(a, stream);
+    if (a.E <= 384) return launch_logits<12>(a, stream);
+    return launch_logits<32>(a, stream);
+  }
+  if (a.x_bf16) {
+    if (a.E <= 128) return launch_fused<__nv_bfloat16, 4>(a, stream);
+    if (a.E <= 384) return launch_fused<__nv_bfloat16, 12>(a, stream);
+    return launch_fused<__nv_bfloat16, 32>(a, stream);
+  }
+  if (a.E <= 128) return launch_fused<float, 4>(a, stream);
+  if (a.E <= 384) return launch_fused<float, 12>(a, stream);
+  return launch_fused<float, 32>(a, stream);
+}
+
+}  // namespace fgs

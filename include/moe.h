@@ -1,0 +1,229 @@
+/*
+ * fine_grained_sparse_gb300 -- C ABI of the fine-grained MoE layer forward
+ * (Kimi-K2 / Kimi-K3 shape) on one GB300 (sm_103a).
+ *
+ * The layer, as the pages state it:
+ *   - "Kimi K2 · Router · OpenModelAtlas", equations under "All 4 steps":
+ *       z = x_ffn W_r,  s = sigmoid(z),  E_sel = [i in top_K(s + b)],
+ *       G_i = 2.827 s_i E_sel_i / sum_j s_j E_sel_j
+ *     and its MoEGate listing (fp32 gate GEMM, noaux_tc biased selection with
+ *     n_group / topk_group group limiting, renormalisation + 1e-20,
+ *     routed_scaling_factor).
+ *   - "Kimi K2 MoE", sections 2-3: output = shared_expert(x) + sum over the
+ *     selected experts of G_i f_i(x); SwiGLU experts of 3 d d_ff parameters.
+ *   - "Kimi K3's router picks 16 of 896 experts", K3 table and the Stable
+ *     LatentMoE paragraph: routed experts work on a 7168 -> 3584 projection
+ *     of x, their combined output is projected back, 2 shared experts stay
+ *     at 7168.
+ *
+ * Conventions shared by every call
+ *   - Pointers are DEVICE pointers unless a parameter says "host".  All
+ *     buffers are owned by the caller; no call allocates device memory.
+ *   - Matrices are dense row-major.  Batch and sequence are flattened:
+ *     T = B * seq_len rows.  Weights follow nn.Linear (out x in).
+ *   - Element type of activations, expert weights and layer outputs is
+ *     cfg->dtype: MOE_BF16 (tensor-core path, fp32 accumulation) or MOE_F32
+ *     (CUDA-core path).  The router weight, bias, logits and gate weights
+ *     are always fp32; expert indices are int32.
+ *   - Every pointer must be 16-byte aligned (MOE_ERR_ALIGNMENT otherwise).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  Argument errors are reported by the return value
+ *     before anything is enqueued.  Errors found on the device (an expert
+ *     index out of range, a bounded wait that expired) are written to the
+ *     status word at the start of the workspace; read them with
+ *     moe_get_device_status().  No exception crosses this interface.
+ *   - The same workspace may not be used by two calls that run concurrently.
+ *     moe_workspace_size(cfg, T) bytes suffice for every call below with
+ *     that cfg and a row count <= T.
+ */
+#ifndef FINE_GRAINED_SPARSE_GB300_MOE_H
+#define FINE_GRAINED_SPARSE_GB300_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,       /* null pointer, T < 1, K > E, ...        */
+  MOE_ERR_UNSUPPORTED_SHAPE = 2, /* shape the chosen path does not cover   */
+  MOE_ERR_ALIGNMENT = 3,         /* a pointer is not 16-byte aligned       */
+  MOE_ERR_WORKSPACE = 4,         /* workspace missing or too small         */
+  MOE_ERR_CUDA = 5,              /* a CUDA runtime/driver call failed      */
+  MOE_ERR_TIMEOUT = 6,           /* a bounded device wait expired          */
+  MOE_ERR_DEVICE_INDEX = 7       /* an expert index outside [0, E_routed)  */
+} moe_status;
+
+typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+/* Layer configuration.  Field names follow the gate config of the
+ * "Kimi K2 · Router" MoEGate listing where it has one. */
+typedef struct moe_config {
+  int32_t d_model;      /* hidden_size d (7168 for K2 and K3)                  */
+  int32_t d_ff;         /* routed expert intermediate width F (K2 2048, K3 3072)*/
+  int32_t E_routed;     /* n_routed_experts E (K2 384, K3 896), <= 1024         */
+  int32_t E_shared;     /* always-on shared experts S (K2 1, K3 2), may be 0    */
+  int32_t d_ff_shared;  /* shared expert intermediate width F_s                 */
+  int32_t K;            /* num_experts_per_tok (K2 8, K3 16), 1 <= K <= E       */
+  int32_t n_group;      /* n_group G, E % G == 0, G <= 32                       */
+  int32_t topk_group;   /* topk_group, 1 <= topk_group <= G                     */
+  float routed_scaling_factor; /* 2.827                                         */
+  int32_t norm_topk_prob;      /* renormalise the K weights when K > 1 (1)      */
+  int32_t d_latent;     /* K3 latent width L (3584); 0 = K2 form (no projection)*/
+  int32_t dtype;        /* moe_dtype of activations, expert weights, outputs    */
+} moe_config;
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t moe_version(void);
+
+/* Static text for a moe_status value. */
+const char* moe_status_string(int32_t status);
+
+/* Text describing the most recent failing call on the calling thread (the
+ * failed check or the CUDA error).  Valid until the next failing call on
+ * that thread. */
+const char* moe_last_error_detail(void);
+
+/* Check cfg and T against the rules every call applies; makes no CUDA call.
+ * Returns MOE_OK, MOE_ERR_INVALID_ARG or MOE_ERR_UNSUPPORTED_SHAPE.  The
+ * MOE_BF16 path needs d_model and d_latent to be multiples of 128 and
+ * d_ff and d_ff_shared multiples of 64; MOE_F32 takes any positive sizes. */
+int32_t moe_validate_config(const moe_config* cfg, int64_t T);
+
+/* Bytes of device workspace any call below needs for (cfg, T); 0 if the
+ * configuration is invalid.  Makes no CUDA call. */
+size_t moe_workspace_size(const moe_config* cfg, int64_t T);
+
+/* Read and clear the device status word of `workspace` (synchronises
+ * `stream` first).  Returns MOE_OK or the first device-side error recorded
+ * since the last read. */
+int32_t moe_get_device_status(void* workspace, void* stream);
+
+/*
+ * Router, all four steps ("Kimi K2 · Router", "All 4 steps"; MoEGate):
+ *   z = x W_r^T in fp32 (x upcast from cfg->dtype), s = sigmoid(z),
+ *   c = s + bias, optional group limiting (G > 1: keep the topk_group groups
+ *   with the largest sum of their two best c, set c of every other expert to
+ *   0.0), then the K largest c.
+ *   x        [T, d_model]  cfg->dtype
+ *   W_r      [E, d_model]  fp32 (gate.weight)
+ *   bias     [E]           fp32 (e_score_correction_bias)
+ *   topk_idx [T, K] int32  out: selected experts, ordered by c descending,
+ *                          equal c by smaller expert index first
+ *   topk_w   [T, K] fp32   out: routed_scaling_factor * s_i / (sum s + 1e-20)
+ *                          (no renormalisation when K == 1 or
+ *                          norm_topk_prob == 0)
+ * The selection is decided on fp32 values with s rounded once from the
+ * exact sigmoid of the fp32 logit. */
+int32_t moe_router(const moe_config* cfg, int64_t T, const void* x, const float* W_r,
+                   const float* bias, int32_t* topk_idx, float* topk_w, void* stream);
+
+/* Router steps 2-4 from given fp32 logits z [T, E] (the parity entry point:
+ * identical logits give identical expert indices on every implementation
+ * that follows the rule above).  Other arguments as moe_router. */
+int32_t moe_router_from_logits(const moe_config* cfg, int64_t T, const float* logits,
+                               const float* bias, int32_t* topk_idx, float* topk_w,
+                               void* stream);
+
+/*
+ * Dispatch: group the T*K (token, slot) pairs by expert ("Kimi K2 MoE",
+ * section 3, dispatch_and_combine; its body is not given).  Order: expert
+ * major, ascending token index within an expert.  Pair j = t * K + k.
+ *   topk_idx [T, K] int32  in
+ *   counts   [E]    int32  out: pairs routed to each expert
+ *   offsets  [E+1]  int32  out: exclusive prefix sum of counts
+ *   perm     [T*K]  int32  out: perm[offsets[e] + r] = j of the r-th pair of e
+ *   inv      [T*K]  int32  out: inv[j] = the slot of pair j
+ * An index outside [0, E) records MOE_ERR_DEVICE_INDEX in the workspace
+ * status and its pair is left out of counts, perm and inv. */
+int32_t moe_permute(const moe_config* cfg, int64_t T, const int32_t* topk_idx,
+                    int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                    void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Grouped SwiGLU experts ("Kimi K2 MoE", section 2: SwiGLU experts,
+ * 3 d d_ff parameters each): for every slot r of expert e,
+ *   Y[r] = w_r * W_down[e] (SiLU(W_gate[e] u) * (W_up[e] u)),  u = x_e[perm[r] / K]
+ * with w_r = topk_w[perm[r]] (or 1 when topk_w is NULL); and for every shared
+ * expert s and token t, Y_shared[s, t] = f_s(x_shared[t]) with weight 1.
+ *   x_e        [T, d_e]        rows the routed experts read (d_e = d_latent if
+ *                              set, else d_model)
+ *   offsets    [E+1], perm [T*K] from moe_permute
+ *   topk_w     [T, K] fp32 or NULL
+ *   W_gate_up  [E, 2F, d_e]    rows 0..F-1 = W_gate, rows F..2F-1 = W_up
+ *   W_down     [E, d_e, F]
+ *   x_shared   [T, d_model] or NULL (then the shared arguments are ignored)
+ *   Ws_gate_up [S, 2F_s, d_model], Ws_down [S, d_model, F_s]
+ *   Y          [T*K, d_e]      out, slot order
+ *   Y_shared   [S, T, d_model] out (may be NULL when x_shared is NULL)
+ * Intermediates (the gathered rows and SwiGLU activations, rounded to
+ * cfg->dtype) live in the workspace. */
+int32_t moe_grouped_swiglu(const moe_config* cfg, int64_t T, const void* x_e,
+                           const int32_t* offsets, const int32_t* perm, const float* topk_w,
+                           const void* W_gate_up, const void* W_down, const void* x_shared,
+                           const void* Ws_gate_up, const void* Ws_down, void* Y, void* Y_shared,
+                           void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Weighted combine ("Kimi K2 MoE", section 3: shared_expert(x) + routed):
+ *   y[t] = sum_{k=0..K-1} Y[inv[t*K + k]] + sum_s Y_shared[s, t]
+ * summed in fp32 in that fixed order.  The gate weights are already in Y
+ * when moe_grouped_swiglu was given topk_w.
+ *   Y        [T*K, D], inv [T*K], Y_shared [S, T, D] or NULL, y [T, D] out;
+ *   D = d_e.  For the K3 form (d_latent != 0) Y_shared must be NULL: the
+ *   routed sum is in latent space. */
+int32_t moe_combine(const moe_config* cfg, int64_t T, const void* Y, const int32_t* inv,
+                    const void* Y_shared, void* y, void* stream);
+
+/*
+ * Plain projection y = x W^T (+ add) for the K3 latent maps ("Kimi K3's
+ * router picks 16 of 896 experts", Stable LatentMoE: 7168 -> 3584 before
+ * the routed experts, 3584 -> 7168 after their combine).  MOE_BF16 only.
+ *   x [T, in] bf16, W [out, in] bf16, add [T, out] bf16 or NULL, y [T, out].
+ * in and out must be multiples of 128. */
+int32_t moe_linear(int64_t T, int32_t in_features, int32_t out_features, const void* x,
+                   const void* W, const void* add, void* y, void* workspace, size_t ws_bytes,
+                   void* stream);
+
+/*
+ * The whole layer forward, one stream:
+ *   K2 form: y = sum_s f_s(x) + sum_k w_k f_{idx_k}(x)
+ *   K3 form: y = sum_s f_s(x) + W_lat_up (sum_k w_k f_{idx_k}(W_lat_down x))
+ * (router on x in both forms).
+ *   x [T, d], W_r [E, d] fp32, bias [E] fp32, W_gate_up/W_down as in
+ *   moe_grouped_swiglu, Ws_gate_up/Ws_down (NULL when E_shared == 0),
+ *   W_lat_down [L, d] and W_lat_up [d, L] (NULL unless d_latent != 0),
+ *   y [T, d] out.
+ *   topk_idx_out [T, K], topk_w_out [T, K], counts_out [E]: optional copies
+ *   of the routing (NULL to skip).
+ *   stage_events: NULL, or MOE_STAGE_COUNT + 1 cudaEvent_t handles recorded
+ *   on `stream` before each stage and after the last (router, dispatch,
+ *   expert gate/up, expert down, combine and projections). */
+#define MOE_STAGE_COUNT 5
+int32_t moe_layer_forward(const moe_config* cfg, int64_t T, const void* x, const float* W_r,
+                          const float* bias, const void* W_gate_up, const void* W_down,
+                          const void* Ws_gate_up, const void* Ws_down, const void* W_lat_down,
+                          const void* W_lat_up, void* y, int32_t* topk_idx_out,
+                          float* topk_w_out, int32_t* counts_out, void* workspace,
+                          size_t ws_bytes, void* const* stage_events, void* stream);
+
+/*
+ * moe_layer_forward with x and y in HOST memory (pinned for asynchronous
+ * copies; pageable memory works but the copies then block).  The call
+ * enqueues the host-to-device copy of x into the workspace, the forward and
+ * the device-to-host copy of y, and returns without waiting: y_host is valid
+ * after `stream` has been synchronised.  Weights stay device pointers. */
+int32_t moe_layer_forward_host(const moe_config* cfg, int64_t T, const void* x_host,
+                               const float* W_r, const float* bias, const void* W_gate_up,
+                               const void* W_down, const void* Ws_gate_up, const void* Ws_down,
+                               const void* W_lat_down, const void* W_lat_up, void* y_host,
+                               void* workspace, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FINE_GRAINED_SPARSE_GB300_MOE_H */

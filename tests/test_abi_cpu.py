@@ -1,0 +1,109 @@
+"""The C-ABI library builds, loads without a GPU and exports every symbol the
+public header declares; argument checks answer before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+@pytest.fixture(scope="module")
+def fgs():
+    from fine_grained_sparse_gb300 import build
+    build.build()
+    import fine_grained_sparse_gb300 as m
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("moe_router", "moe_router_from_logits", "moe_permute", "moe_grouped_swiglu",
+                     "moe_combine", "moe_layer_forward", "moe_workspace_size"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(fgs):
+    lib = ctypes.CDLL(fgs.lib_path())
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(fgs):
+    assert fgs.moe_version() >= 100
+    for code in range(8):
+        assert fgs.moe_status_string(code) != "unknown status"
+
+
+def _k2(fgs, **kw):
+    base = dict(d_model=7168, d_ff=2048, E_routed=384, E_shared=1, d_ff_shared=2048, K=8,
+                n_group=8, topk_group=4, dtype=fgs.MOE_BF16)
+    base.update(kw)
+    return fgs.config(**base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({}, 0),
+    ({"K": 0}, 1),
+    ({"K": 385}, 1),
+    ({"E_routed": 1025, "n_group": 1, "topk_group": 1}, 1),
+    ({"n_group": 5}, 1),                      # 384 % 5 != 0
+    ({"topk_group": 9}, 1),
+    ({"E_routed": 64, "n_group": 8, "topk_group": 1, "K": 9}, 1),  # K > topk_group * E / n_group
+    ({"d_model": 7200}, 2),                   # bf16 path: d % 128
+    ({"d_ff": 2000}, 2),
+    ({"d_latent": 3000}, 2),
+    ({"K": 33, "n_group": 1, "topk_group": 1}, 2),
+    ({"dtype": 7}, 1),
+])
+def test_validate_config(fgs, kw, status):
+    assert fgs.moe_validate_config(_k2(fgs, **kw), 8192) == status
+
+
+def test_validate_rows(fgs):
+    assert fgs.moe_validate_config(_k2(fgs), 0) == 1
+    assert fgs.moe_validate_config(_k2(fgs), 1) == 0
+
+
+def test_workspace_size_grows_with_T(fgs):
+    cfg = _k2(fgs)
+    a, b = fgs.moe_workspace_size(cfg, 128), fgs.moe_workspace_size(cfg, 8192)
+    assert 0 < a < b
+    assert fgs.moe_workspace_size(_k2(fgs, K=0), 128) == 0
+    # the gathered rows alone: T*K rows of d bf16
+    assert b > 8192 * 8 * 7168 * 2
+
+
+def test_argument_errors_return_before_any_cuda_call(fgs):
+    cfg = _k2(fgs)
+    lib = fgs.lib
+    # null pointers
+    assert lib.moe_router(ctypes.byref(cfg), 16, None, None, None, None, None, None) == 1
+    # misaligned pointers (never dereferenced: the check comes first)
+    bad = 0x1001
+    assert lib.moe_router(ctypes.byref(cfg), 16, bad, 0x1000, 0x1000, 0x1000, 0x1000, None) == 3
+    assert lib.moe_router_from_logits(ctypes.byref(cfg), 16, 0x1000, bad, 0x1000, 0x1000, None) == 3
+    # workspace too small
+    ws = fgs.moe_workspace_size(cfg, 16)
+    assert lib.moe_layer_forward(ctypes.byref(cfg), 16, *([0x1000] * 10), None, None, None,
+                                 0x1000, ws - 256, None, None) == 4
+    assert "workspace" in fgs.moe_last_error_detail()
+    # shape the bf16 path does not cover
+    assert lib.moe_linear(16, 100, 128, 0x1000, 0x1000, None, 0x1000, 0x1000, 4096, None) == 2
+    # invalid config reaches every entry point
+    assert lib.moe_permute(ctypes.byref(_k2(fgs, K=0)), 16, *([0x1000] * 5), 0x1000, 4096, None) == 1
+
+
+def test_python_binding_raises(fgs):
+    cfg = _k2(fgs)
+    with pytest.raises(fgs.MoeError) as ei:
+        fgs.moe_router(cfg, 16, None, None, None, None, None, stream=0)
+    assert ei.value.status == 1

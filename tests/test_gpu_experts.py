@@ -1,0 +1,114 @@
+"""Grouped SwiGLU experts (tensor-core bf16 path and fp32 CUDA-core path)
+against the oracle's expert math, slot by slot."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _gpu_common import TOL_BF16, TOL_F32, lib, need_gpu, np64, rel_max_err, workspace
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(T, d, E, K, F, S, Fs, dtype, seed, skew=False):
+    shape = synth.custom(T=T, d_model=d, E_routed=E, K=K, E_shared=S, d_ff=F, d_ff_shared=Fs,
+                         dtype=dtype)
+    g = synth.generate(shape, device="cuda", seed=seed)
+    gen = torch.Generator().manual_seed(seed)
+    wts = torch.ones(E)
+    if skew:
+        wts[:K] = 50.0
+    idx = torch.stack([torch.multinomial(wts, K, replacement=False, generator=gen)
+                       for _ in range(T)])
+    topk_w = torch.rand((T, K), generator=gen) + 0.1
+    return shape, g, idx.numpy(), topk_w
+
+
+def _run(shape, g, idx, topk_w):
+    fgs = lib()
+    T, K, E = shape.T, shape.K, shape.E_routed
+    cfg = fgs.config(shape)
+    p = oracle.permute(idx, E)
+    ws, nws = workspace(cfg, T)
+    dt = g["x"].dtype
+    Y = torch.empty((T * K, shape.d_model), dtype=dt, device="cuda")
+    S = shape.E_shared
+    Ys = torch.empty((S, T, shape.d_model), dtype=dt, device="cuda") if S else None
+    fgs.moe_grouped_swiglu(
+        cfg, T, g["x"], torch.from_numpy(p["offsets"].astype(np.int32)).cuda(),
+        torch.from_numpy(p["perm"].astype(np.int32)).cuda(), topk_w.cuda(), g["W_gate_up"],
+        g["W_down"], g["x"] if S else None, g.get("Ws_gate_up"), g.get("Ws_down"), Y, Ys, ws, nws)
+    assert fgs.moe_get_device_status(ws) == 0
+    return p, Y, Ys
+
+
+def _reference(shape, g, idx, topk_w, p):
+    T, K, F = shape.T, shape.K, shape.d_ff
+    x = np64(g["x"])
+    Wgu, Wd = np64(g["W_gate_up"]), np64(g["W_down"])
+    Yref = np.zeros((T * K, shape.d_model))
+    for e in range(shape.E_routed):
+        slots = np.arange(p["offsets"][e], p["offsets"][e + 1])
+        if slots.size == 0:
+            continue
+        j = p["perm"][slots]
+        t, k = j // K, j % K
+        Yref[slots] = topk_w.numpy()[t, k][:, None] * oracle.swiglu_expert(
+            x[t], Wgu[e, :F], Wgu[e, F:], Wd[e])
+    Ysref = None
+    if shape.E_shared:
+        Fs = shape.d_ff_shared
+        Sgu, Sd = np64(g["Ws_gate_up"]), np64(g["Ws_down"])
+        Ysref = np.stack([oracle.swiglu_expert(x, Sgu[s, :Fs], Sgu[s, Fs:], Sd[s])
+                          for s in range(shape.E_shared)])
+    return Yref, Ysref
+
+
+CASES = [
+    # T, d, E, K, F, S, Fs, skew   -- several k-steps, output blocks and ragged tails
+    (100, 256, 8, 2, 128, 1, 64, False),
+    (600, 384, 4, 2, 192, 1, 128, False),     # experts with > 256 rows: 2 token tiles
+    (37, 512, 16, 4, 64, 2, 128, True),       # T <= 64: 64-row token tile
+    (130, 256, 64, 8, 128, 0, 0, False),      # no shared expert, many 1-3 row experts
+    (1, 128, 4, 2, 64, 1, 64, False),         # a single token
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "T%d_d%d_E%d_K%d_F%d_S%d" % c[:6])
+def test_grouped_swiglu_bf16(case):
+    need_gpu()
+    T, d, E, K, F, S, Fs, skew = case
+    shape, g, idx, topk_w = _case(T, d, E, K, F, S, Fs, "bf16", seed=T + d + E, skew=skew)
+    p, Y, Ys = _run(shape, g, idx, topk_w)
+    Yref, Ysref = _reference(shape, g, idx, topk_w, p)
+    assert rel_max_err(np64(Y), Yref) <= TOL_BF16
+    if S:
+        assert rel_max_err(np64(Ys), Ysref) <= TOL_BF16
+
+
+@pytest.mark.parametrize("case", [(64, 256, 16, 4, 64, 1, 64, False), (45, 96, 6, 3, 40, 2, 24, True)])
+def test_grouped_swiglu_f32(case):
+    need_gpu()
+    T, d, E, K, F, S, Fs, skew = case
+    shape, g, idx, topk_w = _case(T, d, E, K, F, S, Fs, "f32", seed=T + d, skew=skew)
+    p, Y, Ys = _run(shape, g, idx, topk_w)
+    Yref, Ysref = _reference(shape, g, idx, topk_w, p)
+    assert rel_max_err(np64(Y), Yref) <= TOL_F32
+    assert rel_max_err(np64(Ys), Ysref) <= TOL_F32
+
+
+def test_linear_bf16():
+    need_gpu()
+    fgs = lib()
+    gen = torch.Generator(device="cuda").manual_seed(3)
+    for T, i, o in [(5, 256, 384), (300, 512, 256)]:
+        x = torch.randn((T, i), generator=gen, device="cuda").bfloat16()
+        W = (torch.randn((o, i), generator=gen, device="cuda") * 0.05).bfloat16()
+        add = torch.randn((T, o), generator=gen, device="cuda").bfloat16()
+        y = torch.empty((T, o), dtype=torch.bfloat16, device="cuda")
+        ws = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+        fgs.moe_linear(T, i, o, x, W, add, y, ws, 4096)
+        torch.cuda.synchronize()
+        want = np64(x) @ np64(W).T + np64(add)
+        assert rel_max_err(np64(y), want) <= TOL_BF16

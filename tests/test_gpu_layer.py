@@ -1,0 +1,100 @@
+"""Whole-layer parity (moe_layer_forward) against the oracle.
+
+Small configurations are compared on every token; the K2 decode, K2 prefill
+and K3 latent configurations run at full size, in the launch configuration
+the benchmark times, and are compared on a sample of tokens the oracle
+evaluates one by one (its cost is one fp64 upcast per selected expert)."""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _gpu_common import (GAP_MIN, TOL_BF16, TOL_F32, lib, need_gpu, np64, rel_max_err,
+                         to_f64_cpu, workspace)
+
+pytestmark = pytest.mark.gpu
+
+
+def _forward(shape, g):
+    fgs = lib()
+    cfg = fgs.config(shape)
+    T = g["x"].shape[0]
+    ws, nws = workspace(cfg, T)
+    y = torch.empty((T, shape.d_model), dtype=g["x"].dtype, device="cuda")
+    idx = torch.empty((T, shape.K), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, shape.K), dtype=torch.float32, device="cuda")
+    counts = torch.empty(shape.E_routed, dtype=torch.int32, device="cuda")
+    fgs.moe_layer_forward(cfg, T, g["x"], g["W_r"], g["bias"], g["W_gate_up"], g["W_down"],
+                          g.get("Ws_gate_up"), g.get("Ws_down"), g.get("W_lat_down"),
+                          g.get("W_lat_up"), y, idx, w, counts, ws, nws)
+    assert fgs.moe_get_device_status(ws) == 0
+    return y, idx, w, counts
+
+
+def _oracle(shape, g, rows):
+    x = np64(g["x"][rows])
+    return oracle.moe_layer_tokens(
+        x, np64(g["W_r"]), g["bias"].cpu().numpy(), g["W_gate_up"], g["W_down"],
+        g.get("Ws_gate_up"), g.get("Ws_down"), shape.K, shape.n_group, shape.topk_group,
+        shape.routed_scaling_factor, shape.norm_topk_prob,
+        W_lat_down64=np64(g["W_lat_down"]) if shape.d_latent else None,
+        W_lat_up64=np64(g["W_lat_up"]) if shape.d_latent else None,
+        to_f64=to_f64_cpu)
+
+
+def _compare(shape, g, y, idx, w, counts, rows, tol):
+    ref = _oracle(shape, g, rows)
+    clear = ref["gap"] > GAP_MIN
+    got_idx = idx.cpu().numpy()[rows]
+    np.testing.assert_array_equal(got_idx[clear], ref["idx"][clear])
+    assert rel_max_err(w.cpu().numpy()[rows][clear], ref["w"][clear]) <= 1e-4
+    # rows whose routing matches are compared on the layer output
+    same = (got_idx == ref["idx"]).all(axis=1)
+    assert same.mean() > 0.9
+    assert rel_max_err(np64(y[rows])[same], ref["y"][same]) <= tol
+    assert int(counts.sum()) == g["x"].shape[0] * shape.K
+
+
+SMALL = [
+    synth.shape("tiny"),
+    synth.custom(name="small_grouped", T=256, d_model=512, E_routed=32, K=4, E_shared=1,
+                 d_ff=256, d_ff_shared=128, n_group=4, topk_group=2, x_dist="clusters32"),
+    synth.custom(name="small_k3", T=200, d_model=512, d_latent=256, E_routed=16, K=4,
+                 E_shared=2, d_ff=128, d_ff_shared=128),
+    synth.custom(name="small_noshared", T=33, d_model=256, E_routed=8, K=2, d_ff=64),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: s.name)
+def test_layer_small_every_token(shape):
+    need_gpu()
+    g = synth.generate(shape, device="cuda")
+    y, idx, w, counts = _forward(shape, g)
+    rows = np.arange(shape.T)
+    _compare(shape, g, y, idx, w, counts, rows, TOL_F32 if shape.dtype == "f32" else TOL_BF16)
+
+
+@pytest.mark.parametrize("name", ["k2_decode", "k2_prefill", "k3_latent"])
+def test_layer_full_size_sampled(name):
+    need_gpu()
+    shape = synth.shape(name)
+    g = synth.generate(shape, device="cuda")
+    try:
+        y, idx, w, counts = _forward(shape, g)
+        torch.cuda.synchronize()
+        T = shape.T
+        rows = np.unique(np.linspace(0, T - 1, 6).astype(int))
+        _compare(shape, g, y, idx, w, counts, rows, TOL_BF16)
+        # the routing of every token on the gap criterion
+        r = oracle.router_from_x(np64(g["x"]), np64(g["W_r"]), g["bias"].cpu().numpy(), shape.K,
+                                 shape.n_group, shape.topk_group)
+        clear = r["gap"] > GAP_MIN
+        np.testing.assert_array_equal(idx.cpu().numpy()[clear], r["idx"][clear])
+        assert np.isfinite(np64(y)).all()
+    finally:
+        del g
+        gc.collect()
+        torch.cuda.empty_cache()

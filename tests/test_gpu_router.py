@@ -1,0 +1,87 @@
+"""Router parity on the GPU: moe_router_from_logits bit-exact against the
+oracle on shared fp32 logits; moe_router (fused GEMM) on the gap criterion."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _gpu_common import (GAP_MIN, TOL_WEIGHTS, lib, need_gpu, np64, rel_max_err)
+
+pytestmark = pytest.mark.gpu
+
+# (E, K, n_group, topk_group)
+ROUTER_SHAPES = [(16, 4, 1, 1), (384, 8, 1, 1), (384, 8, 8, 4), (896, 16, 1, 1), (64, 6, 4, 2),
+                 (32, 32, 1, 1), (8, 1, 1, 1), (96, 9, 3, 1)]
+
+
+def _logits(kind, T, E, gen):
+    if kind == "normal":
+        return torch.randn((T, E), generator=gen) * 1.5
+    if kind == "grid":  # distinct values on a 2^-10 grid: no near-ties
+        base = (torch.arange(E, dtype=torch.float32) - E / 2) * 2.0 ** -10 * 7
+        return torch.stack([base[torch.randperm(E, generator=gen)] for _ in range(T)])
+    if kind == "ties":  # few distinct values: many exact ties, broken by index
+        vals = torch.tensor([-1.0, -0.5, 0.0, 0.25, 0.5, 1.0])
+        return vals[torch.randint(0, len(vals), (T, E), generator=gen)]
+    raise ValueError(kind)
+
+
+@pytest.mark.parametrize("shape", ROUTER_SHAPES, ids=lambda s: "E%d_K%d_G%d_%d" % s)
+@pytest.mark.parametrize("kind", ["normal", "grid", "ties"])
+@pytest.mark.parametrize("T", [1, 37, 1000])
+def test_router_from_logits_bit_exact(shape, kind, T):
+    need_gpu()
+    fgs = lib()
+    E, K, G, Gk = shape
+    seed = E * 1000 + K * 10 + G + 7 * T + 100000 * ["normal", "grid", "ties"].index(kind)
+    gen = torch.Generator().manual_seed(seed)
+    z = _logits(kind, T, E, gen).float()
+    b = torch.zeros(E) if kind != "normal" else (torch.rand(E, generator=gen) - 0.5) * 0.3
+    cfg = fgs.config(d_model=128, E_routed=E, K=K, n_group=G, topk_group=Gk)
+    idx = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    fgs.moe_router_from_logits(cfg, T, z.cuda(), b.cuda(), idx, w)
+    torch.cuda.synchronize()
+    ref = oracle.router_from_logits(z.numpy(), b.numpy(), K, G, Gk)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref["idx"])
+    assert rel_max_err(w.cpu().numpy(), ref["w"]) <= TOL_WEIGHTS
+
+
+def _check_router_from_x(cfg_shape, x, W_r, bias):
+    fgs = lib()
+    T = x.shape[0]
+    cfg = fgs.config(cfg_shape, d_ff=0)
+    idx = torch.empty((T, cfg.K), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, cfg.K), dtype=torch.float32, device="cuda")
+    fgs.moe_router(cfg, T, x, W_r, bias, idx, w)
+    torch.cuda.synchronize()
+    ref = oracle.router_from_x(np64(x), np64(W_r), bias.cpu().numpy(), cfg.K, cfg.n_group,
+                               cfg.topk_group)
+    got_idx = idx.cpu().numpy()
+    clear = ref["gap"] > GAP_MIN
+    assert clear.mean() > 0.98, "the inputs should leave almost every token with a clear margin"
+    np.testing.assert_array_equal(got_idx[clear], ref["idx"][clear])
+    assert rel_max_err(w.cpu().numpy()[clear], ref["w"][clear]) <= TOL_WEIGHTS
+    # every token, clear or not, selects K distinct valid experts
+    assert ((got_idx >= 0) & (got_idx < cfg.E_routed)).all()
+    srt = np.sort(got_idx, axis=1)
+    assert (np.diff(srt, axis=1) > 0).all()
+
+
+@pytest.mark.parametrize("name,T", [("tiny", None), ("k2_router", None), ("k2_prefill", 700),
+                                    ("k3_latent", 300)])
+def test_router_fused_matches_oracle(name, T):
+    need_gpu()
+    shape = synth.shape(name)
+    g = synth.generate(shape, device="cuda", T=T, weights=False)
+    _check_router_from_x(shape, g["x"], g["W_r"], g["bias"])
+
+
+def test_router_fused_ragged_tokens_and_small_E():
+    need_gpu()
+    for T, E, K, G, Gk in [(1, 16, 4, 1, 1), (65, 40, 5, 4, 2), (130, 130, 7, 1, 1)]:
+        shape = synth.custom(T=T, d_model=256, E_routed=E, K=K, n_group=G, topk_group=Gk,
+                             router_only=True)
+        g = synth.generate(shape, device="cuda", seed=T + E)
+        _check_router_from_x(shape, g["x"], g["W_r"], g["bias"])
