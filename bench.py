@@ -1,0 +1,489 @@
+#!/usr/bin/env python
+"""Throughput of the fine-grained MoE layer forward (Kimi-K2 shape) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+
+One step is one moe_layer_forward over one batch of T synthetic tokens: the
+fused router, the dispatch, the grouped SwiGLU experts with the shared
+expert, and the weighted combine -- every row of the hot path.  Inputs are
+resident in HBM when the timed region starts; the expert weights (34 GB for
+the K2 layer) exceed the 129 MB L2, so every step streams them from HBM.
+
+With N > 1 (torchrun, one rank per GPU) every rank runs an independent
+replica of the layer on its own batch (the layer has no exchange step on one
+GPU; weak scaling); the time is the maximum over ranks.
+
+``--impl reference`` times the CPU oracle instead, on bounded samples of the
+same workload, on the host cores of rank 0.
+
+Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer tokens/s (K2 shape) + % of HBM / bf16 tensor roofline; router tokens/s"
+UNIT = "tokens/s"
+WORKLOADS = {
+    "k2_prefill": "K2 MoE layer prefill with group-limited routing: T=8192 tokens, d_model=7168, "
+                  "384 routed + 1 shared SwiGLU expert (intermediate 2048), top-8, n_group=8, "
+                  "topk_group=4, scale 2.827, bf16 experts with fp32 accumulation, fp32 router, "
+                  "x from a 32-cluster Gaussian mixture, bias U(-0.1,0.1)",
+    "k2_decode": "K2 MoE layer decode: T=128 tokens, d_model=7168, 384 routed + 1 shared SwiGLU "
+                 "expert (intermediate 2048), top-8, scale 2.827, bf16 experts, fp32 router, "
+                 "x from a 32-cluster Gaussian mixture",
+    "k3_latent": "K3-shaped latent MoE layer: T=4096, d_model=7168, latent 3584, 896 routed SwiGLU "
+                 "experts (intermediate 3072), top-16, 2 shared experts at 7168 (intermediate "
+                 "3072), scale 2.827, bf16 experts, fp32 router",
+}
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="k2_prefill", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="own", choices=["own", "reference"])
+    ap.add_argument("--cpu-sample-tokens", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+class ClockSampler:
+    """nvidia-smi sampling every 100 ms while the timed region runs."""
+
+    def __init__(self, device_id: str):
+        fields = ["timestamp", "clocks.sm", "clocks.max.sm", "power.draw",
+                  "clocks_event_reasons.active"] + ["clocks_event_reasons." + r for r in REASONS]
+        self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
+        self.cmd = ["nvidia-smi", "--query-gpu=" + ",".join(fields), "--format=csv,noheader,nounits",
+                    "-lms", "100", "-i", device_id, "-f", self.path]
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.5)
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) < 5 + len(REASONS):
+                        continue
+                    try:
+                        ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                        rows.append((ts, float(parts[1]), float(parts[2]), parts[3], parts[5:]))
+                    except ValueError:
+                        continue
+            os.unlink(self.path)
+        except OSError:
+            return None
+        inside = [r for r in rows if t0 - 0.15 <= r[0] <= t1 + 0.15]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = sorted({REASONS[i] for r in inside for i, v in enumerate(r[4][:len(REASONS)])
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "samples": len(inside)}
+
+
+def device_id(torch, local_rank):
+    try:
+        u = str(torch.cuda.get_device_properties(local_rank).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(local_rank)
+
+
+# --------------------------------------------------------- work accounting
+def per_step_work(shape, counts):
+    """Algorithmic bytes and flops of one layer step and of its kernels.
+
+    Bytes count only what the method must touch: the weights of the experts
+    actually selected (unique, from the per-expert counts), the shared
+    experts, the router weight and bias, x once and y once.  H / Y round
+    trips and gathered copies are implementation costs and are left out."""
+    T, d, E, K = shape.T, shape.d_model, shape.E_routed, shape.K
+    F, S, Fs, L = shape.d_ff, shape.E_shared, shape.d_ff_shared, shape.d_latent
+    de = L if L else d
+    U = int((counts > 0).sum())
+    b16 = 2
+    w_gu = 2 * F * de * b16
+    w_dn = de * F * b16
+    ws_gu = 2 * Fs * d * b16
+    ws_dn = d * Fs * b16
+    xbytes = T * d * b16
+    router_bytes = E * d * 4 + E * 4 + xbytes + T * K * 8
+    # x is read once; with the latent form the routed experts read x_lat instead
+    gate_up_bytes = U * w_gu + S * ws_gu + T * de * b16 + (T * d * b16 if (S and L) else 0)
+    down_bytes = U * w_dn + S * ws_dn
+    layer_bytes = U * (w_gu + w_dn) + S * (ws_gu + ws_dn) + E * d * 4 + E * 4 + 2 * xbytes
+    if L:
+        layer_bytes += 2 * L * d * b16
+    flops_router = 2 * T * d * E
+    flops_gate_up = 2 * T * K * de * 2 * F + 2 * T * S * d * 2 * Fs
+    flops_down = 2 * T * K * F * de + 2 * T * S * Fs * d
+    flops_proj = 2 * 2 * T * d * L if L else 0
+    return {"U": U, "gate_up_bytes": gate_up_bytes, "down_bytes": down_bytes,
+            "router_bytes": router_bytes, "layer_bytes": layer_bytes,
+            "flops_router": flops_router, "flops_gate_up": flops_gate_up, "flops_down": flops_down,
+            "flops_layer": flops_router + flops_gate_up + flops_down + flops_proj}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("gemm_tc.cu", "common.cuh", "internal.h"):
+        with open(os.path.join(ROOT, "fine_grained_sparse_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(config):
+    """DRAM bytes per gate/up launch from the committed ncu summary, if it was
+    taken on the current kernel source."""
+    path = os.path.join(PROFILE_DIR, f"tc_gemm_gate_up_{config}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m_b or not m_h or m_h.group(1) != kernel_source_hash():
+        return None
+    return float(m_b.group(1))
+
+
+# ------------------------------------------------------------ CPU oracle leg
+def oracle_sample(shape, x_rows, W_r, bias, routed, shared, lat):
+    """Run the oracle on the given token rows; returns (seconds, result)."""
+    import numpy as np
+    import torch
+    import oracle
+    f64 = lambda t: t.to(torch.float64).numpy()  # noqa: E731
+    t0 = time.perf_counter()
+    res = oracle.moe_layer(
+        f64(x_rows), f64(W_r), bias.numpy(),
+        routed=lambda e: tuple(f64(w) for w in routed(e)),
+        shared=(lambda s: tuple(f64(w) for w in shared(s))) if shape.E_shared else None,
+        n_shared=shape.E_shared, K=shape.K, n_group=shape.n_group, topk_group=shape.topk_group,
+        scale=shape.routed_scaling_factor, norm_topk_prob=shape.norm_topk_prob,
+        W_lat_down64=f64(lat[0]) if lat else None, W_lat_up64=f64(lat[1]) if lat else None)
+    return time.perf_counter() - t0, res
+
+
+def split_gu(gu, F):
+    return gu[:F], gu[F:]
+
+
+def cpu_baseline_from_device(shape, g, idx, n_tokens):
+    """Oracle on n_tokens of the benchmarked batch (host cores).  The weights
+    the sample selects are staged to host memory before the clock starts."""
+    import numpy as np
+    import torch
+    T = shape.T
+    rows = np.unique(np.linspace(0, T - 1, n_tokens).astype(int))
+    experts = sorted(set(int(e) for e in idx[rows].reshape(-1)))
+    F, Fs = shape.d_ff, shape.d_ff_shared
+    host = {e: (g["W_gate_up"][e].cpu(), g["W_down"][e].cpu()) for e in experts}
+
+    def routed(e):
+        if e not in host:  # the oracle chose an expert the device did not
+            host[e] = (g["W_gate_up"][e].cpu(), g["W_down"][e].cpu())
+        gu, dn = host[e]
+        return (*split_gu(gu, F), dn)
+
+    sh = [(g["Ws_gate_up"][s].cpu(), g["Ws_down"][s].cpu()) for s in range(shape.E_shared)]
+    lat = (g["W_lat_down"].cpu(), g["W_lat_up"].cpu()) if shape.d_latent else None
+    x_rows = g["x"][torch.as_tensor(rows, device=g["x"].device)].cpu()
+    secs, _ = oracle_sample(shape, x_rows, g["W_r"].cpu(), g["bias"].cpu(), routed,
+                            lambda s: (*split_gu(sh[s][0], Fs), sh[s][1]), lat)
+    cores = len(os.sched_getaffinity(0))
+    return {"value": len(rows) / secs, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{len(rows)} of the {T} tokens of the benchmarked batch, full layer "
+                      f"(router over all {shape.E_routed} experts, {shape.K} routed + "
+                      f"{shape.E_shared} shared SwiGLU experts each, fp64); {secs:.1f} s"}
+
+
+# ------------------------------------------------------------------ own arm
+def run_own(args):
+    import numpy as np
+    import torch
+    import synth
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    try:
+        import fine_grained_sparse_gb300 as fgs
+    except ImportError:
+        import __graft_entry__
+        __graft_entry__.build()
+        import fine_grained_sparse_gb300 as fgs
+
+    shape = synth.shape(args.config)
+    T = shape.T
+    seed = synth.SEEDS[shape.name]
+    g = synth.generate(shape, device="cuda", seed=seed)
+    if rank:  # replicas: every rank its own batch, same weights
+        g["x"] = synth.activations(shape, "cuda", seed=seed + 7919 * rank)
+    cfg = fgs.config(shape)
+    nws = fgs.moe_workspace_size(cfg, T)
+    ws = torch.zeros(nws, dtype=torch.uint8, device="cuda")
+    y = torch.empty((T, shape.d_model), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((T, shape.K), dtype=torch.int32, device="cuda")
+    counts = torch.empty(shape.E_routed, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.Stream()
+    nev = fgs.MOE_STAGE_COUNT + 1
+
+    def step(events=None):
+        fgs.moe_layer_forward(cfg, T, g["x"], g["W_r"], g["bias"], g["W_gate_up"], g["W_down"],
+                              g.get("Ws_gate_up"), g.get("Ws_down"), g.get("W_lat_down"),
+                              g.get("W_lat_up"), y, idx, None, counts, ws, nws,
+                              stage_events=events, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    stream.synchronize()
+    status = fgs.moe_get_device_status(ws, stream)
+    if status:
+        raise RuntimeError("device status after warm-up: " + fgs.moe_status_string(status))
+
+    step_events = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)]
+                   for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(device_id(torch, local)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        step(step_events[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop(t0, t1) if sampler else None
+    ms_total = start.elapsed_time(end)
+    if world > 1:
+        tt = torch.tensor([ms_total], device="cuda")
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    status = fgs.moe_get_device_status(ws, stream)
+    if status:
+        raise RuntimeError("device status after the timed steps: " + fgs.moe_status_string(status))
+
+    stage_ms = [statistics.mean(ev[j].elapsed_time(ev[j + 1]) for ev in step_events)
+                for j in range(nev - 1)]
+    ms_step = ms_total / args.steps
+    value = world * T * args.steps / (ms_total / 1e3)
+    counts_h = counts.cpu().numpy()
+    work = per_step_work(shape, counts_h)
+    peaks = load_peaks()
+    gu_ms = stage_ms[2]
+    achieved = work["gate_up_bytes"] / (gu_ms / 1e3) / 1e9
+    traffic = profiled_traffic(args.config)
+    roofline = {"bound": "hbm", "kernel": "tc_gemm_kernel (expert gate/up + SwiGLU, routed + shared)",
+                "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                "peak_source": peaks["source"],
+                "algorithmic_bytes_per_launch": work["gate_up_bytes"],
+                "tensor_frac_of_sustained": round(work["flops_gate_up"] / (gu_ms / 1e3) / 1e12
+                                                  / peaks["bf16_tflops_sustained"], 4)}
+    per_launch = 8 if not shape.d_latent else 11
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; bf16 expert weights N(0,0.02), fp32 router weight "
+                "kaiming-uniform, bias uniform; shapes of the pages' K2/K3 layers)",
+        "config": {"workload": WORKLOADS[args.config], "name": args.config, "tokens_per_step": T,
+                   "l2": "inputs larger than L2: the selected experts' weights (tens of GB) "
+                         "stream from HBM every step",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roofline,
+        "layer": {"hbm_frac": round(work["layer_bytes"] / (ms_step / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                  "tensor_frac_of_sustained": round(work["flops_layer"] / (ms_step / 1e3) / 1e12
+                                                    / peaks["bf16_tflops_sustained"], 4),
+                  "algorithmic_bytes": work["layer_bytes"], "flops": work["flops_layer"],
+                  "unique_experts": work["U"]},
+        "router": {"tokens_per_s": round(T / (stage_ms[0] / 1e3), 1), "ms": round(stage_ms[0], 4),
+                   "fp32_tflops": round(work["flops_router"] / (stage_ms[0] / 1e3) / 1e12, 2)},
+        "stages_ms": {n: round(v, 4) for n, v in zip(fgs.STAGE_NAMES, stage_ms)},
+        "gpu_launches": per_launch * args.steps,
+        "clocks": clocks,
+    }
+
+    # end to end through the C ABI with host buffers (copies inside the region)
+    x_host = g["x"].cpu().pin_memory()
+    y_host = torch.empty((T, shape.d_model), dtype=torch.bfloat16).pin_memory()
+
+    def step_host():
+        fgs.moe_layer_forward_host(cfg, T, x_host, g["W_r"], g["bias"], g["W_gate_up"],
+                                   g["W_down"], g.get("Ws_gate_up"), g.get("Ws_down"),
+                                   g.get("W_lat_down"), g.get("W_lat_up"), y_host, ws, nws,
+                                   stream=stream)
+
+    for _ in range(2):
+        step_host()
+    stream.synchronize()
+    e_steps = max(3, min(args.steps, 50))
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    es.record(stream)
+    for _ in range(e_steps):
+        step_host()
+    ee.record(stream)
+    ee.synchronize()
+    e_ms = es.elapsed_time(ee)
+    if world > 1:
+        tt = torch.tensor([e_ms], device="cuda")
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e_ms = float(tt.item())
+    nbytes = T * shape.d_model * 2
+    line["e2e"] = {"value": round(world * T * e_steps / (e_ms / 1e3), 1), "unit": UNIT,
+                   "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes, "steps": e_steps,
+                   "api": "moe_layer_forward_host (pinned host x and y)"}
+
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_from_device(shape, g, idx.cpu().numpy(),
+                                                        args.cpu_sample_tokens)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+# ------------------------------------------------------------ reference arm
+def run_reference(args):
+    """The CPU oracle on the same workload, one bounded sample per step."""
+    import numpy as np
+    import torch
+    import oracle
+    import synth
+
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    shape = synth.shape(args.config)
+    seed = synth.SEEDS[shape.name]
+    x = synth.activations(shape, "cpu", seed)
+    W_r, bias = synth.router_params(shape, "cpu", seed)
+    lat = synth.latent_projections(shape, "cpu", seed) if shape.d_latent else None
+    sh = [synth.shared_expert(shape, s, "cpu", seed) for s in range(shape.E_shared)]
+    F, Fs = shape.d_ff, shape.d_ff_shared
+    cache = {}
+
+    def routed(e):
+        if e not in cache:
+            cache[e] = synth.routed_expert(shape, e, "cpu", seed)
+        gu, dn = cache[e]
+        return (*split_gu(gu, F), dn)
+
+    # a pool of tokens whose experts are drawn once (drawing weights is not the
+    # oracle's work); each step runs the oracle on the next token of the pool
+    tokens_per_step = 1
+    total = args.warmup + args.steps
+    pool = np.random.default_rng(0).choice(shape.T, size=min(8, total), replace=False)
+    pre = oracle.router_from_x(x[torch.as_tensor(pool)].to(torch.float64).numpy(),
+                               W_r.to(torch.float64).numpy(), bias.numpy(), shape.K,
+                               shape.n_group, shape.topk_group)
+    for e in sorted(set(int(v) for v in pre["idx"].reshape(-1))):
+        routed(e)
+    times = []
+    for i in range(total):
+        rows = pool[i % len(pool): i % len(pool) + tokens_per_step]
+        secs, _ = oracle_sample(shape, x[torch.as_tensor(rows)], W_r, bias, routed,
+                                lambda s: (*split_gu(sh[s][0], Fs), sh[s][1]), lat)
+        if i >= args.warmup:
+            times.append(secs)
+    secs = sum(times)
+    value = tokens_per_step * len(times) / secs
+    cores = len(os.sched_getaffinity(0))
+    sample = (f"{tokens_per_step} token per step, cycling over {len(pool)} tokens drawn from the "
+              f"{shape.T}-token batch, full layer "
+              f"(router over all {shape.E_routed} experts, {shape.K} routed + {shape.E_shared} "
+              f"shared SwiGLU experts, fp64 oracle)")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * secs / len(times), 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOADS[args.config], "name": args.config},
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_own(args)
+
+
+if __name__ == "__main__":
+    main()

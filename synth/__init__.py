@@ -35,7 +35,8 @@ from typing import Dict, Optional
 
 import torch
 
-__all__ = ["LayerShape", "CONFIGS", "SEEDS", "shape", "generate", "custom"]
+__all__ = ["LayerShape", "CONFIGS", "SEEDS", "shape", "generate", "custom", "activations",
+           "router_params", "routed_expert", "shared_expert", "latent_projections"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -96,6 +97,18 @@ def _wdtype(cfg: LayerShape) -> torch.dtype:
     return torch.float32 if cfg.dtype == "f32" else torch.bfloat16
 
 
+# Every tensor has its own generator, seeded from (seed, stream id), so one
+# expert's weights can be drawn without drawing the others.
+_STREAM_X, _STREAM_WR, _STREAM_BIAS, _STREAM_LAT_DOWN, _STREAM_LAT_UP = 1, 2, 3, 4, 5
+_STREAM_SHARED, _STREAM_ROUTED = 100, 1000
+
+
+def _gen(seed: int, stream: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed((seed << 24) + stream)
+    return g
+
+
 def _normal(gen, shp, std, device, dtype):
     t = torch.randn(shp, generator=gen, device=device, dtype=torch.float32)
     if std != 1.0:
@@ -108,7 +121,16 @@ def _uniform(gen, shp, lo, hi, device):
     return t.mul_(hi - lo).add_(lo)
 
 
-def _x(cfg: LayerShape, gen, device, T):
+def _seed(cfg: LayerShape, seed: Optional[int]) -> int:
+    return SEEDS.get(cfg.name, 12345) if seed is None else seed
+
+
+def activations(cfg: LayerShape, device="cpu", seed: Optional[int] = None,
+                T: Optional[int] = None) -> torch.Tensor:
+    """x [T, d_model]: N(0, 1), or a 32-cluster Gaussian mixture (centres
+    N(0, I), cluster chosen uniformly, unit noise)."""
+    T = cfg.T if T is None else T
+    gen = _gen(_seed(cfg, seed), _STREAM_X, device)
     dt = _wdtype(cfg)
     if cfg.x_dist == "normal":
         return _normal(gen, (T, cfg.d_model), 1.0, device, dt)
@@ -120,44 +142,57 @@ def _x(cfg: LayerShape, gen, device, T):
     raise ValueError(cfg.x_dist)
 
 
+def router_params(cfg: LayerShape, device="cpu", seed: Optional[int] = None):
+    """(W_r [E, d] fp32 kaiming-uniform with a = sqrt(5), bias [E] fp32)."""
+    s = _seed(cfg, seed)
+    d, E = cfg.d_model, cfg.E_routed
+    bound = 1.0 / math.sqrt(d)  # kaiming_uniform(a=sqrt(5)): gain*sqrt(3/fan_in)
+    W_r = _uniform(_gen(s, _STREAM_WR, device), (E, d), -bound, bound, device)
+    bias = _uniform(_gen(s, _STREAM_BIAS, device), (E,), -cfg.bias_range, cfg.bias_range, device)
+    return W_r, bias
+
+
+def routed_expert(cfg: LayerShape, e: int, device="cpu", seed: Optional[int] = None):
+    """(W_gate_up [2F, d_e], W_down [d_e, F]) of routed expert e, N(0, 0.02)."""
+    g = _gen(_seed(cfg, seed), _STREAM_ROUTED + e, device)
+    dt, de, F = _wdtype(cfg), cfg.d_expert, cfg.d_ff
+    return _normal(g, (2 * F, de), 0.02, device, dt), _normal(g, (de, F), 0.02, device, dt)
+
+
+def shared_expert(cfg: LayerShape, s_idx: int, device="cpu", seed: Optional[int] = None):
+    """(Ws_gate_up [2Fs, d], Ws_down [d, Fs]) of shared expert s_idx."""
+    g = _gen(_seed(cfg, seed), _STREAM_SHARED + s_idx, device)
+    dt, d, Fs = _wdtype(cfg), cfg.d_model, cfg.d_ff_shared
+    return _normal(g, (2 * Fs, d), 0.02, device, dt), _normal(g, (d, Fs), 0.02, device, dt)
+
+
+def latent_projections(cfg: LayerShape, device="cpu", seed: Optional[int] = None):
+    """(W_lat_down [L, d], W_lat_up [d, L]), N(0, 0.02)."""
+    s, dt, d, L = _seed(cfg, seed), _wdtype(cfg), cfg.d_model, cfg.d_latent
+    return (_normal(_gen(s, _STREAM_LAT_DOWN, device), (L, d), 0.02, device, dt),
+            _normal(_gen(s, _STREAM_LAT_UP, device), (d, L), 0.02, device, dt))
+
+
 def generate(cfg: LayerShape, device="cpu", seed: Optional[int] = None,
              T: Optional[int] = None, weights: bool = True) -> Dict[str, torch.Tensor]:
-    """Draw every input of one layer call.  Deterministic for (seed, device).
-
-    Tensors are drawn in a fixed order, one expert at a time so that the peak
-    temporary stays at one expert's worth of fp32.
-    """
-    if seed is None:
-        seed = SEEDS.get(cfg.name, 12345)
-    T = cfg.T if T is None else T
-    gen = torch.Generator(device=device)
-    gen.manual_seed(seed)
-    out: Dict[str, torch.Tensor] = {}
-    d, E = cfg.d_model, cfg.E_routed
-    out["x"] = _x(cfg, gen, device, T)
-    bound = 1.0 / math.sqrt(d)  # kaiming_uniform(a=sqrt(5)): gain*sqrt(3/fan_in)
-    out["W_r"] = _uniform(gen, (E, d), -bound, bound, device)
-    out["bias"] = _uniform(gen, (E,), -cfg.bias_range, cfg.bias_range, device)
+    """Draw every input of one layer call.  Deterministic for (seed, device)."""
+    out: Dict[str, torch.Tensor] = {"x": activations(cfg, device, seed, T)}
+    out["W_r"], out["bias"] = router_params(cfg, device, seed)
     if cfg.router_only or not weights:
         return out
-    dt = _wdtype(cfg)
-    de, F = cfg.d_expert, cfg.d_ff
+    dt, de, F, E = _wdtype(cfg), cfg.d_expert, cfg.d_ff, cfg.E_routed
     W_gate_up = torch.empty((E, 2 * F, de), device=device, dtype=dt)
     W_down = torch.empty((E, de, F), device=device, dtype=dt)
     for e in range(E):
-        W_gate_up[e] = _normal(gen, (2 * F, de), 0.02, device, dt)
-        W_down[e] = _normal(gen, (de, F), 0.02, device, dt)
+        W_gate_up[e], W_down[e] = routed_expert(cfg, e, device, seed)
     out["W_gate_up"], out["W_down"] = W_gate_up, W_down
     S, Fs = cfg.E_shared, cfg.d_ff_shared
     if S:
-        Ws_gate_up = torch.empty((S, 2 * Fs, d), device=device, dtype=dt)
-        Ws_down = torch.empty((S, d, Fs), device=device, dtype=dt)
+        Ws_gate_up = torch.empty((S, 2 * Fs, cfg.d_model), device=device, dtype=dt)
+        Ws_down = torch.empty((S, cfg.d_model, Fs), device=device, dtype=dt)
         for s in range(S):
-            Ws_gate_up[s] = _normal(gen, (2 * Fs, d), 0.02, device, dt)
-            Ws_down[s] = _normal(gen, (d, Fs), 0.02, device, dt)
+            Ws_gate_up[s], Ws_down[s] = shared_expert(cfg, s, device, seed)
         out["Ws_gate_up"], out["Ws_down"] = Ws_gate_up, Ws_down
     if cfg.d_latent:
-        L = cfg.d_latent
-        out["W_lat_down"] = _normal(gen, (L, d), 0.02, device, dt)
-        out["W_lat_up"] = _normal(gen, (d, L), 0.02, device, dt)
+        out["W_lat_down"], out["W_lat_up"] = latent_projections(cfg, device, seed)
     return out

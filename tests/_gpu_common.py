@@ -57,3 +57,16 @@ TOL_F32 = 1e-4
 # Tokens whose K-th vs (K+1)-th biased score gap (or group gap) is below this
 # may legitimately select differently when the logits come from the fp32 GEMM.
 GAP_MIN = 1e-5
+
+
+def by_expert(idx, w=None):
+    """Selected sets in ascending expert order (and the weights aligned to
+    them).  The order inside the selected set is a convention that near-equal
+    scores may flip when the two sides' logits differ by rounding; the set is
+    what the margin criterion fixes."""
+    idx = np.asarray(idx)
+    order = np.argsort(idx, axis=1, kind="stable")
+    sidx = np.take_along_axis(idx, order, axis=1)
+    if w is None:
+        return sidx
+    return sidx, np.take_along_axis(np.asarray(w), order, axis=1)

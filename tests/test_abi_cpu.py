@@ -12,8 +12,8 @@ HEADER = os.path.join(ROOT, "include", "moe.h")
 
 @pytest.fixture(scope="module")
 def fgs():
-    from fine_grained_sparse_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import fine_grained_sparse_gb300 as m
     return m
 

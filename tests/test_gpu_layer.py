@@ -12,8 +12,8 @@ import torch
 
 import oracle
 import synth
-from _gpu_common import (GAP_MIN, TOL_BF16, TOL_F32, lib, need_gpu, np64, rel_max_err,
-                         to_f64_cpu, workspace)
+from _gpu_common import (GAP_MIN, TOL_BF16, TOL_F32, by_expert, lib, need_gpu, np64,
+                         rel_max_err, to_f64_cpu, workspace)
 
 pytestmark = pytest.mark.gpu
 
@@ -48,11 +48,12 @@ def _oracle(shape, g, rows):
 def _compare(shape, g, y, idx, w, counts, rows, tol):
     ref = _oracle(shape, g, rows)
     clear = ref["gap"] > GAP_MIN
-    got_idx = idx.cpu().numpy()[rows]
-    np.testing.assert_array_equal(got_idx[clear], ref["idx"][clear])
-    assert rel_max_err(w.cpu().numpy()[rows][clear], ref["w"][clear]) <= 1e-4
-    # rows whose routing matches are compared on the layer output
-    same = (got_idx == ref["idx"]).all(axis=1)
+    got_set, got_w = by_expert(idx.cpu().numpy()[rows], w.cpu().numpy()[rows])
+    ref_set, ref_w = by_expert(ref["idx"], ref["w"])
+    np.testing.assert_array_equal(got_set[clear], ref_set[clear])
+    assert rel_max_err(got_w[clear], ref_w[clear]) <= 1e-4
+    # rows whose selected set matches are compared on the layer output
+    same = (got_set == ref_set).all(axis=1)
     assert same.mean() > 0.9
     assert rel_max_err(np64(y[rows])[same], ref["y"][same]) <= tol
     assert int(counts.sum()) == g["x"].shape[0] * shape.K
@@ -92,7 +93,7 @@ def test_layer_full_size_sampled(name):
         r = oracle.router_from_x(np64(g["x"]), np64(g["W_r"]), g["bias"].cpu().numpy(), shape.K,
                                  shape.n_group, shape.topk_group)
         clear = r["gap"] > GAP_MIN
-        np.testing.assert_array_equal(idx.cpu().numpy()[clear], r["idx"][clear])
+        np.testing.assert_array_equal(by_expert(idx.cpu().numpy())[clear], by_expert(r["idx"])[clear])
         assert np.isfinite(np64(y)).all()
     finally:
         del g
