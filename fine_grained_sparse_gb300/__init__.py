@@ -191,7 +191,15 @@ def moe_layer_forward(cfg, T, x, W_r, bias, W_gate_up, W_down, Ws_gate_up, Ws_do
                       stream=None):
     ev_array = None
     if stage_events is not None:
-        handles = [e.cuda_event if hasattr(e, "cuda_event") else int(e) for e in stage_events]
+        handles = []
+        for e in stage_events:
+            if hasattr(e, "cuda_event"):
+                if not e.cuda_event:  # torch creates its events lazily, on first record
+                    import torch
+                    e.record(torch.cuda.current_stream() if stream is None else stream)
+                handles.append(e.cuda_event)
+            else:
+                handles.append(int(e))
         if len(handles) != MOE_STAGE_COUNT + 1:
             raise ValueError("stage_events needs MOE_STAGE_COUNT + 1 events")
         ev_array = (ctypes.c_void_p * len(handles))(*handles)
