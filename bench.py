@@ -61,7 +61,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="k2_prefill", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="own", choices=["own", "reference"])
-    ap.add_argument("--cpu-sample-tokens", type=int, default=8)
+    ap.add_argument("--cpu-sample-tokens", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
