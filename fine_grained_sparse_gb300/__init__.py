@@ -70,7 +70,7 @@ _SIGS = {
     "moe_validate_config": ([_CFG, _I64], _I32),
     "moe_workspace_size": ([_CFG, _I64], _SZ),
     "moe_get_device_status": ([_P, _P], _I32),
-    "moe_router": ([_CFG, _I64, _P, _P, _P, _P, _P, _P], _I32),
+    "moe_router": ([_CFG, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P], _I32),
     "moe_router_from_logits": ([_CFG, _I64, _P, _P, _P, _P, _P], _I32),
     "moe_permute": ([_CFG, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P], _I32),
     "moe_grouped_swiglu": ([_CFG, _I64] + [_P] * 12 + [_SZ, _P], _I32),
@@ -149,9 +149,9 @@ def moe_get_device_status(workspace, stream=None) -> int:
     return lib.moe_get_device_status(_ptr(workspace), _stream(stream))
 
 
-def moe_router(cfg, T, x, W_r, bias, topk_idx, topk_w, stream=None):
+def moe_router(cfg, T, x, W_r, bias, topk_idx, topk_w, workspace=None, ws_bytes=0, stream=None):
     _check(lib.moe_router(ctypes.byref(cfg), T, _ptr(x), _ptr(W_r), _ptr(bias), _ptr(topk_idx),
-                          _ptr(topk_w), _stream(stream)), "moe_router")
+                          _ptr(topk_w), _ptr(workspace), ws_bytes, _stream(stream)), "moe_router")
 
 
 def moe_router_from_logits(cfg, T, logits, bias, topk_idx, topk_w, stream=None):

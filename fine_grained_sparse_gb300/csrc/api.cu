@@ -44,13 +44,9 @@ int elem_bytes(const moe_config* c) { return c->dtype == MOE_BF16 ? 2 : 4; }
 
 int d_expert(const moe_config* c) { return c->d_latent ? c->d_latent : c->d_model; }
 
-// token tile of the tensor-core GEMMs: no expert holds more than T rows
-int token_tile(int64_t T) {
-  if (T <= 32) return 32;
-  if (T <= 64) return 64;
-  if (T <= 128) return 128;
-  return 256;
-}
+// token tile of the tensor-core GEMMs: small batches (few rows per expert)
+// take 32-row tiles and a deeper pipeline; large ones 128-row tiles
+int token_tile(int64_t T) { return T <= 256 ? 32 : 128; }
 
 int32_t check_router_cfg(const moe_config* c, int64_t T) {
   if (!c) return fail(MOE_ERR_INVALID_ARG, "cfg is null");
@@ -95,8 +91,8 @@ int32_t check_layer_cfg(const moe_config* c, int64_t T) {
 
 // Workspace regions, each 256-byte aligned, in this order.
 struct Layout {
-  size_t status, topk_idx, topk_w, counts, offsets, perm, inv, tiles, ntiles, w_perm, Xp, H, Hs,
-      Y, U, Ysh, x_lat, r_lat, x_stage, y_stage, total;
+  size_t status, topk_idx, topk_w, counts, offsets, perm, inv, tiles, ntiles, w_perm, w_split,
+      logits, Xp, H, Hs, Y, U, Ysh, x_lat, r_lat, x_stage, y_stage, total;
 };
 
 Layout layout(const moe_config* c, int64_t T) {
@@ -119,9 +115,11 @@ Layout layout(const moe_config* c, int64_t T) {
   L.offsets = take(4 * static_cast<size_t>(c->E_routed + 1));
   L.perm = take(4 * TK);
   L.inv = take(4 * TK);
-  L.tiles = take(16 * tiles);
+  L.tiles = take(sizeof(RowTile) * tiles);
   L.ntiles = take(16);
   L.w_perm = take(4 * TK);
+  L.w_split = take(c->dtype == MOE_BF16 ? 3ull * c->E_routed * c->d_model * 2 : 0);
+  L.logits = take(c->dtype == MOE_BF16 ? 4ull * T * c->E_routed : 0);
   L.Xp = take(static_cast<size_t>(TK) * de * eb);
   L.H = take(static_cast<size_t>(TK) * c->d_ff * eb);
   L.Hs = take(static_cast<size_t>(S) * T * c->d_ff_shared * eb);
@@ -212,7 +210,7 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
   const int Fs = c->d_ff_shared, d = c->d_model;
   const int64_t TK = T * K;
   int* status = at<int>(ws, L.status);
-  int4* tiles = at<int4>(ws, L.tiles);
+  RowTile* tiles = at<RowTile>(ws, L.tiles);
   int* ntiles = at<int>(ws, L.ntiles);
   float* w_perm = at<float>(ws, L.w_perm);
   void* Xp = at<void>(ws, L.Xp);
@@ -239,7 +237,7 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
     int32_t e;
     if ((e = set_gate_up_A(r, io.W_gate_up, E, F, de)) != MOE_OK) return e;
     if ((e = set_B(r, Xp, TK, de)) != MOE_OK) return e;
-    r.o_blocks = F / 64;
+    r.a128 = F / 64;
     r.tiles = tiles;
     r.ntiles = ntiles;
     r.out = static_cast<__nv_bfloat16*>(H);
@@ -249,7 +247,7 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
       clear(s);
       if ((e = set_gate_up_A(s, io.Ws_gate_up, S, Fs, d)) != MOE_OK) return e;
       if ((e = set_B(s, io.x_shared, T, d)) != MOE_OK) return e;
-      s.o_blocks = Fs / 64;
+      s.a128 = Fs / 64;
       s.groups = S;
       s.rows = static_cast<int>(T);
       s.b_group_stride = 0;
@@ -266,7 +264,8 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
     clear(r2);
     if ((e = set_store_A(r2, io.W_down, E, de, F)) != MOE_OK) return e;
     if ((e = set_B(r2, H, TK, F)) != MOE_OK) return e;
-    r2.o_blocks = de / 128;
+    r2.a128 = de / 128;
+    r2.o_limit = de;
     r2.tiles = tiles;
     r2.ntiles = ntiles;
     r2.out = static_cast<__nv_bfloat16*>(io.Y);
@@ -277,7 +276,8 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
       clear(s2);
       if ((e = set_store_A(s2, io.Ws_down, S, d, Fs)) != MOE_OK) return e;
       if ((e = set_B(s2, Hs, S * T, Fs)) != MOE_OK) return e;
-      s2.o_blocks = d / 128;
+      s2.a128 = d / 128;
+      s2.o_limit = d;
       s2.groups = S;
       s2.rows = static_cast<int>(T);
       s2.b_group_stride = T;
@@ -361,7 +361,8 @@ int32_t run_linear(int64_t T, int in_f, int out_f, const void* x, const void* W,
   int32_t e;
   if ((e = set_store_A(s, W, 1, out_f, in_f)) != MOE_OK) return e;
   if ((e = set_B(s, x, T, in_f)) != MOE_OK) return e;
-  s.o_blocks = out_f / 128;
+  s.a128 = out_f / 128;
+  s.o_limit = out_f;
   s.groups = 1;
   s.rows = static_cast<int>(T);
   s.out = static_cast<__nv_bfloat16*>(y);
@@ -415,15 +416,16 @@ int32_t moe_get_device_status(void* workspace, void* stream) {
 }
 
 int32_t moe_router(const moe_config* cfg, int64_t T, const void* x, const float* W_r,
-                   const float* bias, int32_t* topk_idx, float* topk_w, void* stream) {
+                   const float* bias, int32_t* topk_idx, float* topk_w, void* workspace,
+                   size_t ws_bytes, void* stream) {
   int32_t st = check_router_cfg(cfg, T);
   if (st != MOE_OK) return st;
   if (!x || !W_r || !bias || !topk_idx || !topk_w) return fail(MOE_ERR_INVALID_ARG, "null pointer");
   if (!aligned16(x) || !aligned16(W_r) || !aligned16(bias) || !aligned16(topk_idx) ||
-      !aligned16(topk_w))
+      !aligned16(topk_w) || (workspace && !aligned16(workspace)))
     return fail(MOE_ERR_ALIGNMENT, "pointer not 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   RouterArgs a;
-  a.x = x;
   a.W_r = W_r;
   a.bias = bias;
   a.T = T;
@@ -437,7 +439,40 @@ int32_t moe_router(const moe_config* cfg, int64_t T, const void* x, const float*
   a.x_bf16 = cfg->dtype == MOE_BF16;
   a.topk_idx = topk_idx;
   a.topk_w = topk_w;
-  MOE_CUDA(launch_router(a, static_cast<cudaStream_t>(stream)));
+  if (workspace && cfg->dtype == MOE_BF16 && cfg->d_model % 64 == 0) {
+    const Layout L = layout(cfg, T);
+    if (ws_bytes < L.total) return fail(MOE_ERR_WORKSPACE, "workspace too small");
+    // logits = x (W_hi + W_mid + W_lo)^T on the tensor cores
+    __nv_bfloat16* w_split = at<__nv_bfloat16>(workspace, L.w_split);
+    float* logits = at<float>(workspace, L.logits);
+    const int d = cfg->d_model, E = cfg->E_routed;
+    MOE_CUDA(launch_split_router_weight(W_r, E, d, w_split, s));
+    GemmParams p;
+    memset(&p, 0, sizeof(p));
+    p.mode = kModeStore;
+    p.nt = token_tile(T);
+    p.status = at<int>(workspace, L.status);
+    p.nseg = 1;
+    GemmSegment& g = p.seg[0];
+    clear(g);
+    if (encode_tmap_weights_3d(&g.tmA, w_split, 1, E, 3ll * d, 128) != CUDA_SUCCESS)
+      return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for the split router weight");
+    int32_t e;
+    if ((e = set_B(g, x, T, d)) != MOE_OK) return e;
+    g.k_steps = 3 * d / 64;
+    g.b_k_period = d / 64;
+    g.a128 = (E + 127) / 128;
+    g.o_limit = E;
+    g.groups = 1;
+    g.rows = static_cast<int>(T);
+    g.out_f32 = logits;
+    g.out_ld = E;
+    MOE_CUDA(launch_tc_gemm(p, num_sms(), s));
+    a.logits = logits;
+  } else {
+    a.x = x;
+  }
+  MOE_CUDA(launch_router(a, s));
   return MOE_OK;
 }
 
@@ -565,7 +600,7 @@ int32_t moe_layer_forward(const moe_config* cfg, int64_t T, const void* x, const
   const bool bf16 = cfg->dtype == MOE_BF16;
 
   if (ev(0)) MOE_CUDA(cudaEventRecord(ev(0), s));
-  st = moe_router(cfg, T, x, W_r, bias, idx, w, s);
+  st = moe_router(cfg, T, x, W_r, bias, idx, w, ws, ws_bytes, s);
   if (st != MOE_OK) return st;
   if (ev(1)) MOE_CUDA(cudaEventRecord(ev(1), s));
   MOE_CUDA(launch_permute(idx, T, cfg->K, cfg->E_routed, counts, offsets, perm, inv, status, s));

@@ -97,7 +97,8 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
 }
 
 __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __restrict__ offsets,
-                                                           int E, int nt, int4* __restrict__ tiles,
+                                                           int E, int nt,
+                                                           RowTile* __restrict__ tiles,
                                                            int* __restrict__ ntiles) {
   __shared__ int scan[1024];
   const int e = threadIdx.x;
@@ -119,7 +120,14 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __rest
   const int row0 = offsets[e];
   for (int i = 0; i < nti; ++i) {
     const int start = i * per;
-    tiles[first + i] = make_int4(e, row0 + start, min(per, m - start), 0);
+    RowTile t;
+    t.expert = e;
+    t.row_start = row0 + start;
+    t.n_rows = min(per, m - start);
+    t.first_tile = first;
+    t.ntiles = nti;
+    t.pad0 = t.pad1 = t.pad2 = 0;
+    tiles[first + i] = t;
   }
 }
 
@@ -235,7 +243,7 @@ cudaError_t launch_permute(const int32_t* topk_idx, int64_t T, int K, int E, int
 
 int64_t max_tiles(int64_t rows, int E, int nt) { return rows / nt + E; }
 
-cudaError_t launch_build_tiles(const int32_t* offsets, int E, int nt, int4* tiles, int* ntiles,
+cudaError_t launch_build_tiles(const int32_t* offsets, int E, int nt, RowTile* tiles, int* ntiles,
                                cudaStream_t stream) {
   build_tiles_kernel<<<1, 1024, 0, stream>>>(offsets, E, nt, tiles, ntiles);
   return cudaGetLastError();

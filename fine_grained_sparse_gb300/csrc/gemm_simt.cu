@@ -22,11 +22,11 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtGemm g) {
   int group, b_row, out_row, n_rows;
   if (g.tiles) {
     if (tile >= *g.ntiles) return;
-    const int4 t = g.tiles[tile];
-    group = t.x;
-    b_row = t.y;
-    out_row = t.y;
-    n_rows = t.z;
+    const RowTile t = g.tiles[tile];
+    group = t.expert;
+    b_row = t.row_start;
+    out_row = t.row_start;
+    n_rows = t.n_rows;
   } else {
     const int tpg = (g.rows + TS - 1) / TS;
     if (tile >= g.groups * tpg) return;

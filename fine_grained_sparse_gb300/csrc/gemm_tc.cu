@@ -7,26 +7,35 @@
 //   down pass:     Y[r, o] = w_r * sum_f H[r,f] W_down[e,o,f]
 // for every row r of every routed expert e (rows come in tiles from the
 // dispatch) and, as a second segment of the same launch, for every token of
-// every shared expert.  The K3 latent projections use the down-pass form with
-// one group and no scale.
+// every shared expert.  The K3 latent projections and the router logits use
+// the down-pass form (store mode) with one group.
 //
-// Swap-AB tiling.  The MMA's M side (128 rows) is a block of WEIGHT rows and
-// its N side (16..256, a multiple of 16) is the block of token rows of one
-// expert, so an expert with few tokens still streams its weights through
-// full-height MMAs and each weight byte is read from HBM once per token tile.
-//   A tile: 128 weight rows x 64 k, bf16, K-major, 128-byte swizzle (16 KB)
-//   B tile: up to nt token rows x 64 k, same layout, loaded as 32-row boxes
-//   D:      128 lanes x N fp32 columns of TMEM, two accumulators so the
-//           epilogue of one tile overlaps the main loop of the next.
-// For the gate/up pass the A tile interleaves the two halves of W_gate_up
+// Swap-AB tiling.  The MMA's M side is a block of WEIGHT rows and its N side
+// (16..128, a multiple of 16) a block of token rows of one expert, so an
+// expert with few tokens still streams its weights through full-height MMAs.
+// A unit is 256 weight rows -- two 128-row A tiles, two TMEM accumulators --
+// against one token tile: each B (token) tile in shared memory feeds twice
+// the MMA work, and two thirds of every pipeline stage are weights, which
+// keeps ~128 KB of weight bytes in flight per SM for the HBM stream.
+//   A tiles: 2 x (128 rows x 64 k) bf16, K-major, 128-byte swizzle (32 KB)
+//   B tile:  up to nt rows x 64 k, same layout, loaded as 32-row boxes
+//   D:       2 accumulators x N fp32 columns, double-buffered (4 nt <= 512
+//            TMEM columns) so the epilogue of one unit overlaps the main loop
+//            of the next.
+// For the gate/up pass each A tile interleaves the two halves of W_gate_up
 // [E, 2F, d] in 16-row slices: rows 32q..32q+15 are gate features
-// 64 ob + 16q + (0..15) and rows 32q+16..32q+31 the up features with the same
-// indices.  TMEM lane quadrant q (the one warp q%4 may read) therefore holds
-// both halves of 16 features, and the SwiGLU is one shuffle away.
+// 16q + (0..15) of the tile's 64 and rows 32q+16..32q+31 the up features with
+// the same indices.  TMEM lane quadrant q (the one warp q%4 may read) thus
+// holds both halves of 16 features, and the SwiGLU is one shuffle away.
 //
-// Warp roles (one CTA per SM, persistent over the tile list):
+// Units are ordered (segment, expert, output block, token tile) with the
+// token tile fastest, so the CTAs that share an expert's weight block run
+// side by side and the second reader finds the block in L2.
+//
+// Warp roles (one CTA per SM, persistent over the units):
 //   warp 0 lane 0: TMA producer; warp 1 lane 0: MMA issuer;
-//   warps 2..5: epilogue (TMEM -> registers -> bf16 global stores).
+//   warps 2..9: epilogue, warp w reads lane quadrant w%4 of accumulator
+//   (w-2)/4 (TMEM -> registers -> global stores).
 // Every wait is bounded (%globaltimer); on expiry the CTA records
 // MOE_ERR_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
 #include <cudaTypedefs.h>
@@ -40,21 +49,24 @@ namespace fgs {
 
 namespace {
 
-constexpr int kBK = 64;                    // k per stage: one 128-byte swizzle row
-constexpr uint32_t kABytes = 128 * 128;    // A stage: 128 rows x 128 B
+constexpr int kBK = 64;                      // k per stage: one 128-byte swizzle row
+constexpr uint32_t kATileBytes = 128 * 128;  // one A tile: 128 rows x 128 B
+constexpr uint32_t kABytes = 2 * kATileBytes;
 constexpr int kBBoxRows = 32;
 constexpr uint32_t kBBoxBytes = kBBoxRows * 128;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int kMaxStages = 8;
-constexpr size_t kSmemBudget = 196608;     // pipeline bytes per CTA
+constexpr size_t kSmemBudget = 221184;  // pipeline bytes per CTA (216 KB)
 
 struct Unit {
-  int seg, group, b_row, out_row, n_rows, ob;
+  int seg, group, b_row, out_row, n_rows, ob, n_a, ntiles;
 };
 
-__device__ __forceinline__ int segment_tiles(const GemmSegment* s, int nt) {
-  if (s->tiles) return *s->ntiles;
-  return s->groups * ((s->rows + nt - 1) / nt);
+__device__ __forceinline__ int segment_units(const GemmSegment* s, int nt) {
+  const int ob = (s->a128 + 1) / 2;
+  if (s->tiles) return *s->ntiles * ob;
+  return s->groups * ((s->rows + nt - 1) / nt) * ob;
 }
 
 __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int units0, int nt) {
@@ -62,28 +74,36 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int unit
   x.seg = u >= units0 ? 1 : 0;
   const int local = u - (x.seg ? units0 : 0);
   const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
-  const int tile = local / s->o_blocks;
-  x.ob = local - tile * s->o_blocks;
+  const int OB = (s->a128 + 1) / 2;
   if (s->tiles) {
-    const int4 t = s->tiles[tile];
-    x.group = t.x;
-    x.b_row = t.y;
-    x.out_row = t.y;
-    x.n_rows = t.z;
+    // the units of one expert are [first_tile * OB, (first_tile + ntiles) * OB)
+    const RowTile& any = s->tiles[local / OB];
+    const int r = local - any.first_tile * OB;
+    x.ob = r / any.ntiles;
+    const RowTile& t = s->tiles[any.first_tile + (r - x.ob * any.ntiles)];
+    x.group = t.expert;
+    x.b_row = t.row_start;
+    x.out_row = t.row_start;
+    x.n_rows = t.n_rows;
+    x.ntiles = any.ntiles;
   } else {
     const int tpg = (s->rows + nt - 1) / nt;
-    const int g = tile / tpg;
-    const int t0 = (tile - g * tpg) * nt;
+    const int g = local / (tpg * OB);
+    const int r = local - g * tpg * OB;
+    x.ob = r / tpg;
+    const int t0 = (r - x.ob * tpg) * nt;
     x.group = g;
     x.n_rows = min(nt, s->rows - t0);
     x.b_row = static_cast<int>(g * s->b_group_stride + t0);
     x.out_row = static_cast<int>(g * s->out_group_stride + t0);
+    x.ntiles = tpg;
   }
+  x.n_a = min(2, s->a128 - 2 * x.ob);
   return x;
 }
 
-// Wait on a barrier for the whole warp: lane 0 polls (bounded), the verdict
-// is broadcast so the warp stays converged for the .sync.aligned tcgen05 ops.
+// Wait on a barrier for a whole warp: lane 0 polls (bounded) and the verdict
+// is broadcast, so the warp stays converged for the .sync.aligned tcgen05 ops.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           int* status) {
   bool ok = false;
@@ -106,24 +126,24 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   const int stages = p.stages;
   const int nt = p.nt;
   const uint32_t b_stage_bytes = static_cast<uint32_t>(nt) * 128u;
-  uint8_t* smem_a = smem;
-  uint8_t* smem_b = smem_a + stages * kABytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_b + stages * b_stage_bytes);
+  const uint32_t stage_bytes = kABytes + b_stage_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + stages * stage_bytes);
   // bars: full[stages] | empty[stages] | tmem_full[2] | tmem_empty[2] | drain
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * stages + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t a_base = smem_u32(smem_a);
-  const uint32_t b_base = smem_u32(smem_b);
+  const uint32_t s_base = smem_u32(smem);
   const uint32_t bar_base = smem_u32(bars);
+  auto stage_a = [&](int s) { return s_base + s * stage_bytes; };
+  auto stage_b = [&](int s) { return s_base + s * stage_bytes + kABytes; };
   auto full_bar = [&](int s) { return bar_base + 8u * s; };
   auto empty_bar = [&](int s) { return bar_base + 8u * (stages + s); };
-  auto tfull_bar = [&](int a) { return bar_base + 8u * (2 * stages + a); };
-  auto tempty_bar = [&](int a) { return bar_base + 8u * (2 * stages + 2 + a); };
+  auto tfull_bar = [&](int b) { return bar_base + 8u * (2 * stages + b); };
+  auto tempty_bar = [&](int b) { return bar_base + 8u * (2 * stages + 2 + b); };
   const uint32_t drain_bar = bar_base + 8u * (2 * stages + 4);
-  const uint32_t tmem_cols = 2u * static_cast<uint32_t>(nt);
+  const uint32_t tmem_cols = 4u * static_cast<uint32_t>(nt);  // 2 buffers x 2 accumulators
 
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), tmem_cols);
@@ -134,9 +154,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), kEpiWarps);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -147,8 +167,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int units0 = segment_tiles(&p.seg[0], nt) * p.seg[0].o_blocks;
-  const int units1 = p.nseg > 1 ? segment_tiles(&p.seg[1], nt) * p.seg[1].o_blocks : 0;
+  const int units0 = segment_units(&p.seg[0], nt);
+  const int units1 = p.nseg > 1 ? segment_units(&p.seg[1], nt) : 0;
   const int total = units0 + units1;
 
   if (warp == 0 && lane == 0) {
@@ -157,8 +177,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       prefetch_tensormap(&p.seg[s].tmA);
       prefetch_tensormap(&p.seg[s].tmB);
     }
-    const uint64_t pol_w = l2_policy_evict_first();
-    const uint64_t pol_x = l2_policy_evict_last();
+    const uint64_t pol_stream = l2_policy_evict_first();
+    const uint64_t pol_keep = l2_policy_evict_last();
+    const uint64_t pol_normal = l2_policy_evict_normal();
     int stage = 0;
     uint32_t phase = 0;
     int64_t issued = 0;
@@ -166,7 +187,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       const Unit x = decode_unit(p, u, units0, nt);
       const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
       const int nbox = (x.n_rows + kBBoxRows - 1) / kBBoxRows;
-      const uint32_t tx = kABytes + static_cast<uint32_t>(nbox) * kBBoxBytes;
+      const uint32_t tx = kATileBytes * x.n_a + static_cast<uint32_t>(nbox) * kBBoxBytes;
+      // a weight block read by one token tile is streamed; one shared by
+      // several token tiles (running side by side) is kept for the others
+      const uint64_t pol_w = x.ntiles > 1 ? pol_normal : pol_stream;
       bool ok = true;
       for (int ks = 0; ks < s->k_steps; ++ks) {
         if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) {
@@ -175,22 +199,28 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         }
         const uint32_t fb = full_bar(stage);
         mbar_arrive_expect_tx(fb, tx);
-        const uint32_t a_dst = a_base + stage * kABytes;
-        const uint32_t b_dst = b_base + stage * b_stage_bytes;
+        const uint32_t a_dst = stage_a(stage);
+        const uint32_t b_dst = stage_b(stage);
         const int kc = ks * kBK;
-        if (p.mode == kModeSwiGLU) {
-          if (s->a_boxes == 1) {
-            tma_load_5d(a_dst, &s->tmA, fb, kc, 0, 0, x.ob * 4, x.group, pol_w);
+        for (int a = 0; a < x.n_a; ++a) {
+          const int blk = 2 * x.ob + a;  // 128-row A tile index along O
+          const uint32_t dst = a_dst + a * kATileBytes;
+          if (p.mode == kModeSwiGLU) {
+            if (s->a_boxes == 1) {
+              tma_load_5d(dst, &s->tmA, fb, kc, 0, 0, blk * 4, x.group, pol_w);
+            } else {
+              for (int j = 0; j < 8; ++j)
+                tma_load_3d(dst + j * 2048u, &s->tmA, fb, kc,
+                            (j & 1) * s->a_rows + blk * 64 + (j >> 1) * 16, x.group, pol_w);
+            }
           } else {
-            for (int j = 0; j < 8; ++j)
-              tma_load_3d(a_dst + j * 2048u, &s->tmA, fb, kc,
-                          (j & 1) * s->a_rows + x.ob * 64 + (j >> 1) * 16, x.group, pol_w);
+            tma_load_3d(dst, &s->tmA, fb, kc, blk * 128, x.group, pol_w);
           }
-        } else {
-          tma_load_3d(a_dst, &s->tmA, fb, kc, x.ob * 128, x.group, pol_w);
         }
+        const int kb = s->b_k_period ? (ks % s->b_k_period) * kBK : kc;
         for (int bx = 0; bx < nbox; ++bx)
-          tma_load_2d(b_dst + bx * kBBoxBytes, &s->tmB, fb, kc, x.b_row + bx * kBBoxRows, pol_x);
+          tma_load_2d(b_dst + bx * kBBoxBytes, &s->tmB, fb, kb, x.b_row + bx * kBBoxRows,
+                      pol_keep);
         ++issued;
         if (++stage == stages) {
           stage = 0;
@@ -212,11 +242,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     for (int u = blockIdx.x; u < total; u += gridDim.x, ++i) {
       const Unit x = decode_unit(p, u, units0, nt);
       const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
-      const int acc = i & 1;
-      const uint32_t acc_phase = static_cast<uint32_t>(i >> 1) & 1u;
-      if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) break;
+      const int buf = i & 1;
+      const uint32_t buf_phase = static_cast<uint32_t>(i >> 1) & 1u;
+      if (!mbar_wait_bounded(tempty_bar(buf), buf_phase ^ 1u, abort_flag, p.status)) break;
       tc_fence_after();
-      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * nt);
+      const uint32_t d0 = tmem_base + static_cast<uint32_t>(2 * buf * nt);
       const uint32_t n = static_cast<uint32_t>((x.n_rows + 15) & ~15);
       const uint32_t idesc = idesc_bf16_f32(128, n);
       bool ok = true;
@@ -226,11 +256,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           break;
         }
         tc_fence_after();
-        const uint64_t adesc = smem_desc_sw128(a_base + stage * kABytes);
-        const uint64_t bdesc = smem_desc_sw128(b_base + stage * b_stage_bytes);
+        const uint64_t bdesc = smem_desc_sw128(stage_b(stage));
+        for (int a = 0; a < x.n_a; ++a) {
+          const uint64_t adesc = smem_desc_sw128(stage_a(stage) + a * kATileBytes);
+          const uint32_t d = d0 + static_cast<uint32_t>(a * nt);
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk)
-          tc_mma_bf16(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc, (ks | kk) != 0);
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            tc_mma_bf16(d, adesc + 2u * kk, bdesc + 2u * kk, idesc, (ks | kk) != 0);
+        }
         tc_commit(empty_bar(stage));
         if (++stage == stages) {
           stage = 0;
@@ -238,68 +271,76 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         }
       }
       if (!ok) break;
-      tc_commit(tfull_bar(acc));
+      tc_commit(tfull_bar(buf));
     }
     tc_commit(drain_bar);
     drain_wait(drain_bar, 0, p.status);
   } else if (warp >= 2) {
     // ---------------------------------------------------------- epilogue
-    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int q = warp & 3;           // TMEM lane quadrant this warp may access
+    const int acc = (warp - 2) >> 2;  // which of the unit's two accumulators
     int i = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x, ++i) {
       const Unit x = decode_unit(p, u, units0, nt);
       const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
-      const int acc = i & 1;
-      const uint32_t acc_phase = static_cast<uint32_t>(i >> 1) & 1u;
-      if (!warp_wait(tfull_bar(acc), acc_phase, abort_flag, p.status)) break;
+      const int buf = i & 1;
+      const uint32_t buf_phase = static_cast<uint32_t>(i >> 1) & 1u;
+      if (!warp_wait(tfull_bar(buf), buf_phase, abort_flag, p.status)) break;
       tc_fence_after();
-      const uint32_t taddr0 =
-          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * nt);
-      const int nchunks = (x.n_rows + 15) / 16;
-      __nv_bfloat16* out = s->out;
-      const int64_t ld = s->out_ld;
-      for (int c = 0; c < nchunks; ++c) {
-        uint32_t v[16];
-        tmem_ld_x16(taddr0 + static_cast<uint32_t>(c * 16), v);
-        tmem_ld_wait();
-        const int tok0 = c * 16;
-        if (p.mode == kModeSwiGLU) {
-          const bool is_gate = lane < 16;
-          const int f = x.ob * 64 + q * 16 + (lane & 15);
-          float h[16];
+      if (acc < x.n_a) {
+        const uint32_t taddr0 = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                static_cast<uint32_t>((2 * buf + acc) * nt);
+        const int blk = 2 * x.ob + acc;
+        const int nchunks = (x.n_rows + 15) / 16;
+        const int64_t ld = s->out_ld;
+        for (int c = 0; c < nchunks; ++c) {
+          uint32_t v[16];
+          tmem_ld_x16(taddr0 + static_cast<uint32_t>(c * 16), v);
+          tmem_ld_wait();
+          const int tok0 = c * 16;
+          if (p.mode == kModeSwiGLU) {
+            const bool is_gate = lane < 16;
+            const int f = blk * 64 + q * 16 + (lane & 15);
+            float h[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float mine = __uint_as_float(v[j]);
-            const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
-            const float g = is_gate ? mine : other;
-            const float up = is_gate ? other : mine;
-            h[j] = silu_f(g) * up;
-          }
+            for (int j = 0; j < 16; ++j) {
+              const float mine = __uint_as_float(v[j]);
+              const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
+              const float g = is_gate ? mine : other;
+              const float up = is_gate ? other : mine;
+              h[j] = silu_f(g) * up;
+            }
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            const int tok = tok0 + (is_gate ? jj : 8 + jj);
-            const float val = is_gate ? h[jj] : h[8 + jj];
-            if (tok < x.n_rows)
-              out[static_cast<int64_t>(x.out_row + tok) * ld + f] = __float2bfloat16_rn(val);
-          }
-        } else {
-          const int o = x.ob * 128 + q * 32 + lane;
+            for (int jj = 0; jj < 8; ++jj) {
+              const int tok = tok0 + (is_gate ? jj : 8 + jj);
+              const float val = is_gate ? h[jj] : h[8 + jj];
+              if (tok < x.n_rows)
+                s->out[static_cast<int64_t>(x.out_row + tok) * ld + f] = __float2bfloat16_rn(val);
+            }
+          } else {
+            const int o = blk * 128 + q * 32 + lane;
+            if (o < s->o_limit) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int tok = tok0 + j;
-            if (tok < x.n_rows) {
-              float val = __uint_as_float(v[j]);
-              if (s->row_scale) val *= __ldg(s->row_scale + x.out_row + tok);
-              if (s->add)
-                val += __bfloat162float(s->add[static_cast<int64_t>(x.out_row + tok) * s->add_ld + o]);
-              out[static_cast<int64_t>(x.out_row + tok) * ld + o] = __float2bfloat16_rn(val);
+              for (int j = 0; j < 16; ++j) {
+                const int tok = tok0 + j;
+                if (tok < x.n_rows) {
+                  const int64_t row = x.out_row + tok;
+                  float val = __uint_as_float(v[j]);
+                  if (s->row_scale) val *= __ldg(s->row_scale + row);
+                  if (s->add) val += __bfloat162float(s->add[row * s->add_ld + o]);
+                  if (s->out_f32)
+                    s->out_f32[row * ld + o] = val;
+                  else
+                    s->out[row * ld + o] = __float2bfloat16_rn(val);
+                }
+              }
             }
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if (lane == 0) mbar_arrive(tempty_bar(buf));
     }
   }
 
@@ -307,6 +348,28 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem_base, tmem_cols);
+  }
+}
+
+// W_split[e, 0:d] = hi, [d:2d] = mid, [2d:3d] = lo: successive bf16 roundings
+// of what is left of W_r[e, :], so hi + mid + lo keeps ~24 significant bits.
+__global__ void __launch_bounds__(256) split_router_weight_kernel(const float* __restrict__ W,
+                                                                  int E, int d,
+                                                                  __nv_bfloat16* __restrict__ out) {
+  const int64_t n = static_cast<int64_t>(E) * d;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t e = i / d, k = i - e * d;
+    const float w = __ldg(W + i);
+    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+    const float r1 = w - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
+    __nv_bfloat16* row = out + e * 3 * d;
+    row[k] = hi;
+    row[d + k] = mid;
+    row[2 * d + k] = lo;
   }
 }
 
@@ -383,17 +446,27 @@ cudaError_t launch_tc_gemm(const GemmParams& params, int num_sms, cudaStream_t s
   const GemmPlan plan = plan_gemm(params.nt);
   GemmParams p = params;
   p.stages = plan.stages;
-  static int configured_bytes[64] = {0};
+  static int configured[64] = {0};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  if (dev < 64 && configured_bytes[dev] < static_cast<int>(plan.smem_bytes)) {
+  if (dev >= 64 || !configured[dev]) {
     err = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(kSmemBudget + 4096));
     if (err != cudaSuccess) return err;
-    configured_bytes[dev] = static_cast<int>(kSmemBudget + 4096);
+    if (dev < 64) configured[dev] = 1;
   }
   tc_gemm_kernel<<<num_sms, kThreads, plan.smem_bytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_router_weight(const float* W_r, int E, int d, __nv_bfloat16* W_split,
+                                       cudaStream_t stream) {
+  const int64_t n = static_cast<int64_t>(E) * d;
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  split_router_weight_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(W_r, E, d,
+                                                                                W_split);
   return cudaGetLastError();
 }
 

@@ -25,14 +25,22 @@ struct RouterArgs {
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream);
 
 // --------------------------------------------------------------- dispatch
+// One row tile of a routed expert: rows [row_start, row_start + n_rows) of
+// the gathered activations, all belonging to `expert`, whose tiles are
+// [first_tile, first_tile + ntiles) of the table.
+struct __align__(16) RowTile {
+  int expert, row_start, n_rows, first_tile;
+  int ntiles, pad0, pad1, pad2;
+};
+
 cudaError_t launch_permute(const int32_t* topk_idx, int64_t T, int K, int E, int32_t* counts,
                            int32_t* offsets, int32_t* perm, int32_t* inv, int* status,
                            cudaStream_t stream);
 
 // Row tiles of the routed experts: for expert e with m_e rows starting at
-// offsets[e], ceil(m_e / nt) tiles of near-equal height.  Entry
-// {expert, first row, rows, 0}; *ntiles receives the count.
-cudaError_t launch_build_tiles(const int32_t* offsets, int E, int nt, int4* tiles, int* ntiles,
+// offsets[e], ceil(m_e / nt) tiles of near-equal height; *ntiles receives
+// the count.
+cudaError_t launch_build_tiles(const int32_t* offsets, int E, int nt, RowTile* tiles, int* ntiles,
                                cudaStream_t stream);
 int64_t max_tiles(int64_t rows, int E, int nt);
 
@@ -51,25 +59,30 @@ cudaError_t launch_combine(const void* Y, const int32_t* inv, int64_t T, int K, 
 // ------------------------------------------------- tensor-core grouped GEMM
 enum GemmMode : int { kModeSwiGLU = 0, kModeStore = 1 };
 
+// One launch runs up to two segments (routed experts, then shared experts or
+// a dense projection).  A unit is 256 weight rows (two 128-row A tiles; one
+// at the tail of O) times one row tile of at most nt activation rows.
 struct GemmSegment {
   CUtensorMap tmA;  // weights (see gemm_tc.cu for the layouts)
   CUtensorMap tmB;  // activation rows [rows, K] bf16, box 64 x 32
-  int k_steps;      // K / 64
-  int o_blocks;     // output blocks per row tile (F/64 SwiGLU, O/128 store)
-  int a_boxes;      // 1: one A box per stage; 8: eight 16-row boxes (SwiGLU only)
-  int a_rows;       // SwiGLU: F (row offset of the up half); store: unused
-  // explicit tiles (routed experts)
-  const int4* tiles;
+  int k_steps;      // A's K / 64
+  int b_k_period;   // B's k coordinate wraps every b_k_period steps (0: never)
+  int a128;         // 128-row A tiles along O (SwiGLU: F/64, store: O/128)
+  int a_boxes;      // SwiGLU A tile: 1 = one 5-D box, 8 = eight 16-row boxes
+  int a_rows;       // SwiGLU: F (row offset of the up half)
+  int o_limit;      // store mode: columns o >= o_limit are not written
+  // explicit tiles (routed experts) or implicit ones (groups x rows)
+  const RowTile* tiles;
   const int* ntiles;
-  // implicit tiles: groups x ceil(rows / nt) over rows [0, rows)
   int groups;
   int rows;
   int64_t b_group_stride;
   int64_t out_group_stride;
-  __nv_bfloat16* out;
+  __nv_bfloat16* out;  // bf16 output, or
+  float* out_f32;      // fp32 output (store mode)
   int64_t out_ld;
-  const float* row_scale;  // per output row, may be null
-  const __nv_bfloat16* add;  // store mode: added to the output (same shape), may be null
+  const float* row_scale;    // store mode: per output row, may be null
+  const __nv_bfloat16* add;  // store mode: added to the output, may be null
   int64_t add_ld;
 };
 
@@ -77,7 +90,7 @@ struct GemmParams {
   GemmSegment seg[2];
   int nseg;
   int mode;
-  int nt;      // token tile (MMA N upper bound): 32, 64, 128 or 256
+  int nt;      // token tile (MMA N upper bound): 32, 64 or 128
   int stages;  // pipeline depth
   int* status;
 };
@@ -89,6 +102,11 @@ struct GemmPlan {
 GemmPlan plan_gemm(int nt);
 
 cudaError_t launch_tc_gemm(const GemmParams& p, int num_sms, cudaStream_t stream);
+
+// W_split[e] = [hi | mid | lo] (bf16, 3 d wide) with hi + mid + lo = W_r[e]
+// to about 2^-24 relative: the router GEMM on bf16 tensor cores.
+cudaError_t launch_split_router_weight(const float* W_r, int E, int d, __nv_bfloat16* W_split,
+                                       cudaStream_t stream);
 
 // Encode tensor maps (driver entry point fetched through the runtime).
 CUresult encode_tmap_2d_rows(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
@@ -109,7 +127,7 @@ struct SimtGemm {
   int Kdim = 0;
   int O = 0;
   bool swiglu = false;
-  const int4* tiles = nullptr;   // explicit tiles, or null for implicit ones
+  const RowTile* tiles = nullptr;  // explicit tiles, or null for implicit ones
   const int* ntiles = nullptr;
   int groups = 0, rows = 0;      // implicit tiles over [0, rows) per group
   int64_t b_group_stride = 0, out_group_stride = 0;

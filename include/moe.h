@@ -117,9 +117,15 @@ int32_t moe_get_device_status(void* workspace, void* stream);
  *                          (no renormalisation when K == 1 or
  *                          norm_topk_prob == 0)
  * The selection is decided on fp32 values with s rounded once from the
- * exact sigmoid of the fp32 logit. */
+ * exact sigmoid of the fp32 logit.
+ *   workspace: NULL, or moe_workspace_size(cfg, T) bytes (ws_bytes).  With a
+ *   workspace and bf16 x (d_model % 64 == 0) the logits come from a
+ *   tensor-core GEMM against a three-way bf16 split of W_r (hi + mid + lo
+ *   carries W_r to ~2^-24 relative; bf16 x bf16 products are exact and the
+ *   sums fp32); otherwise from a fused fp32 CUDA-core kernel. */
 int32_t moe_router(const moe_config* cfg, int64_t T, const void* x, const float* W_r,
-                   const float* bias, int32_t* topk_idx, float* topk_w, void* stream);
+                   const float* bias, int32_t* topk_idx, float* topk_w, void* workspace,
+                   size_t ws_bytes, void* stream);
 
 /* Router steps 2-4 from given fp32 logits z [T, E] (the parity entry point:
  * identical logits give identical expert indices on every implementation

@@ -86,10 +86,11 @@ def test_argument_errors_return_before_any_cuda_call(fgs):
     cfg = _k2(fgs)
     lib = fgs.lib
     # null pointers
-    assert lib.moe_router(ctypes.byref(cfg), 16, None, None, None, None, None, None) == 1
+    assert lib.moe_router(ctypes.byref(cfg), 16, None, None, None, None, None, None, 0, None) == 1
     # misaligned pointers (never dereferenced: the check comes first)
     bad = 0x1001
-    assert lib.moe_router(ctypes.byref(cfg), 16, bad, 0x1000, 0x1000, 0x1000, 0x1000, None) == 3
+    assert lib.moe_router(ctypes.byref(cfg), 16, bad, 0x1000, 0x1000, 0x1000, 0x1000, None, 0,
+                          None) == 3
     assert lib.moe_router_from_logits(ctypes.byref(cfg), 16, 0x1000, bad, 0x1000, 0x1000, None) == 3
     # workspace too small
     ws = fgs.moe_workspace_size(cfg, 16)

@@ -6,7 +6,8 @@ import torch
 
 import oracle
 import synth
-from _gpu_common import (GAP_MIN, TOL_WEIGHTS, by_expert, lib, need_gpu, np64, rel_max_err)
+from _gpu_common import (GAP_MIN, TOL_WEIGHTS, by_expert, lib, need_gpu, np64, rel_max_err,
+                         workspace)
 
 pytestmark = pytest.mark.gpu
 
@@ -48,13 +49,18 @@ def test_router_from_logits_bit_exact(shape, kind, T):
     assert rel_max_err(w.cpu().numpy(), ref["w"]) <= TOL_WEIGHTS
 
 
-def _check_router_from_x(cfg_shape, x, W_r, bias):
+def _check_router_from_x(cfg_shape, x, W_r, bias, tensor_cores=True):
     fgs = lib()
     T = x.shape[0]
     cfg = fgs.config(cfg_shape, d_ff=0)
     idx = torch.empty((T, cfg.K), dtype=torch.int32, device="cuda")
     w = torch.empty((T, cfg.K), dtype=torch.float32, device="cuda")
-    fgs.moe_router(cfg, T, x, W_r, bias, idx, w)
+    if tensor_cores:  # a workspace selects the split-bf16 tensor-core GEMM for bf16 x
+        ws, nws = workspace(cfg, T)
+        fgs.moe_router(cfg, T, x, W_r, bias, idx, w, ws, nws)
+        assert fgs.moe_get_device_status(ws) == 0
+    else:             # no workspace: the fused fp32 CUDA-core kernel
+        fgs.moe_router(cfg, T, x, W_r, bias, idx, w)
     torch.cuda.synchronize()
     ref = oracle.router_from_x(np64(x), np64(W_r), bias.cpu().numpy(), cfg.K, cfg.n_group,
                                cfg.topk_group)
@@ -71,19 +77,22 @@ def _check_router_from_x(cfg_shape, x, W_r, bias):
     assert (np.diff(srt, axis=1) > 0).all()
 
 
+@pytest.mark.parametrize("tensor_cores", [True, False], ids=["split_bf16_tc", "fp32_ffma"])
 @pytest.mark.parametrize("name,T", [("tiny", None), ("k2_router", None), ("k2_prefill", 700),
                                     ("k3_latent", 300)])
-def test_router_fused_matches_oracle(name, T):
+def test_router_matches_oracle(name, T, tensor_cores):
     need_gpu()
     shape = synth.shape(name)
     g = synth.generate(shape, device="cuda", T=T, weights=False)
-    _check_router_from_x(shape, g["x"], g["W_r"], g["bias"])
+    _check_router_from_x(shape, g["x"], g["W_r"], g["bias"], tensor_cores)
 
 
-def test_router_fused_ragged_tokens_and_small_E():
+@pytest.mark.parametrize("tensor_cores", [True, False], ids=["split_bf16_tc", "fp32_ffma"])
+def test_router_ragged_tokens_and_small_E(tensor_cores):
     need_gpu()
-    for T, E, K, G, Gk in [(1, 16, 4, 1, 1), (65, 40, 5, 4, 2), (130, 130, 7, 1, 1)]:
+    for T, E, K, G, Gk in [(1, 16, 4, 1, 1), (65, 40, 5, 4, 2), (130, 130, 7, 1, 1),
+                           (300, 200, 6, 1, 1)]:
         shape = synth.custom(T=T, d_model=256, E_routed=E, K=K, n_group=G, topk_group=Gk,
                              router_only=True)
         g = synth.generate(shape, device="cuda", seed=T + E)
-        _check_router_from_x(shape, g["x"], g["W_r"], g["bias"])
+        _check_router_from_x(shape, g["x"], g["W_r"], g["bias"], tensor_cores)
