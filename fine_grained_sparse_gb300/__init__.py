@@ -5,7 +5,7 @@ function here has the C name, marshals tensors to pointers and raises
 ``MoeError`` on a non-zero status.  All arithmetic runs in the library's
 CUDA kernels; there is no other implementation behind these names, and
 importing the package fails when the library has not been built
-(``python -m fine_grained_sparse_gb300.build``).
+(``python fine_grained_sparse_gb300/build.py``, or ``__graft_entry__.build()``).
 
 Tensors are torch tensors on the current CUDA device (PyTorch provides the
 device memory and the stream); plain integers are accepted as raw pointers.
@@ -23,10 +23,13 @@ __all__ = [
     "config", "moe_version", "moe_status_string", "moe_validate_config", "moe_workspace_size",
     "moe_get_device_status", "moe_router", "moe_router_from_logits", "moe_permute",
     "moe_grouped_swiglu", "moe_combine", "moe_linear", "moe_layer_forward",
-    "moe_layer_forward_host", "moe_last_error_detail",
+    "moe_layer_forward_host", "moe_last_error_detail", "moe_pack_weights", "pack_layer_weights",
+    "MOE_WEIGHTS_NATURAL", "MOE_WEIGHTS_PACKED", "MOE_PACK_GATE_UP", "MOE_PACK_PLAIN",
 ]
 
 MOE_F32, MOE_BF16 = 0, 1
+MOE_WEIGHTS_NATURAL, MOE_WEIGHTS_PACKED = 0, 1
+MOE_PACK_GATE_UP, MOE_PACK_PLAIN = 0, 1
 MOE_STAGE_COUNT = 5
 STAGE_NAMES = ("router", "dispatch", "expert_gate_up", "expert_down", "combine")
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
@@ -47,6 +50,7 @@ class MoeConfig(ctypes.Structure):
         ("n_group", ctypes.c_int32), ("topk_group", ctypes.c_int32),
         ("routed_scaling_factor", ctypes.c_float), ("norm_topk_prob", ctypes.c_int32),
         ("d_latent", ctypes.c_int32), ("dtype", ctypes.c_int32),
+        ("weight_layout", ctypes.c_int32),
     ]
 
 
@@ -55,7 +59,7 @@ def _load():
     if not os.path.exists(path):
         raise ImportError(
             f"fine_grained_sparse_gb300: CUDA library {path} is missing; build it with "
-            "`python -m fine_grained_sparse_gb300.build`")
+            "`python fine_grained_sparse_gb300/build.py`")
     return ctypes.CDLL(path)
 
 
@@ -76,6 +80,7 @@ _SIGS = {
     "moe_grouped_swiglu": ([_CFG, _I64] + [_P] * 12 + [_SZ, _P], _I32),
     "moe_combine": ([_CFG, _I64, _P, _P, _P, _P, _P], _I32),
     "moe_linear": ([_I64, _I32, _I32, _P, _P, _P, _P, _P, _SZ, _P], _I32),
+    "moe_pack_weights": ([_I32, _I64, _I64, _I64, _P, _P, _P], _I32),
     "moe_layer_forward": ([_CFG, _I64] + [_P] * 14 + [_SZ, _P, _P], _I32),
     "moe_layer_forward_host": ([_CFG, _I64] + [_P] * 11 + [_SZ, _P], _I32),
 }
@@ -111,7 +116,7 @@ def config(shape=None, **kw) -> MoeConfig:
     """MoeConfig from a ``synth.LayerShape``-like object and/or keywords."""
     vals = dict(d_model=0, d_ff=0, E_routed=0, E_shared=0, d_ff_shared=0, K=1, n_group=1,
                 topk_group=1, routed_scaling_factor=2.827, norm_topk_prob=1, d_latent=0,
-                dtype=MOE_BF16)
+                dtype=MOE_BF16, weight_layout=MOE_WEIGHTS_NATURAL)
     if shape is not None:
         for k in vals:
             if hasattr(shape, k):
@@ -218,3 +223,29 @@ def moe_layer_forward_host(cfg, T, x_host, W_r, bias, W_gate_up, W_down, Ws_gate
                                       _ptr(Ws_down), _ptr(W_lat_down), _ptr(W_lat_up),
                                       _ptr(y_host), _ptr(workspace), ws_bytes, _stream(stream)),
            "moe_layer_forward_host")
+
+
+def moe_pack_weights(kind, groups, rows, cols, src, dst, stream=None):
+    _check(lib.moe_pack_weights(kind, groups, rows, cols, _ptr(src), _ptr(dst), _stream(stream)),
+           "moe_pack_weights")
+
+
+def pack_layer_weights(weights: dict, stream=None) -> dict:
+    """Copies of the bf16 weight banks of one layer (keys as produced by
+    ``synth.generate``: W_gate_up, W_down, Ws_gate_up, Ws_down, W_lat_down,
+    W_lat_up) in MOE_WEIGHTS_PACKED order; other entries are passed through.
+    Use with a config whose weight_layout is MOE_WEIGHTS_PACKED."""
+    import torch
+    out = dict(weights)
+    kinds = {"W_gate_up": MOE_PACK_GATE_UP, "Ws_gate_up": MOE_PACK_GATE_UP,
+             "W_down": MOE_PACK_PLAIN, "Ws_down": MOE_PACK_PLAIN,
+             "W_lat_down": MOE_PACK_PLAIN, "W_lat_up": MOE_PACK_PLAIN}
+    for key, kind in kinds.items():
+        w = weights.get(key)
+        if w is None:
+            continue
+        w3 = w if w.dim() == 3 else w.unsqueeze(0)
+        dst = torch.empty_like(w3)
+        moe_pack_weights(kind, w3.shape[0], w3.shape[1], w3.shape[2], w3, dst, stream)
+        out[key] = dst if w.dim() == 3 else dst.squeeze(0)
+    return out

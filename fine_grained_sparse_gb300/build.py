@@ -1,7 +1,9 @@
 """Build the CUDA library in-tree: nvcc for sm_103a, one object per source
 file compiled in parallel, linked into ``_lib/libfgsmoe.so``.
 
-    python -m fine_grained_sparse_gb300.build [--verbose-ptxas]
+    python fine_grained_sparse_gb300/build.py [--verbose-ptxas] [--force]
+
+(run as a script: importing the package loads the library this builds)
 """
 from __future__ import annotations
 

@@ -77,6 +77,10 @@ int32_t check_layer_cfg(const moe_config* c, int64_t T) {
   if (c->E_shared < 0 || c->E_shared > 8) return fail(MOE_ERR_INVALID_ARG, "E_shared not in [0, 8]");
   if (c->E_shared > 0 && c->d_ff_shared < 1) return fail(MOE_ERR_INVALID_ARG, "d_ff_shared < 1");
   if (c->d_latent < 0) return fail(MOE_ERR_INVALID_ARG, "d_latent < 0");
+  if (c->weight_layout != MOE_WEIGHTS_NATURAL && c->weight_layout != MOE_WEIGHTS_PACKED)
+    return fail(MOE_ERR_INVALID_ARG, "weight_layout");
+  if (c->weight_layout == MOE_WEIGHTS_PACKED && c->dtype != MOE_BF16)
+    return fail(MOE_ERR_UNSUPPORTED_SHAPE, "packed weights are bf16 only");
   if (c->dtype == MOE_BF16) {
     if (c->d_model % 128) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "bf16 path: d_model % 128 != 0");
     if (c->d_ff % 64) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "bf16 path: d_ff % 64 != 0");
@@ -156,8 +160,17 @@ int num_sms() {
   return cached[dev];
 }
 
-// 5-D gate/up tensor map when the driver accepts it, else eight 16-row boxes
-int32_t set_gate_up_A(GemmSegment& s, const void* W, int groups, int F, int Kd) {
+// Weights in MOE_WEIGHTS_PACKED order stream as one bulk copy per stage;
+// natural ones through tensor maps: for gate/up a 5-D map when the driver
+// accepts it, else eight 16-row boxes.
+int32_t set_gate_up_A(GemmSegment& s, const void* W, int groups, int F, int Kd, bool packed) {
+  s.a_rows = F;
+  if (packed) {
+    s.a_packed = static_cast<const uint8_t*>(W);
+    s.a_group_bytes = 2ll * F * Kd * 2;
+    s.a_boxes = 1;
+    return MOE_OK;
+  }
   if (encode_tmap_gate_up_5d(&s.tmA, W, groups, F, Kd) == CUDA_SUCCESS) {
     s.a_boxes = 1;
   } else if (encode_tmap_weights_3d(&s.tmA, W, groups, 2 * static_cast<int64_t>(F), Kd, 16) ==
@@ -177,7 +190,14 @@ int32_t set_B(GemmSegment& s, const void* B, int64_t rows, int Kd) {
   return MOE_OK;
 }
 
-int32_t set_store_A(GemmSegment& s, const void* W, int groups, int O, int Kd) {
+int32_t set_store_A(GemmSegment& s, const void* W, int groups, int O, int Kd, bool packed) {
+  if (packed) {
+    s.a_packed = static_cast<const uint8_t*>(W);
+    s.a_group_bytes = static_cast<int64_t>(O) * Kd * 2;
+    s.a_boxes = 1;
+    s.a_rows = 0;
+    return MOE_OK;
+  }
   if (encode_tmap_weights_3d(&s.tmA, W, groups, O, Kd, 128) != CUDA_SUCCESS)
     return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for weights");
   s.a_boxes = 1;
@@ -217,6 +237,7 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
   void* H = at<void>(ws, L.H);
   void* Hs = at<void>(ws, L.Hs);
   const bool bf16 = c->dtype == MOE_BF16;
+  const bool packed = c->weight_layout == MOE_WEIGHTS_PACKED;
   const int nt = bf16 ? token_tile(T) : kSimtTile;
 
   MOE_CUDA(launch_build_tiles(io.offsets, E, nt, tiles, ntiles, st));
@@ -235,7 +256,7 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
     GemmSegment& r = p.seg[0];
     clear(r);
     int32_t e;
-    if ((e = set_gate_up_A(r, io.W_gate_up, E, F, de)) != MOE_OK) return e;
+    if ((e = set_gate_up_A(r, io.W_gate_up, E, F, de, packed)) != MOE_OK) return e;
     if ((e = set_B(r, Xp, TK, de)) != MOE_OK) return e;
     r.a128 = F / 64;
     r.tiles = tiles;
@@ -245,7 +266,7 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
     if (S) {
       GemmSegment& s = p.seg[1];
       clear(s);
-      if ((e = set_gate_up_A(s, io.Ws_gate_up, S, Fs, d)) != MOE_OK) return e;
+      if ((e = set_gate_up_A(s, io.Ws_gate_up, S, Fs, d, packed)) != MOE_OK) return e;
       if ((e = set_B(s, io.x_shared, T, d)) != MOE_OK) return e;
       s.a128 = Fs / 64;
       s.groups = S;
@@ -262,7 +283,7 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
     p.mode = kModeStore;
     GemmSegment& r2 = p.seg[0];
     clear(r2);
-    if ((e = set_store_A(r2, io.W_down, E, de, F)) != MOE_OK) return e;
+    if ((e = set_store_A(r2, io.W_down, E, de, F, packed)) != MOE_OK) return e;
     if ((e = set_B(r2, H, TK, F)) != MOE_OK) return e;
     r2.a128 = de / 128;
     r2.o_limit = de;
@@ -274,7 +295,7 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
     if (S) {
       GemmSegment& s2 = p.seg[1];
       clear(s2);
-      if ((e = set_store_A(s2, io.Ws_down, S, d, Fs)) != MOE_OK) return e;
+      if ((e = set_store_A(s2, io.Ws_down, S, d, Fs, packed)) != MOE_OK) return e;
       if ((e = set_B(s2, Hs, S * T, Fs)) != MOE_OK) return e;
       s2.a128 = d / 128;
       s2.o_limit = d;
@@ -349,7 +370,7 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
 }
 
 int32_t run_linear(int64_t T, int in_f, int out_f, const void* x, const void* W, const void* add,
-                   void* y, int* status, cudaStream_t st) {
+                   void* y, int* status, cudaStream_t st, bool packed = false) {
   GemmParams p;
   memset(&p, 0, sizeof(p));
   p.mode = kModeStore;
@@ -359,7 +380,7 @@ int32_t run_linear(int64_t T, int in_f, int out_f, const void* x, const void* W,
   GemmSegment& s = p.seg[0];
   clear(s);
   int32_t e;
-  if ((e = set_store_A(s, W, 1, out_f, in_f)) != MOE_OK) return e;
+  if ((e = set_store_A(s, W, 1, out_f, in_f, packed)) != MOE_OK) return e;
   if ((e = set_B(s, x, T, in_f)) != MOE_OK) return e;
   s.a128 = out_f / 128;
   s.o_limit = out_f;
@@ -553,6 +574,21 @@ int32_t moe_combine(const moe_config* cfg, int64_t T, const void* Y, const int32
   return MOE_OK;
 }
 
+int32_t moe_pack_weights(int32_t kind, int64_t groups, int64_t rows, int64_t cols,
+                         const void* src, void* dst, void* stream) {
+  if (kind != MOE_PACK_GATE_UP && kind != MOE_PACK_PLAIN) return fail(MOE_ERR_INVALID_ARG, "kind");
+  if (groups < 1 || rows < 128 || cols < 64) return fail(MOE_ERR_INVALID_ARG, "sizes");
+  if (rows % 128 || cols % 64) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "rows % 128 or cols % 64");
+  if (!src || !dst) return fail(MOE_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(src) || !aligned16(dst)) return fail(MOE_ERR_ALIGNMENT, "pointer not 16-byte aligned");
+  const size_t bytes = static_cast<size_t>(groups * rows * cols) * 2;
+  const char* a = static_cast<const char*>(src);
+  const char* b = static_cast<const char*>(dst);
+  if (a < b + bytes && b < a + bytes) return fail(MOE_ERR_INVALID_ARG, "src and dst overlap");
+  MOE_CUDA(launch_pack_weights(kind, groups, rows, cols, src, dst, static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
 int32_t moe_linear(int64_t T, int32_t in_features, int32_t out_features, const void* x,
                    const void* W, const void* add, void* y, void* workspace, size_t ws_bytes,
                    void* stream) {
@@ -607,7 +643,7 @@ int32_t moe_layer_forward(const moe_config* cfg, int64_t T, const void* x, const
   const void* x_e = x;
   if (cfg->d_latent) {
     st = run_linear(T, cfg->d_model, cfg->d_latent, x, W_lat_down, nullptr, at<void>(ws, L.x_lat),
-                    status, s);
+                    status, s, cfg->weight_layout == MOE_WEIGHTS_PACKED);
     if (st != MOE_OK) return st;
     x_e = at<void>(ws, L.x_lat);
   }
@@ -624,7 +660,7 @@ int32_t moe_layer_forward(const moe_config* cfg, int64_t T, const void* x, const
     MOE_CUDA(launch_combine(at<void>(ws, L.Y), inv, T, cfg->K, cfg->d_latent, nullptr, 0, 0,
                             at<void>(ws, L.r_lat), bf16, s));
     st = run_linear(T, cfg->d_latent, cfg->d_model, at<void>(ws, L.r_lat), W_lat_up, nullptr,
-                    at<void>(ws, L.U), status, s);
+                    at<void>(ws, L.U), status, s, cfg->weight_layout == MOE_WEIGHTS_PACKED);
     if (st != MOE_OK) return st;
     MOE_CUDA(launch_combine(nullptr, nullptr, T, 0, cfg->d_model, at<void>(ws, L.U), 1 + S, T, y,
                             bf16, s));

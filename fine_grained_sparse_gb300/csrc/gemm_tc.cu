@@ -202,7 +202,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         const uint32_t a_dst = stage_a(stage);
         const uint32_t b_dst = stage_b(stage);
         const int kc = ks * kBK;
-        for (int a = 0; a < x.n_a; ++a) {
+        if (s->a_packed) {
+          // packed weights: the unit's n_a tiles of this k step are adjacent
+          const uint8_t* src = s->a_packed + x.group * s->a_group_bytes +
+                               (2ll * x.ob * s->k_steps + static_cast<int64_t>(ks) * x.n_a) *
+                                   kATileBytes;
+          bulk_load(a_dst, src, kATileBytes * x.n_a, fb, pol_w);
+        }
+        for (int a = 0; a < (s->a_packed ? 0 : x.n_a); ++a) {
           const int blk = 2 * x.ob + a;  // 128-row A tile index along O
           const uint32_t dst = a_dst + a * kATileBytes;
           if (p.mode == kModeSwiGLU) {
@@ -373,6 +380,48 @@ __global__ void __launch_bounds__(256) split_router_weight_kernel(const float* _
   }
 }
 
+// One 16-byte chunk of the packed bank per thread step: dst is written in
+// order, src gathered (a one-time load step).
+__global__ void __launch_bounds__(256) pack_weights_kernel(int kind, int64_t groups, int64_t rows,
+                                                           int64_t cols,
+                                                           const uint4* __restrict__ src,
+                                                           uint4* __restrict__ dst) {
+  const int64_t ksteps = cols / kBK;
+  const int64_t a128 = rows / 128;
+  const int64_t per_group = a128 * ksteps;  // 16 KB tiles per group
+  const int64_t full_pairs = a128 / 2;
+  const int64_t n = groups * per_group * 1024;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t t = i >> 10;
+    const int r = static_cast<int>((i >> 3) & 127);
+    const int pos = static_cast<int>(i & 7);
+    const int64_t g = t / per_group;
+    const int64_t tg = t - g * per_group;
+    int64_t pair, ks, a;
+    if (tg < full_pairs * 2 * ksteps) {
+      pair = tg / (2 * ksteps);
+      const int64_t rem = tg - pair * 2 * ksteps;
+      ks = rem >> 1;
+      a = rem & 1;
+    } else {
+      pair = full_pairs;
+      ks = tg - full_pairs * 2 * ksteps;
+      a = 0;
+    }
+    const int64_t blk = 2 * pair + a;
+    const int chunk = pos ^ (r & 7);
+    int64_t row;
+    if (kind == 0) {
+      const int64_t F = rows / 2;
+      row = ((r >> 4) & 1) * F + 64 * blk + 16 * (r >> 5) + (r & 15);
+    } else {
+      row = blk * 128 + r;
+    }
+    dst[i] = src[((g * rows + row) * cols + ks * kBK + chunk * 8) >> 3];
+  }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -457,6 +506,17 @@ cudaError_t launch_tc_gemm(const GemmParams& params, int num_sms, cudaStream_t s
     if (dev < 64) configured[dev] = 1;
   }
   tc_gemm_kernel<<<num_sms, kThreads, plan.smem_bytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_weights(int kind, int64_t groups, int64_t rows, int64_t cols,
+                                const void* src, void* dst, cudaStream_t stream) {
+  const int64_t n = groups * rows * cols / 8;
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 65536) blocks = 65536;
+  if (blocks < 1) return cudaSuccess;
+  pack_weights_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      kind, groups, rows, cols, static_cast<const uint4*>(src), static_cast<uint4*>(dst));
   return cudaGetLastError();
 }
 

@@ -71,6 +71,9 @@ struct GemmSegment {
   int a_boxes;      // SwiGLU A tile: 1 = one 5-D box, 8 = eight 16-row boxes
   int a_rows;       // SwiGLU: F (row offset of the up half)
   int o_limit;      // store mode: columns o >= o_limit are not written
+  // packed weights (one contiguous bulk copy per stage) instead of tmA
+  const uint8_t* a_packed;
+  int64_t a_group_bytes;
   // explicit tiles (routed experts) or implicit ones (groups x rows)
   const RowTile* tiles;
   const int* ntiles;
@@ -102,6 +105,10 @@ struct GemmPlan {
 GemmPlan plan_gemm(int nt);
 
 cudaError_t launch_tc_gemm(const GemmParams& p, int num_sms, cudaStream_t stream);
+
+// Rearrange a bf16 weight bank into the packed order (see moe_pack_weights).
+cudaError_t launch_pack_weights(int kind, int64_t groups, int64_t rows, int64_t cols,
+                                const void* src, void* dst, cudaStream_t stream);
 
 // W_split[e] = [hi | mid | lo] (bf16, 3 d wide) with hi + mid + lo = W_r[e]
 // to about 2^-24 relative: the router GEMM on bf16 tensor cores.

@@ -35,12 +35,16 @@ def main(argv=None):
     ap.add_argument("--L", type=int, default=0)
     ap.add_argument("--x-dist", default="clusters32")
     ap.add_argument("--iters", type=int, default=2)
+    ap.add_argument("--natural", action="store_true", help="natural (unpacked) weight layout")
     a = ap.parse_args(argv)
     shape = synth.custom(name="profile_case", T=a.T, d_model=a.d, E_routed=a.E, K=a.K,
                          E_shared=a.S, d_ff=a.F, d_ff_shared=a.Fs or a.F, n_group=a.G,
                          topk_group=a.Gk, d_latent=a.L, x_dist=a.x_dist)
     g = synth.generate(shape, device="cuda")
     cfg = fgs.config(shape)
+    if not a.natural:
+        cfg.weight_layout = fgs.MOE_WEIGHTS_PACKED
+        g = fgs.pack_layer_weights(g)
     nws = fgs.moe_workspace_size(cfg, a.T)
     ws = torch.zeros(nws, dtype=torch.uint8, device="cuda")
     y = torch.empty((a.T, a.d), dtype=torch.bfloat16, device="cuda")

@@ -74,7 +74,41 @@ typedef struct moe_config {
   int32_t norm_topk_prob;      /* renormalise the K weights when K > 1 (1)      */
   int32_t d_latent;     /* K3 latent width L (3584); 0 = K2 form (no projection)*/
   int32_t dtype;        /* moe_dtype of activations, expert weights, outputs    */
+  int32_t weight_layout;/* moe_weight_layout of the bf16 expert, shared-expert
+                           and latent-projection weights                       */
 } moe_config;
+
+/* Layouts of the bf16 weight matrices the expert GEMMs stream.
+ *   MOE_WEIGHTS_NATURAL: row-major [G, O, K] as documented per argument.
+ *   MOE_WEIGHTS_PACKED:  the same values rearranged by moe_pack_weights()
+ *     into the order the tensor cores consume them, so that every pipeline
+ *     stage of a GEMM is one contiguous bulk copy (see moe_pack_weights). */
+typedef enum moe_weight_layout { MOE_WEIGHTS_NATURAL = 0, MOE_WEIGHTS_PACKED = 1 } moe_weight_layout;
+
+/* Kinds of packed matrices. */
+typedef enum moe_pack_kind {
+  MOE_PACK_GATE_UP = 0, /* [G, 2F, K]: rows 0..F-1 gate, F..2F-1 up (W_gate_up) */
+  MOE_PACK_PLAIN = 1    /* [G, O, K] (W_down, Ws_down, W_lat_down, W_lat_up)     */
+} moe_pack_kind;
+
+/*
+ * Rearrange a bf16 weight bank into MOE_WEIGHTS_PACKED order (no call of the
+ * forward pass needs it: it is a one-time load step).  src and dst are
+ * device buffers of groups * rows * cols bf16 (the same size); they must not
+ * overlap.  rows % 128 == 0 (MOE_PACK_GATE_UP: F = rows / 2, F % 64 == 0),
+ * cols % 64 == 0.
+ * Packed order, per group g: the 128-row tiles along O are taken in pairs
+ * (u = 0, 1, ...; the last "pair" may hold one tile), and for each pair and
+ * each 64-column step k of K the pair's tiles follow each other, each tile
+ * 128 rows x 64 columns = 16 KB.  Inside a tile, row r occupies bytes
+ * [128 r, 128 r + 128) and its 16-byte chunk c (columns 8c..8c+7) sits at
+ * chunk position c XOR (r mod 8) -- the 128-byte swizzle of the tensor
+ * cores' shared-memory operand layout.  For MOE_PACK_GATE_UP tile t of a
+ * group holds, in rows 32 q + 16 h + i (q < 4, h < 2, i < 16), row
+ * h * F + 64 t + 16 q + i of the source: the gate and up rows of 16 features
+ * side by side. */
+int32_t moe_pack_weights(int32_t kind, int64_t groups, int64_t rows, int64_t cols,
+                         const void* src, void* dst, void* stream);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int32_t moe_version(void);

@@ -112,3 +112,67 @@ def test_linear_bf16():
         torch.cuda.synchronize()
         want = np64(x) @ np64(W).T + np64(add)
         assert rel_max_err(np64(y), want) <= TOL_BF16
+
+
+def _pack_reference(W: torch.Tensor, gate_up: bool) -> torch.Tensor:
+    """The documented MOE_WEIGHTS_PACKED order, written with torch indexing."""
+    G, R, C = W.shape
+    a128, ks = R // 128, C // 64
+    r = torch.arange(128)
+    rows = []
+    for t in range(a128):
+        if gate_up:
+            F = R // 2
+            rows.append(((r >> 4) & 1) * F + 64 * t + 16 * (r >> 5) + (r & 15))
+        else:
+            rows.append(128 * t + r)
+    tiles = W[:, torch.cat(rows), :].reshape(G, a128, 128, ks, 8, 8)   # g, t, row, k-step, chunk, elem
+    pos = torch.arange(8)
+    chunk_at = pos[None, :] ^ (r[:, None] & 7)                           # [row, position] -> chunk
+    idx = chunk_at[None, None, :, None, :, None].expand(G, a128, 128, ks, 8, 8)
+    sw = torch.gather(tiles, 4, idx)                                     # swizzled tiles
+    sw = sw.permute(0, 1, 3, 2, 4, 5)                                    # g, t, k-step, row, pos, elem
+    out = []
+    for g in range(G):
+        for u in range((a128 + 1) // 2):
+            for k in range(ks):
+                for t in range(2 * u, min(2 * u + 2, a128)):
+                    out.append(sw[g, t, k].reshape(-1))
+    return torch.cat(out).reshape(G, R, C)
+
+
+@pytest.mark.parametrize("gate_up", [True, False])
+@pytest.mark.parametrize("G,R,C", [(2, 256, 128), (3, 384, 192), (1, 128, 64)])
+def test_pack_weights_layout(gate_up, G, R, C):
+    need_gpu()
+    fgs = lib()
+    W = torch.randn((G, R, C), generator=torch.Generator().manual_seed(R + C)).bfloat16()
+    dst = torch.empty_like(W, device="cuda")
+    fgs.moe_pack_weights(fgs.MOE_PACK_GATE_UP if gate_up else fgs.MOE_PACK_PLAIN, G, R, C,
+                         W.cuda(), dst)
+    torch.cuda.synchronize()
+    assert torch.equal(dst.cpu(), _pack_reference(W, gate_up))
+
+
+@pytest.mark.parametrize("case", CASES[:4], ids=lambda c: "T%d_d%d_E%d_K%d_F%d_S%d" % c[:6])
+def test_grouped_swiglu_packed_equals_natural(case):
+    """The packed layout feeds the tensor cores the same operands: bit-exact."""
+    need_gpu()
+    fgs = lib()
+    T, d, E, K, F, S, Fs, skew = case
+    shape, g, idx, topk_w = _case(T, d, E, K, F, S, Fs, "bf16", seed=T + d + E, skew=skew)
+    p, Y, Ys = _run(shape, g, idx, topk_w)
+    gp = fgs.pack_layer_weights(g)
+    cfg = fgs.config(shape, weight_layout=fgs.MOE_WEIGHTS_PACKED)
+    ws, nws = workspace(cfg, T)
+    Y2 = torch.empty_like(Y)
+    Ys2 = torch.empty_like(Ys) if S else None
+    fgs.moe_grouped_swiglu(
+        cfg, T, g["x"], torch.from_numpy(p["offsets"].astype(np.int32)).cuda(),
+        torch.from_numpy(p["perm"].astype(np.int32)).cuda(), topk_w.cuda(), gp["W_gate_up"],
+        gp["W_down"], g["x"] if S else None, gp.get("Ws_gate_up"), gp.get("Ws_down"), Y2, Ys2,
+        ws, nws)
+    assert fgs.moe_get_device_status(ws) == 0
+    assert torch.equal(Y, Y2)
+    if S:
+        assert torch.equal(Ys, Ys2)

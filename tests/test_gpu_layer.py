@@ -18,9 +18,12 @@ from _gpu_common import (GAP_MIN, TOL_BF16, TOL_F32, by_expert, lib, need_gpu, n
 pytestmark = pytest.mark.gpu
 
 
-def _forward(shape, g):
+def _forward(shape, g, packed=False):
     fgs = lib()
     cfg = fgs.config(shape)
+    if packed:  # weights rearranged once into the order the tensor cores stream
+        cfg.weight_layout = fgs.MOE_WEIGHTS_PACKED
+        g = fgs.pack_layer_weights(g)
     T = g["x"].shape[0]
     ws, nws = workspace(cfg, T)
     y = torch.empty((T, shape.d_model), dtype=g["x"].dtype, device="cuda")
@@ -69,11 +72,14 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("packed", [False, True], ids=["natural", "packed"])
 @pytest.mark.parametrize("shape", SMALL, ids=lambda s: s.name)
-def test_layer_small_every_token(shape):
+def test_layer_small_every_token(shape, packed):
     need_gpu()
+    if packed and shape.dtype == "f32":
+        pytest.skip("packed weights are bf16 only")
     g = synth.generate(shape, device="cuda")
-    y, idx, w, counts = _forward(shape, g)
+    y, idx, w, counts = _forward(shape, g, packed)
     rows = np.arange(shape.T)
     _compare(shape, g, y, idx, w, counts, rows, TOL_F32 if shape.dtype == "f32" else TOL_BF16)
 
@@ -84,7 +90,7 @@ def test_layer_full_size_sampled(name):
     shape = synth.shape(name)
     g = synth.generate(shape, device="cuda")
     try:
-        y, idx, w, counts = _forward(shape, g)
+        y, idx, w, counts = _forward(shape, g, packed=True)
         torch.cuda.synchronize()
         T = shape.T
         rows = np.unique(np.linspace(0, T - 1, 6).astype(int))
