@@ -44,9 +44,23 @@ int elem_bytes(const moe_config* c) { return c->dtype == MOE_BF16 ? 2 : 4; }
 
 int d_expert(const moe_config* c) { return c->d_latent ? c->d_latent : c->d_model; }
 
+// Parts of the router's K (= 3 d: the hi, mid and lo weight pieces) summed
+// separately: one per piece, and each piece cut further when T is small so
+// that the GEMM has enough independent units.
+int router_ksplit(int64_t T, int d) {
+  int h = 1;
+  const int kd = d / 64;
+  for (int c = 1; c <= 16 && static_cast<int64_t>(c) * T <= 2048; ++c)
+    if (kd % c == 0) h = c;
+  return 3 * h;
+}
+
+int router_tile(int64_t T) { return T <= 256 ? 32 : 128; }
+
 // token tile of the tensor-core GEMMs: small batches (few rows per expert)
-// take 32-row tiles and a deeper pipeline; large ones 128-row tiles
-int token_tile(int64_t T) { return T <= 256 ? 32 : 128; }
+// take 32-row tiles and the deepest weight ring; large ones 256-row tiles,
+// so that most experts are one tile and their weights are read once
+int token_tile(int64_t T) { return T <= 256 ? 32 : 256; }
 
 int32_t check_router_cfg(const moe_config* c, int64_t T) {
   if (!c) return fail(MOE_ERR_INVALID_ARG, "cfg is null");
@@ -123,7 +137,9 @@ Layout layout(const moe_config* c, int64_t T) {
   L.ntiles = take(16);
   L.w_perm = take(4 * TK);
   L.w_split = take(c->dtype == MOE_BF16 ? 3ull * c->E_routed * c->d_model * 2 : 0);
-  L.logits = take(c->dtype == MOE_BF16 ? 4ull * T * c->E_routed : 0);
+  L.logits = take(c->dtype == MOE_BF16 && c->d_model % 64 == 0
+                      ? 4ull * router_ksplit(T, c->d_model) * T * c->E_routed
+                      : 0);
   L.Xp = take(static_cast<size_t>(TK) * de * eb);
   L.H = take(static_cast<size_t>(TK) * c->d_ff * eb);
   L.Hs = take(static_cast<size_t>(S) * T * c->d_ff_shared * eb);
@@ -471,7 +487,7 @@ int32_t moe_router(const moe_config* cfg, int64_t T, const void* x, const float*
     GemmParams p;
     memset(&p, 0, sizeof(p));
     p.mode = kModeStore;
-    p.nt = token_tile(T);
+    p.nt = router_tile(T);
     p.status = at<int>(workspace, L.status);
     p.nseg = 1;
     GemmSegment& g = p.seg[0];
@@ -488,8 +504,12 @@ int32_t moe_router(const moe_config* cfg, int64_t T, const void* x, const float*
     g.rows = static_cast<int>(T);
     g.out_f32 = logits;
     g.out_ld = E;
+    g.ksplit = router_ksplit(T, d);
+    g.out_split_stride = T * E;
     MOE_CUDA(launch_tc_gemm(p, num_sms(), s));
     a.logits = logits;
+    a.logit_parts = g.ksplit;
+    a.logit_part_stride = T * E;
   } else {
     a.x = x;
   }

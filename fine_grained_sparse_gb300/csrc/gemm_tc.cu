@@ -11,17 +11,16 @@
 // the down-pass form (store mode) with one group.
 //
 // Swap-AB tiling.  The MMA's M side is a block of WEIGHT rows and its N side
-// (16..128, a multiple of 16) a block of token rows of one expert, so an
+// (16..256, a multiple of 16) a block of token rows of one expert, so an
 // expert with few tokens still streams its weights through full-height MMAs.
 // A unit is 256 weight rows -- two 128-row A tiles, two TMEM accumulators --
-// against one token tile: each B (token) tile in shared memory feeds twice
-// the MMA work, and two thirds of every pipeline stage are weights, which
-// keeps ~128 KB of weight bytes in flight per SM for the HBM stream.
+// against one token tile, so each token tile in shared memory feeds twice
+// the MMA work.  Weights and tokens flow through separate rings with their
+// own producer warps: the weight ring is deep (5-6 stages of 32 KB, the HBM
+// stream), the token ring shallow (2-3 stages, mostly L2 hits).
 //   A tiles: 2 x (128 rows x 64 k) bf16, K-major, 128-byte swizzle (32 KB)
 //   B tile:  up to nt rows x 64 k, same layout, loaded as 32-row boxes
-//   D:       2 accumulators x N fp32 columns, double-buffered (4 nt <= 512
-//            TMEM columns) so the epilogue of one unit overlaps the main loop
-//            of the next.
+//   D:       2 accumulators x N fp32 columns in TMEM (regions below).
 // For the gate/up pass each A tile interleaves the two halves of W_gate_up
 // [E, 2F, d] in 16-row slices: rows 32q..32q+15 are gate features
 // 16q + (0..15) of the tile's 64 and rows 32q+16..32q+31 the up features with
@@ -33,9 +32,10 @@
 // side by side and the second reader finds the block in L2.
 //
 // Warp roles (one CTA per SM, persistent over the units):
-//   warp 0 lane 0: TMA producer; warp 1 lane 0: MMA issuer;
-//   warps 2..9: epilogue, warp w reads lane quadrant w%4 of accumulator
-//   (w-2)/4 (TMEM -> registers -> global stores).
+//   warp 0 lane 0: weight producer (bulk copies of packed weights, or TMA);
+//   warp 1 lane 0: MMA issuer; warp 2 lane 0: token producer (TMA);
+//   warps 3..10: epilogue, warp w reads lane quadrant w%4 of accumulator
+//   (w-3)/4 (TMEM -> registers -> global stores).
 // Every wait is bounded (%globaltimer); on expiry the CTA records
 // MOE_ERR_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
 #include <cudaTypedefs.h>
@@ -55,26 +55,40 @@ constexpr uint32_t kABytes = 2 * kATileBytes;
 constexpr int kBBoxRows = 32;
 constexpr uint32_t kBBoxBytes = kBBoxRows * 128;
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kThreads = 32 * (3 + kEpiWarps);
 constexpr int kMaxStages = 8;
 constexpr size_t kSmemBudget = 221184;  // pipeline bytes per CTA (216 KB)
 
 struct Unit {
   int seg, group, b_row, out_row, n_rows, ob, n_a, ntiles;
+  int k0, k1;  // k steps [k0, k1) of this unit (all of K unless split)
+  int split;
 };
+
+__device__ __forceinline__ int ksplit_of(const GemmSegment* s) { return s->ksplit > 1 ? s->ksplit : 1; }
 
 __device__ __forceinline__ int segment_units(const GemmSegment* s, int nt) {
   const int ob = (s->a128 + 1) / 2;
   if (s->tiles) return *s->ntiles * ob;
-  return s->groups * ((s->rows + nt - 1) / nt) * ob;
+  return s->groups * ((s->rows + nt - 1) / nt) * ob * ksplit_of(s);
 }
 
 __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int units0, int nt) {
   Unit x;
   x.seg = u >= units0 ? 1 : 0;
-  const int local = u - (x.seg ? units0 : 0);
+  int local = u - (x.seg ? units0 : 0);
   const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
   const int OB = (s->a128 + 1) / 2;
+  const int ns = ksplit_of(s);
+  const int kps = s->k_steps / ns;
+  x.split = 0;
+  if (ns > 1) {  // the K part is the outermost index of a split segment
+    const int per = s->groups * ((s->rows + nt - 1) / nt) * OB;
+    x.split = local / per;
+    local -= x.split * per;
+  }
+  x.k0 = x.split * kps;
+  x.k1 = x.k0 + kps;
   if (s->tiles) {
     // the units of one expert are [first_tile * OB, (first_tile + ntiles) * OB)
     const RowTile& any = s->tiles[local / OB];
@@ -119,44 +133,71 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int* s
   mbar_wait_bounded(bar, parity, &local_abort, status);
 }
 
+// TMEM: two regions of 256 columns.  A unit whose token tile fits in 128
+// columns keeps both accumulators in one region (columns 0 and 128 of it),
+// so consecutive small units alternate regions and the epilogue overlaps the
+// next main loop; a larger unit takes one region per accumulator.  Every
+// unit advances a region counter c by the regions it uses; region use c is
+// region c % 2 in its (c / 2)-th phase -- the same sequence in every role.
+struct Regions {
+  bool big;
+  int c;  // first region use of the unit
+};
+
+__device__ __forceinline__ int region_of(const Regions& r, int acc) {
+  return r.big ? ((r.c + acc) & 1) : (r.c & 1);
+}
+__device__ __forceinline__ uint32_t region_phase(int use) { return static_cast<uint32_t>(use >> 1) & 1u; }
+__device__ __forceinline__ uint32_t acc_column(const Regions& r, int acc) {
+  return r.big ? 256u * static_cast<uint32_t>((r.c + acc) & 1)
+               : 256u * static_cast<uint32_t>(r.c & 1) + 128u * static_cast<uint32_t>(acc);
+}
+
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const int stages = p.stages;
+  const int sa_n = p.a_stages;
+  const int sb_n = p.b_stages;
   const int nt = p.nt;
   const uint32_t b_stage_bytes = static_cast<uint32_t>(nt) * 128u;
-  const uint32_t stage_bytes = kABytes + b_stage_bytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + stages * stage_bytes);
-  // bars: full[stages] | empty[stages] | tmem_full[2] | tmem_empty[2] | drain
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * stages + 5);
+  uint8_t* smem_b = smem + sa_n * kABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_b + sb_n * b_stage_bytes);
+  // bars: a_full[Sa] | a_empty[Sa] | b_full[Sb] | b_empty[Sb] | tfull[2] | tempty[2] | drain
+  const int nbars = 2 * sa_n + 2 * sb_n + 5;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + nbars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t s_base = smem_u32(smem);
+  const uint32_t a_base = smem_u32(smem);
+  const uint32_t b_base = smem_u32(smem_b);
   const uint32_t bar_base = smem_u32(bars);
-  auto stage_a = [&](int s) { return s_base + s * stage_bytes; };
-  auto stage_b = [&](int s) { return s_base + s * stage_bytes + kABytes; };
-  auto full_bar = [&](int s) { return bar_base + 8u * s; };
-  auto empty_bar = [&](int s) { return bar_base + 8u * (stages + s); };
-  auto tfull_bar = [&](int b) { return bar_base + 8u * (2 * stages + b); };
-  auto tempty_bar = [&](int b) { return bar_base + 8u * (2 * stages + 2 + b); };
-  const uint32_t drain_bar = bar_base + 8u * (2 * stages + 4);
-  const uint32_t tmem_cols = 4u * static_cast<uint32_t>(nt);  // 2 buffers x 2 accumulators
+  auto a_full = [&](int s) { return bar_base + 8u * s; };
+  auto a_empty = [&](int s) { return bar_base + 8u * (sa_n + s); };
+  auto b_full = [&](int s) { return bar_base + 8u * (2 * sa_n + s); };
+  auto b_empty = [&](int s) { return bar_base + 8u * (2 * sa_n + sb_n + s); };
+  auto tfull_bar = [&](int r) { return bar_base + 8u * (2 * sa_n + 2 * sb_n + r); };
+  auto tempty_bar = [&](int r) { return bar_base + 8u * (2 * sa_n + 2 * sb_n + 2 + r); };
+  const uint32_t drain_bar = bar_base + 8u * (2 * sa_n + 2 * sb_n + 4);
+  constexpr uint32_t kTmemCols = 512;
 
   if (warp == 0) {
-    tmem_alloc(smem_u32(tmem_slot), tmem_cols);
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
   if (warp == 1 && lane == 0) {
-    for (int s = 0; s < stages; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+    for (int s = 0; s < sa_n; ++s) {
+      mbar_init(a_full(s), 1);
+      mbar_init(a_empty(s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), kEpiWarps);
+    for (int s = 0; s < sb_n; ++s) {
+      mbar_init(b_full(s), 1);
+      mbar_init(b_empty(s), 1);
+    }
+    for (int r = 0; r < 2; ++r) {
+      mbar_init(tfull_bar(r), 1);
+      mbar_init(tempty_bar(r), kEpiWarps);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -172,13 +213,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   const int total = units0 + units1;
 
   if (warp == 0 && lane == 0) {
-    // ------------------------------------------------------ TMA producer
-    for (int s = 0; s < p.nseg; ++s) {
-      prefetch_tensormap(&p.seg[s].tmA);
-      prefetch_tensormap(&p.seg[s].tmB);
-    }
+    // ------------------------------------------------ weight (A) producer
+    for (int s = 0; s < p.nseg; ++s) prefetch_tensormap(&p.seg[s].tmA);
     const uint64_t pol_stream = l2_policy_evict_first();
-    const uint64_t pol_keep = l2_policy_evict_last();
     const uint64_t pol_normal = l2_policy_evict_normal();
     int stage = 0;
     uint32_t phase = 0;
@@ -186,125 +223,167 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const Unit x = decode_unit(p, u, units0, nt);
       const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
-      const int nbox = (x.n_rows + kBBoxRows - 1) / kBBoxRows;
-      const uint32_t tx = kATileBytes * x.n_a + static_cast<uint32_t>(nbox) * kBBoxBytes;
+      const uint32_t tx = kATileBytes * x.n_a;
       // a weight block read by one token tile is streamed; one shared by
       // several token tiles (running side by side) is kept for the others
       const uint64_t pol_w = x.ntiles > 1 ? pol_normal : pol_stream;
       bool ok = true;
-      for (int ks = 0; ks < s->k_steps; ++ks) {
-        if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) {
+      for (int ks = x.k0; ks < x.k1; ++ks) {
+        if (!mbar_wait_bounded(a_empty(stage), phase ^ 1u, abort_flag, p.status)) {
           ok = false;
           break;
         }
-        const uint32_t fb = full_bar(stage);
+        const uint32_t fb = a_full(stage);
         mbar_arrive_expect_tx(fb, tx);
-        const uint32_t a_dst = stage_a(stage);
-        const uint32_t b_dst = stage_b(stage);
+        const uint32_t a_dst = a_base + stage * kABytes;
         const int kc = ks * kBK;
         if (s->a_packed) {
           // packed weights: the unit's n_a tiles of this k step are adjacent
           const uint8_t* src = s->a_packed + x.group * s->a_group_bytes +
                                (2ll * x.ob * s->k_steps + static_cast<int64_t>(ks) * x.n_a) *
                                    kATileBytes;
-          bulk_load(a_dst, src, kATileBytes * x.n_a, fb, pol_w);
-        }
-        for (int a = 0; a < (s->a_packed ? 0 : x.n_a); ++a) {
-          const int blk = 2 * x.ob + a;  // 128-row A tile index along O
-          const uint32_t dst = a_dst + a * kATileBytes;
-          if (p.mode == kModeSwiGLU) {
-            if (s->a_boxes == 1) {
-              tma_load_5d(dst, &s->tmA, fb, kc, 0, 0, blk * 4, x.group, pol_w);
+          bulk_load(a_dst, src, tx, fb, pol_w);
+        } else {
+          for (int a = 0; a < x.n_a; ++a) {
+            const int blk = 2 * x.ob + a;  // 128-row A tile index along O
+            const uint32_t dst = a_dst + a * kATileBytes;
+            if (p.mode == kModeSwiGLU) {
+              if (s->a_boxes == 1) {
+                tma_load_5d(dst, &s->tmA, fb, kc, 0, 0, blk * 4, x.group, pol_w);
+              } else {
+                for (int j = 0; j < 8; ++j)
+                  tma_load_3d(dst + j * 2048u, &s->tmA, fb, kc,
+                              (j & 1) * s->a_rows + blk * 64 + (j >> 1) * 16, x.group, pol_w);
+              }
             } else {
-              for (int j = 0; j < 8; ++j)
-                tma_load_3d(dst + j * 2048u, &s->tmA, fb, kc,
-                            (j & 1) * s->a_rows + blk * 64 + (j >> 1) * 16, x.group, pol_w);
+              tma_load_3d(dst, &s->tmA, fb, kc, blk * 128, x.group, pol_w);
             }
-          } else {
-            tma_load_3d(dst, &s->tmA, fb, kc, blk * 128, x.group, pol_w);
           }
         }
-        const int kb = s->b_k_period ? (ks % s->b_k_period) * kBK : kc;
+        ++issued;
+        if (++stage == sa_n) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+    }
+    const int64_t first = issued > sa_n ? issued - sa_n : 0;
+    for (int64_t q = first; q < issued; ++q)
+      drain_wait(a_full(static_cast<int>(q % sa_n)), static_cast<uint32_t>((q / sa_n) & 1),
+                 p.status);
+  } else if (warp == 2 && lane == 0) {
+    // ------------------------------------------------- token (B) producer
+    for (int s = 0; s < p.nseg; ++s) prefetch_tensormap(&p.seg[s].tmB);
+    const uint64_t pol_keep = l2_policy_evict_last();
+    int stage = 0;
+    uint32_t phase = 0;
+    int64_t issued = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      const Unit x = decode_unit(p, u, units0, nt);
+      const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
+      const int nbox = (x.n_rows + kBBoxRows - 1) / kBBoxRows;
+      const uint32_t tx = static_cast<uint32_t>(nbox) * kBBoxBytes;
+      bool ok = true;
+      for (int ks = x.k0; ks < x.k1; ++ks) {
+        if (!mbar_wait_bounded(b_empty(stage), phase ^ 1u, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = b_full(stage);
+        mbar_arrive_expect_tx(fb, tx);
+        const uint32_t b_dst = b_base + stage * b_stage_bytes;
+        const int kb = s->b_k_period ? (ks % s->b_k_period) * kBK : ks * kBK;
         for (int bx = 0; bx < nbox; ++bx)
           tma_load_2d(b_dst + bx * kBBoxBytes, &s->tmB, fb, kb, x.b_row + bx * kBBoxRows,
                       pol_keep);
         ++issued;
-        if (++stage == stages) {
+        if (++stage == sb_n) {
           stage = 0;
           phase ^= 1u;
         }
       }
       if (!ok) break;
     }
-    // wait for the copies still in flight (normally long complete)
-    const int64_t first = issued > stages ? issued - stages : 0;
+    const int64_t first = issued > sb_n ? issued - sb_n : 0;
     for (int64_t q = first; q < issued; ++q)
-      drain_wait(full_bar(static_cast<int>(q % stages)), static_cast<uint32_t>((q / stages) & 1),
+      drain_wait(b_full(static_cast<int>(q % sb_n)), static_cast<uint32_t>((q / sb_n) & 1),
                  p.status);
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------- MMA issuer
-    int stage = 0;
-    uint32_t phase = 0;
-    int i = 0;
-    for (int u = blockIdx.x; u < total; u += gridDim.x, ++i) {
+    int sa = 0, sb = 0;
+    uint32_t pa = 0, pb = 0;
+    int c = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const Unit x = decode_unit(p, u, units0, nt);
       const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
-      const int buf = i & 1;
-      const uint32_t buf_phase = static_cast<uint32_t>(i >> 1) & 1u;
-      if (!mbar_wait_bounded(tempty_bar(buf), buf_phase ^ 1u, abort_flag, p.status)) break;
-      tc_fence_after();
-      const uint32_t d0 = tmem_base + static_cast<uint32_t>(2 * buf * nt);
       const uint32_t n = static_cast<uint32_t>((x.n_rows + 15) & ~15);
+      const Regions rg = {n > 128, c};
+      bool ok = mbar_wait_bounded(tempty_bar(c & 1), region_phase(c) ^ 1u, abort_flag, p.status);
+      if (ok && rg.big)
+        ok = mbar_wait_bounded(tempty_bar((c + 1) & 1), region_phase(c + 1) ^ 1u, abort_flag,
+                               p.status);
+      if (!ok) break;
+      tc_fence_after();
       const uint32_t idesc = idesc_bf16_f32(128, n);
-      bool ok = true;
-      for (int ks = 0; ks < s->k_steps; ++ks) {
-        if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.status)) {
+      for (int ks = x.k0; ks < x.k1; ++ks) {
+        if (!mbar_wait_bounded(a_full(sa), pa, abort_flag, p.status) ||
+            !mbar_wait_bounded(b_full(sb), pb, abort_flag, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint64_t bdesc = smem_desc_sw128(stage_b(stage));
+        const uint64_t bdesc = smem_desc_sw128(b_base + sb * b_stage_bytes);
         for (int a = 0; a < x.n_a; ++a) {
-          const uint64_t adesc = smem_desc_sw128(stage_a(stage) + a * kATileBytes);
-          const uint32_t d = d0 + static_cast<uint32_t>(a * nt);
+          const uint64_t adesc = smem_desc_sw128(a_base + sa * kABytes + a * kATileBytes);
+          const uint32_t d = tmem_base + acc_column(rg, a);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
-            tc_mma_bf16(d, adesc + 2u * kk, bdesc + 2u * kk, idesc, (ks | kk) != 0);
+            tc_mma_bf16(d, adesc + 2u * kk, bdesc + 2u * kk, idesc, ((ks - x.k0) | kk) != 0);
         }
-        tc_commit(empty_bar(stage));
-        if (++stage == stages) {
-          stage = 0;
-          phase ^= 1u;
+        tc_commit(a_empty(sa));
+        tc_commit(b_empty(sb));
+        if (++sa == sa_n) {
+          sa = 0;
+          pa ^= 1u;
+        }
+        if (++sb == sb_n) {
+          sb = 0;
+          pb ^= 1u;
         }
       }
       if (!ok) break;
-      tc_commit(tfull_bar(buf));
+      tc_commit(tfull_bar(c & 1));
+      if (rg.big) tc_commit(tfull_bar((c + 1) & 1));
+      c += rg.big ? 2 : 1;
     }
     tc_commit(drain_bar);
     drain_wait(drain_bar, 0, p.status);
-  } else if (warp >= 2) {
+  } else if (warp >= 3) {
     // ---------------------------------------------------------- epilogue
     const int q = warp & 3;           // TMEM lane quadrant this warp may access
-    const int acc = (warp - 2) >> 2;  // which of the unit's two accumulators
-    int i = 0;
-    for (int u = blockIdx.x; u < total; u += gridDim.x, ++i) {
+    const int acc = (warp - 3) >> 2;  // which of the unit's two accumulators
+    int c = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const Unit x = decode_unit(p, u, units0, nt);
       const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
-      const int buf = i & 1;
-      const uint32_t buf_phase = static_cast<uint32_t>(i >> 1) & 1u;
-      if (!warp_wait(tfull_bar(buf), buf_phase, abort_flag, p.status)) break;
+      const uint32_t n = static_cast<uint32_t>((x.n_rows + 15) & ~15);
+      const Regions rg = {n > 128, c};
+      const int use = rg.big ? c + acc : c;
+      const int region = region_of(rg, acc);
+      if (!warp_wait(tfull_bar(region), region_phase(use), abort_flag, p.status)) break;
       tc_fence_after();
       if (acc < x.n_a) {
-        const uint32_t taddr0 = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                static_cast<uint32_t>((2 * buf + acc) * nt);
+        const uint32_t taddr0 =
+            tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc_column(rg, acc);
         const int blk = 2 * x.ob + acc;
         const int nchunks = (x.n_rows + 15) / 16;
         const int64_t ld = s->out_ld;
-        for (int c = 0; c < nchunks; ++c) {
+        for (int ch = 0; ch < nchunks; ++ch) {
           uint32_t v[16];
-          tmem_ld_x16(taddr0 + static_cast<uint32_t>(c * 16), v);
+          tmem_ld_x16(taddr0 + static_cast<uint32_t>(ch * 16), v);
           tmem_ld_wait();
-          const int tok0 = c * 16;
+          const int tok0 = ch * 16;
           if (p.mode == kModeSwiGLU) {
             const bool is_gate = lane < 16;
             const int f = blk * 64 + q * 16 + (lane & 15);
@@ -336,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                   if (s->row_scale) val *= __ldg(s->row_scale + row);
                   if (s->add) val += __bfloat162float(s->add[row * s->add_ld + o]);
                   if (s->out_f32)
-                    s->out_f32[row * ld + o] = val;
+                    s->out_f32[x.split * s->out_split_stride + row * ld + o] = val;
                   else
                     s->out[row * ld + o] = __float2bfloat16_rn(val);
                 }
@@ -347,14 +426,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(buf));
+      if (lane == 0) {
+        // a region holding one accumulator gets both arrivals from its 4 warps
+        mbar_arrive(tempty_bar(region));
+        if (rg.big) mbar_arrive(tempty_bar(region));
+      }
+      c += rg.big ? 2 : 1;
     }
   }
 
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, tmem_cols);
+    tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -481,20 +565,24 @@ CUresult encode_tmap_gate_up_5d(CUtensorMap* map, const void* base, int64_t grou
 }
 
 GemmPlan plan_gemm(int nt) {
+  // token ring: 3 stages (2 for 256-row tiles); weight ring: the rest
   GemmPlan g;
   g.nt = nt;
-  const size_t per_stage = kABytes + static_cast<size_t>(nt) * 128;
-  int st = static_cast<int>(kSmemBudget / per_stage);
-  if (st > kMaxStages) st = kMaxStages;
-  g.stages = st;
-  g.smem_bytes = 1024 + per_stage * st + 8 * (2 * st + 5) + 16;
+  const size_t b_stage = static_cast<size_t>(nt) * 128;
+  g.b_stages = nt >= 256 ? 2 : 3;
+  int sa = static_cast<int>((kSmemBudget - g.b_stages * b_stage) / kABytes);
+  if (sa > kMaxStages) sa = kMaxStages;
+  g.a_stages = sa;
+  g.smem_bytes = 1024 + kABytes * sa + b_stage * g.b_stages +
+                 8 * (2 * sa + 2 * g.b_stages + 5) + 16;
   return g;
 }
 
 cudaError_t launch_tc_gemm(const GemmParams& params, int num_sms, cudaStream_t stream) {
   const GemmPlan plan = plan_gemm(params.nt);
   GemmParams p = params;
-  p.stages = plan.stages;
+  p.a_stages = plan.a_stages;
+  p.b_stages = plan.b_stages;
   static int configured[64] = {0};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);

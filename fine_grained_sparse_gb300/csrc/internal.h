@@ -12,6 +12,8 @@ namespace fgs {
 struct RouterArgs {
   const void* x = nullptr;        // [T, d] (bf16 when x_bf16, else fp32)
   const float* logits = nullptr;  // [T, E]; when set the GEMM is skipped
+  int logit_parts = 1;            // logits = sum of this many [T, E] arrays
+  int64_t logit_part_stride = 0;  // elements between the parts
   const float* W_r = nullptr;     // [E, d]
   const float* bias = nullptr;    // [E]
   int64_t T = 0;
@@ -71,6 +73,9 @@ struct GemmSegment {
   int a_boxes;      // SwiGLU A tile: 1 = one 5-D box, 8 = eight 16-row boxes
   int a_rows;       // SwiGLU: F (row offset of the up half)
   int o_limit;      // store mode: columns o >= o_limit are not written
+  int ksplit;       // K split into ksplit equal parts (0 or 1: none); part j
+                    // writes out_f32 + j * out_split_stride (fp32 store only)
+  int64_t out_split_stride;
   // packed weights (one contiguous bulk copy per stage) instead of tmA
   const uint8_t* a_packed;
   int64_t a_group_bytes;
@@ -93,13 +98,14 @@ struct GemmParams {
   GemmSegment seg[2];
   int nseg;
   int mode;
-  int nt;      // token tile (MMA N upper bound): 32, 64 or 128
-  int stages;  // pipeline depth
+  int nt;        // token tile (MMA N upper bound): 32, 64, 128 or 256
+  int a_stages;  // weight ring depth
+  int b_stages;  // token ring depth
   int* status;
 };
 
 struct GemmPlan {
-  int nt, stages;
+  int nt, a_stages, b_stages;
   size_t smem_bytes;
 };
 GemmPlan plan_gemm(int nt);

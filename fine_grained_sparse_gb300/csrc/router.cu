@@ -9,13 +9,17 @@
 // renormalisation with + 1e-20 (only when K > 1 and norm_topk_prob) and the
 // final routed_scaling_factor.
 //
-// Design (GB300): one thread-block cluster per 64 tokens, one CTA per 128
-// experts (K2: 3 CTAs, K3: 7).  Each CTA runs the fp32 FFMA GEMM for its
-// 64 x 128 logit tile, keeps the tile in shared memory, and after a cluster
-// barrier every CTA selects for a share of the 64 tokens by reading the
-// whole 64 x E logit row set through distributed shared memory -- the logits
-// never touch HBM.  Selection is one warp per token: sigmoid + bias per lane,
-// group top-2 sums by warp shuffles, then K rounds of a warp arg-max.
+// Two ways to the logits:
+//  * bf16 x with a workspace: a tensor-core GEMM (gemm_tc.cu) against a
+//    three-way bf16 split of W_r, written as K-split partial sums that
+//    router_logits_kernel adds in a fixed order before it selects;
+//  * otherwise router_fused_kernel: one thread-block cluster per 64 tokens,
+//    one CTA per 128 experts (K2: 3 CTAs, K3: 7).  Each CTA runs the fp32 FFMA
+//    GEMM for its 64 x 128 logit tile, keeps the tile in shared memory, and
+//    after a cluster barrier every CTA selects for a share of the 64 tokens by
+//    reading the whole 64 x E logit row set through distributed shared memory.
+// Selection is one warp per token: sigmoid + bias per lane, group top-2 sums
+// by warp shuffles, then K rounds of a warp arg-max.
 #include <cooperative_groups.h>
 #include <math_constants.h>
 
@@ -46,6 +50,56 @@ __device__ __forceinline__ bool before(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
 
+// The selection decides on c = fp32(s + b) with s the correctly rounded fp32
+// sigmoid (computed in fp64 and rounded once).  Every value is first taken
+// from a fast fp32 sigmoid (relative error < 2^-20 for |z| <= 32); only the
+// experts whose fast value lies within kMargin of a decision threshold are
+// recomputed exactly.  Any expert left at its fast value is provably more
+// than kMargin - 2 * (fast error) below the exact threshold, so every decision
+// equals the one taken on exact values everywhere.
+constexpr float kMargin = 1.0f / 4096.0f;
+constexpr float kFastRange = 32.0f;  // beyond |z| > 32 the value is always exact
+
+__device__ __forceinline__ float exact_c(float z, float b) {
+  return __fadd_rn(static_cast<float>(sigmoid_f64(z)), b);
+}
+
+// Top-2 values over the warp of the lane-local pair (m1 >= m2).
+__device__ __forceinline__ void warp_top2(float& m1, float& m2) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float o1 = __shfl_xor_sync(0xffffffffu, m1, off);
+    const float o2 = __shfl_xor_sync(0xffffffffu, m2, off);
+    if (m1 >= o1) {
+      m2 = fmaxf(m2, o1);
+    } else {
+      m2 = fmaxf(m1, o2);
+      m1 = o1;
+    }
+  }
+}
+
+template <int PM>
+__device__ __forceinline__ void group_top2(const float (&c)[PM], int lane, int E, int gsize, int g,
+                                          float& m1, float& m2) {
+  m1 = -CUDART_INF_F;
+  m2 = -CUDART_INF_F;
+#pragma unroll
+  for (int j = 0; j < PM; ++j) {
+    const int e = lane + 32 * j;
+    if (e < E && e / gsize == g) {
+      const float v = c[j];
+      if (v > m1) {
+        m2 = m1;
+        m1 = v;
+      } else if (v > m2) {
+        m2 = v;
+      }
+    }
+  }
+  warp_top2(m1, m2);
+}
+
 // Selection for one token by one warp.  Lane `lane` holds the logits of
 // experts e = lane + 32 j, j < PM.  Writes topk_idx[0..K) and topk_w[0..K).
 template <int PM>
@@ -56,47 +110,46 @@ __device__ __forceinline__ void select_token(const float (&z)[PM], int lane, int
                                              float* __restrict__ out_w) {
   const unsigned full = 0xffffffffu;
   float c[PM];
+  float bj[PM];
+  unsigned exact = 0u;  // bit j: c[j] holds the exact value
 #pragma unroll
   for (int j = 0; j < PM; ++j) {
     const int e = lane + 32 * j;
     if (e < E) {
-      const float s = static_cast<float>(sigmoid_f64(z[j]));
-      c[j] = __fadd_rn(s, __ldg(bias + e));  // c = s + b, one fp32 rounding
+      bj[j] = __ldg(bias + e);
+      if (fabsf(z[j]) <= kFastRange) {
+        const float sf = __frcp_rn(1.0f + __expf(-z[j]));
+        c[j] = sf + bj[j];
+      } else {
+        c[j] = exact_c(z[j], bj[j]);
+        exact |= 1u << j;
+      }
     } else {
+      bj[j] = 0.0f;
       c[j] = -CUDART_INF_F;  // no such expert
+      exact |= 1u << j;
     }
   }
+  auto refine_above = [&](float threshold, int only_group, int gsize) {
+#pragma unroll
+    for (int j = 0; j < PM; ++j) {
+      const int e = lane + 32 * j;
+      if (!((exact >> j) & 1u) && c[j] >= threshold && (only_group < 0 || e / gsize == only_group)) {
+        c[j] = exact_c(z[j], bj[j]);
+        exact |= 1u << j;
+      }
+    }
+  };
 
   if (G > 1) {
     // group score = sum of the two largest biased scores in the group
     const int gsize = E / G;
     float my_gscore = -CUDART_INF_F;
     for (int g = 0; g < G; ++g) {
-      float m1 = -CUDART_INF_F, m2 = -CUDART_INF_F;
-#pragma unroll
-      for (int j = 0; j < PM; ++j) {
-        const int e = lane + 32 * j;
-        if (e < E && e / gsize == g) {
-          const float v = c[j];
-          if (v > m1) {
-            m2 = m1;
-            m1 = v;
-          } else if (v > m2) {
-            m2 = v;
-          }
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float o1 = __shfl_xor_sync(full, m1, off);
-        const float o2 = __shfl_xor_sync(full, m2, off);
-        if (m1 >= o1) {
-          m2 = fmaxf(m2, o1);
-        } else {
-          m2 = fmaxf(m1, o2);
-          m1 = o1;
-        }
-      }
+      float m1, m2;
+      group_top2(c, lane, E, gsize, g, m1, m2);
+      refine_above(m2 - kMargin, g, gsize);
+      group_top2(c, lane, E, gsize, g, m1, m2);
       if (lane == g) my_gscore = __fadd_rn(m1, m2);
     }
     // keep the Gk best groups (ties: smaller group index)
@@ -119,57 +172,75 @@ __device__ __forceinline__ void select_token(const float (&z)[PM], int lane, int
 #pragma unroll
     for (int j = 0; j < PM; ++j) {
       const int e = lane + 32 * j;
-      if (e < E && !((kept_mask >> (e / gsize)) & 1u)) c[j] = 0.0f;  // literal 0.0 fill
+      if (e < E && !((kept_mask >> (e / gsize)) & 1u)) {
+        c[j] = 0.0f;  // literal 0.0 fill
+        exact |= 1u << j;
+      }
     }
   }
 
   // K rounds of warp arg-max over the (masked) biased scores
-  unsigned taken = 0u;
-  int my_idx = 0;
-  double my_s = 0.0;
-  for (int k = 0; k < K; ++k) {
+  auto select_rounds = [&](bool final_pass, float& kth) {
+    unsigned taken = 0u;
+    int my_idx = 0;
+    double my_s = 0.0;
     float bv = -CUDART_INF_F;
-    int bi = 0x7fffffff;
-    float bz = 0.0f;
+    for (int k = 0; k < K; ++k) {
+      bv = -CUDART_INF_F;
+      int bi = 0x7fffffff;
+      float bz = 0.0f;
 #pragma unroll
-    for (int j = 0; j < PM; ++j) {
-      const int e = lane + 32 * j;
-      if (e < E && !((taken >> j) & 1u) && before(c[j], e, bv, bi)) {
-        bv = c[j];
-        bi = e;
-        bz = z[j];
+      for (int j = 0; j < PM; ++j) {
+        const int e = lane + 32 * j;
+        if (e < E && !((taken >> j) & 1u) && before(c[j], e, bv, bi)) {
+          bv = c[j];
+          bi = e;
+          bz = z[j];
+        }
+      }
+      const int mine = bi;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(full, bv, off);
+        const int oi = __shfl_xor_sync(full, bi, off);
+        if (before(ov, oi, bv, bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      const int owner = bi & 31;
+      double sv = 0.0;
+      if (lane == owner && mine == bi) {
+        taken |= 1u << (bi >> 5);
+        if (final_pass) sv = sigmoid_f64(bz);  // unbiased score of the winner
+      }
+      if (final_pass) {
+        sv = __shfl_sync(full, sv, owner);
+        if (lane == k) {
+          my_idx = bi;
+          my_s = sv;
+        }
       }
     }
-    const int mine = bi;
+    kth = bv;
+    if (!final_pass) return;
+    double sum = (lane < K) ? my_s : 0.0;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(full, bv, off);
-      const int oi = __shfl_xor_sync(full, bi, off);
-      if (before(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
-      }
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(full, sum, off);
+    if (lane < K) {
+      const double w = (K > 1 && norm) ? my_s / (sum + 1e-20) : my_s;
+      out_idx[lane] = my_idx;
+      out_w[lane] = static_cast<float>(w * static_cast<double>(scale));
     }
-    const int owner = bi & 31;
-    double s = 0.0;
-    if (lane == owner && mine == bi) {
-      taken |= 1u << (bi >> 5);
-      s = sigmoid_f64(bz);  // unbiased score of the winner
-    }
-    s = __shfl_sync(full, s, owner);
-    if (lane == k) {
-      my_idx = bi;
-      my_s = s;
-    }
+  };
+  float kth;
+  // pass 1 locates the K-th value; everything near or above it becomes exact
+  const unsigned all_slots = PM >= 32 ? 0xffffffffu : ((1u << PM) - 1u);
+  if (__any_sync(full, exact != all_slots)) {
+    select_rounds(false, kth);
+    refine_above(kth - kMargin, -1, 1);
   }
-  double sum = (lane < K) ? my_s : 0.0;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(full, sum, off);
-  if (lane < K) {
-    const double w = (K > 1 && norm) ? my_s / (sum + 1e-20) : my_s;
-    out_idx[lane] = my_idx;
-    out_w[lane] = static_cast<float>(w * static_cast<double>(scale));
-  }
+  select_rounds(true, kth);
 }
 
 template <typename XT>
@@ -322,10 +393,13 @@ __global__ void __launch_bounds__(kThreads) router_fused_kernel(
   cluster.sync();  // peers may still read this CTA's tile
 }
 
+// Logits given as `parts` partial arrays (a split reduction) are summed in
+// ascending part order, so the result does not depend on scheduling.
 template <int PM>
 __global__ void __launch_bounds__(256) router_logits_kernel(
-    const float* __restrict__ logits, const float* __restrict__ bias, int T, int E, int K, int G,
-    int Gk, float scale, int norm, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+    const float* __restrict__ logits, int parts, int64_t part_stride,
+    const float* __restrict__ bias, int T, int E, int K, int G, int Gk, float scale, int norm,
+    int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
   const int lane = threadIdx.x % 32;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
   if (t >= T) return;
@@ -333,7 +407,12 @@ __global__ void __launch_bounds__(256) router_logits_kernel(
 #pragma unroll
   for (int j = 0; j < PM; ++j) {
     const int e = lane + 32 * j;
-    z[j] = e < E ? __ldg(logits + t * E + e) : 0.0f;
+    float v = 0.0f;
+    if (e < E) {
+      v = __ldg(logits + t * E + e);
+      for (int q = 1; q < parts; ++q) v += __ldg(logits + q * part_stride + t * E + e);
+    }
+    z[j] = v;
   }
   select_token<PM>(z, lane, E, bias, K, G, Gk, scale, norm, topk_idx + t * K, topk_w + t * K);
 }
@@ -363,8 +442,8 @@ cudaError_t launch_logits(const RouterArgs& a, cudaStream_t stream) {
   const int warps = 8;
   const unsigned blocks = static_cast<unsigned>((a.T + warps - 1) / warps);
   router_logits_kernel<PM><<<blocks, warps * 32, 0, stream>>>(
-      a.logits, a.bias, static_cast<int>(a.T), a.E, a.K, a.G, a.Gk, a.scale, a.norm, a.topk_idx,
-      a.topk_w);
+      a.logits, a.logit_parts, a.logit_part_stride, a.bias, static_cast<int>(a.T), a.E, a.K, a.G,
+      a.Gk, a.scale, a.norm, a.topk_idx, a.topk_w);
   return cudaGetLastError();
 }
 
