@@ -6,6 +6,7 @@
 //   router -> dispatch -> grouped SwiGLU experts (+ shared experts)
 //          -> weighted combine (+ K3 latent projections)
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <cmath>
@@ -60,7 +61,16 @@ int router_tile(int64_t T) { return T <= 256 ? 32 : 128; }
 // token tile of the tensor-core GEMMs: small batches (few rows per expert)
 // take 32-row tiles and the deepest weight ring; large ones 256-row tiles,
 // so that most experts are one tile and their weights are read once
-int token_tile(int64_t T) { return T <= 256 ? 32 : 256; }
+int env_int(const char* name, int fallback) {
+  const char* v = getenv(name);
+  return (v && *v) ? atoi(v) : fallback;
+}
+
+int token_tile(int64_t T) {
+  static const int forced = env_int("FGS_TOKEN_TILE", 0);  // tuning override
+  if (forced == 32 || forced == 64 || forced == 128 || forced == 256) return forced;
+  return T <= 256 ? 32 : 256;
+}
 
 int32_t check_router_cfg(const moe_config* c, int64_t T) {
   if (!c) return fail(MOE_ERR_INVALID_ARG, "cfg is null");

@@ -40,6 +40,8 @@
 // MOE_ERR_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
 #include <cudaTypedefs.h>
 
+#include <stdlib.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -57,7 +59,8 @@ constexpr uint32_t kBBoxBytes = kBBoxRows * 128;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (3 + kEpiWarps);
 constexpr int kMaxStages = 8;
-constexpr size_t kSmemBudget = 221184;  // pipeline bytes per CTA (216 KB)
+constexpr size_t kSmemBudget = 229376;  // pipeline bytes per CTA (224 KB)
+constexpr int kSmemMax = 232448;        // the per-block limit (227 KB)
 
 struct Unit {
   int seg, group, b_row, out_row, n_rows, ob, n_a, ntiles;
@@ -569,9 +572,19 @@ GemmPlan plan_gemm(int nt) {
   GemmPlan g;
   g.nt = nt;
   const size_t b_stage = static_cast<size_t>(nt) * 128;
+  static const int forced_b = [] {  // tuning override of the token ring depth
+    const char* v = getenv("FGS_B_STAGES");
+    return (v && *v) ? atoi(v) : 0;
+  }();
   g.b_stages = nt >= 256 ? 2 : 3;
-  int sa = static_cast<int>((kSmemBudget - g.b_stages * b_stage) / kABytes);
+  if (forced_b >= 2 && forced_b <= 6) g.b_stages = forced_b;
+  const size_t b_bytes = g.b_stages * b_stage;
+  int sa = b_bytes < kSmemBudget ? static_cast<int>((kSmemBudget - b_bytes) / kABytes) : 0;
   if (sa > kMaxStages) sa = kMaxStages;
+  if (sa < 2) {  // keep at least two weight stages
+    sa = 2;
+    g.b_stages = static_cast<int>((kSmemBudget - 2 * kABytes) / b_stage);
+  }
   g.a_stages = sa;
   g.smem_bytes = 1024 + kABytes * sa + b_stage * g.b_stages +
                  8 * (2 * sa + 2 * g.b_stages + 5) + 16;
@@ -589,7 +602,7 @@ cudaError_t launch_tc_gemm(const GemmParams& params, int num_sms, cudaStream_t s
   if (err != cudaSuccess) return err;
   if (dev >= 64 || !configured[dev]) {
     err = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(kSmemBudget + 4096));
+                               kSmemMax);
     if (err != cudaSuccess) return err;
     if (dev < 64) configured[dev] = 1;
   }

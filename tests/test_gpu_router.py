@@ -25,17 +25,22 @@ def _logits(kind, T, E, gen):
     if kind == "ties":  # few distinct values: many exact ties, broken by index
         vals = torch.tensor([-1.0, -0.5, 0.0, 0.25, 0.5, 1.0])
         return vals[torch.randint(0, len(vals), (T, E), generator=gen)]
+    if kind == "crowded":  # scores packed within 1e-5: every fast value is near a threshold
+        return 0.3 + torch.rand((T, E), generator=gen) * 1e-5
+    if kind == "wide":  # logits beyond the fast range mixed with ordinary ones
+        return torch.randn((T, E), generator=gen) * 40.0
     raise ValueError(kind)
 
 
 @pytest.mark.parametrize("shape", ROUTER_SHAPES, ids=lambda s: "E%d_K%d_G%d_%d" % s)
-@pytest.mark.parametrize("kind", ["normal", "grid", "ties"])
+@pytest.mark.parametrize("kind", ["normal", "grid", "ties", "crowded", "wide"])
 @pytest.mark.parametrize("T", [1, 37, 1000])
 def test_router_from_logits_bit_exact(shape, kind, T):
     need_gpu()
     fgs = lib()
     E, K, G, Gk = shape
-    seed = E * 1000 + K * 10 + G + 7 * T + 100000 * ["normal", "grid", "ties"].index(kind)
+    seed = E * 1000 + K * 10 + G + 7 * T + 100000 * ["normal", "grid", "ties", "crowded",
+                                                      "wide"].index(kind)
     gen = torch.Generator().manual_seed(seed)
     z = _logits(kind, T, E, gen).float()
     b = torch.zeros(E) if kind != "normal" else (torch.rand(E, generator=gen) - 0.5) * 0.3
