@@ -66,10 +66,15 @@ int env_int(const char* name, int fallback) {
   return (v && *v) ? atoi(v) : fallback;
 }
 
-int token_tile(int64_t T) {
+// The gate/up pass (K = d, long) takes 256-row tiles: most experts are one
+// tile and their weights stream once.  The down pass (K = d_ff, short) takes
+// 128-row tiles, whose two accumulators share one TMEM region, so its
+// epilogue overlaps the next unit's main loop.
+int token_tile(int64_t T, bool down_pass = false) {
   static const int forced = env_int("FGS_TOKEN_TILE", 0);  // tuning override
-  if (forced == 32 || forced == 64 || forced == 128 || forced == 256) return forced;
-  return T <= 256 ? 32 : 256;
+  if (!down_pass && (forced == 32 || forced == 64 || forced == 128 || forced == 256)) return forced;
+  if (T <= 256) return 32;
+  return down_pass ? 128 : 256;
 }
 
 int32_t check_router_cfg(const moe_config* c, int64_t T) {
@@ -119,7 +124,8 @@ int32_t check_layer_cfg(const moe_config* c, int64_t T) {
 
 // Workspace regions, each 256-byte aligned, in this order.
 struct Layout {
-  size_t status, topk_idx, topk_w, counts, offsets, perm, inv, tiles, ntiles, w_perm, w_split,
+  size_t status, topk_idx, topk_w, counts, offsets, perm, inv, tiles, ntiles, tiles_down, w_perm,
+      w_split,
       logits, Xp, H, Hs, Y, U, Ysh, x_lat, r_lat, x_stage, y_stage, total;
 };
 
@@ -145,6 +151,7 @@ Layout layout(const moe_config* c, int64_t T) {
   L.inv = take(4 * TK);
   L.tiles = take(sizeof(RowTile) * tiles);
   L.ntiles = take(16);
+  L.tiles_down = take(sizeof(RowTile) * tiles);
   L.w_perm = take(4 * TK);
   L.w_split = take(c->dtype == MOE_BF16 ? 3ull * c->E_routed * c->d_model * 2 : 0);
   L.logits = take(c->dtype == MOE_BF16 && c->d_model % 64 == 0
@@ -265,8 +272,16 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
   const bool bf16 = c->dtype == MOE_BF16;
   const bool packed = c->weight_layout == MOE_WEIGHTS_PACKED;
   const int nt = bf16 ? token_tile(T) : kSimtTile;
+  const int nt_down = bf16 ? token_tile(T, true) : kSimtTile;
+  RowTile* tiles_down = tiles;
+  int* ntiles_down = ntiles;
 
   MOE_CUDA(launch_build_tiles(io.offsets, E, nt, tiles, ntiles, st));
+  if (nt_down != nt) {
+    tiles_down = at<RowTile>(ws, L.tiles_down);
+    ntiles_down = ntiles + 1;
+    MOE_CUDA(launch_build_tiles(io.offsets, E, nt_down, tiles_down, ntiles_down, st));
+  }
   MOE_CUDA(launch_gather(io.x_e, T, K, de, elem_bytes(c), io.perm, io.offsets, E, io.topk_w, Xp,
                          w_perm, st));
   if (ev_up) MOE_CUDA(cudaEventRecord(ev_up, st));
@@ -307,14 +322,15 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
 
     // down: routed rows scaled by their gate weight, shared rows unscaled
     p.mode = kModeStore;
+    p.nt = nt_down;
     GemmSegment& r2 = p.seg[0];
     clear(r2);
     if ((e = set_store_A(r2, io.W_down, E, de, F, packed)) != MOE_OK) return e;
     if ((e = set_B(r2, H, TK, F)) != MOE_OK) return e;
     r2.a128 = de / 128;
     r2.o_limit = de;
-    r2.tiles = tiles;
-    r2.ntiles = ntiles;
+    r2.tiles = tiles_down;
+    r2.ntiles = ntiles_down;
     r2.out = static_cast<__nv_bfloat16*>(io.Y);
     r2.out_ld = de;
     r2.row_scale = io.topk_w ? w_perm : nullptr;
