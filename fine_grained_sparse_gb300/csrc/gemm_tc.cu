@@ -568,7 +568,7 @@ CUresult encode_tmap_gate_up_5d(CUtensorMap* map, const void* base, int64_t grou
 }
 
 GemmPlan plan_gemm(int nt) {
-  // token ring: 3 stages (2 for 256-row tiles); weight ring: the rest
+  // token ring: 3 stages; weight ring: the rest of the budget (4-7 stages)
   GemmPlan g;
   g.nt = nt;
   const size_t b_stage = static_cast<size_t>(nt) * 128;
@@ -576,7 +576,7 @@ GemmPlan plan_gemm(int nt) {
     const char* v = getenv("FGS_B_STAGES");
     return (v && *v) ? atoi(v) : 0;
   }();
-  g.b_stages = nt >= 256 ? 2 : 3;
+  g.b_stages = 3;
   if (forced_b >= 2 && forced_b <= 6) g.b_stages = forced_b;
   const size_t b_bytes = g.b_stages * b_stage;
   int sa = b_bytes < kSmemBudget ? static_cast<int>((kSmemBudget - b_bytes) / kABytes) : 0;

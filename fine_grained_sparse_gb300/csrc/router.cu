@@ -40,7 +40,7 @@ constexpr int kThreads = 256;
 // s rounded once from the fp64 sigmoid of the fp32 logit: the correctly
 // rounded fp32 sigmoid except when the fp64 value lies within one fp64 ulp
 // of an fp32 rounding boundary.
-__device__ __forceinline__ double sigmoid_f64(float z) {
+__device__ __noinline__ double sigmoid_f64(float z) {
   return 1.0 / (1.0 + exp(-static_cast<double>(z)));
 }
 
@@ -51,16 +51,21 @@ __device__ __forceinline__ bool before(float va, int ia, float vb, int ib) {
 }
 
 // The selection decides on c = fp32(s + b) with s the correctly rounded fp32
-// sigmoid (computed in fp64 and rounded once).  Every value is first taken
-// from a fast fp32 sigmoid (relative error < 2^-20 for |z| <= 32); only the
-// experts whose fast value lies within kMargin of a decision threshold are
-// recomputed exactly.  Any expert left at its fast value is provably more
-// than kMargin - 2 * (fast error) below the exact threshold, so every decision
-// equals the one taken on exact values everywhere.
-constexpr float kMargin = 1.0f / 4096.0f;
-constexpr float kFastRange = 32.0f;  // beyond |z| > 32 the value is always exact
+// sigmoid (computed in fp64 and rounded once).  Each value is first taken
+// from an fp32 sigmoid, rcp_rn(1 + expf(-z)) with expf within 2 ulp, whose
+// distance to the exact c is below kFastErr.  A discrete decision taken on
+// these values is the exact decision whenever the two values it separates
+// are more than twice that apart; only when some decision is closer (a
+// near-tie) are the values around it recomputed exactly and the decision
+// taken again.  Either way the result equals the one taken on exact values.
+constexpr float kFastErr = 5e-7f;            // |fast c - exact c| bound (|z| <= kFastRange)
+constexpr float kMargin = 1.0f / 262144.0f;  // 3.8e-6 > 2 kFastErr
+constexpr float kGroupMargin = 1.0f / 131072.0f;  // group sums: 7.6e-6 > 2 (2 kFastErr + rounding)
+constexpr float kFastRange = 80.0f;           // beyond |z| > 80 the value is always exact
 
-__device__ __forceinline__ float exact_c(float z, float b) {
+// Out of line: the exact path is rare, and inlining its fp64 exponential at
+// every call site would cost registers on the common path.
+__device__ __noinline__ float exact_c(float z, float b) {
   return __fadd_rn(static_cast<float>(sigmoid_f64(z)), b);
 }
 
@@ -84,10 +89,11 @@ __device__ __forceinline__ void group_top2(const float (&c)[PM], int lane, int E
                                           float& m1, float& m2) {
   m1 = -CUDART_INF_F;
   m2 = -CUDART_INF_F;
+  const int lo = g * gsize, hi = lo + gsize;
 #pragma unroll
   for (int j = 0; j < PM; ++j) {
     const int e = lane + 32 * j;
-    if (e < E && e / gsize == g) {
+    if (e >= lo && e < hi && e < E) {
       const float v = c[j];
       if (v > m1) {
         m2 = m1;
@@ -100,6 +106,19 @@ __device__ __forceinline__ void group_top2(const float (&c)[PM], int lane, int E
   warp_top2(m1, m2);
 }
 
+// Warp arg-max of (value, index) in the selection order.
+__device__ __forceinline__ void warp_best(float& bv, int& bi) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+    if (before(ov, oi, bv, bi)) {
+      bv = ov;
+      bi = oi;
+    }
+  }
+}
+
 // Selection for one token by one warp.  Lane `lane` holds the logits of
 // experts e = lane + 32 j, j < PM.  Writes topk_idx[0..K) and topk_w[0..K).
 template <int PM>
@@ -110,32 +129,30 @@ __device__ __forceinline__ void select_token(const float (&z)[PM], int lane, int
                                              float* __restrict__ out_w) {
   const unsigned full = 0xffffffffu;
   float c[PM];
-  float bj[PM];
   unsigned exact = 0u;  // bit j: c[j] holds the exact value
 #pragma unroll
   for (int j = 0; j < PM; ++j) {
     const int e = lane + 32 * j;
     if (e < E) {
-      bj[j] = __ldg(bias + e);
+      const float b = __ldg(bias + e);
       if (fabsf(z[j]) <= kFastRange) {
-        const float sf = __frcp_rn(1.0f + __expf(-z[j]));
-        c[j] = sf + bj[j];
+        c[j] = __fadd_rn(__frcp_rn(1.0f + expf(-z[j])), b);
       } else {
-        c[j] = exact_c(z[j], bj[j]);
+        c[j] = exact_c(z[j], b);
         exact |= 1u << j;
       }
     } else {
-      bj[j] = 0.0f;
       c[j] = -CUDART_INF_F;  // no such expert
       exact |= 1u << j;
     }
   }
-  auto refine_above = [&](float threshold, int only_group, int gsize) {
+  // recompute exactly every value >= threshold (optionally of one group)
+  auto refine_above = [&](float threshold, int lo, int hi) {
 #pragma unroll
     for (int j = 0; j < PM; ++j) {
       const int e = lane + 32 * j;
-      if (!((exact >> j) & 1u) && c[j] >= threshold && (only_group < 0 || e / gsize == only_group)) {
-        c[j] = exact_c(z[j], bj[j]);
+      if (!((exact >> j) & 1u) && c[j] >= threshold && e >= lo && e < hi) {
+        c[j] = exact_c(z[j], __ldg(bias + e));
         exact |= 1u << j;
       }
     }
@@ -144,31 +161,46 @@ __device__ __forceinline__ void select_token(const float (&z)[PM], int lane, int
   if (G > 1) {
     // group score = sum of the two largest biased scores in the group
     const int gsize = E / G;
-    float my_gscore = -CUDART_INF_F;
-    for (int g = 0; g < G; ++g) {
-      float m1, m2;
-      group_top2(c, lane, E, gsize, g, m1, m2);
-      refine_above(m2 - kMargin, g, gsize);
-      group_top2(c, lane, E, gsize, g, m1, m2);
-      if (lane == g) my_gscore = __fadd_rn(m1, m2);
-    }
-    // keep the Gk best groups (ties: smaller group index)
-    bool kept = false;
-    for (int r = 0; r < Gk; ++r) {
-      float bv = (lane < G && !kept) ? my_gscore : -CUDART_INF_F;
-      int bi = (lane < G && !kept) ? lane : 0x7fffffff;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(full, bv, off);
-        const int oi = __shfl_xor_sync(full, bi, off);
-        if (before(ov, oi, bv, bi)) {
-          bv = ov;
-          bi = oi;
+    auto group_scores = [&]() {
+      float mine = -CUDART_INF_F;
+      for (int g = 0; g < G; ++g) {
+        float m1, m2;
+        group_top2(c, lane, E, gsize, g, m1, m2);
+        if (lane == g) mine = __fadd_rn(m1, m2);
+      }
+      return mine;
+    };
+    // keep the Gk best groups (ties: smaller group index); returns the
+    // margin between the last kept and the best dropped group
+    auto choose = [&](float score, unsigned& kept_mask) {
+      bool kept = false;
+      float last = 0.0f, next = -CUDART_INF_F;
+      for (int r = 0; r <= Gk && r < G; ++r) {
+        float bv = (lane < G && !kept) ? score : -CUDART_INF_F;
+        int bi = (lane < G && !kept) ? lane : 0x7fffffff;
+        warp_best(bv, bi);
+        if (r < Gk) {
+          if (lane == bi) kept = true;
+          last = bv;
+        } else {
+          next = bv;
         }
       }
-      if (lane == bi) kept = true;
+      kept_mask = __ballot_sync(full, kept);
+      return last - next;
+    };
+    unsigned kept_mask;
+    float gscore = group_scores();
+    if (choose(gscore, kept_mask) <= kGroupMargin) {
+      // near-tie between groups: make every possible top-2 member exact
+      for (int g = 0; g < G; ++g) {
+        float m1, m2;
+        group_top2(c, lane, E, gsize, g, m1, m2);
+        refine_above(m2 - kMargin, g * gsize, (g + 1) * gsize);
+      }
+      gscore = group_scores();
+      choose(gscore, kept_mask);
     }
-    const unsigned kept_mask = __ballot_sync(full, kept);
 #pragma unroll
     for (int j = 0; j < PM; ++j) {
       const int e = lane + 32 * j;
@@ -179,14 +211,15 @@ __device__ __forceinline__ void select_token(const float (&z)[PM], int lane, int
     }
   }
 
-  // K rounds of warp arg-max over the (masked) biased scores
-  auto select_rounds = [&](bool final_pass, float& kth) {
+  // K (+1 for the boundary) rounds of warp arg-max; lane k keeps the k-th
+  // winner's index, logit and value
+  int sel_idx = 0;
+  float sel_z = 0.0f, sel_v = -CUDART_INF_F;
+  auto rounds = [&]() {
     unsigned taken = 0u;
-    int my_idx = 0;
-    double my_s = 0.0;
-    float bv = -CUDART_INF_F;
-    for (int k = 0; k < K; ++k) {
-      bv = -CUDART_INF_F;
+    const int R = K < E ? K + 1 : K;
+    for (int k = 0; k < R; ++k) {
+      float bv = -CUDART_INF_F;
       int bi = 0x7fffffff;
       float bz = 0.0f;
 #pragma unroll
@@ -199,48 +232,36 @@ __device__ __forceinline__ void select_token(const float (&z)[PM], int lane, int
         }
       }
       const int mine = bi;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(full, bv, off);
-        const int oi = __shfl_xor_sync(full, bi, off);
-        if (before(ov, oi, bv, bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
+      warp_best(bv, bi);
       const int owner = bi & 31;
-      double sv = 0.0;
-      if (lane == owner && mine == bi) {
-        taken |= 1u << (bi >> 5);
-        if (final_pass) sv = sigmoid_f64(bz);  // unbiased score of the winner
+      if (lane == owner && mine == bi) taken |= 1u << (bi >> 5);
+      bz = __shfl_sync(full, bz, owner);
+      if (lane == k) {
+        sel_idx = bi;
+        sel_z = bz;
+        sel_v = bv;
       }
-      if (final_pass) {
-        sv = __shfl_sync(full, sv, owner);
-        if (lane == k) {
-          my_idx = bi;
-          my_s = sv;
-        }
-      }
-    }
-    kth = bv;
-    if (!final_pass) return;
-    double sum = (lane < K) ? my_s : 0.0;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(full, sum, off);
-    if (lane < K) {
-      const double w = (K > 1 && norm) ? my_s / (sum + 1e-20) : my_s;
-      out_idx[lane] = my_idx;
-      out_w[lane] = static_cast<float>(w * static_cast<double>(scale));
     }
   };
-  float kth;
-  // pass 1 locates the K-th value; everything near or above it becomes exact
-  const unsigned all_slots = PM >= 32 ? 0xffffffffu : ((1u << PM) - 1u);
-  if (__any_sync(full, exact != all_slots)) {
-    select_rounds(false, kth);
-    refine_above(kth - kMargin, -1, 1);
+  rounds();
+  // a near-tie among the K+1 best (order or boundary) -> exact values there
+  const float next_v = __shfl_down_sync(full, sel_v, 1);
+  const bool near = lane + 1 < (K < E ? K + 1 : K) && sel_v - next_v <= kMargin;
+  if (__any_sync(full, near)) {
+    const float floor_v = __shfl_sync(full, sel_v, K < E ? K : K - 1);
+    refine_above(floor_v - kMargin, 0, E);
+    rounds();
   }
-  select_rounds(true, kth);
+  // weights from the unbiased scores, in fp64, one lane per selected expert
+  const double sk = lane < K ? sigmoid_f64(sel_z) : 0.0;
+  double sum = sk;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(full, sum, off);
+  if (lane < K) {
+    const double w = (K > 1 && norm) ? sk / (sum + 1e-20) : sk;
+    out_idx[lane] = sel_idx;
+    out_w[lane] = static_cast<float>(w * static_cast<double>(scale));
+  }
 }
 
 template <typename XT>
