@@ -72,9 +72,19 @@ int env_int(const char* name, int fallback) {
 // epilogue overlaps the next unit's main loop.
 int token_tile(int64_t T, bool down_pass = false) {
   static const int forced = env_int("FGS_TOKEN_TILE", 0);  // tuning override
-  if (!down_pass && (forced == 32 || forced == 64 || forced == 128 || forced == 256)) return forced;
-  if (T <= 256) return 32;
-  return down_pass ? 128 : 256;
+  static const int forced_down = env_int("FGS_DOWN_TILE", 0);
+  const int f = down_pass ? forced_down : forced;
+  if (f == 32 || f == 64 || f == 128 || f == 256) return f;
+  return T <= 256 ? 32 : 256;
+}
+
+// Weight tiles per unit of the down pass: with 256-row token tiles, one
+// 128-row tile per unit keeps the unit's accumulator within one TMEM region
+// (double-buffered) and streams each expert's weights once.
+int down_a_per_unit(int nt_down) {
+  static const int forced = env_int("FGS_DOWN_A", 0);  // tuning override
+  if (forced == 1 || forced == 2) return forced;
+  return nt_down > 128 ? 1 : 2;
 }
 
 int32_t check_router_cfg(const moe_config* c, int64_t T) {
@@ -323,6 +333,7 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
     // down: routed rows scaled by their gate weight, shared rows unscaled
     p.mode = kModeStore;
     p.nt = nt_down;
+    p.a_per_unit = down_a_per_unit(nt_down);
     GemmSegment& r2 = p.seg[0];
     clear(r2);
     if ((e = set_store_A(r2, io.W_down, E, de, F, packed)) != MOE_OK) return e;

@@ -64,14 +64,20 @@ constexpr int kSmemMax = 232448;        // the per-block limit (227 KB)
 
 struct Unit {
   int seg, group, b_row, out_row, n_rows, ob, n_a, ntiles;
+  int blk0;    // first 128-row A tile of the unit along O
   int k0, k1;  // k steps [k0, k1) of this unit (all of K unless split)
   int split;
 };
 
 __device__ __forceinline__ int ksplit_of(const GemmSegment* s) { return s->ksplit > 1 ? s->ksplit : 1; }
 
-__device__ __forceinline__ int segment_units(const GemmSegment* s, int nt) {
-  const int ob = (s->a128 + 1) / 2;
+// output blocks of a segment: pairs of A tiles, or single tiles
+__device__ __forceinline__ int out_blocks(const GemmParams& p, const GemmSegment* s) {
+  return p.a_per_unit == 2 ? (s->a128 + 1) / 2 : s->a128;
+}
+
+__device__ __forceinline__ int segment_units(const GemmParams& p, const GemmSegment* s, int nt) {
+  const int ob = out_blocks(p, s);
   if (s->tiles) return *s->ntiles * ob;
   return s->groups * ((s->rows + nt - 1) / nt) * ob * ksplit_of(s);
 }
@@ -81,7 +87,7 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int unit
   x.seg = u >= units0 ? 1 : 0;
   int local = u - (x.seg ? units0 : 0);
   const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
-  const int OB = (s->a128 + 1) / 2;
+  const int OB = out_blocks(p, s);
   const int ns = ksplit_of(s);
   const int kps = s->k_steps / ns;
   x.split = 0;
@@ -115,7 +121,13 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int unit
     x.out_row = static_cast<int>(g * s->out_group_stride + t0);
     x.ntiles = tpg;
   }
-  x.n_a = min(2, s->a128 - 2 * x.ob);
+  if (p.a_per_unit == 2) {
+    x.blk0 = 2 * x.ob;
+    x.n_a = min(2, s->a128 - 2 * x.ob);
+  } else {
+    x.blk0 = x.ob;
+    x.n_a = 1;
+  }
   return x;
 }
 
@@ -138,15 +150,20 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int* s
 
 // TMEM: two regions of 256 columns.  A unit whose token tile fits in 128
 // columns keeps both accumulators in one region (columns 0 and 128 of it),
-// so consecutive small units alternate regions and the epilogue overlaps the
-// next main loop; a larger unit takes one region per accumulator.  Every
-// unit advances a region counter c by the regions it uses; region use c is
-// region c % 2 in its (c / 2)-th phase -- the same sequence in every role.
+// and a single-tile unit keeps its one accumulator (up to 256 columns) in one
+// region, so consecutive such units alternate regions and the epilogue
+// overlaps the next main loop; a two-tile unit with a larger token tile takes
+// one region per accumulator.  Every unit advances a region counter c by the
+// regions it uses; region use c is region c % 2 in its (c / 2)-th phase --
+// the same sequence in every role.
 struct Regions {
-  bool big;
-  int c;  // first region use of the unit
+  bool big;  // two accumulators of more than 128 columns: one region each
+  int c;     // first region use of the unit
 };
 
+__device__ __forceinline__ Regions regions_of(const GemmParams& p, uint32_t n, int c) {
+  return Regions{p.a_per_unit == 2 && n > 128, c};
+}
 __device__ __forceinline__ int region_of(const Regions& r, int acc) {
   return r.big ? ((r.c + acc) & 1) : (r.c & 1);
 }
@@ -164,7 +181,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   const int sb_n = p.b_stages;
   const int nt = p.nt;
   const uint32_t b_stage_bytes = static_cast<uint32_t>(nt) * 128u;
-  uint8_t* smem_b = smem + sa_n * kABytes;
+  const uint32_t a_stage_bytes = kATileBytes * static_cast<uint32_t>(p.a_per_unit);
+  uint8_t* smem_b = smem + sa_n * a_stage_bytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem_b + sb_n * b_stage_bytes);
   // bars: a_full[Sa] | a_empty[Sa] | b_full[Sb] | b_empty[Sb] | tfull[2] | tempty[2] | drain
   const int nbars = 2 * sa_n + 2 * sb_n + 5;
@@ -211,8 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int units0 = segment_units(&p.seg[0], nt);
-  const int units1 = p.nseg > 1 ? segment_units(&p.seg[1], nt) : 0;
+  const int units0 = segment_units(p, &p.seg[0], nt);
+  const int units1 = p.nseg > 1 ? segment_units(p, &p.seg[1], nt) : 0;
   const int total = units0 + units1;
 
   if (warp == 0 && lane == 0) {
@@ -238,17 +256,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         }
         const uint32_t fb = a_full(stage);
         mbar_arrive_expect_tx(fb, tx);
-        const uint32_t a_dst = a_base + stage * kABytes;
+        const uint32_t a_dst = a_base + stage * a_stage_bytes;
         const int kc = ks * kBK;
         if (s->a_packed) {
-          // packed weights: the unit's n_a tiles of this k step are adjacent
+          // packed weights: the tiles of a pair at one k step are adjacent
+          const int pair = x.blk0 >> 1;
+          const int in_pair = min(2, s->a128 - 2 * pair);
           const uint8_t* src = s->a_packed + x.group * s->a_group_bytes +
-                               (2ll * x.ob * s->k_steps + static_cast<int64_t>(ks) * x.n_a) *
+                               (2ll * pair * s->k_steps + static_cast<int64_t>(ks) * in_pair +
+                                (x.blk0 & 1)) *
                                    kATileBytes;
           bulk_load(a_dst, src, tx, fb, pol_w);
         } else {
           for (int a = 0; a < x.n_a; ++a) {
-            const int blk = 2 * x.ob + a;  // 128-row A tile index along O
+            const int blk = x.blk0 + a;  // 128-row A tile index along O
             const uint32_t dst = a_dst + a * kATileBytes;
             if (p.mode == kModeSwiGLU) {
               if (s->a_boxes == 1) {
@@ -321,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       const Unit x = decode_unit(p, u, units0, nt);
       const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
       const uint32_t n = static_cast<uint32_t>((x.n_rows + 15) & ~15);
-      const Regions rg = {n > 128, c};
+      const Regions rg = regions_of(p, n, c);
       bool ok = mbar_wait_bounded(tempty_bar(c & 1), region_phase(c) ^ 1u, abort_flag, p.status);
       if (ok && rg.big)
         ok = mbar_wait_bounded(tempty_bar((c + 1) & 1), region_phase(c + 1) ^ 1u, abort_flag,
@@ -338,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         tc_fence_after();
         const uint64_t bdesc = smem_desc_sw128(b_base + sb * b_stage_bytes);
         for (int a = 0; a < x.n_a; ++a) {
-          const uint64_t adesc = smem_desc_sw128(a_base + sa * kABytes + a * kATileBytes);
+          const uint64_t adesc = smem_desc_sw128(a_base + sa * a_stage_bytes + a * kATileBytes);
           const uint32_t d = tmem_base + acc_column(rg, a);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
@@ -365,13 +386,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   } else if (warp >= 3) {
     // ---------------------------------------------------------- epilogue
     const int q = warp & 3;           // TMEM lane quadrant this warp may access
-    const int acc = (warp - 3) >> 2;  // which of the unit's two accumulators
+    const int grp = (warp - 3) >> 2;  // warp group: accumulator (two-tile units)
+                                      // or column half (single-tile units)
     int c = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const Unit x = decode_unit(p, u, units0, nt);
       const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
       const uint32_t n = static_cast<uint32_t>((x.n_rows + 15) & ~15);
-      const Regions rg = {n > 128, c};
+      const Regions rg = regions_of(p, n, c);
+      const bool single = p.a_per_unit == 1;
+      const int acc = single ? 0 : grp;
       const int use = rg.big ? c + acc : c;
       const int region = region_of(rg, acc);
       if (!warp_wait(tfull_bar(region), region_phase(use), abort_flag, p.status)) break;
@@ -379,10 +403,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       if (acc < x.n_a) {
         const uint32_t taddr0 =
             tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc_column(rg, acc);
-        const int blk = 2 * x.ob + acc;
+        const int blk = x.blk0 + acc;
         const int nchunks = (x.n_rows + 15) / 16;
         const int64_t ld = s->out_ld;
-        for (int ch = 0; ch < nchunks; ++ch) {
+        // a single accumulator is split between the two warp groups
+        for (int ch = single ? grp : 0; ch < nchunks; ch += single ? 2 : 1) {
           uint32_t v[16];
           tmem_ld_x16(taddr0 + static_cast<uint32_t>(ch * 16), v);
           tmem_ld_wait();
@@ -430,7 +455,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        // a region holding one accumulator gets both arrivals from its 4 warps
+        // a region holding one accumulator of a two-tile unit gets both
+        // arrivals from its 4 warps
         mbar_arrive(tempty_bar(region));
         if (rg.big) mbar_arrive(tempty_bar(region));
       }
@@ -567,33 +593,35 @@ CUresult encode_tmap_gate_up_5d(CUtensorMap* map, const void* base, int64_t grou
   return encode(map, base, 5, dims, strides, box);
 }
 
-GemmPlan plan_gemm(int nt) {
-  // token ring: 3 stages; weight ring: the rest of the budget (4-7 stages)
-  GemmPlan g;
-  g.nt = nt;
-  const size_t b_stage = static_cast<size_t>(nt) * 128;
+GemmPlan plan_gemm(int nt, int a_per_unit) {
+  // token ring: 3 stages; weight ring: the rest of the budget
   static const int forced_b = [] {  // tuning override of the token ring depth
     const char* v = getenv("FGS_B_STAGES");
     return (v && *v) ? atoi(v) : 0;
   }();
+  GemmPlan g;
+  g.nt = nt;
+  const size_t b_stage = static_cast<size_t>(nt) * 128;
+  const size_t a_stage = static_cast<size_t>(kATileBytes) * a_per_unit;
   g.b_stages = 3;
   if (forced_b >= 2 && forced_b <= 6) g.b_stages = forced_b;
   const size_t b_bytes = g.b_stages * b_stage;
-  int sa = b_bytes < kSmemBudget ? static_cast<int>((kSmemBudget - b_bytes) / kABytes) : 0;
+  int sa = b_bytes < kSmemBudget ? static_cast<int>((kSmemBudget - b_bytes) / a_stage) : 0;
   if (sa > kMaxStages) sa = kMaxStages;
   if (sa < 2) {  // keep at least two weight stages
     sa = 2;
-    g.b_stages = static_cast<int>((kSmemBudget - 2 * kABytes) / b_stage);
+    g.b_stages = static_cast<int>((kSmemBudget - 2 * a_stage) / b_stage);
   }
   g.a_stages = sa;
-  g.smem_bytes = 1024 + kABytes * sa + b_stage * g.b_stages +
+  g.smem_bytes = 1024 + a_stage * sa + b_stage * g.b_stages +
                  8 * (2 * sa + 2 * g.b_stages + 5) + 16;
   return g;
 }
 
 cudaError_t launch_tc_gemm(const GemmParams& params, int num_sms, cudaStream_t stream) {
-  const GemmPlan plan = plan_gemm(params.nt);
+  const GemmPlan plan = plan_gemm(params.nt, params.a_per_unit == 1 ? 1 : 2);
   GemmParams p = params;
+  p.a_per_unit = params.a_per_unit == 1 ? 1 : 2;
   p.a_stages = plan.a_stages;
   p.b_stages = plan.b_stages;
   static int configured[64] = {0};

@@ -99,6 +99,7 @@ struct GemmParams {
   int nseg;
   int mode;
   int nt;        // token tile (MMA N upper bound): 32, 64, 128 or 256
+  int a_per_unit;  // 128-row weight tiles per unit: 2 (default) or 1
   int a_stages;  // weight ring depth
   int b_stages;  // token ring depth
   int* status;
@@ -108,7 +109,7 @@ struct GemmPlan {
   int nt, a_stages, b_stages;
   size_t smem_bytes;
 };
-GemmPlan plan_gemm(int nt);
+GemmPlan plan_gemm(int nt, int a_per_unit);
 
 cudaError_t launch_tc_gemm(const GemmParams& p, int num_sms, cudaStream_t stream);
 
