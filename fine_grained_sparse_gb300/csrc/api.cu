@@ -75,7 +75,8 @@ int token_tile(int64_t T, bool down_pass = false) {
   static const int forced_down = env_int("FGS_DOWN_TILE", 0);
   const int f = down_pass ? forced_down : forced;
   if (f == 32 || f == 64 || f == 128 || f == 256) return f;
-  return T <= 256 ? 32 : 256;
+  if (T <= 256) return 32;
+  return down_pass ? 128 : 256;
 }
 
 // Weight tiles per unit of the down pass: with 256-row token tiles, one
@@ -134,9 +135,11 @@ int32_t check_layer_cfg(const moe_config* c, int64_t T) {
 
 // Workspace regions, each 256-byte aligned, in this order.
 struct Layout {
-  size_t status, topk_idx, topk_w, counts, offsets, perm, inv, tiles, ntiles, tiles_down, w_perm,
-      w_split,
-      logits, Xp, H, Hs, Y, U, Ysh, x_lat, r_lat, x_stage, y_stage, total;
+  size_t status, topk_idx, topk_w, counts, offsets, poffsets, perm, inv, tiles, ntiles, tiles_down,
+      w_perm, w_split, logits, Xp, H, Hs, Y, U, Ysh, x_lat, r_lat, x_stage, y_stage, total;
+  int64_t plane_rows;    // packed activation planes of the routed rows
+  int64_t plane_rows_s;  // and of the shared experts' rows
+  int64_t Ts;            // shared-expert rows per group in the packed planes
 };
 
 Layout layout(const moe_config* c, int64_t T) {
@@ -157,6 +160,7 @@ Layout layout(const moe_config* c, int64_t T) {
   L.topk_w = take(4 * TK);
   L.counts = take(4 * static_cast<size_t>(c->E_routed));
   L.offsets = take(4 * static_cast<size_t>(c->E_routed + 1));
+  L.poffsets = take(4 * static_cast<size_t>(c->E_routed + 1));
   L.perm = take(4 * TK);
   L.inv = take(4 * TK);
   L.tiles = take(sizeof(RowTile) * tiles);
@@ -167,9 +171,18 @@ Layout layout(const moe_config* c, int64_t T) {
   L.logits = take(c->dtype == MOE_BF16 && c->d_model % 64 == 0
                       ? 4ull * router_ksplit(T, c->d_model) * T * c->E_routed
                       : 0);
-  L.Xp = take(static_cast<size_t>(TK) * de * eb);
-  L.H = take(static_cast<size_t>(TK) * c->d_ff * eb);
-  L.Hs = take(static_cast<size_t>(S) * T * c->d_ff_shared * eb);
+  // bf16: gathered rows and SwiGLU outputs in the packed activation layout
+  // (64-column planes of 128-byte rows, experts 8-row aligned); fp32: plain
+  L.Ts = (T + 7) & ~7ll;
+  L.plane_rows = packed_plane_rows(TK, c->E_routed);
+  L.plane_rows_s = packed_plane_rows(S * L.Ts, 0);
+  const bool pk = c->dtype == MOE_BF16;
+  L.Xp = take(pk ? static_cast<size_t>(de / 64) * L.plane_rows * 128
+                 : static_cast<size_t>(TK) * de * eb);
+  L.H = take(pk ? static_cast<size_t>(c->d_ff / 64) * L.plane_rows * 128
+                : static_cast<size_t>(TK) * c->d_ff * eb);
+  L.Hs = take(pk ? static_cast<size_t>(c->d_ff_shared / 64) * L.plane_rows_s * 128
+                 : static_cast<size_t>(S) * T * c->d_ff_shared * eb);
   L.Y = take(static_cast<size_t>(TK) * de * eb);
   // U and Ysh are adjacent (no padding: both are whole rows of d) so that
   // the final combine reads them as one strided list of addends
@@ -233,6 +246,13 @@ int32_t set_B(GemmSegment& s, const void* B, int64_t rows, int Kd) {
   return MOE_OK;
 }
 
+// Activations in the packed layout: one bulk copy per stage.
+void set_B_packed(GemmSegment& s, const void* B, int64_t plane_rows, int Kd) {
+  s.b_packed = static_cast<const uint8_t*>(B);
+  s.b_plane_rows = plane_rows;
+  s.k_steps = Kd / 64;
+}
+
 int32_t set_store_A(GemmSegment& s, const void* W, int groups, int O, int Kd, bool packed) {
   if (packed) {
     s.a_packed = static_cast<const uint8_t*>(W);
@@ -286,14 +306,20 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
   RowTile* tiles_down = tiles;
   int* ntiles_down = ntiles;
 
-  MOE_CUDA(launch_build_tiles(io.offsets, E, nt, tiles, ntiles, st));
+  int32_t* poffsets = at<int32_t>(ws, L.poffsets);
+  MOE_CUDA(launch_build_tiles(io.offsets, E, nt, tiles, ntiles, poffsets, st));
   if (nt_down != nt) {
     tiles_down = at<RowTile>(ws, L.tiles_down);
     ntiles_down = ntiles + 1;
-    MOE_CUDA(launch_build_tiles(io.offsets, E, nt_down, tiles_down, ntiles_down, st));
+    MOE_CUDA(launch_build_tiles(io.offsets, E, nt_down, tiles_down, ntiles_down, nullptr, st));
   }
-  MOE_CUDA(launch_gather(io.x_e, T, K, de, elem_bytes(c), io.perm, io.offsets, E, io.topk_w, Xp,
-                         w_perm, st));
+  if (bf16) {
+    MOE_CUDA(launch_gather_packed(io.x_e, K, de, io.perm, io.offsets, poffsets, E, io.topk_w, Xp,
+                                  L.plane_rows, w_perm, st));
+  } else {
+    MOE_CUDA(launch_gather(io.x_e, T, K, de, elem_bytes(c), io.perm, io.offsets, E, io.topk_w,
+                           Xp, w_perm, st));
+  }
   if (ev_up) MOE_CUDA(cudaEventRecord(ev_up, st));
 
   if (bf16) {
@@ -308,12 +334,13 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
     clear(r);
     int32_t e;
     if ((e = set_gate_up_A(r, io.W_gate_up, E, F, de, packed)) != MOE_OK) return e;
-    if ((e = set_B(r, Xp, TK, de)) != MOE_OK) return e;
+    set_B_packed(r, Xp, L.plane_rows, de);
     r.a128 = F / 64;
     r.tiles = tiles;
     r.ntiles = ntiles;
     r.out = static_cast<__nv_bfloat16*>(H);
-    r.out_ld = F;
+    r.out_packed = 1;
+    r.out_plane_rows = L.plane_rows;
     if (S) {
       GemmSegment& s = p.seg[1];
       clear(s);
@@ -323,9 +350,10 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
       s.groups = S;
       s.rows = static_cast<int>(T);
       s.b_group_stride = 0;
-      s.out_group_stride = T;
+      s.out_group_stride = L.Ts;
       s.out = static_cast<__nv_bfloat16*>(Hs);
-      s.out_ld = Fs;
+      s.out_packed = 1;
+      s.out_plane_rows = L.plane_rows_s;
     }
     MOE_CUDA(launch_tc_gemm(p, num_sms(), st));
     if (ev_down) MOE_CUDA(cudaEventRecord(ev_down, st));
@@ -337,7 +365,7 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
     GemmSegment& r2 = p.seg[0];
     clear(r2);
     if ((e = set_store_A(r2, io.W_down, E, de, F, packed)) != MOE_OK) return e;
-    if ((e = set_B(r2, H, TK, F)) != MOE_OK) return e;
+    set_B_packed(r2, H, L.plane_rows, F);
     r2.a128 = de / 128;
     r2.o_limit = de;
     r2.tiles = tiles_down;
@@ -349,12 +377,12 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
       GemmSegment& s2 = p.seg[1];
       clear(s2);
       if ((e = set_store_A(s2, io.Ws_down, S, d, Fs, packed)) != MOE_OK) return e;
-      if ((e = set_B(s2, Hs, S * T, Fs)) != MOE_OK) return e;
+      set_B_packed(s2, Hs, L.plane_rows_s, Fs);
       s2.a128 = d / 128;
       s2.o_limit = d;
       s2.groups = S;
       s2.rows = static_cast<int>(T);
-      s2.b_group_stride = T;
+      s2.b_group_stride = L.Ts;
       s2.out_group_stride = T;
       s2.out = static_cast<__nv_bfloat16*>(io.Y_shared);
       s2.out_ld = d;

@@ -99,24 +99,40 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
 __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __restrict__ offsets,
                                                            int E, int nt,
                                                            RowTile* __restrict__ tiles,
-                                                           int* __restrict__ ntiles) {
+                                                           int* __restrict__ ntiles,
+                                                           int32_t* __restrict__ poffsets) {
   __shared__ int scan[1024];
+  __shared__ int pscan[1024];
   const int e = threadIdx.x;
   const int m = e < E ? offsets[e + 1] - offsets[e] : 0;
-  const int nti = (m + nt - 1) / nt;
+  // tile height: a multiple of 8, at most nt, tiles as even as that allows
+  int per = 0, nti = 0;
+  if (m > 0) {
+    const int n0 = (m + nt - 1) / nt;
+    per = (((m + n0 - 1) / n0) + 7) & ~7;
+    if (per > nt) per = nt;
+    nti = (m + per - 1) / per;
+  }
   scan[e] = nti;
+  pscan[e] = (m + 7) & ~7;
   __syncthreads();
-  // inclusive Hillis-Steele scan over 1024 entries
+  // inclusive Hillis-Steele scans over 1024 entries
   for (int off = 1; off < 1024; off <<= 1) {
     const int v = e >= off ? scan[e - off] : 0;
+    const int pv = e >= off ? pscan[e - off] : 0;
     __syncthreads();
     scan[e] += v;
+    pscan[e] += pv;
     __syncthreads();
   }
   const int first = scan[e] - nti;
+  const int pfirst = pscan[e] - ((m + 7) & ~7);
   if (e == 1023) *ntiles = scan[1023];
+  if (poffsets && e < E) {
+    poffsets[e] = pfirst;
+    if (e == E - 1) poffsets[E] = pscan[e];
+  }
   if (nti == 0) return;
-  const int per = (m + nti - 1) / nti;
   const int row0 = offsets[e];
   for (int i = 0; i < nti; ++i) {
     const int start = i * per;
@@ -126,8 +142,40 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __rest
     t.n_rows = min(per, m - start);
     t.first_tile = first;
     t.ntiles = nti;
-    t.pad0 = t.pad1 = t.pad2 = 0;
+    t.prow = pfirst + start;
+    t.pad0 = t.pad1 = 0;
     tiles[first + i] = t;
+  }
+}
+
+// Packed gather: one warp per slot row.  Row r of expert e (found by binary
+// search in offsets) goes to padded row R = poffsets[e] + (r - offsets[e]);
+// its 16-byte chunk v (columns 8v..8v+7) to plane v / 8 at chunk position
+// (v % 8) XOR (R % 8) -- the 128-byte swizzle the tensor cores read.
+__global__ void __launch_bounds__(256) gather_packed_kernel(
+    const uint4* __restrict__ x, int K, int vec_per_row, const int32_t* __restrict__ perm,
+    const int32_t* __restrict__ offsets, const int32_t* __restrict__ poffsets, int E,
+    const float* __restrict__ topk_w, uint4* __restrict__ Xp, int64_t plane_rows,
+    float* __restrict__ w_perm) {
+  const int rows = offsets[E];
+  const int lane = threadIdx.x & 31;
+  const int64_t warp_global = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t r = warp_global; r < rows; r += nwarps) {
+    int lo = 0, hi = E;  // offsets[lo] <= r < offsets[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(offsets + mid) <= r) lo = mid; else hi = mid;
+    }
+    const int64_t R = __ldg(poffsets + lo) + (r - __ldg(offsets + lo));
+    const int j = __ldg(perm + r);
+    const uint4* src = x + static_cast<int64_t>(j / K) * vec_per_row;
+    const int sw = static_cast<int>(R & 7);
+    for (int v = lane; v < vec_per_row; v += 32) {
+      const int64_t plane = v >> 3;
+      Xp[(plane * plane_rows + R) * 8 + ((v & 7) ^ sw)] = __ldg(src + v);
+    }
+    if (lane == 0 && w_perm) w_perm[r] = topk_w ? __ldg(topk_w + j) : 1.0f;
   }
 }
 
@@ -244,8 +292,21 @@ cudaError_t launch_permute(const int32_t* topk_idx, int64_t T, int K, int E, int
 int64_t max_tiles(int64_t rows, int E, int nt) { return rows / nt + E; }
 
 cudaError_t launch_build_tiles(const int32_t* offsets, int E, int nt, RowTile* tiles, int* ntiles,
-                               cudaStream_t stream) {
-  build_tiles_kernel<<<1, 1024, 0, stream>>>(offsets, E, nt, tiles, ntiles);
+                               int32_t* poffsets, cudaStream_t stream) {
+  build_tiles_kernel<<<1, 1024, 0, stream>>>(offsets, E, nt, tiles, ntiles, poffsets);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_packed(const void* x, int K, int width, const int32_t* perm,
+                                 const int32_t* offsets, const int32_t* poffsets, int E,
+                                 const float* topk_w, void* Xp, int64_t plane_rows,
+                                 float* w_perm, cudaStream_t stream) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  gather_packed_kernel<<<sms * 8, 256, 0, stream>>>(
+      static_cast<const uint4*>(x), K, width / 8, perm, offsets, poffsets, E, topk_w,
+      static_cast<uint4*>(Xp), plane_rows, w_perm);
   return cudaGetLastError();
 }
 

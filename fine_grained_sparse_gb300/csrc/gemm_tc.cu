@@ -105,8 +105,9 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int unit
     x.ob = r / any.ntiles;
     const RowTile& t = s->tiles[any.first_tile + (r - x.ob * any.ntiles)];
     x.group = t.expert;
-    x.b_row = t.row_start;
-    x.out_row = t.row_start;
+    // packed activations live in the padded row space
+    x.b_row = s->b_packed ? t.prow : t.row_start;
+    x.out_row = s->out_packed ? t.prow : t.row_start;
     x.n_rows = t.n_rows;
     x.ntiles = any.ntiles;
   } else {
@@ -298,7 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                  p.status);
   } else if (warp == 2 && lane == 0) {
     // ------------------------------------------------- token (B) producer
-    for (int s = 0; s < p.nseg; ++s) prefetch_tensormap(&p.seg[s].tmB);
+    for (int s = 0; s < p.nseg; ++s)
+      if (!p.seg[s].b_packed) prefetch_tensormap(&p.seg[s].tmB);
     const uint64_t pol_keep = l2_policy_evict_last();
     int stage = 0;
     uint32_t phase = 0;
@@ -307,7 +309,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       const Unit x = decode_unit(p, u, units0, nt);
       const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
       const int nbox = (x.n_rows + kBBoxRows - 1) / kBBoxRows;
-      const uint32_t tx = static_cast<uint32_t>(nbox) * kBBoxBytes;
+      // packed: the tile's rows (rounded up to 16) are one contiguous run
+      const uint32_t tx = s->b_packed ? static_cast<uint32_t>((x.n_rows + 15) & ~15) * 128u
+                                      : static_cast<uint32_t>(nbox) * kBBoxBytes;
       bool ok = true;
       for (int ks = x.k0; ks < x.k1; ++ks) {
         if (!mbar_wait_bounded(b_empty(stage), phase ^ 1u, abort_flag, p.status)) {
@@ -317,10 +321,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         const uint32_t fb = b_full(stage);
         mbar_arrive_expect_tx(fb, tx);
         const uint32_t b_dst = b_base + stage * b_stage_bytes;
-        const int kb = s->b_k_period ? (ks % s->b_k_period) * kBK : ks * kBK;
-        for (int bx = 0; bx < nbox; ++bx)
-          tma_load_2d(b_dst + bx * kBBoxBytes, &s->tmB, fb, kb, x.b_row + bx * kBBoxRows,
-                      pol_keep);
+        const int kstep = s->b_k_period ? ks % s->b_k_period : ks;
+        if (s->b_packed) {
+          const uint8_t* src =
+              s->b_packed + (static_cast<int64_t>(kstep) * s->b_plane_rows + x.b_row) * 128;
+          bulk_load(b_dst, src, tx, fb, pol_keep);
+        } else {
+          for (int bx = 0; bx < nbox; ++bx)
+            tma_load_2d(b_dst + bx * kBBoxBytes, &s->tmB, fb, kstep * kBK,
+                        x.b_row + bx * kBBoxRows, pol_keep);
+        }
         ++issued;
         if (++stage == sb_n) {
           stage = 0;
@@ -428,8 +438,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             for (int jj = 0; jj < 8; ++jj) {
               const int tok = tok0 + (is_gate ? jj : 8 + jj);
               const float val = is_gate ? h[jj] : h[8 + jj];
-              if (tok < x.n_rows)
-                s->out[static_cast<int64_t>(x.out_row + tok) * ld + f] = __float2bfloat16_rn(val);
+              if (tok < x.n_rows) {
+                const int64_t row = x.out_row + tok;
+                int64_t off;
+                if (s->out_packed) {  // plane f/64, chunk (f%64)/8 swizzled by row%8
+                  off = (((f >> 6) * s->out_plane_rows + row) << 6) +
+                        ((((f & 63) >> 3) ^ static_cast<int>(row & 7)) << 3) + (f & 7);
+                } else {
+                  off = row * ld + f;
+                }
+                s->out[off] = __float2bfloat16_rn(val);
+              }
             }
           } else {
             const int o = blk * 128 + q * 32 + lane;

@@ -32,7 +32,9 @@ cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream);
 // [first_tile, first_tile + ntiles) of the table.
 struct __align__(16) RowTile {
   int expert, row_start, n_rows, first_tile;
-  int ntiles, pad0, pad1, pad2;
+  int ntiles;
+  int prow;  // first row in the padded (8-row aligned per expert) row space
+  int pad0, pad1;
 };
 
 cudaError_t launch_permute(const int32_t* topk_idx, int64_t T, int K, int E, int32_t* counts,
@@ -40,10 +42,23 @@ cudaError_t launch_permute(const int32_t* topk_idx, int64_t T, int K, int E, int
                            cudaStream_t stream);
 
 // Row tiles of the routed experts: for expert e with m_e rows starting at
-// offsets[e], ceil(m_e / nt) tiles of near-equal height; *ntiles receives
-// the count.
+// offsets[e], tiles of near-equal height (multiples of 8 but the last) and at
+// most nt rows; *ntiles receives the count.  poffsets (E+1 entries, may be
+// null) receives the padded offsets: expert e's rows start at poffsets[e] in
+// a row space where every expert begins on a multiple of 8.
 cudaError_t launch_build_tiles(const int32_t* offsets, int E, int nt, RowTile* tiles, int* ntiles,
-                               cudaStream_t stream);
+                               int32_t* poffsets, cudaStream_t stream);
+
+// Padded rows of the packed activation planes: T*K rows, up to 7 padding
+// rows per expert, 32 rows of slack for whole-16-row reads.
+inline int64_t packed_plane_rows(int64_t rows, int groups) { return rows + 8ll * groups + 32; }
+
+// Xp in the packed activation layout: plane p (columns 64p..64p+63) holds
+// one 128-byte row per padded row, its 16-byte chunks swizzled by (row % 8).
+cudaError_t launch_gather_packed(const void* x, int K, int width, const int32_t* perm,
+                                 const int32_t* offsets, const int32_t* poffsets, int E,
+                                 const float* topk_w, void* Xp, int64_t plane_rows,
+                                 float* w_perm, cudaStream_t stream);
 int64_t max_tiles(int64_t rows, int E, int nt);
 
 // Xp[r] = x[perm[r] / K] and w_perm[r] = topk_w[perm[r]] (1 if topk_w null)
@@ -92,6 +107,13 @@ struct GemmSegment {
   const float* row_scale;    // store mode: per output row, may be null
   const __nv_bfloat16* add;  // store mode: added to the output, may be null
   int64_t add_ld;
+  // packed activations (see launch_gather_packed): B read by one bulk copy
+  // per stage from b_packed, and/or the SwiGLU output written to `out` in
+  // that layout (plane rows out_plane_rows)
+  const uint8_t* b_packed;
+  int64_t b_plane_rows;
+  int out_packed;
+  int64_t out_plane_rows;
 };
 
 struct GemmParams {
