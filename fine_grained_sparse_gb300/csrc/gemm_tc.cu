@@ -398,13 +398,24 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     const int q = warp & 3;           // TMEM lane quadrant this warp may access
     const int grp = (warp - 3) >> 2;  // warp group: accumulator (two-tile units)
                                       // or column half (single-tile units)
+    const bool swiglu = p.mode == kModeSwiGLU;
+    const bool single = p.a_per_unit == 1;
     int c = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const Unit x = decode_unit(p, u, units0, nt);
       const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
+      // the segment's output description, once per unit, in registers
+      __nv_bfloat16* const out = s->out;
+      float* const out_f32 = s->out_f32 ? s->out_f32 + x.split * s->out_split_stride : nullptr;
+      const int64_t ld = s->out_ld;
+      const float* const row_scale = s->row_scale;
+      const __nv_bfloat16* const add = s->add;
+      const int64_t add_ld = s->add_ld;
+      const bool out_packed = s->out_packed != 0;
+      const int64_t plane_rows = s->out_plane_rows;
+      const int o_limit = s->o_limit;
       const uint32_t n = static_cast<uint32_t>((x.n_rows + 15) & ~15);
       const Regions rg = regions_of(p, n, c);
-      const bool single = p.a_per_unit == 1;
       const int acc = single ? 0 : grp;
       const int use = rg.big ? c + acc : c;
       const int region = region_of(rg, acc);
@@ -415,14 +426,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc_column(rg, acc);
         const int blk = x.blk0 + acc;
         const int nchunks = (x.n_rows + 15) / 16;
-        const int64_t ld = s->out_ld;
         // a single accumulator is split between the two warp groups
-        for (int ch = single ? grp : 0; ch < nchunks; ch += single ? 2 : 1) {
+        const int step = single ? 2 : 1;
+        int ch = single ? grp : 0;
+        uint32_t nxt[16];
+        if (ch < nchunks) tmem_ld_x16(taddr0 + static_cast<uint32_t>(ch * 16), nxt);
+        for (; ch < nchunks; ch += step) {
           uint32_t v[16];
-          tmem_ld_x16(taddr0 + static_cast<uint32_t>(ch * 16), v);
-          tmem_ld_wait();
+          tmem_ld_wait(nxt);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = nxt[j];
+          // the next chunk's TMEM load overlaps this chunk's math and stores
+          if (ch + step < nchunks) tmem_ld_x16(taddr0 + static_cast<uint32_t>((ch + step) * 16), nxt);
           const int tok0 = ch * 16;
-          if (p.mode == kModeSwiGLU) {
+          if (swiglu) {
             const bool is_gate = lane < 16;
             const int f = blk * 64 + q * 16 + (lane & 15);
             float h[16];
@@ -434,37 +451,37 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
               const float up = is_gate ? other : mine;
               h[j] = silu_f(g) * up;
             }
+            // packed: plane f/64, chunk (f%64)/8 swizzled by row%8
+            const int64_t f_plane = static_cast<int64_t>(f >> 6) * plane_rows;
+            const int f_chunk = (f & 63) >> 3, f_lo = f & 7;
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) {
               const int tok = tok0 + (is_gate ? jj : 8 + jj);
               const float val = is_gate ? h[jj] : h[8 + jj];
               if (tok < x.n_rows) {
                 const int64_t row = x.out_row + tok;
-                int64_t off;
-                if (s->out_packed) {  // plane f/64, chunk (f%64)/8 swizzled by row%8
-                  off = (((f >> 6) * s->out_plane_rows + row) << 6) +
-                        ((((f & 63) >> 3) ^ static_cast<int>(row & 7)) << 3) + (f & 7);
-                } else {
-                  off = row * ld + f;
-                }
-                s->out[off] = __float2bfloat16_rn(val);
+                const int64_t off =
+                    out_packed ? (((f_plane + row) << 6) +
+                                  ((f_chunk ^ static_cast<int>(row & 7)) << 3) + f_lo)
+                               : row * ld + f;
+                out[off] = __float2bfloat16_rn(val);
               }
             }
           } else {
             const int o = blk * 128 + q * 32 + lane;
-            if (o < s->o_limit) {
+            if (o < o_limit) {
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
                 const int tok = tok0 + j;
                 if (tok < x.n_rows) {
                   const int64_t row = x.out_row + tok;
                   float val = __uint_as_float(v[j]);
-                  if (s->row_scale) val *= __ldg(s->row_scale + row);
-                  if (s->add) val += __bfloat162float(s->add[row * s->add_ld + o]);
-                  if (s->out_f32)
-                    s->out_f32[x.split * s->out_split_stride + row * ld + o] = val;
+                  if (row_scale) val *= __ldg(row_scale + row);
+                  if (add) val += __bfloat162float(add[row * add_ld + o]);
+                  if (out_f32)
+                    out_f32[row * ld + o] = val;
                   else
-                    s->out[row * ld + o] = __float2bfloat16_rn(val);
+                    out[row * ld + o] = __float2bfloat16_rn(val);
                 }
               }
             }
