@@ -24,6 +24,7 @@ __all__ = [
     "moe_get_device_status", "moe_router", "moe_router_from_logits", "moe_permute",
     "moe_grouped_swiglu", "moe_combine", "moe_linear", "moe_layer_forward",
     "moe_layer_forward_host", "moe_last_error_detail", "moe_pack_weights", "pack_layer_weights",
+    "moe_router_noalloc",
     "MOE_WEIGHTS_NATURAL", "MOE_WEIGHTS_PACKED", "MOE_PACK_GATE_UP", "MOE_PACK_PLAIN",
 ]
 
@@ -81,6 +82,7 @@ _SIGS = {
     "moe_combine": ([_CFG, _I64, _P, _P, _P, _P, _P], _I32),
     "moe_linear": ([_I64, _I32, _I32, _P, _P, _P, _P, _P, _SZ, _P], _I32),
     "moe_pack_weights": ([_I32, _I64, _I64, _I64, _P, _P, _P], _I32),
+    "moe_router_noalloc": ([_CFG, _I64, _P, _P, _P, _P, _P, _P], _I32),
     "moe_layer_forward": ([_CFG, _I64] + [_P] * 14 + [_SZ, _P, _P], _I32),
     "moe_layer_forward_host": ([_CFG, _I64] + [_P] * 11 + [_SZ, _P], _I32),
 }
@@ -157,6 +159,13 @@ def moe_get_device_status(workspace, stream=None) -> int:
 def moe_router(cfg, T, x, W_r, bias, topk_idx, topk_w, workspace=None, ws_bytes=0, stream=None):
     _check(lib.moe_router(ctypes.byref(cfg), T, _ptr(x), _ptr(W_r), _ptr(bias), _ptr(topk_idx),
                           _ptr(topk_w), _ptr(workspace), ws_bytes, _stream(stream)), "moe_router")
+
+
+def moe_router_noalloc(cfg, T, x, W_r, bias, topk_idx, topk_w, stream=None):
+    """moe_router on the library's static device scratch (no workspace)."""
+    _check(lib.moe_router_noalloc(ctypes.byref(cfg), T, _ptr(x), _ptr(W_r), _ptr(bias),
+                                  _ptr(topk_idx), _ptr(topk_w), _stream(stream)),
+           "moe_router_noalloc")
 
 
 def moe_router_from_logits(cfg, T, logits, bias, topk_idx, topk_w, stream=None):

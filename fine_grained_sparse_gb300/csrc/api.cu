@@ -477,6 +477,38 @@ int32_t run_linear(int64_t T, int in_f, int out_f, const void* x, const void* W,
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// Fixed scratch for moe_router_noalloc: some callers may not allocate device
+// memory at the moment they route tokens, so this one entry point takes its
+// scratch from a statically sized device array that exists for as long as
+// the library is loaded on a device.
+constexpr size_t kNoAllocScratchBytes = 64ull << 20;  // 64 MiB per device
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[64] = {nullptr};
+
+// Device address of g_noalloc_scratch for the current device, looked up once
+// per device.  In host code the array's name is only a stand-in for the
+// device object, so kernels must be given this address instead.
+int32_t noalloc_scratch(void** out) {
+  int dev = 0;
+  MOE_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return fail(MOE_ERR_CUDA, "device ordinal beyond 63");
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    MOE_CUDA(cudaGetSymbolAddress(&p, g_noalloc_scratch));
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 int32_t moe_version(void) { return 100; }
@@ -774,6 +806,79 @@ int32_t moe_layer_forward_host(const moe_config* cfg, int64_t T, const void* x_h
                          nullptr, stream);
   if (st != MOE_OK) return st;
   MOE_CUDA(cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s));
+  return MOE_OK;
+}
+
+int32_t moe_router_noalloc(const moe_config* cfg, int64_t T, const void* x, const float* W_r,
+                           const float* bias, int32_t* topk_idx, float* topk_w, void* stream) {
+  int32_t st = check_router_cfg(cfg, T);
+  if (st != MOE_OK) return st;
+  if (cfg->dtype != MOE_BF16 || cfg->d_model % 64)
+    return fail(MOE_ERR_UNSUPPORTED_SHAPE, "moe_router_noalloc needs bf16 x and d_model % 64 == 0");
+  if (!x || !W_r || !bias || !topk_idx || !topk_w) return fail(MOE_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(x) || !aligned16(W_r) || !aligned16(bias) || !aligned16(topk_idx) ||
+      !aligned16(topk_w))
+    return fail(MOE_ERR_ALIGNMENT, "pointer not 16-byte aligned");
+  const int d = cfg->d_model, E = cfg->E_routed;
+  const int ksplit = router_ksplit(T, d);
+  // scratch: status word | split router weight | partial logits
+  const size_t split_off = kWsHeader;
+  const size_t logits_off = split_off + round256(3ull * E * d * 2);
+  const size_t need = logits_off + round256(4ull * ksplit * T * E);
+  if (need > kNoAllocScratchBytes) {
+    snprintf(g_detail, sizeof(g_detail),
+             "moe_router_noalloc needs %zu bytes of scratch; its static scratch holds %zu",
+             need, kNoAllocScratchBytes);
+    return MOE_ERR_WORKSPACE;
+  }
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != MOE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* status = at<int>(scratch, 0);
+  __nv_bfloat16* w_split = at<__nv_bfloat16>(scratch, split_off);
+  float* logits = at<float>(scratch, logits_off);
+  // the array keeps the previous call's contents: only the status word must
+  // start at zero (the split weight and every partial logit are rewritten)
+  MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int), s));
+  MOE_CUDA(launch_split_router_weight(W_r, E, d, w_split, s));
+  GemmParams p;
+  memset(&p, 0, sizeof(p));
+  p.mode = kModeStore;
+  p.nt = router_tile(T);
+  p.status = status;
+  p.nseg = 1;
+  GemmSegment& g = p.seg[0];
+  clear(g);
+  if (encode_tmap_weights_3d(&g.tmA, w_split, 1, E, 3ll * d, 128) != CUDA_SUCCESS)
+    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for the split router weight");
+  if ((st = set_B(g, x, T, d)) != MOE_OK) return st;
+  g.k_steps = 3 * d / 64;
+  g.b_k_period = d / 64;
+  g.a128 = (E + 127) / 128;
+  g.o_limit = E;
+  g.groups = 1;
+  g.rows = static_cast<int>(T);
+  g.out_f32 = logits;
+  g.out_ld = E;
+  g.ksplit = ksplit;
+  g.out_split_stride = T * E;
+  MOE_CUDA(launch_tc_gemm(p, num_sms(), s));
+  RouterArgs a;
+  a.logits = logits;
+  a.logit_parts = ksplit;
+  a.logit_part_stride = T * E;
+  a.bias = bias;
+  a.T = T;
+  a.d = d;
+  a.E = E;
+  a.K = cfg->K;
+  a.G = cfg->n_group;
+  a.Gk = cfg->topk_group;
+  a.scale = cfg->routed_scaling_factor;
+  a.norm = cfg->norm_topk_prob;
+  a.topk_idx = topk_idx;
+  a.topk_w = topk_w;
+  MOE_CUDA(launch_router(a, s));
   return MOE_OK;
 }
 

@@ -262,6 +262,31 @@ int32_t moe_layer_forward_host(const moe_config* cfg, int64_t T, const void* x_h
                                const void* W_lat_down, const void* W_lat_up, void* y_host,
                                void* workspace, size_t ws_bytes, void* stream);
 
+/*
+ * moe_router without a caller-provided workspace.  This entry point has no
+ * counterpart on the pages: it exists for callers that cannot allocate
+ * device memory when they route tokens -- for example code running inside
+ * an allocator-free runtime or a plugin interface that hands over only its
+ * input and output buffers.  It computes exactly what moe_router computes
+ * with a workspace and bf16 x (the split-bf16 tensor-core router), taking
+ * its scratch (the three-way split of W_r and the partial logits) from a
+ * static device array of 64 MiB that every GPU loading this library holds
+ * until the process exits; it calls no allocating routine.
+ *   Arguments as moe_router.  cfg->dtype must be MOE_BF16 and d_model a
+ *   multiple of 64 (MOE_ERR_UNSUPPORTED_SHAPE otherwise).
+ *   Scratch needed: 256 + 6 E d + 4 T E P bytes (each term rounded up to
+ *   256), P = 3 for T >= 2048 and up to 48 for small T; more than 64 MiB is
+ *   rejected with MOE_ERR_WORKSPACE before anything is enqueued (the K2
+ *   router fits up to T = 8192; the K3 router up to T = 2048).
+ *   The first call on a device looks up the array's device address; make
+ *   that first call before any stream capture.  All calls on a device share
+ *   the array, which keeps the previous call's contents: calls whose work
+ *   overlaps on the GPU (other streams, other threads) race and must be
+ *   serialised by the caller.  A bounded device wait that expires leaves the
+ *   outputs incomplete and is not reported by this entry point. */
+int32_t moe_router_noalloc(const moe_config* cfg, int64_t T, const void* x, const float* W_r,
+                           const float* bias, int32_t* topk_idx, float* topk_w, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
