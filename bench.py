@@ -320,10 +320,12 @@ def run_own(args):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t0 = time.time()
+    launches0 = fgs.moe_launch_count()
     start.record(stream)
     for i in range(args.steps):
         step(step_events[i])
     end.record(stream)
+    launches = fgs.moe_launch_count() - launches0
     torch.cuda.synchronize()
     t1 = time.time()
     if world > 1:
@@ -355,7 +357,6 @@ def run_own(args):
                 "algorithmic_bytes_per_launch": work["gate_up_bytes"],
                 "tensor_frac_of_sustained": round(work["flops_gate_up"] / (gu_ms / 1e3) / 1e12
                                                   / peaks["bf16_tflops_sustained"], 4)}
-    per_launch = 8 if not shape.d_latent else 11
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
@@ -376,7 +377,7 @@ def run_own(args):
         "router": {"tokens_per_s": round(T / (stage_ms[0] / 1e3), 1), "ms": round(stage_ms[0], 4),
                    "fp32_tflops": round(work["flops_router"] / (stage_ms[0] / 1e3) / 1e12, 2)},
         "stages_ms": {n: round(v, 4) for n, v in zip(fgs.STAGE_NAMES, stage_ms)},
-        "gpu_launches": per_launch * args.steps,
+        "gpu_launches": launches,
         "clocks": clocks,
     }
 

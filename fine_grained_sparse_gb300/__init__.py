@@ -24,7 +24,7 @@ __all__ = [
     "moe_get_device_status", "moe_router", "moe_router_from_logits", "moe_permute",
     "moe_grouped_swiglu", "moe_combine", "moe_linear", "moe_layer_forward",
     "moe_layer_forward_host", "moe_last_error_detail", "moe_pack_weights", "pack_layer_weights",
-    "moe_router_noalloc",
+    "moe_router_noalloc", "moe_launch_count",
     "MOE_WEIGHTS_NATURAL", "MOE_WEIGHTS_PACKED", "MOE_PACK_GATE_UP", "MOE_PACK_PLAIN",
 ]
 
@@ -70,6 +70,7 @@ _P, _I32, _I64, _SZ, _F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctype
 _CFG = ctypes.POINTER(MoeConfig)
 _SIGS = {
     "moe_version": ([], _I32),
+    "moe_launch_count": ([], ctypes.c_uint64),
     "moe_status_string": ([_I32], ctypes.c_char_p),
     "moe_last_error_detail": ([], ctypes.c_char_p),
     "moe_validate_config": ([_CFG, _I64], _I32),
@@ -134,6 +135,11 @@ def config(shape=None, **kw) -> MoeConfig:
 
 def moe_version() -> int:
     return lib.moe_version()
+
+
+def moe_launch_count() -> int:
+    """Kernels the library has enqueued in this process so far."""
+    return int(lib.moe_launch_count())
 
 
 def moe_status_string(status: int) -> str:

@@ -10,12 +10,20 @@
 #include <string.h>
 
 #include <cmath>
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
 
 using namespace fgs;
+
+namespace fgs {
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}  // namespace
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+}  // namespace fgs
 
 namespace {
 
@@ -86,6 +94,13 @@ int down_a_per_unit(int nt_down) {
   static const int forced = env_int("FGS_DOWN_A", 0);  // tuning override
   if (forced == 1 || forced == 2) return forced;
   return nt_down > 128 ? 1 : 2;
+}
+
+// Weight tiles per unit of the gate/up pass (two: the token tile's B stages
+// are shared by two 128-row tiles).
+int gate_up_a_per_unit() {
+  static const int forced = env_int("FGS_GATE_UP_A", 0);  // tuning override
+  return forced == 1 ? 1 : 2;
 }
 
 int32_t check_router_cfg(const moe_config* c, int64_t T) {
@@ -327,6 +342,7 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
     memset(&p, 0, sizeof(p));
     p.mode = kModeSwiGLU;
     p.nt = nt;
+    p.a_per_unit = gate_up_a_per_unit();
     p.status = status;
     p.nseg = S ? 2 : 1;
     // gate/up: routed experts over the gathered rows
@@ -512,6 +528,8 @@ int32_t noalloc_scratch(void** out) {
 extern "C" {
 
 int32_t moe_version(void) { return 100; }
+
+uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char* moe_status_string(int32_t s) {
   switch (s) {

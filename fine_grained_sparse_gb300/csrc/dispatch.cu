@@ -281,10 +281,12 @@ cudaError_t launch_permute(const int32_t* topk_idx, int64_t T, int K, int E, int
   int64_t blocks = (n + threads * 4 - 1) / (threads * 4);
   if (blocks > 1024) blocks = 1024;
   if (blocks < 1) blocks = 1;
+  note_launch();
   histogram_kernel<<<static_cast<unsigned>(blocks), threads, sizeof(int) * E, stream>>>(
       topk_idx, n, E, counts, status);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
+  note_launch();
   scatter_kernel<<<E, kScatterThreads, 0, stream>>>(topk_idx, n, E, counts, offsets, perm, inv);
   return cudaGetLastError();
 }
@@ -293,6 +295,7 @@ int64_t max_tiles(int64_t rows, int E, int nt) { return rows / nt + E; }
 
 cudaError_t launch_build_tiles(const int32_t* offsets, int E, int nt, RowTile* tiles, int* ntiles,
                                int32_t* poffsets, cudaStream_t stream) {
+  note_launch();
   build_tiles_kernel<<<1, 1024, 0, stream>>>(offsets, E, nt, tiles, ntiles, poffsets);
   return cudaGetLastError();
 }
@@ -304,6 +307,7 @@ cudaError_t launch_gather_packed(const void* x, int K, int width, const int32_t*
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  note_launch();
   gather_packed_kernel<<<sms * 8, 256, 0, stream>>>(
       static_cast<const uint4*>(x), K, width / 8, perm, offsets, poffsets, E, topk_w,
       static_cast<uint4*>(Xp), plane_rows, w_perm);
@@ -318,6 +322,7 @@ cudaError_t launch_gather(const void* x, int64_t T, int K, int width, int elem_b
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  note_launch();
   gather_kernel<<<sms * 8, 256, 0, stream>>>(static_cast<const uint4*>(x), K, vec_per_row, perm,
                                              offsets, E, topk_w, static_cast<uint4*>(Xp), w_perm);
   return cudaGetLastError();
@@ -328,9 +333,11 @@ cudaError_t launch_combine(const void* Y, const int32_t* inv, int64_t T, int K, 
                            bool bf16, cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
   if (bf16) {
+    note_launch();
     combine_kernel<true><<<static_cast<unsigned>(T), 128, 0, stream>>>(Y, inv, K, D, adds, n_add,
                                                                        add_stride_rows, y);
   } else {
+    note_launch();
     combine_kernel<false><<<static_cast<unsigned>(T), 128, 0, stream>>>(Y, inv, K, D, adds, n_add,
                                                                         add_stride_rows, y);
   }

@@ -72,6 +72,7 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtGemm g) {
 cudaError_t launch_simt_gemm(const SimtGemm& g, int64_t tiles_bound, cudaStream_t stream) {
   if (tiles_bound <= 0) return cudaSuccess;
   const dim3 grid(static_cast<unsigned>(tiles_bound), static_cast<unsigned>((g.O + kSimtTile - 1) / kSimtTile));
+  note_launch();
   simt_gemm_kernel<<<grid, kSimtTile * kSimtTile, 0, stream>>>(g);
   return cudaGetLastError();
 }

@@ -53,7 +53,6 @@ namespace {
 
 constexpr int kBK = 64;                      // k per stage: one 128-byte swizzle row
 constexpr uint32_t kATileBytes = 128 * 128;  // one A tile: 128 rows x 128 B
-constexpr uint32_t kABytes = 2 * kATileBytes;
 constexpr int kBBoxRows = 32;
 constexpr uint32_t kBBoxBytes = kBBoxRows * 128;
 constexpr int kEpiWarps = 8;
@@ -350,7 +349,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     int c = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const Unit x = decode_unit(p, u, units0, nt);
-      const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
       const uint32_t n = static_cast<uint32_t>((x.n_rows + 15) & ~15);
       const Regions rg = regions_of(p, n, c);
       bool ok = mbar_wait_bounded(tempty_bar(c & 1), region_phase(c) ^ 1u, abort_flag, p.status);
@@ -425,63 +423,65 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         const uint32_t taddr0 =
             tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc_column(rg, acc);
         const int blk = x.blk0 + acc;
-        const int nchunks = (x.n_rows + 15) / 16;
-        // a single accumulator is split between the two warp groups
+        // 64 columns per TMEM load (one wait each); a single accumulator is
+        // split between the two warp groups by 64-column chunk
+        const int nchunks = (x.n_rows + 63) / 64;
         const int step = single ? 2 : 1;
-        int ch = single ? grp : 0;
-        uint32_t nxt[16];
-        if (ch < nchunks) tmem_ld_x16(taddr0 + static_cast<uint32_t>(ch * 16), nxt);
-        for (; ch < nchunks; ch += step) {
-          uint32_t v[16];
-          tmem_ld_wait(nxt);
+        for (int ch = single ? grp : 0; ch < nchunks; ch += step) {
+          uint32_t v64[64];
+          tmem_ld_x64(taddr0 + static_cast<uint32_t>(ch * 64), v64);
+          tmem_ld_wait(v64);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = nxt[j];
-          // the next chunk's TMEM load overlaps this chunk's math and stores
-          if (ch + step < nchunks) tmem_ld_x16(taddr0 + static_cast<uint32_t>((ch + step) * 16), nxt);
-          const int tok0 = ch * 16;
-          if (swiglu) {
-            const bool is_gate = lane < 16;
-            const int f = blk * 64 + q * 16 + (lane & 15);
-            float h[16];
+          for (int sub = 0; sub < 4; ++sub) {
+            const int tok0 = ch * 64 + sub * 16;
+            if (tok0 >= x.n_rows) break;
+            uint32_t v[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float mine = __uint_as_float(v[j]);
-              const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
-              const float g = is_gate ? mine : other;
-              const float up = is_gate ? other : mine;
-              h[j] = silu_f(g) * up;
-            }
-            // packed: plane f/64, chunk (f%64)/8 swizzled by row%8
-            const int64_t f_plane = static_cast<int64_t>(f >> 6) * plane_rows;
-            const int f_chunk = (f & 63) >> 3, f_lo = f & 7;
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-              const int tok = tok0 + (is_gate ? jj : 8 + jj);
-              const float val = is_gate ? h[jj] : h[8 + jj];
-              if (tok < x.n_rows) {
-                const int64_t row = x.out_row + tok;
-                const int64_t off =
-                    out_packed ? (((f_plane + row) << 6) +
-                                  ((f_chunk ^ static_cast<int>(row & 7)) << 3) + f_lo)
-                               : row * ld + f;
-                out[off] = __float2bfloat16_rn(val);
-              }
-            }
-          } else {
-            const int o = blk * 128 + q * 32 + lane;
-            if (o < o_limit) {
+            for (int j = 0; j < 16; ++j) v[j] = v64[sub * 16 + j];
+            if (swiglu) {
+              const bool is_gate = lane < 16;
+              const int f = blk * 64 + q * 16 + (lane & 15);
+              float h[16];
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
-                const int tok = tok0 + j;
+                const float mine = __uint_as_float(v[j]);
+                const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
+                const float g = is_gate ? mine : other;
+                const float up = is_gate ? other : mine;
+                h[j] = silu_f(g) * up;
+              }
+              // packed: plane f/64, chunk (f%64)/8 swizzled by row%8
+              const int64_t f_plane = static_cast<int64_t>(f >> 6) * plane_rows;
+              const int f_chunk = (f & 63) >> 3, f_lo = f & 7;
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj) {
+                const int tok = tok0 + (is_gate ? jj : 8 + jj);
+                const float val = is_gate ? h[jj] : h[8 + jj];
                 if (tok < x.n_rows) {
                   const int64_t row = x.out_row + tok;
-                  float val = __uint_as_float(v[j]);
-                  if (row_scale) val *= __ldg(row_scale + row);
-                  if (add) val += __bfloat162float(add[row * add_ld + o]);
-                  if (out_f32)
-                    out_f32[row * ld + o] = val;
-                  else
-                    out[row * ld + o] = __float2bfloat16_rn(val);
+                  const int64_t off =
+                      out_packed ? (((f_plane + row) << 6) +
+                                    ((f_chunk ^ static_cast<int>(row & 7)) << 3) + f_lo)
+                                 : row * ld + f;
+                  out[off] = __float2bfloat16_rn(val);
+                }
+              }
+            } else {
+              const int o = blk * 128 + q * 32 + lane;
+              if (o < o_limit) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  const int tok = tok0 + j;
+                  if (tok < x.n_rows) {
+                    const int64_t row = x.out_row + tok;
+                    float val = __uint_as_float(v[j]);
+                    if (row_scale) val *= __ldg(row_scale + row);
+                    if (add) val += __bfloat162float(add[row * add_ld + o]);
+                    if (out_f32)
+                      out_f32[row * ld + o] = val;
+                    else
+                      out[row * ld + o] = __float2bfloat16_rn(val);
+                  }
                 }
               }
             }
@@ -670,6 +670,7 @@ cudaError_t launch_tc_gemm(const GemmParams& params, int num_sms, cudaStream_t s
     if (err != cudaSuccess) return err;
     if (dev < 64) configured[dev] = 1;
   }
+  note_launch();
   tc_gemm_kernel<<<num_sms, kThreads, plan.smem_bytes, stream>>>(p);
   return cudaGetLastError();
 }
@@ -680,6 +681,7 @@ cudaError_t launch_pack_weights(int kind, int64_t groups, int64_t rows, int64_t 
   int64_t blocks = (n + 255) / 256;
   if (blocks > 65536) blocks = 65536;
   if (blocks < 1) return cudaSuccess;
+  note_launch();
   pack_weights_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
       kind, groups, rows, cols, static_cast<const uint4*>(src), static_cast<uint4*>(dst));
   return cudaGetLastError();
@@ -690,6 +692,7 @@ cudaError_t launch_split_router_weight(const float* W_r, int E, int d, __nv_bflo
   const int64_t n = static_cast<int64_t>(E) * d;
   int64_t blocks = (n + 255) / 256;
   if (blocks > 4096) blocks = 4096;
+  note_launch();
   split_router_weight_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(W_r, E, d,
                                                                                 W_split);
   return cudaGetLastError();

@@ -8,6 +8,11 @@
 
 namespace fgs {
 
+// Every kernel launch of the library is counted once, on the host, when it is
+// enqueued (read through moe_launch_count).
+void note_launch();
+
+
 // ----------------------------------------------------------------- router
 struct RouterArgs {
   const void* x = nullptr;        // [T, d] (bf16 when x_bf16, else fp32)

@@ -58,7 +58,7 @@ __device__ __forceinline__ bool before(float va, int ia, float vb, int ib) {
 // are more than twice that apart; only when some decision is closer (a
 // near-tie) are the values around it recomputed exactly and the decision
 // taken again.  Either way the result equals the one taken on exact values.
-constexpr float kFastErr = 5e-7f;            // |fast c - exact c| bound (|z| <= kFastRange)
+// kFastErr = 5e-7 bounds |fast c - exact c| for |z| <= kFastRange.
 constexpr float kMargin = 1.0f / 262144.0f;  // 3.8e-6 > 2 kFastErr
 constexpr float kGroupMargin = 1.0f / 131072.0f;  // group sums: 7.6e-6 > 2 (2 kFastErr + rounding)
 constexpr float kFastRange = 80.0f;           // beyond |z| > 80 the value is always exact
@@ -453,6 +453,7 @@ cudaError_t launch_fused(const RouterArgs& a, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  note_launch();
   return cudaLaunchKernelEx(&cfg, router_fused_kernel<XT, PM>, static_cast<const XT*>(a.x), a.W_r,
                             a.bias, static_cast<int>(a.T), a.d, a.E, a.K, a.G, a.Gk, a.scale,
                             a.norm, a.topk_idx, a.topk_w);
@@ -462,6 +463,7 @@ template <int PM>
 cudaError_t launch_logits(const RouterArgs& a, cudaStream_t stream) {
   const int warps = 8;
   const unsigned blocks = static_cast<unsigned>((a.T + warps - 1) / warps);
+  note_launch();
   router_logits_kernel<PM><<<blocks, warps * 32, 0, stream>>>(
       a.logits, a.logit_parts, a.logit_part_stride, a.bias, static_cast<int>(a.T), a.E, a.K, a.G,
       a.Gk, a.scale, a.norm, a.topk_idx, a.topk_w);

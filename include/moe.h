@@ -113,6 +113,13 @@ int32_t moe_pack_weights(int32_t kind, int64_t groups, int64_t rows, int64_t col
 /* Library version, major * 10000 + minor * 100 + patch. */
 int32_t moe_version(void);
 
+/* Number of kernels the library has enqueued in this process since it was
+ * loaded, on every device, stream and thread; counted on the host when each
+ * launch is issued (a launch that CUDA rejects is counted too).  The paper
+ * has no counterpart: it lets a caller check how many kernels one call
+ * enqueues.  Never fails. */
+uint64_t moe_launch_count(void);
+
 /* Static text for a moe_status value. */
 const char* moe_status_string(int32_t status);
 

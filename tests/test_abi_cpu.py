@@ -39,6 +39,7 @@ def test_library_exports_every_declared_symbol(fgs):
 
 def test_status_strings(fgs):
     assert fgs.moe_version() >= 100
+    assert fgs.moe_launch_count() == fgs.moe_launch_count()  # no launch without a GPU
     for code in range(8):
         assert fgs.moe_status_string(code) != "unknown status"
 
