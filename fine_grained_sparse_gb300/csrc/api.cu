@@ -103,6 +103,14 @@ int gate_up_a_per_unit() {
   return forced == 1 ? 1 : 2;
 }
 
+// CTA pairs (see GemmParams::pair) for the expert passes; launch_tc_gemm
+// applies them where the segments allow.
+bool use_pairs(bool down_pass) {
+  static const int gate_up = env_int("FGS_PAIR_GATE_UP", 0);  // tuning override
+  static const int down = env_int("FGS_PAIR_DOWN", 0);
+  return (down_pass ? down : gate_up) == 1;
+}
+
 int32_t check_router_cfg(const moe_config* c, int64_t T) {
   if (!c) return fail(MOE_ERR_INVALID_ARG, "cfg is null");
   if (T < 1 || T > (1ll << 30)) return fail(MOE_ERR_INVALID_ARG, "T out of range");
@@ -239,6 +247,7 @@ int32_t set_gate_up_A(GemmSegment& s, const void* W, int groups, int F, int Kd, 
   if (packed) {
     s.a_packed = static_cast<const uint8_t*>(W);
     s.a_group_bytes = 2ll * F * Kd * 2;
+    s.a_groups = groups;
     s.a_boxes = 1;
     return MOE_OK;
   }
@@ -272,6 +281,7 @@ int32_t set_store_A(GemmSegment& s, const void* W, int groups, int O, int Kd, bo
   if (packed) {
     s.a_packed = static_cast<const uint8_t*>(W);
     s.a_group_bytes = static_cast<int64_t>(O) * Kd * 2;
+    s.a_groups = groups;
     s.a_boxes = 1;
     s.a_rows = 0;
     return MOE_OK;
@@ -371,6 +381,7 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
       s.out_packed = 1;
       s.out_plane_rows = L.plane_rows_s;
     }
+    p.pair = use_pairs(false);
     MOE_CUDA(launch_tc_gemm(p, num_sms(), st));
     if (ev_down) MOE_CUDA(cudaEventRecord(ev_down, st));
 
@@ -403,6 +414,7 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
       s2.out = static_cast<__nv_bfloat16*>(io.Y_shared);
       s2.out_ld = d;
     }
+    p.pair = use_pairs(true);
     MOE_CUDA(launch_tc_gemm(p, num_sms(), st));
     return MOE_OK;
   }

@@ -50,26 +50,39 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// kCluster: acquire at cluster scope, for phases completed by another CTA of
+// the cluster.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
+  if (kCluster)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
   return ok != 0;
 }
 
 // Wait for the phase of `bar` with the given parity to complete.  Returns
 // false (and raises the CTA's abort flag and the status word) when the wait
 // outlives kWaitLimitNs, or at once when another thread already aborted.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile int* abort_flag, int* status) {
   unsigned long long t0 = 0;
   for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<kCluster>(bar, parity)) return true;
     if ((it & 63u) == 63u) {
       if (*abort_flag) return false;
       unsigned long long now = globaltimer_ns();
@@ -113,6 +126,27 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Copies of one CTA of a pair whose completion is counted on a barrier of
+// either CTA (bar: a cluster address), for MMAs issued over the pair.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar, int c0, int c1, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(map), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar, int c0, int c1, int c2,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 // Plain (untiled) bulk copy global -> shared; size and both addresses
 // multiples of 16 bytes.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
@@ -122,6 +156,47 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
       "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
+}
+
+// ---------------------------------------------------------------- cluster
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_index_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_count_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+
+// Address of the same shared-memory location (e.g. a barrier) in CTA
+// `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// Arrive on a barrier of any CTA of the cluster (address from cluster_map).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+// Every thread of every CTA of the cluster arrives; release/acquire at
+// cluster scope (barrier inits and shared-memory writes become visible).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
@@ -147,19 +222,39 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
 }
 
 // ---------------------------------------------------------------- tcgen05
+// TMEM allocation: one warp per CTA; for a CTA pair (kPair) one warp of
+// each CTA, together, and every tcgen05 operation of that kernel is then a
+// pair operation.
+template <bool kPair = false>
 __device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
-               "r"(ncols)
-               : "memory");
+  if (kPair)
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     slot_smem),
+                 "r"(ncols)
+                 : "memory");
+  else
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     slot_smem),
+                 "r"(ncols)
+                 : "memory");
 }
 
+template <bool kPair = false>
 __device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  if (kPair)
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  else
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
 
+template <bool kPair = false>
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
+  if (kPair)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -170,14 +265,36 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulator, one CTA.
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulator.  One CTA
+// (M = 128), or a CTA pair (kPair, M = 256): each CTA supplies 128 rows of A
+// and half of B's rows at the same shared-memory offsets, and each CTA's
+// TMEM receives its 128 rows x all of N.
+template <bool kPair = false>
 __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
+  if (kPair)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Pair form of tc_commit: arrive once on the barrier at offset `bar` of
+// every CTA named in cta_mask when the pair MMAs issued so far completed.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t cta_mask) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
       : "memory");
 }
 
@@ -254,8 +371,57 @@ __device__ __forceinline__ uint32_t idesc_bf16_f32(uint32_t m, uint32_t n) {
          | ((m >> 4) << 24);  // M / 16
 }
 
-__device__ __forceinline__ float silu_f(float v) {
-  return v * __frcp_rn(1.0f + __expf(-v));  // v * sigmoid(v)
+// v * sigmoid(v) = v / (1 + e^-v); for v < -87 the divisor overflows and
+// the fast division returns 0, the function's limit.
+__device__ __forceinline__ float silu_f(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&p);
+}
+
+// 8 x 8 transpose of 16-bit values within each octet of lanes: before, lane
+// i of the octet holds row i (word k = columns 2k and 2k + 1, low half
+// first); after, it holds column i in the same form.  Three exchange steps,
+// at lane distances 4, 2 and 1, each swapping the half of a lane's row that
+// belongs to its partner.
+__device__ __forceinline__ void transpose8x8_b16(uint32_t (&w)[4], int lane) {
+  const bool b4 = lane & 4, b2 = lane & 2, b1 = lane & 1;
+  uint32_t s0 = b4 ? w[0] : w[2], s1 = b4 ? w[1] : w[3];
+  uint32_t r0 = __shfl_xor_sync(0xffffffffu, s0, 4), r1 = __shfl_xor_sync(0xffffffffu, s1, 4);
+  if (b4) {
+    w[0] = r0;
+    w[1] = r1;
+  } else {
+    w[2] = r0;
+    w[3] = r1;
+  }
+  s0 = b2 ? w[0] : w[1];
+  s1 = b2 ? w[2] : w[3];
+  r0 = __shfl_xor_sync(0xffffffffu, s0, 2);
+  r1 = __shfl_xor_sync(0xffffffffu, s1, 2);
+  if (b2) {
+    w[0] = r0;
+    w[2] = r1;
+  } else {
+    w[1] = r0;
+    w[3] = r1;
+  }
+  s0 = b1 ? __byte_perm(w[0], w[1], 0x5410) : __byte_perm(w[0], w[1], 0x7632);
+  s1 = b1 ? __byte_perm(w[2], w[3], 0x5410) : __byte_perm(w[2], w[3], 0x7632);
+  r0 = __shfl_xor_sync(0xffffffffu, s0, 1);
+  r1 = __shfl_xor_sync(0xffffffffu, s1, 1);
+  if (b1) {
+    w[0] = __byte_perm(r0, w[0], 0x7610);
+    w[1] = __byte_perm(r0, w[1], 0x7632);
+    w[2] = __byte_perm(r1, w[2], 0x7610);
+    w[3] = __byte_perm(r1, w[3], 0x7632);
+  } else {
+    w[0] = __byte_perm(w[0], r0, 0x5410);
+    w[1] = __byte_perm(w[1], r0, 0x7610);
+    w[2] = __byte_perm(w[2], r1, 0x5410);
+    w[3] = __byte_perm(w[3], r1, 0x7610);
+  }
 }
 
 }  // namespace fgs

@@ -57,9 +57,16 @@ constexpr int kBBoxRows = 32;
 constexpr uint32_t kBBoxBytes = kBBoxRows * 128;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (3 + kEpiWarps);
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 12;
 constexpr size_t kSmemBudget = 229376;  // pipeline bytes per CTA (224 KB)
 constexpr int kSmemMax = 232448;        // the per-block limit (227 KB)
+
+// Token-ring stage: nt rows; for a CTA pair, this CTA's half rounded up to
+// whole 32-row boxes.
+__host__ __device__ constexpr uint32_t b_stage_bytes_of(int nt, bool pair) {
+  return pair ? static_cast<uint32_t>((nt / 2 + kBBoxRows - 1) / kBBoxRows) * kBBoxRows * 128u
+              : static_cast<uint32_t>(nt) * 128u;
+}
 
 struct Unit {
   int seg, group, b_row, out_row, n_rows, ob, n_a, ntiles;
@@ -70,9 +77,10 @@ struct Unit {
 
 __device__ __forceinline__ int ksplit_of(const GemmSegment* s) { return s->ksplit > 1 ? s->ksplit : 1; }
 
-// output blocks of a segment: pairs of A tiles, or single tiles
+// output blocks of a segment: pairs of A tiles (one unit, or one unit of a
+// CTA pair), or single tiles
 __device__ __forceinline__ int out_blocks(const GemmParams& p, const GemmSegment* s) {
-  return p.a_per_unit == 2 ? (s->a128 + 1) / 2 : s->a128;
+  return (p.a_per_unit == 2 || p.pair) ? (s->a128 + 1) / 2 : s->a128;
 }
 
 __device__ __forceinline__ int segment_units(const GemmParams& p, const GemmSegment* s, int nt) {
@@ -81,7 +89,8 @@ __device__ __forceinline__ int segment_units(const GemmParams& p, const GemmSegm
   return s->groups * ((s->rows + nt - 1) / nt) * ob * ksplit_of(s);
 }
 
-__device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int units0, int nt) {
+__device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int units0, int nt,
+                                            int rank) {
   Unit x;
   x.seg = u >= units0 ? 1 : 0;
   int local = u - (x.seg ? units0 : 0);
@@ -124,6 +133,9 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int unit
   if (p.a_per_unit == 2) {
     x.blk0 = 2 * x.ob;
     x.n_a = min(2, s->a128 - 2 * x.ob);
+  } else if (p.pair) {  // CTA `rank` of the pair takes tile 2 ob + rank
+    x.blk0 = 2 * x.ob + rank;
+    x.n_a = 1;
   } else {
     x.blk0 = x.ob;
     x.n_a = 1;
@@ -143,9 +155,9 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 // Drain wait: bounded by time only (ignores the abort flag).
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int* status) {
+__device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, int* status) {
   int local_abort = 0;
-  mbar_wait_bounded(bar, parity, &local_abort, status);
+  return mbar_wait_bounded<true>(bar, parity, &local_abort, status);
 }
 
 // TMEM: two regions of 256 columns.  A unit whose token tile fits in 128
@@ -173,6 +185,20 @@ __device__ __forceinline__ uint32_t acc_column(const Regions& r, int acc) {
                : 256u * static_cast<uint32_t>(r.c & 1) + 128u * static_cast<uint32_t>(acc);
 }
 
+// One kernel body, two tensor-core modes:
+//   kPair = false: one CTA per unit; units of two 128-row weight tiles (or
+//     one); MMAs of M = 128 issued by the CTA itself.
+//   kPair = true: clusters of two CTAs share each unit of two weight tiles:
+//     CTA r holds weight tile 2 ob + r and half of the token tile (rows
+//     [r N/2, (r+1) N/2)), and CTA 0 issues MMAs of M = 256 over the pair
+//     (tcgen05 cta_group::2): each CTA's TMEM receives its 128 weight rows x
+//     all N tokens.  Each CTA keeps one accumulator per unit, so the two TMEM
+//     regions alternate and the epilogue of a unit overlaps the next main
+//     loop whatever the token tile; the token tile is split, not repeated,
+//     across the pair.  Both CTAs' copies complete on CTA 0's full barriers;
+//     CTA 0's commits release both CTAs' stages and signal both epilogues;
+//     both epilogues release TMEM on CTA 0's barrier.
+template <bool kPair>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -180,45 +206,54 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   const int sa_n = p.a_stages;
   const int sb_n = p.b_stages;
   const int nt = p.nt;
-  const uint32_t b_stage_bytes = static_cast<uint32_t>(nt) * 128u;
+  const uint32_t b_stage_bytes = b_stage_bytes_of(nt, kPair);
   const uint32_t a_stage_bytes = kATileBytes * static_cast<uint32_t>(p.a_per_unit);
   uint8_t* smem_b = smem + sa_n * a_stage_bytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem_b + sb_n * b_stage_bytes);
-  // bars: a_full[Sa] | a_empty[Sa] | b_full[Sb] | b_empty[Sb] | tfull[2] | tempty[2] | drain
-  const int nbars = 2 * sa_n + 2 * sb_n + 5;
+  // bars: full[Sa] | empty[Sa] | tfull[2] | tempty[2] | drain
+  // k step i of the CTA's sequence uses weight stage i % Sa and token stage
+  // i % Sb.  full[i % Sa] counts the bytes of both (one wait per k step for
+  // the MMA issuer) and empty[i % Sa] frees both (one commit per k step):
+  // token stage i % Sb is reused by k step i + Sb once empty[i % Sa]
+  // completes k step i's phase.  With Sb <= Sa that phase is never
+  // ambiguous, and no token copy reaches a full barrier before the
+  // barrier's previous phase completed.
+  const int nbars = 2 * sa_n + 5;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + nbars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // a CTA pair walks the units together: unit u belongs to cluster u % count
+  const int rank = kPair ? static_cast<int>(cluster_ctarank()) : 0;
+  const int u_first = kPair ? static_cast<int>(cluster_index_x()) : static_cast<int>(blockIdx.x);
+  const int u_step = kPair ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
+  constexpr uint16_t kPairMask = 3;
+  const uint32_t bar_base = smem_u32(bars);
   const uint32_t a_base = smem_u32(smem);
   const uint32_t b_base = smem_u32(smem_b);
-  const uint32_t bar_base = smem_u32(bars);
   auto a_full = [&](int s) { return bar_base + 8u * s; };
   auto a_empty = [&](int s) { return bar_base + 8u * (sa_n + s); };
-  auto b_full = [&](int s) { return bar_base + 8u * (2 * sa_n + s); };
-  auto b_empty = [&](int s) { return bar_base + 8u * (2 * sa_n + sb_n + s); };
-  auto tfull_bar = [&](int r) { return bar_base + 8u * (2 * sa_n + 2 * sb_n + r); };
-  auto tempty_bar = [&](int r) { return bar_base + 8u * (2 * sa_n + 2 * sb_n + 2 + r); };
-  const uint32_t drain_bar = bar_base + 8u * (2 * sa_n + 2 * sb_n + 4);
+  auto tfull_bar = [&](int r) { return bar_base + 8u * (2 * sa_n + r); };
+  auto tempty_bar = [&](int r) { return bar_base + 8u * (2 * sa_n + 2 + r); };
+  const uint32_t drain_bar = bar_base + 8u * (2 * sa_n + 4);
+  // the same barrier in CTA 0 of the pair (the MMA issuer's)
+  auto lead = [&](uint32_t bar) { return kPair ? cluster_map(bar, 0) : bar; };
   constexpr uint32_t kTmemCols = 512;
 
   if (warp == 0) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
+    tmem_alloc<kPair>(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish<kPair>();
   }
   if (warp == 1 && lane == 0) {
     for (int s = 0; s < sa_n; ++s) {
-      mbar_init(a_full(s), 1);
+      mbar_init(a_full(s), 2);  // the two producers' arrivals (CTA 0's in a pair)
       mbar_init(a_empty(s), 1);
-    }
-    for (int s = 0; s < sb_n; ++s) {
-      mbar_init(b_full(s), 1);
-      mbar_init(b_empty(s), 1);
     }
     for (int r = 0; r < 2; ++r) {
       mbar_init(tfull_bar(r), 1);
-      mbar_init(tempty_bar(r), kEpiWarps);
+      // paired: both CTAs' epilogue warps release CTA 0's regions
+      mbar_init(tempty_bar(r), kPair ? 2 * kEpiWarps : kEpiWarps);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -226,6 +261,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   }
   tc_fence_before();
   __syncthreads();
+  // the peer's barriers and TMEM must exist before any copy, commit or
+  // arrival reaches them
+  if (kPair) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -241,8 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     int stage = 0;
     uint32_t phase = 0;
     int64_t issued = 0;
-    for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      const Unit x = decode_unit(p, u, units0, nt);
+    for (int u = u_first; u < total; u += u_step) {
+      const Unit x = decode_unit(p, u, units0, nt, rank);
       const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
       const uint32_t tx = kATileBytes * x.n_a;
       // a weight block read by one token tile is streamed; one shared by
@@ -255,19 +293,25 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           break;
         }
         const uint32_t fb = a_full(stage);
-        mbar_arrive_expect_tx(fb, tx);
         const uint32_t a_dst = a_base + stage * a_stage_bytes;
         const int kc = ks * kBK;
-        if (s->a_packed) {
-          // packed weights: the tiles of a pair at one k step are adjacent
-          const int pair = x.blk0 >> 1;
-          const int in_pair = min(2, s->a128 - 2 * pair);
-          const uint8_t* src = s->a_packed + x.group * s->a_group_bytes +
-                               (2ll * pair * s->k_steps + static_cast<int64_t>(ks) * in_pair +
-                                (x.blk0 & 1)) *
-                                   kATileBytes;
-          bulk_load(a_dst, src, tx, fb, pol_w);
+        // packed weights: the unit's tiles at k step ks (a pair, or the
+        // pair member of this CTA) are contiguous
+        const int pair_idx = x.blk0 >> 1;
+        const int in_pair = min(2, s->a128 - 2 * pair_idx);
+        const int64_t tile = 2ll * pair_idx * s->k_steps + static_cast<int64_t>(ks) * in_pair +
+                             (x.blk0 & 1);
+        if (kPair) {
+          // CTA 0 expects both CTAs' tiles on its barrier
+          if (rank == 0) mbar_arrive_expect_tx(fb, 2 * kATileBytes);
+          tma_load_2d_pair(a_dst, &s->tmA, lead(fb), 0,
+                           static_cast<int>(x.group * (s->a_group_bytes >> 7) + tile * 128), pol_w);
+        } else if (s->a_packed) {
+          mbar_arrive_expect_tx(fb, tx);
+          bulk_load(a_dst, s->a_packed + x.group * s->a_group_bytes + tile * kATileBytes, tx, fb,
+                    pol_w);
         } else {
+          mbar_arrive_expect_tx(fb, tx);
           for (int a = 0; a < x.n_a; ++a) {
             const int blk = x.blk0 + a;  // 128-row A tile index along O
             const uint32_t dst = a_dst + a * kATileBytes;
@@ -292,104 +336,138 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       }
       if (!ok) break;
     }
+    // drain: wait until the last stages issued were consumed (so every copy
+    // into them, of either producer and either CTA, has landed)
     const int64_t first = issued > sa_n ? issued - sa_n : 0;
-    for (int64_t q = first; q < issued; ++q)
-      drain_wait(a_full(static_cast<int>(q % sa_n)), static_cast<uint32_t>((q / sa_n) & 1),
-                 p.status);
+    for (int64_t q = first; q < issued; ++q) {
+      const int st = static_cast<int>(q % sa_n);
+      const uint32_t par = static_cast<uint32_t>((q / sa_n) & 1);
+      if (!drain_wait(a_empty(st), par, p.status)) break;
+    }
   } else if (warp == 2 && lane == 0) {
     // ------------------------------------------------- token (B) producer
     for (int s = 0; s < p.nseg; ++s)
-      if (!p.seg[s].b_packed) prefetch_tensormap(&p.seg[s].tmB);
+      if (kPair || !p.seg[s].b_packed) prefetch_tensormap(&p.seg[s].tmB);
     const uint64_t pol_keep = l2_policy_evict_last();
-    int stage = 0;
-    uint32_t phase = 0;
+    int stage = 0, fstage = 0;  // token stage, and the k step's full barrier
+    int estage = 0;             // weight stage of k step issued - Sb
+    uint32_t ephase = 0;
     int64_t issued = 0;
-    for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      const Unit x = decode_unit(p, u, units0, nt);
+    for (int u = u_first; u < total; u += u_step) {
+      const Unit x = decode_unit(p, u, units0, nt, rank);
       const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
-      const int nbox = (x.n_rows + kBBoxRows - 1) / kBBoxRows;
+      // paired: this CTA's half of the tile's rows (rounded up to 16), as
+      // 32-row boxes; the rows past the half that a box brings in are not
+      // read by the MMA
+      const int half = ((x.n_rows + 15) & ~15) >> 1;
+      const int b_row = kPair ? x.b_row + rank * half : x.b_row;
+      const int nbox = kPair ? (half + kBBoxRows - 1) / kBBoxRows
+                             : (x.n_rows + kBBoxRows - 1) / kBBoxRows;
       // packed: the tile's rows (rounded up to 16) are one contiguous run
-      const uint32_t tx = s->b_packed ? static_cast<uint32_t>((x.n_rows + 15) & ~15) * 128u
-                                      : static_cast<uint32_t>(nbox) * kBBoxBytes;
+      const uint32_t tx = kPair ? 2u * static_cast<uint32_t>(nbox) * kBBoxBytes
+                          : s->b_packed ? static_cast<uint32_t>((x.n_rows + 15) & ~15) * 128u
+                                        : static_cast<uint32_t>(nbox) * kBBoxBytes;
       bool ok = true;
       for (int ks = x.k0; ks < x.k1; ++ks) {
-        if (!mbar_wait_bounded(b_empty(stage), phase ^ 1u, abort_flag, p.status)) {
-          ok = false;
-          break;
+        if (issued >= sb_n) {  // token stage free once k step issued - Sb was consumed
+          if (!mbar_wait_bounded(a_empty(estage), ephase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          if (++estage == sa_n) {
+            estage = 0;
+            ephase ^= 1u;
+          }
         }
-        const uint32_t fb = b_full(stage);
-        mbar_arrive_expect_tx(fb, tx);
+        const uint32_t fb = a_full(fstage);
+        if (!kPair || rank == 0) mbar_arrive_expect_tx(fb, tx);
         const uint32_t b_dst = b_base + stage * b_stage_bytes;
         const int kstep = s->b_k_period ? ks % s->b_k_period : ks;
-        if (s->b_packed) {
+        if (kPair) {
+          for (int bx = 0; bx < nbox; ++bx) {
+            if (s->b_packed)
+              tma_load_3d_pair(b_dst + bx * kBBoxBytes, &s->tmB, lead(fb), 0,
+                               b_row + bx * kBBoxRows, kstep, pol_keep);
+            else
+              tma_load_2d_pair(b_dst + bx * kBBoxBytes, &s->tmB, lead(fb), kstep * kBK,
+                               b_row + bx * kBBoxRows, pol_keep);
+          }
+        } else if (s->b_packed) {
           const uint8_t* src =
-              s->b_packed + (static_cast<int64_t>(kstep) * s->b_plane_rows + x.b_row) * 128;
+              s->b_packed + (static_cast<int64_t>(kstep) * s->b_plane_rows + b_row) * 128;
           bulk_load(b_dst, src, tx, fb, pol_keep);
         } else {
           for (int bx = 0; bx < nbox; ++bx)
             tma_load_2d(b_dst + bx * kBBoxBytes, &s->tmB, fb, kstep * kBK,
-                        x.b_row + bx * kBBoxRows, pol_keep);
+                        b_row + bx * kBBoxRows, pol_keep);
         }
         ++issued;
-        if (++stage == sb_n) {
-          stage = 0;
-          phase ^= 1u;
-        }
+        if (++fstage == sa_n) fstage = 0;
+        if (++stage == sb_n) stage = 0;
       }
       if (!ok) break;
     }
     const int64_t first = issued > sb_n ? issued - sb_n : 0;
-    for (int64_t q = first; q < issued; ++q)
-      drain_wait(b_full(static_cast<int>(q % sb_n)), static_cast<uint32_t>((q / sb_n) & 1),
-                 p.status);
-  } else if (warp == 1 && lane == 0) {
+    for (int64_t q = first; q < issued; ++q) {
+      const int st = static_cast<int>(q % sa_n);
+      const uint32_t par = static_cast<uint32_t>((q / sa_n) & 1);
+      if (!drain_wait(a_empty(st), par, p.status)) break;
+    }
+  } else if (warp == 1 && lane == 0 && rank == 0) {
     // ------------------------------------------------------- MMA issuer
     int sa = 0, sb = 0;
-    uint32_t pa = 0, pb = 0;
+    uint32_t pa = 0;
     int c = 0;
-    for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      const Unit x = decode_unit(p, u, units0, nt);
+    for (int u = u_first; u < total; u += u_step) {
+      const Unit x = decode_unit(p, u, units0, nt, rank);
       const uint32_t n = static_cast<uint32_t>((x.n_rows + 15) & ~15);
       const Regions rg = regions_of(p, n, c);
-      bool ok = mbar_wait_bounded(tempty_bar(c & 1), region_phase(c) ^ 1u, abort_flag, p.status);
+      bool ok = mbar_wait_bounded<kPair>(tempty_bar(c & 1), region_phase(c) ^ 1u, abort_flag,
+                                         p.status);
       if (ok && rg.big)
         ok = mbar_wait_bounded(tempty_bar((c + 1) & 1), region_phase(c + 1) ^ 1u, abort_flag,
                                p.status);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t idesc = idesc_bf16_f32(128, n);
+      const uint32_t idesc = idesc_bf16_f32(kPair ? 256 : 128, n);
       for (int ks = x.k0; ks < x.k1; ++ks) {
-        if (!mbar_wait_bounded(a_full(sa), pa, abort_flag, p.status) ||
-            !mbar_wait_bounded(b_full(sb), pb, abort_flag, p.status)) {
+        if (!mbar_wait_bounded<kPair>(a_full(sa), pa, abort_flag, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint64_t bdesc = smem_desc_sw128(b_base + sb * b_stage_bytes);
-        for (int a = 0; a < x.n_a; ++a) {
+        for (int a = 0; a < (kPair ? 1 : x.n_a); ++a) {
           const uint64_t adesc = smem_desc_sw128(a_base + sa * a_stage_bytes + a * kATileBytes);
           const uint32_t d = tmem_base + acc_column(rg, a);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
-            tc_mma_bf16(d, adesc + 2u * kk, bdesc + 2u * kk, idesc, ((ks - x.k0) | kk) != 0);
+            tc_mma_bf16<kPair>(d, adesc + 2u * kk, bdesc + 2u * kk, idesc,
+                               ((ks - x.k0) | kk) != 0);
         }
-        tc_commit(a_empty(sa));
-        tc_commit(b_empty(sb));
+        if (kPair)  // release the stages of both CTAs
+          tc_commit_pair(a_empty(sa), kPairMask);
+        else
+          tc_commit(a_empty(sa));
         if (++sa == sa_n) {
           sa = 0;
           pa ^= 1u;
         }
-        if (++sb == sb_n) {
-          sb = 0;
-          pb ^= 1u;
-        }
+        if (++sb == sb_n) sb = 0;
       }
       if (!ok) break;
-      tc_commit(tfull_bar(c & 1));
-      if (rg.big) tc_commit(tfull_bar((c + 1) & 1));
+      if (kPair) {  // both CTAs' accumulators are ready
+        tc_commit_pair(tfull_bar(c & 1), kPairMask);
+      } else {
+        tc_commit(tfull_bar(c & 1));
+        if (rg.big) tc_commit(tfull_bar((c + 1) & 1));
+      }
       c += rg.big ? 2 : 1;
     }
-    tc_commit(drain_bar);
+    if (kPair)
+      tc_commit_pair(drain_bar, 1);
+    else
+      tc_commit(drain_bar);
     drain_wait(drain_bar, 0, p.status);
   } else if (warp >= 3) {
     // ---------------------------------------------------------- epilogue
@@ -399,8 +477,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     const bool swiglu = p.mode == kModeSwiGLU;
     const bool single = p.a_per_unit == 1;
     int c = 0;
-    for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      const Unit x = decode_unit(p, u, units0, nt);
+    for (int u = u_first; u < total; u += u_step) {
+      const Unit x = decode_unit(p, u, units0, nt, rank);
       const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
       // the segment's output description, once per unit, in registers
       __nv_bfloat16* const out = s->out;
@@ -439,32 +517,40 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = v64[sub * 16 + j];
             if (swiglu) {
+              // lane l < 16 holds the gate and lane l + 16 the up value of
+              // feature blk*64 + 16q + (l & 15) for these 16 tokens: the
+              // gate lane forms h for tokens 0..7, the up lane for 8..15,
+              // each receiving the other half's values for its tokens
               const bool is_gate = lane < 16;
-              const int f = blk * 64 + q * 16 + (lane & 15);
-              float h[16];
+              uint32_t w[4];
 #pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const float mine = __uint_as_float(v[j]);
-                const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
-                const float g = is_gate ? mine : other;
-                const float up = is_gate ? other : mine;
-                h[j] = silu_f(g) * up;
-              }
-              // packed: plane f/64, chunk (f%64)/8 swizzled by row%8
-              const int64_t f_plane = static_cast<int64_t>(f >> 6) * plane_rows;
-              const int f_chunk = (f & 63) >> 3, f_lo = f & 7;
+              for (int j = 0; j < 8; j += 2) {
+                float hh[2];
 #pragma unroll
-              for (int jj = 0; jj < 8; ++jj) {
-                const int tok = tok0 + (is_gate ? jj : 8 + jj);
-                const float val = is_gate ? h[jj] : h[8 + jj];
-                if (tok < x.n_rows) {
-                  const int64_t row = x.out_row + tok;
-                  const int64_t off =
-                      out_packed ? (((f_plane + row) << 6) +
-                                    ((f_chunk ^ static_cast<int>(row & 7)) << 3) + f_lo)
-                                 : row * ld + f;
-                  out[off] = __float2bfloat16_rn(val);
+                for (int e = 0; e < 2; ++e) {
+                  const float own = __uint_as_float(is_gate ? v[j + e] : v[8 + j + e]);
+                  const float send = __uint_as_float(is_gate ? v[8 + j + e] : v[j + e]);
+                  const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+                  const float g = is_gate ? own : recv;
+                  const float u = is_gate ? recv : own;
+                  hh[e] = silu_f(g) * u;
                 }
+                w[j >> 1] = pack_bf16x2(hh[0], hh[1]);
+              }
+              // each lane octet now holds 8 features x 8 tokens; transposed,
+              // lane i holds token i's 8 features: one 16-byte store
+              transpose8x8_b16(w, lane);
+              const int oct = lane >> 3;
+              const int tok = tok0 + (oct >> 1) * 8 + (lane & 7);
+              if (tok < x.n_rows) {
+                const int64_t row = x.out_row + tok;
+                const int fc = 2 * q + (oct & 1);  // 8-feature chunk in the 64-feature block
+                // packed: plane blk, chunk fc swizzled by row % 8
+                const int64_t off =
+                    out_packed ? (((static_cast<int64_t>(blk) * plane_rows + row) << 6) +
+                                  ((fc ^ static_cast<int>(row & 7)) << 3))
+                               : row * ld + blk * 64 + fc * 8;
+                *reinterpret_cast<uint4*>(out + off) = make_uint4(w[0], w[1], w[2], w[3]);
               }
             } else {
               const int o = blk * 128 + q * 32 + lane;
@@ -492,18 +578,25 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       __syncwarp();
       if (lane == 0) {
         // a region holding one accumulator of a two-tile unit gets both
-        // arrivals from its 4 warps
-        mbar_arrive(tempty_bar(region));
-        if (rg.big) mbar_arrive(tempty_bar(region));
+        // arrivals from its 4 warps; paired CTAs release CTA 0's region
+        if (kPair) {
+          mbar_arrive_cluster(lead(tempty_bar(region)));
+        } else {
+          mbar_arrive(tempty_bar(region));
+          if (rg.big) mbar_arrive(tempty_bar(region));
+        }
       }
       c += rg.big ? 2 : 1;
     }
   }
 
   __syncthreads();
+  // neither CTA of a pair leaves (or frees TMEM) while the other may still
+  // reach its shared memory, barriers or accumulators
+  if (kPair) cluster_sync_all();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc<kPair>(tmem_base, kTmemCols);
   }
 }
 
@@ -629,7 +722,7 @@ CUresult encode_tmap_gate_up_5d(CUtensorMap* map, const void* base, int64_t grou
   return encode(map, base, 5, dims, strides, box);
 }
 
-GemmPlan plan_gemm(int nt, int a_per_unit) {
+GemmPlan plan_gemm(int nt, int a_per_unit, bool pair) {
   // token ring: 3 stages; weight ring: the rest of the budget
   static const int forced_b = [] {  // tuning override of the token ring depth
     const char* v = getenv("FGS_B_STAGES");
@@ -637,41 +730,108 @@ GemmPlan plan_gemm(int nt, int a_per_unit) {
   }();
   GemmPlan g;
   g.nt = nt;
-  const size_t b_stage = static_cast<size_t>(nt) * 128;
+  const size_t b_stage = b_stage_bytes_of(nt, pair);
   const size_t a_stage = static_cast<size_t>(kATileBytes) * a_per_unit;
   g.b_stages = 3;
-  if (forced_b >= 2 && forced_b <= 6) g.b_stages = forced_b;
+  if (forced_b >= 2 && forced_b <= 8) g.b_stages = forced_b;
   const size_t b_bytes = g.b_stages * b_stage;
   int sa = b_bytes < kSmemBudget ? static_cast<int>((kSmemBudget - b_bytes) / a_stage) : 0;
+  static const int forced_a = [] {  // tuning override: cap on the weight ring depth
+    const char* v = getenv("FGS_A_STAGES");
+    return (v && *v) ? atoi(v) : 0;
+  }();
   if (sa > kMaxStages) sa = kMaxStages;
+  if (forced_a >= 2 && sa > forced_a) sa = forced_a;
   if (sa < 2) {  // keep at least two weight stages
     sa = 2;
     g.b_stages = static_cast<int>((kSmemBudget - 2 * a_stage) / b_stage);
   }
+  if (g.b_stages > sa) g.b_stages = sa;  // see the barrier layout in the kernel
   g.a_stages = sa;
-  g.smem_bytes = 1024 + a_stage * sa + b_stage * g.b_stages +
-                 8 * (2 * sa + 2 * g.b_stages + 5) + 16;
+  g.smem_bytes = 1024 + a_stage * sa + b_stage * g.b_stages + 8 * (2 * sa + 5) + 16;
   return g;
 }
 
+namespace {
+
+// Paired launches read packed weights and packed activations through tensor
+// maps (the pair's copies complete on one CTA's barriers, which only tensor
+// copies can do): weights as rows of 128 bytes, one 128-row tile per box;
+// activation planes as (64 columns, plane rows, planes), 32-row boxes.  The
+// data are stored pre-swizzled, so the maps do not swizzle again.
+CUresult encode_pair_maps(GemmSegment& s) {
+  auto fn = encode_fn();
+  if (!fn) return CUDA_ERROR_NOT_INITIALIZED;
+  cuuint32_t estr[3] = {1, 1, 1};
+  const cuuint64_t a_dims[2] = {kBK, static_cast<cuuint64_t>(s.a_groups) *
+                                         static_cast<cuuint64_t>(s.a_group_bytes / 128)};
+  const cuuint64_t a_strides[1] = {128};
+  const cuuint32_t a_box[2] = {kBK, 128};
+  CUresult r = fn(&s.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint8_t*>(s.a_packed),
+                  a_dims, a_strides, a_box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS || !s.b_packed) return r;
+  const cuuint64_t b_dims[3] = {kBK, static_cast<cuuint64_t>(s.b_plane_rows),
+                                static_cast<cuuint64_t>(s.k_steps)};
+  const cuuint64_t b_strides[2] = {128, static_cast<cuuint64_t>(s.b_plane_rows) * 128};
+  const cuuint32_t b_box[3] = {kBK, kBBoxRows, 1};
+  return fn(&s.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint8_t*>(s.b_packed), b_dims,
+            b_strides, b_box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace
+
+bool pair_capable(const GemmParams& p) {
+  for (int i = 0; i < p.nseg; ++i) {
+    const GemmSegment& s = p.seg[i];
+    if (!s.a_packed || s.a_groups < 1 || s.a128 % 2 || s.ksplit > 1 || s.b_k_period) return false;
+  }
+  return p.nseg > 0;
+}
+
 cudaError_t launch_tc_gemm(const GemmParams& params, int num_sms, cudaStream_t stream) {
-  const GemmPlan plan = plan_gemm(params.nt, params.a_per_unit == 1 ? 1 : 2);
   GemmParams p = params;
-  p.a_per_unit = params.a_per_unit == 1 ? 1 : 2;
+  p.pair = (params.pair && pair_capable(params) && num_sms >= 2) ? 1 : 0;
+  p.a_per_unit = (p.pair || params.a_per_unit == 1) ? 1 : 2;
+  const GemmPlan plan = plan_gemm(p.nt, p.a_per_unit, p.pair != 0);
   p.a_stages = plan.a_stages;
   p.b_stages = plan.b_stages;
+  if (p.pair)
+    for (int i = 0; i < p.nseg; ++i)
+      if (encode_pair_maps(p.seg[i]) != CUDA_SUCCESS) return cudaErrorInvalidValue;
   static int configured[64] = {0};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev >= 64 || !configured[dev]) {
-    err = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    err = cudaFuncSetAttribute(tc_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kSmemMax);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(tc_gemm_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
     if (err != cudaSuccess) return err;
     if (dev < 64) configured[dev] = 1;
   }
+  if (p.pair) {  // clusters of two CTAs, one CTA per SM
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(num_sms / 2 * 2));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = plan.smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    note_launch();
+    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<true>, p);
+  }
   note_launch();
-  tc_gemm_kernel<<<num_sms, kThreads, plan.smem_bytes, stream>>>(p);
+  tc_gemm_kernel<false><<<num_sms, kThreads, plan.smem_bytes, stream>>>(p);
   return cudaGetLastError();
 }
 

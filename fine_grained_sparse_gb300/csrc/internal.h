@@ -99,6 +99,7 @@ struct GemmSegment {
   // packed weights (one contiguous bulk copy per stage) instead of tmA
   const uint8_t* a_packed;
   int64_t a_group_bytes;
+  int a_groups;  // groups in the packed bank
   // explicit tiles (routed experts) or implicit ones (groups x rows)
   const RowTile* tiles;
   const int* ntiles;
@@ -127,6 +128,11 @@ struct GemmParams {
   int mode;
   int nt;        // token tile (MMA N upper bound): 32, 64, 128 or 256
   int a_per_unit;  // 128-row weight tiles per unit: 2 (default) or 1
+  // 1: run on CTA pairs (clusters of two) with MMAs of M = 256 over the pair;
+  // each CTA takes one of a unit's two 128-row weight tiles and half of its
+  // token tile.  Applied only when pair_capable(); implies one weight tile
+  // per CTA.
+  int pair;
   int a_stages;  // weight ring depth
   int b_stages;  // token ring depth
   int* status;
@@ -136,7 +142,10 @@ struct GemmPlan {
   int nt, a_stages, b_stages;
   size_t smem_bytes;
 };
-GemmPlan plan_gemm(int nt, int a_per_unit);
+GemmPlan plan_gemm(int nt, int a_per_unit, bool pair);
+// Whether a launch can run on CTA pairs (packed weights with an even number
+// of 128-row tiles in every segment, no K split).
+bool pair_capable(const GemmParams& p);
 
 cudaError_t launch_tc_gemm(const GemmParams& p, int num_sms, cudaStream_t stream);
 
