@@ -89,11 +89,14 @@ __device__ __forceinline__ int segment_units(const GemmParams& p, const GemmSegm
   return s->groups * ((s->rows + nt - 1) / nt) * ob * ksplit_of(s);
 }
 
-__device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int units0, int nt,
-                                            int rank) {
+// The second segment's units (the shared experts: compute-heavy, their
+// weights shared by all token tiles) come first, the first segment's
+// weight-streaming units after them.
+__device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int units0, int units1,
+                                            int nt, int rank) {
   Unit x;
-  x.seg = u >= units0 ? 1 : 0;
-  int local = u - (x.seg ? units0 : 0);
+  x.seg = u < units1 ? 1 : 0;
+  int local = x.seg ? u : u - units1;
   const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
   const int OB = out_blocks(p, s);
   const int ns = ksplit_of(s);
@@ -280,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     uint32_t phase = 0;
     int64_t issued = 0;
     for (int u = u_first; u < total; u += u_step) {
-      const Unit x = decode_unit(p, u, units0, nt, rank);
+      const Unit x = decode_unit(p, u, units0, units1, nt, rank);
       const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
       const uint32_t tx = kATileBytes * x.n_a;
       // a weight block read by one token tile is streamed; one shared by
@@ -354,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     uint32_t ephase = 0;
     int64_t issued = 0;
     for (int u = u_first; u < total; u += u_step) {
-      const Unit x = decode_unit(p, u, units0, nt, rank);
+      const Unit x = decode_unit(p, u, units0, units1, nt, rank);
       const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
       // paired: this CTA's half of the tile's rows (rounded up to 16), as
       // 32-row boxes; the rows past the half that a box brings in are not
@@ -419,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     uint32_t pa = 0;
     int c = 0;
     for (int u = u_first; u < total; u += u_step) {
-      const Unit x = decode_unit(p, u, units0, nt, rank);
+      const Unit x = decode_unit(p, u, units0, units1, nt, rank);
       const uint32_t n = static_cast<uint32_t>((x.n_rows + 15) & ~15);
       const Regions rg = regions_of(p, n, c);
       bool ok = mbar_wait_bounded<kPair>(tempty_bar(c & 1), region_phase(c) ^ 1u, abort_flag,
@@ -478,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     const bool single = p.a_per_unit == 1;
     int c = 0;
     for (int u = u_first; u < total; u += u_step) {
-      const Unit x = decode_unit(p, u, units0, nt, rank);
+      const Unit x = decode_unit(p, u, units0, units1, nt, rank);
       const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
       // the segment's output description, once per unit, in registers
       __nv_bfloat16* const out = s->out;
@@ -490,6 +493,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       const bool out_packed = s->out_packed != 0;
       const int64_t plane_rows = s->out_plane_rows;
       const int o_limit = s->o_limit;
+      // store mode, bf16 output without an addend, rows of whole 16-byte
+      // chunks: written by 16-byte stores
+      const bool rows8 = !add && !out_f32 && o_limit % 8 == 0 && ld % 8 == 0;
       const uint32_t n = static_cast<uint32_t>((x.n_rows + 15) & ~15);
       const Regions rg = regions_of(p, n, c);
       const int acc = single ? 0 : grp;
@@ -551,6 +557,30 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                                   ((fc ^ static_cast<int>(row & 7)) << 3))
                                : row * ld + blk * 64 + fc * 8;
                 *reinterpret_cast<uint4*>(out + off) = make_uint4(w[0], w[1], w[2], w[3]);
+              }
+            } else if (rows8) {
+              // bf16 rows of 8 output columns: lane i of each octet holds
+              // column o0 + i for 16 tokens; two 8 x 8 transposes give it
+              // token i's and token 8 + i's 8 columns, two 16-byte stores
+              const int o0 = blk * 128 + q * 32 + (lane & ~7);
+              float val[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                val[j] = __uint_as_float(v[j]);
+                if (row_scale)  // padding tokens read the tile's last row's scale
+                  val[j] *= __ldg(row_scale + x.out_row + min(tok0 + j, x.n_rows - 1));
+              }
+#pragma unroll
+              for (int hlf = 0; hlf < 2; ++hlf) {
+                uint32_t w[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  w[k] = pack_bf16x2(val[8 * hlf + 2 * k], val[8 * hlf + 2 * k + 1]);
+                transpose8x8_b16(w, lane);
+                const int tok = tok0 + 8 * hlf + (lane & 7);
+                if (tok < x.n_rows && o0 < o_limit)
+                  *reinterpret_cast<uint4*>(out + (x.out_row + tok) * ld + o0) =
+                      make_uint4(w[0], w[1], w[2], w[3]);
               }
             } else {
               const int o = blk * 128 + q * 32 + lane;
