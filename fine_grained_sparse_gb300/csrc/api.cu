@@ -74,26 +74,23 @@ int env_int(const char* name, int fallback) {
   return (v && *v) ? atoi(v) : fallback;
 }
 
-// The gate/up pass (K = d, long) takes 256-row tiles: most experts are one
-// tile and their weights stream once.  The down pass (K = d_ff, short) takes
-// 128-row tiles, whose two accumulators share one TMEM region, so its
-// epilogue overlaps the next unit's main loop.
+// Token tiles: 32 rows for small batches; otherwise 256, so most experts are
+// one tile and their weights stream once per pass.  A unit of two 128-row
+// weight tiles against a tile of more than 128 tokens fills both TMEM
+// regions; its epilogue is short next to its main loop.
 int token_tile(int64_t T, bool down_pass = false) {
   static const int forced = env_int("FGS_TOKEN_TILE", 0);  // tuning override
   static const int forced_down = env_int("FGS_DOWN_TILE", 0);
   const int f = down_pass ? forced_down : forced;
   if (f == 32 || f == 64 || f == 128 || f == 256) return f;
-  if (T <= 256) return 32;
-  return down_pass ? 128 : 256;
+  return T <= 256 ? 32 : 256;
 }
 
-// Weight tiles per unit of the down pass: with 256-row token tiles, one
-// 128-row tile per unit keeps the unit's accumulator within one TMEM region
-// (double-buffered) and streams each expert's weights once.
-int down_a_per_unit(int nt_down) {
+// Weight tiles per unit of the down pass: two, so each token tile read into
+// shared memory feeds two 128-row weight tiles.
+int down_a_per_unit() {
   static const int forced = env_int("FGS_DOWN_A", 0);  // tuning override
-  if (forced == 1 || forced == 2) return forced;
-  return nt_down > 128 ? 1 : 2;
+  return forced == 1 ? 1 : 2;
 }
 
 // Weight tiles per unit of the gate/up pass (two: the token tile's B stages
@@ -388,7 +385,7 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
     // down: routed rows scaled by their gate weight, shared rows unscaled
     p.mode = kModeStore;
     p.nt = nt_down;
-    p.a_per_unit = down_a_per_unit(nt_down);
+    p.a_per_unit = down_a_per_unit();
     GemmSegment& r2 = p.seg[0];
     clear(r2);
     if ((e = set_store_A(r2, io.W_down, E, de, F, packed)) != MOE_OK) return e;
