@@ -307,8 +307,12 @@ struct ExpertIO {
   void* Y_shared;        // [S, T, d] or null
 };
 
+// weights_in_Y: scale the routed rows of Y by their routing weights (the
+// moe_grouped_swiglu contract); the layer forward leaves Y unscaled and
+// weights the rows in its combine instead, which keeps the scale out of the
+// GEMM epilogues.
 int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws,
-                    cudaEvent_t ev_up, cudaEvent_t ev_down, cudaStream_t st) {
+                    cudaEvent_t ev_up, cudaEvent_t ev_down, cudaStream_t st, bool weights_in_Y) {
   const Layout L = layout(c, T);
   const int E = c->E_routed, K = c->K, F = c->d_ff, de = d_expert(c);
   const int S = io.x_shared ? c->E_shared : 0;
@@ -317,7 +321,7 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
   int* status = at<int>(ws, L.status);
   RowTile* tiles = at<RowTile>(ws, L.tiles);
   int* ntiles = at<int>(ws, L.ntiles);
-  float* w_perm = at<float>(ws, L.w_perm);
+  float* w_perm = weights_in_Y && io.topk_w ? at<float>(ws, L.w_perm) : nullptr;
   void* Xp = at<void>(ws, L.Xp);
   void* H = at<void>(ws, L.H);
   void* Hs = at<void>(ws, L.Hs);
@@ -396,7 +400,7 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
     r2.ntiles = ntiles_down;
     r2.out = static_cast<__nv_bfloat16*>(io.Y);
     r2.out_ld = de;
-    r2.row_scale = io.topk_w ? w_perm : nullptr;
+    r2.row_scale = w_perm;  // null unless the weights go into Y
     if (S) {
       GemmSegment& s2 = p.seg[1];
       clear(s2);
@@ -455,7 +459,7 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
   g2.tiles = tiles;
   g2.ntiles = ntiles;
   g2.out = static_cast<float*>(io.Y);
-  g2.row_scale = io.topk_w ? w_perm : nullptr;
+  g2.row_scale = w_perm;
   MOE_CUDA(launch_simt_gemm(g2, bound_r, st));
   if (S) {
     SimtGemm g3;
@@ -700,7 +704,8 @@ int32_t moe_grouped_swiglu(const moe_config* cfg, int64_t T, const void* x_e,
   if (!workspace || ws_bytes < layout(cfg, T).total) return fail(MOE_ERR_WORKSPACE, "workspace too small");
   ExpertIO io = {x_e, offsets, perm, topk_w, W_gate_up, W_down, shared ? x_shared : nullptr,
                  Ws_gate_up, Ws_down, Y, Y_shared};
-  return run_experts(cfg, T, io, workspace, nullptr, nullptr, static_cast<cudaStream_t>(stream));
+  return run_experts(cfg, T, io, workspace, nullptr, nullptr, static_cast<cudaStream_t>(stream),
+                     true);
 }
 
 int32_t moe_combine(const moe_config* cfg, int64_t T, const void* Y, const int32_t* inv,
@@ -713,7 +718,7 @@ int32_t moe_combine(const moe_config* cfg, int64_t T, const void* Y, const int32
     return fail(MOE_ERR_ALIGNMENT, "pointer not 16-byte aligned");
   const int D = d_expert(cfg);
   if (D % 8) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "width % 8 != 0");
-  MOE_CUDA(launch_combine(Y, inv, T, cfg->K, D, Y_shared, Y_shared ? cfg->E_shared : 0, T, y,
+  MOE_CUDA(launch_combine(Y, inv, nullptr, T, cfg->K, D, Y_shared, Y_shared ? cfg->E_shared : 0, T, y,
                           cfg->dtype == MOE_BF16, static_cast<cudaStream_t>(stream)));
   return MOE_OK;
 }
@@ -793,21 +798,21 @@ int32_t moe_layer_forward(const moe_config* cfg, int64_t T, const void* x, const
   }
   ExpertIO io = {x_e, offsets, perm, w, W_gate_up, W_down, S ? x : nullptr, Ws_gate_up, Ws_down,
                  at<void>(ws, L.Y), S ? at<void>(ws, L.Ysh) : nullptr};
-  st = run_experts(cfg, T, io, ws, ev(2), ev(3), s);
+  st = run_experts(cfg, T, io, ws, ev(2), ev(3), s, false);
   if (st != MOE_OK) return st;
   if (ev(4)) MOE_CUDA(cudaEventRecord(ev(4), s));
   if (!cfg->d_latent) {
-    MOE_CUDA(launch_combine(at<void>(ws, L.Y), inv, T, cfg->K, cfg->d_model, at<void>(ws, L.Ysh),
-                            S, T, y, bf16, s));
+    MOE_CUDA(launch_combine(at<void>(ws, L.Y), inv, w, T, cfg->K, cfg->d_model,
+                            at<void>(ws, L.Ysh), S, T, y, bf16, s));
   } else {
     // routed sum in latent space, project back, add the shared experts
-    MOE_CUDA(launch_combine(at<void>(ws, L.Y), inv, T, cfg->K, cfg->d_latent, nullptr, 0, 0,
+    MOE_CUDA(launch_combine(at<void>(ws, L.Y), inv, w, T, cfg->K, cfg->d_latent, nullptr, 0, 0,
                             at<void>(ws, L.r_lat), bf16, s));
     st = run_linear(T, cfg->d_latent, cfg->d_model, at<void>(ws, L.r_lat), W_lat_up, nullptr,
                     at<void>(ws, L.U), status, s, cfg->weight_layout == MOE_WEIGHTS_PACKED);
     if (st != MOE_OK) return st;
-    MOE_CUDA(launch_combine(nullptr, nullptr, T, 0, cfg->d_model, at<void>(ws, L.U), 1 + S, T, y,
-                            bf16, s));
+    MOE_CUDA(launch_combine(nullptr, nullptr, nullptr, T, 0, cfg->d_model, at<void>(ws, L.U), 1 + S,
+                            T, y, bf16, s));
   }
   if (ev(5)) MOE_CUDA(cudaEventRecord(ev(5), s));
   return MOE_OK;

@@ -15,7 +15,8 @@
 //                     the T*K pairs -> perm / inv
 //   build_tiles_kernel  row tiles for the grouped GEMMs (one CTA, E <= 1024)
 //   gather_kernel     Xp[r] = x[perm[r] / K], w_perm[r] = topk_w[perm[r]]
-//   combine_kernel    y[t] = sum_k Y[inv[t K + k]] + dense addends, fp32 sums
+//   combine_kernel    y[t] = sum_k w[t, k] Y[inv[t K + k]] + dense addends, fp32
+//                     sums in that order (w = 1 when absent)
 #include "common.cuh"
 #include "internal.h"
 
@@ -242,7 +243,8 @@ struct Vec8<false> {
 // One CTA per token row; D must be a multiple of 8.
 template <bool BF16>
 __global__ void __launch_bounds__(128) combine_kernel(const void* __restrict__ Y,
-                                                      const int32_t* __restrict__ inv, int K,
+                                                      const int32_t* __restrict__ inv,
+                                                      const float* __restrict__ w, int K,
                                                       int D, const void* __restrict__ adds,
                                                       int n_add, int64_t add_stride_rows,
                                                       void* __restrict__ y) {
@@ -250,15 +252,20 @@ __global__ void __launch_bounds__(128) combine_kernel(const void* __restrict__ Y
   const int64_t t = blockIdx.x;
   const int nvec = D / 8;
   __shared__ int slots[64];
-  if (threadIdx.x < K) slots[threadIdx.x] = __ldg(inv + t * K + threadIdx.x);
+  __shared__ float wts[64];
+  if (threadIdx.x < K) {
+    slots[threadIdx.x] = __ldg(inv + t * K + threadIdx.x);
+    wts[threadIdx.x] = w ? __ldg(w + t * K + threadIdx.x) : 1.0f;
+  }
   __syncthreads();
   for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     float tmp[8];
     for (int k = 0; k < K; ++k) {
       V::load(Y, static_cast<int64_t>(slots[k]) * nvec + v, tmp);
+      const float wk = wts[k];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] += tmp[q];
+      for (int q = 0; q < 8; ++q) acc[q] = fmaf(wk, tmp[q], acc[q]);
     }
     for (int a = 0; a < n_add; ++a) {
       V::load(adds, (a * add_stride_rows + t) * nvec + v, tmp);
@@ -328,18 +335,18 @@ cudaError_t launch_gather(const void* x, int64_t T, int K, int width, int elem_b
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const void* Y, const int32_t* inv, int64_t T, int K, int D,
-                           const void* adds, int n_add, int64_t add_stride_rows, void* y,
+cudaError_t launch_combine(const void* Y, const int32_t* inv, const float* w, int64_t T, int K,
+                           int D, const void* adds, int n_add, int64_t add_stride_rows, void* y,
                            bool bf16, cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
   if (bf16) {
     note_launch();
-    combine_kernel<true><<<static_cast<unsigned>(T), 128, 0, stream>>>(Y, inv, K, D, adds, n_add,
-                                                                       add_stride_rows, y);
+    combine_kernel<true><<<static_cast<unsigned>(T), 128, 0, stream>>>(Y, inv, w, K, D, adds,
+                                                                       n_add, add_stride_rows, y);
   } else {
     note_launch();
-    combine_kernel<false><<<static_cast<unsigned>(T), 128, 0, stream>>>(Y, inv, K, D, adds, n_add,
-                                                                        add_stride_rows, y);
+    combine_kernel<false><<<static_cast<unsigned>(T), 128, 0, stream>>>(Y, inv, w, K, D, adds,
+                                                                        n_add, add_stride_rows, y);
   }
   return cudaGetLastError();
 }

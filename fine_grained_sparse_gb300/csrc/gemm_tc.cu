@@ -70,6 +70,7 @@ __host__ __device__ constexpr uint32_t b_stage_bytes_of(int nt, bool pair) {
 
 struct Unit {
   int seg, group, b_row, out_row, n_rows, ob, n_a, ntiles;
+  int scale_row;  // row of the tile's first token in row_scale (the unpadded row space)
   int blk0;    // first 128-row A tile of the unit along O
   int k0, k1;  // k steps [k0, k1) of this unit (all of K unless split)
   int split;
@@ -119,6 +120,7 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int unit
     // packed activations live in the padded row space
     x.b_row = s->b_packed ? t.prow : t.row_start;
     x.out_row = s->out_packed ? t.prow : t.row_start;
+    x.scale_row = t.row_start;
     x.n_rows = t.n_rows;
     x.ntiles = any.ntiles;
   } else {
@@ -131,6 +133,7 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int unit
     x.n_rows = min(nt, s->rows - t0);
     x.b_row = static_cast<int>(g * s->b_group_stride + t0);
     x.out_row = static_cast<int>(g * s->out_group_stride + t0);
+    x.scale_row = x.out_row;
     x.ntiles = tpg;
   }
   if (p.a_per_unit == 2) {
@@ -568,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
               for (int j = 0; j < 16; ++j) {
                 val[j] = __uint_as_float(v[j]);
                 if (row_scale)  // padding tokens read the tile's last row's scale
-                  val[j] *= __ldg(row_scale + x.out_row + min(tok0 + j, x.n_rows - 1));
+                  val[j] *= __ldg(row_scale + x.scale_row + min(tok0 + j, x.n_rows - 1));
               }
 #pragma unroll
               for (int hlf = 0; hlf < 2; ++hlf) {
@@ -591,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                   if (tok < x.n_rows) {
                     const int64_t row = x.out_row + tok;
                     float val = __uint_as_float(v[j]);
-                    if (row_scale) val *= __ldg(row_scale + row);
+                    if (row_scale) val *= __ldg(row_scale + x.scale_row + tok);
                     if (add) val += __bfloat162float(add[row * add_ld + o]);
                     if (out_f32)
                       out_f32[row * ld + o] = val;

@@ -74,8 +74,10 @@ cudaError_t launch_gather(const void* x, int64_t T, int K, int width, int elem_b
 
 // y[t] = sum_k Y[inv[t*K+k]] (K may be 0) + sum_{a < n_add} add_a[t] where
 // add_a = adds + a * add_stride rows of width D.  fp32 sums, fixed order.
-cudaError_t launch_combine(const void* Y, const int32_t* inv, int64_t T, int K, int D,
-                           const void* adds, int n_add, int64_t add_stride_rows, void* y,
+// w: routing weights [T, K] in token order applied to the routed rows, or
+// null (weights already in Y).
+cudaError_t launch_combine(const void* Y, const int32_t* inv, const float* w, int64_t T, int K,
+                           int D, const void* adds, int n_add, int64_t add_stride_rows, void* y,
                            bool bf16, cudaStream_t stream);
 
 // ------------------------------------------------- tensor-core grouped GEMM
@@ -110,7 +112,8 @@ struct GemmSegment {
   __nv_bfloat16* out;  // bf16 output, or
   float* out_f32;      // fp32 output (store mode)
   int64_t out_ld;
-  const float* row_scale;    // store mode: per output row, may be null
+  const float* row_scale;    // store mode: per token row (the unpadded row space),
+                             // scales the output row; may be null
   const __nv_bfloat16* add;  // store mode: added to the output, may be null
   int64_t add_ld;
   // packed activations (see launch_gather_packed): B read by one bulk copy
