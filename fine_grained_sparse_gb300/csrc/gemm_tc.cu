@@ -149,6 +149,91 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int unit
   return x;
 }
 
+// Epilogue helpers over one 64-column TMEM load (64 tokens from tok0): the
+// whole chunk is one straight-line block, so the 8 x 8 transposes of its
+// four 16-token groups overlap; tokens past n_rows are computed on the
+// accumulator's padding columns and not stored.
+
+// SwiGLU: lane l < 16 holds the gate and lane l + 16 the up value of feature
+// blk*64 + 16q + (l & 15); for each 16-token group the gate lane forms h for
+// tokens 0..7 and the up lane for 8..15, each receiving the other half's
+// values for its tokens, and after the transpose within each lane octet
+// lane i holds one token's 8 features: one 16-byte store.  Packed output:
+// plane blk, 8-feature chunk fc swizzled by row % 8.
+__device__ __forceinline__ void swiglu_chunk(const uint32_t (&v)[64], int tok0, int n_rows,
+                                             int lane, int q, int blk, __nv_bfloat16* out,
+                                             bool out_packed, int64_t plane_rows, int64_t out_row,
+                                             int64_t ld) {
+  const bool is_gate = lane < 16;
+  uint32_t w[4][4];
+#pragma unroll
+  for (int sub = 0; sub < 4; ++sub) {
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+      float hh[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int a = sub * 16 + j + e, b = sub * 16 + 8 + j + e;
+        const float own = __uint_as_float(is_gate ? v[a] : v[b]);
+        const float send = __uint_as_float(is_gate ? v[b] : v[a]);
+        const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+        const float g = is_gate ? own : recv;
+        const float u = is_gate ? recv : own;
+        hh[e] = silu_f(g) * u;
+      }
+      w[sub][j >> 1] = pack_bf16x2(hh[0], hh[1]);
+    }
+  }
+#pragma unroll
+  for (int sub = 0; sub < 4; ++sub) transpose8x8_b16(w[sub], lane);
+  const int oct = lane >> 3;
+  const int fc = 2 * q + (oct & 1);
+#pragma unroll
+  for (int sub = 0; sub < 4; ++sub) {
+    const int tok = tok0 + sub * 16 + (oct >> 1) * 8 + (lane & 7);
+    if (tok < n_rows) {
+      const int64_t row = out_row + tok;
+      const int64_t off = out_packed ? (((static_cast<int64_t>(blk) * plane_rows + row) << 6) +
+                                        ((fc ^ static_cast<int>(row & 7)) << 3))
+                                     : row * ld + blk * 64 + fc * 8;
+      *reinterpret_cast<uint4*>(out + off) =
+          make_uint4(w[sub][0], w[sub][1], w[sub][2], w[sub][3]);
+    }
+  }
+}
+
+// Store mode, bf16 rows of whole 16-byte chunks: v holds this lane's output
+// column for the 64 tokens (scaled by scale[t] when kScale); after the
+// transposes lane i of each octet writes tokens i, 8 + i, ... of its
+// octet's 8 columns, dst being the octet's first column in row tok0's row
+// minus tok0 (the tile's first row).
+template <bool kScale>
+__device__ __forceinline__ void store_rows8_chunk(const uint32_t (&v)[64], const float* scale,
+                                                  int tok0, int n_rows, __nv_bfloat16* dst,
+                                                  int64_t ld, bool col_ok, int lane) {
+  uint32_t w[8][4];
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float a = __uint_as_float(v[8 * m + 2 * k]), b = __uint_as_float(v[8 * m + 2 * k + 1]);
+      if (kScale) {  // padding tokens read the tile's last row's scale
+        a *= __ldg(scale + min(tok0 + 8 * m + 2 * k, n_rows - 1));
+        b *= __ldg(scale + min(tok0 + 8 * m + 2 * k + 1, n_rows - 1));
+      }
+      w[m][k] = pack_bf16x2(a, b);
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < 8; ++m) transpose8x8_b16(w[m], lane);
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const int tok = tok0 + 8 * m + (lane & 7);
+    if (tok < n_rows && col_ok)
+      *reinterpret_cast<uint4*>(dst + tok * ld) = make_uint4(w[m][0], w[m][1], w[m][2], w[m][3]);
+  }
+}
+
 // Wait on a barrier for a whole warp: lane 0 polls (bounded) and the verdict
 // is broadcast, so the warp stays converged for the .sync.aligned tcgen05 ops.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
@@ -518,90 +603,33 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           uint32_t v64[64];
           tmem_ld_x64(taddr0 + static_cast<uint32_t>(ch * 64), v64);
           tmem_ld_wait(v64);
+          if (swiglu) {
+            swiglu_chunk(v64, ch * 64, x.n_rows, lane, q, blk, out, out_packed, plane_rows,
+                         x.out_row, ld);
+          } else if (rows8) {
+            const int o0 = blk * 128 + q * 32 + (lane & ~7);
+            __nv_bfloat16* const dst = out + static_cast<int64_t>(x.out_row) * ld + o0;
+            const bool col_ok = o0 < o_limit;
+            if (row_scale)
+              store_rows8_chunk<true>(v64, row_scale + x.scale_row, ch * 64, x.n_rows, dst, ld,
+                                      col_ok, lane);
+            else
+              store_rows8_chunk<false>(v64, nullptr, ch * 64, x.n_rows, dst, ld, col_ok, lane);
+          } else {
+            const int o = blk * 128 + q * 32 + lane;
+            if (o < o_limit) {
 #pragma unroll
-          for (int sub = 0; sub < 4; ++sub) {
-            const int tok0 = ch * 64 + sub * 16;
-            if (tok0 >= x.n_rows) break;
-            uint32_t v[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = v64[sub * 16 + j];
-            if (swiglu) {
-              // lane l < 16 holds the gate and lane l + 16 the up value of
-              // feature blk*64 + 16q + (l & 15) for these 16 tokens: the
-              // gate lane forms h for tokens 0..7, the up lane for 8..15,
-              // each receiving the other half's values for its tokens
-              const bool is_gate = lane < 16;
-              uint32_t w[4];
-#pragma unroll
-              for (int j = 0; j < 8; j += 2) {
-                float hh[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                  const float own = __uint_as_float(is_gate ? v[j + e] : v[8 + j + e]);
-                  const float send = __uint_as_float(is_gate ? v[8 + j + e] : v[j + e]);
-                  const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
-                  const float g = is_gate ? own : recv;
-                  const float u = is_gate ? recv : own;
-                  hh[e] = silu_f(g) * u;
-                }
-                w[j >> 1] = pack_bf16x2(hh[0], hh[1]);
-              }
-              // each lane octet now holds 8 features x 8 tokens; transposed,
-              // lane i holds token i's 8 features: one 16-byte store
-              transpose8x8_b16(w, lane);
-              const int oct = lane >> 3;
-              const int tok = tok0 + (oct >> 1) * 8 + (lane & 7);
-              if (tok < x.n_rows) {
+              for (int j = 0; j < 64; ++j) {
+                const int tok = ch * 64 + j;
+                if (tok >= x.n_rows) break;
                 const int64_t row = x.out_row + tok;
-                const int fc = 2 * q + (oct & 1);  // 8-feature chunk in the 64-feature block
-                // packed: plane blk, chunk fc swizzled by row % 8
-                const int64_t off =
-                    out_packed ? (((static_cast<int64_t>(blk) * plane_rows + row) << 6) +
-                                  ((fc ^ static_cast<int>(row & 7)) << 3))
-                               : row * ld + blk * 64 + fc * 8;
-                *reinterpret_cast<uint4*>(out + off) = make_uint4(w[0], w[1], w[2], w[3]);
-              }
-            } else if (rows8) {
-              // bf16 rows of 8 output columns: lane i of each octet holds
-              // column o0 + i for 16 tokens; two 8 x 8 transposes give it
-              // token i's and token 8 + i's 8 columns, two 16-byte stores
-              const int o0 = blk * 128 + q * 32 + (lane & ~7);
-              float val[16];
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                val[j] = __uint_as_float(v[j]);
-                if (row_scale)  // padding tokens read the tile's last row's scale
-                  val[j] *= __ldg(row_scale + x.scale_row + min(tok0 + j, x.n_rows - 1));
-              }
-#pragma unroll
-              for (int hlf = 0; hlf < 2; ++hlf) {
-                uint32_t w[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                  w[k] = pack_bf16x2(val[8 * hlf + 2 * k], val[8 * hlf + 2 * k + 1]);
-                transpose8x8_b16(w, lane);
-                const int tok = tok0 + 8 * hlf + (lane & 7);
-                if (tok < x.n_rows && o0 < o_limit)
-                  *reinterpret_cast<uint4*>(out + (x.out_row + tok) * ld + o0) =
-                      make_uint4(w[0], w[1], w[2], w[3]);
-              }
-            } else {
-              const int o = blk * 128 + q * 32 + lane;
-              if (o < o_limit) {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                  const int tok = tok0 + j;
-                  if (tok < x.n_rows) {
-                    const int64_t row = x.out_row + tok;
-                    float val = __uint_as_float(v[j]);
-                    if (row_scale) val *= __ldg(row_scale + x.scale_row + tok);
-                    if (add) val += __bfloat162float(add[row * add_ld + o]);
-                    if (out_f32)
-                      out_f32[row * ld + o] = val;
-                    else
-                      out[row * ld + o] = __float2bfloat16_rn(val);
-                  }
-                }
+                float val = __uint_as_float(v64[j]);
+                if (row_scale) val *= __ldg(row_scale + x.scale_row + tok);
+                if (add) val += __bfloat162float(add[row * add_ld + o]);
+                if (out_f32)
+                  out_f32[row * ld + o] = val;
+                else
+                  out[row * ld + o] = __float2bfloat16_rn(val);
               }
             }
           }
