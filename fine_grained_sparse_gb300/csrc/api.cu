@@ -155,7 +155,8 @@ int32_t check_layer_cfg(const moe_config* c, int64_t T) {
 
 // Workspace regions, each 256-byte aligned, in this order.
 struct Layout {
-  size_t status, topk_idx, topk_w, counts, offsets, poffsets, perm, inv, tiles, ntiles, tiles_down,
+  size_t status, topk_idx, topk_w, counts, offsets, poffsets, perm, inv, ccount, tiles, ntiles,
+      tiles_down,
       w_perm, w_split, logits, Xp, H, Hs, Y, U, Ysh, x_lat, r_lat, x_stage, y_stage, total;
   int64_t plane_rows;    // packed activation planes of the routed rows
   int64_t plane_rows_s;  // and of the shared experts' rows
@@ -183,6 +184,7 @@ Layout layout(const moe_config* c, int64_t T) {
   L.poffsets = take(4 * static_cast<size_t>(c->E_routed + 1));
   L.perm = take(4 * TK);
   L.inv = take(4 * TK);
+  L.ccount = take(4 * static_cast<size_t>(permute_chunks(TK)) * c->E_routed);
   L.tiles = take(sizeof(RowTile) * tiles);
   L.ntiles = take(16);
   L.tiles_down = take(sizeof(RowTile) * tiles);
@@ -678,10 +680,14 @@ int32_t moe_permute(const moe_config* cfg, int64_t T, const int32_t* topk_idx, i
   if (!aligned16(topk_idx) || !aligned16(counts) || !aligned16(offsets) || !aligned16(perm) ||
       !aligned16(inv))
     return fail(MOE_ERR_ALIGNMENT, "pointer not 16-byte aligned");
-  if (!workspace || ws_bytes < kWsHeader) return fail(MOE_ERR_WORKSPACE, "workspace too small");
+  // status word, then the per-chunk counts
+  const size_t need = kWsHeader + 4 * static_cast<size_t>(permute_chunks(T * cfg->K)) *
+                                      static_cast<size_t>(cfg->E_routed);
+  if (!workspace || ws_bytes < need) return fail(MOE_ERR_WORKSPACE, "workspace too small");
   if (!aligned16(workspace)) return fail(MOE_ERR_ALIGNMENT, "workspace not aligned");
   MOE_CUDA(launch_permute(topk_idx, T, cfg->K, cfg->E_routed, counts, offsets, perm, inv,
-                          static_cast<int*>(workspace), static_cast<cudaStream_t>(stream)));
+                          at<int32_t>(workspace, kWsHeader), static_cast<int*>(workspace),
+                          static_cast<cudaStream_t>(stream)));
   return MOE_OK;
 }
 
@@ -788,7 +794,8 @@ int32_t moe_layer_forward(const moe_config* cfg, int64_t T, const void* x, const
   st = moe_router(cfg, T, x, W_r, bias, idx, w, ws, ws_bytes, s);
   if (st != MOE_OK) return st;
   if (ev(1)) MOE_CUDA(cudaEventRecord(ev(1), s));
-  MOE_CUDA(launch_permute(idx, T, cfg->K, cfg->E_routed, counts, offsets, perm, inv, status, s));
+  MOE_CUDA(launch_permute(idx, T, cfg->K, cfg->E_routed, counts, offsets, perm, inv,
+                          at<int32_t>(ws, L.ccount), status, s));
   const void* x_e = x;
   if (cfg->d_latent) {
     st = run_linear(T, cfg->d_model, cfg->d_latent, x, W_lat_down, nullptr, at<void>(ws, L.x_lat),

@@ -8,11 +8,17 @@
 // reproducible.
 //
 // Kernels
-//   histogram_kernel  per-expert counts (shared-memory atomics; counts are
-//                     integers, so the result does not depend on their order)
-//   scatter_kernel    one CTA per expert: its offset from a block reduction
-//                     over the counts, then a stable ballot/prefix scan over
-//                     the T*K pairs -> perm / inv
+// A stable counting sort of the T*K (token, expert) pairs in chunks of
+// consecutive pairs (a power of two from 32 to 1024, about 256 chunks):
+//   chunk_count_kernel  per-chunk, per-expert counts (shared-memory atomics;
+//                       integer counts do not depend on their order)
+//   chunk_scan_kernel   one CTA: counts[e] and offsets (exclusive scan over
+//                       experts), and each chunk's start within each expert
+//                       (exclusive scan over chunks)
+//   chunk_scatter_kernel one warp per chunk, its pairs in order, 32 at a
+//                       time: a pair's slot is its expert's running position
+//                       in the chunk plus its rank among the lanes of the
+//                       same expert (match_any) -> perm / inv
 //   build_tiles_kernel  row tiles for the grouped GEMMs (one CTA, E <= 1024)
 //   gather_kernel     Xp[r] = x[perm[r] / K], w_perm[r] = topk_w[perm[r]]
 //   combine_kernel    y[t] = sum_k w[t, k] Y[inv[t K + k]] + dense addends, fp32
@@ -24,76 +30,91 @@ namespace fgs {
 
 namespace {
 
-__global__ void histogram_kernel(const int32_t* __restrict__ idx, int64_t n, int E,
-                                 int32_t* __restrict__ counts, int* status) {
+constexpr int kChunkThreads = 256;
+constexpr int kScatterWarps = 8;       // chunks per CTA of the scatter
+
+__global__ void __launch_bounds__(kChunkThreads) chunk_count_kernel(
+    const int32_t* __restrict__ idx, int64_t n, int chunk, int E, int32_t* __restrict__ ccount,
+    int* status) {
   extern __shared__ int hist[];
   for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < n; j += stride) {
+  const int64_t j0 = static_cast<int64_t>(blockIdx.x) * chunk;
+  for (int i = threadIdx.x; i < chunk; i += blockDim.x) {
+    const int64_t j = j0 + i;
+    if (j >= n) break;
     const int e = __ldg(idx + j);
-    if (e >= 0 && e < E) {
+    if (e >= 0 && e < E)
       atomicAdd(&hist[e], 1);
-    } else {
+    else
       record_status(status, MOE_ERR_DEVICE_INDEX);
-    }
   }
   __syncthreads();
   for (int i = threadIdx.x; i < E; i += blockDim.x)
-    if (hist[i]) atomicAdd(counts + i, hist[i]);
+    ccount[static_cast<int64_t>(blockIdx.x) * E + i] = hist[i];
 }
 
-__device__ __forceinline__ int block_sum(int v, int* red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  int tot = 0;
-  for (int w = 0; w < nw; ++w) tot += red[w];
-  __syncthreads();
-  return tot;
-}
-
-constexpr int kScatterThreads = 512;
-
-__global__ void __launch_bounds__(kScatterThreads) scatter_kernel(
-    const int32_t* __restrict__ idx, int64_t n, int E, const int32_t* __restrict__ counts,
-    int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
-  __shared__ int red[kScatterThreads / 32];
-  __shared__ int wcnt[kScatterThreads / 32];
-  const int e = blockIdx.x;
-  int part = 0;
-  for (int i = threadIdx.x; i < e; i += blockDim.x) part += counts[i];
-  const int base = block_sum(part, red);
-  const int mine = counts[e];
-  if (threadIdx.x == 0) {
-    offsets[e] = base;
-    if (e == E - 1) offsets[E] = base + mine;
-  }
-  if (mine == 0) return;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const unsigned lt_mask = (1u << lane) - 1u;
-  int running = 0;
-  for (int64_t j0 = 0; j0 < n && running < mine; j0 += blockDim.x) {
-    const int64_t j = j0 + threadIdx.x;
-    const bool hit = j < n && __ldg(idx + j) == e;
-    const unsigned ballot = __ballot_sync(0xffffffffu, hit);
-    if (lane == 0) wcnt[warp] = __popc(ballot);
-    __syncthreads();
-    int before = 0, total = 0;
-    for (int w = 0; w < nw; ++w) {
-      const int c = wcnt[w];
-      before += (w < warp) ? c : 0;
-      total += c;
+// One CTA of 1024 threads (E <= 1024): thread e turns ccount[c][e] into the
+// count of e in chunks before c, sums counts[e], and the CTA scans the
+// counts into offsets.
+__global__ void __launch_bounds__(1024) chunk_scan_kernel(int32_t* __restrict__ ccount,
+                                                          int nchunks, int E,
+                                                          int32_t* __restrict__ counts,
+                                                          int32_t* __restrict__ offsets) {
+  __shared__ int scan[1024];
+  const int e = threadIdx.x;
+  int total = 0;
+  if (e < E) {
+    for (int c = 0; c < nchunks; ++c) {
+      int32_t* q = ccount + static_cast<int64_t>(c) * E + e;
+      const int v = *q;
+      *q = total;
+      total += v;
     }
-    if (hit) {
-      const int slot = base + running + before + __popc(ballot & lt_mask);
+    counts[e] = total;
+  }
+  scan[e] = total;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {  // inclusive Hillis-Steele scan
+    const int v = e >= off ? scan[e - off] : 0;
+    __syncthreads();
+    scan[e] += v;
+    __syncthreads();
+  }
+  if (e < E) offsets[e] = scan[e] - total;
+  if (e == E - 1) offsets[E] = scan[e];
+}
+
+__global__ void __launch_bounds__(32 * kScatterWarps) chunk_scatter_kernel(
+    const int32_t* __restrict__ idx, int64_t n, int chunk, int E,
+    const int32_t* __restrict__ ccount, const int32_t* __restrict__ offsets, int nchunks,
+    int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+  extern __shared__ int cnt_all[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c = blockIdx.x * kScatterWarps + warp;
+  if (c >= nchunks) return;
+  int* cnt = cnt_all + warp * E;  // this chunk's next slot per expert
+  for (int e = lane; e < E; e += 32)
+    cnt[e] = __ldg(offsets + e) + __ldg(ccount + static_cast<int64_t>(c) * E + e);
+  __syncwarp();
+  const unsigned lt_mask = (1u << lane) - 1u;
+  const int64_t j0 = static_cast<int64_t>(c) * chunk;
+  for (int s = 0; s < chunk; s += 32) {
+    const int64_t j = j0 + s + lane;
+    if (j0 + s >= n) break;
+    const int e = j < n ? __ldg(idx + j) : -1;
+    const bool ok = e >= 0 && e < E;
+    // lanes of one expert share a key; every other lane has a key of its own
+    const unsigned mask = __match_any_sync(0xffffffffu, ok ? e : E + lane);
+    const int base = ok ? cnt[e] : 0;
+    __syncwarp();
+    if (ok) {
+      const int slot = base + __popc(mask & lt_mask);
       perm[slot] = static_cast<int32_t>(j);
       inv[j] = slot;
+      if ((mask & lt_mask) == 0) cnt[e] = base + __popc(mask);  // the group's first lane
     }
-    running += total;
-    __syncthreads();
+    __syncwarp();
   }
 }
 
@@ -172,9 +193,17 @@ __global__ void __launch_bounds__(256) gather_packed_kernel(
     const int j = __ldg(perm + r);
     const uint4* src = x + static_cast<int64_t>(j / K) * vec_per_row;
     const int sw = static_cast<int>(R & 7);
-    for (int v = lane; v < vec_per_row; v += 32) {
-      const int64_t plane = v >> 3;
-      Xp[(plane * plane_rows + R) * 8 + ((v & 7) ^ sw)] = __ldg(src + v);
+    // four 16-byte loads in flight per lane before their stores
+    for (int v0 = lane; v0 < vec_per_row; v0 += 128) {
+      uint4 t[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (v0 + 32 * u < vec_per_row) t[u] = __ldg(src + v0 + 32 * u);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int v = v0 + 32 * u;
+        if (v < vec_per_row) Xp[((v >> 3) * plane_rows + R) * 8 + ((v & 7) ^ sw)] = t[u];
+      }
     }
     if (lane == 0 && w_perm) w_perm[r] = topk_w ? __ldg(topk_w + j) : 1.0f;
   }
@@ -278,23 +307,38 @@ __global__ void __launch_bounds__(128) combine_kernel(const void* __restrict__ Y
 
 }  // namespace
 
+int permute_chunk(int64_t n) {
+  int c = 32;
+  while (c < 1024 && static_cast<int64_t>(c) * 256 < n) c <<= 1;
+  return c;
+}
+
+int64_t permute_chunks(int64_t n) {
+  const int c = permute_chunk(n);
+  return (n + c - 1) / c;
+}
+
 cudaError_t launch_permute(const int32_t* topk_idx, int64_t T, int K, int E, int32_t* counts,
-                           int32_t* offsets, int32_t* perm, int32_t* inv, int* status,
-                           cudaStream_t stream) {
+                           int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* ccount,
+                           int* status, cudaStream_t stream) {
   const int64_t n = T * K;
-  cudaError_t err = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, stream);
-  if (err != cudaSuccess) return err;
-  const int threads = 256;
-  int64_t blocks = (n + threads * 4 - 1) / (threads * 4);
-  if (blocks > 1024) blocks = 1024;
-  if (blocks < 1) blocks = 1;
+  const int chunk = permute_chunk(n);
+  const int64_t nchunks = permute_chunks(n);
+  if (nchunks < 1) return cudaSuccess;
   note_launch();
-  histogram_kernel<<<static_cast<unsigned>(blocks), threads, sizeof(int) * E, stream>>>(
-      topk_idx, n, E, counts, status);
+  chunk_count_kernel<<<static_cast<unsigned>(nchunks), kChunkThreads, sizeof(int) * E, stream>>>(
+      topk_idx, n, chunk, E, ccount, status);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  note_launch();
+  chunk_scan_kernel<<<1, 1024, 0, stream>>>(ccount, static_cast<int>(nchunks), E, counts,
+                                            offsets);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
+  const unsigned blocks = static_cast<unsigned>((nchunks + kScatterWarps - 1) / kScatterWarps);
   note_launch();
-  scatter_kernel<<<E, kScatterThreads, 0, stream>>>(topk_idx, n, E, counts, offsets, perm, inv);
+  chunk_scatter_kernel<<<blocks, 32 * kScatterWarps, sizeof(int) * E * kScatterWarps, stream>>>(
+      topk_idx, n, chunk, E, ccount, offsets, static_cast<int>(nchunks), perm, inv);
   return cudaGetLastError();
 }
 

@@ -42,9 +42,12 @@ struct __align__(16) RowTile {
   int pad0, pad1;
 };
 
+// Chunks of the pair sequence the permute counts separately (scratch:
+// permute_chunks(T*K) * E int32 in ccount).
+int64_t permute_chunks(int64_t n);
 cudaError_t launch_permute(const int32_t* topk_idx, int64_t T, int K, int E, int32_t* counts,
-                           int32_t* offsets, int32_t* perm, int32_t* inv, int* status,
-                           cudaStream_t stream);
+                           int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* ccount,
+                           int* status, cudaStream_t stream);
 
 // Row tiles of the routed experts: for expert e with m_e rows starting at
 // offsets[e], tiles of near-equal height (multiples of 8 but the last) and at
