@@ -65,11 +65,17 @@ __global__ void __launch_bounds__(1024) chunk_scan_kernel(int32_t* __restrict__ 
   const int e = threadIdx.x;
   int total = 0;
   if (e < E) {
-    for (int c = 0; c < nchunks; ++c) {
-      int32_t* q = ccount + static_cast<int64_t>(c) * E + e;
-      const int v = *q;
-      *q = total;
-      total += v;
+    // 16 independent loads in flight, then their prefix
+    for (int c0 = 0; c0 < nchunks; c0 += 16) {
+      int v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        v[i] = c0 + i < nchunks ? ccount[static_cast<int64_t>(c0 + i) * E + e] : 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (c0 + i < nchunks) ccount[static_cast<int64_t>(c0 + i) * E + e] = total;
+        total += v[i];
+      }
     }
     counts[e] = total;
   }
@@ -193,14 +199,14 @@ __global__ void __launch_bounds__(256) gather_packed_kernel(
     const int j = __ldg(perm + r);
     const uint4* src = x + static_cast<int64_t>(j / K) * vec_per_row;
     const int sw = static_cast<int>(R & 7);
-    // four 16-byte loads in flight per lane before their stores
-    for (int v0 = lane; v0 < vec_per_row; v0 += 128) {
-      uint4 t[4];
+    // eight 16-byte loads in flight per lane before their stores
+    for (int v0 = lane; v0 < vec_per_row; v0 += 256) {
+      uint4 t[8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int u = 0; u < 8; ++u)
         if (v0 + 32 * u < vec_per_row) t[u] = __ldg(src + v0 + 32 * u);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 8; ++u) {
         const int v = v0 + 32 * u;
         if (v < vec_per_row) Xp[((v >> 3) * plane_rows + R) * 8 + ((v & 7) ^ sw)] = t[u];
       }
