@@ -370,8 +370,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     int stage = 0;
     uint32_t phase = 0;
     int64_t issued = 0;
+    Unit nx = u_first < total ? decode_unit(p, u_first, units0, units1, nt, rank) : Unit{};
     for (int u = u_first; u < total; u += u_step) {
-      const Unit x = decode_unit(p, u, units0, units1, nt, rank);
+      // the next unit's tile-table loads overlap this unit's work
+      const Unit x = nx;
+      if (u + u_step < total) nx = decode_unit(p, u + u_step, units0, units1, nt, rank);
       const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
       const uint32_t tx = kATileBytes * x.n_a;
       // a weight block read by one token tile is streamed; one shared by
@@ -444,8 +447,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     int estage = 0;             // weight stage of k step issued - Sb
     uint32_t ephase = 0;
     int64_t issued = 0;
+    Unit nx = u_first < total ? decode_unit(p, u_first, units0, units1, nt, rank) : Unit{};
     for (int u = u_first; u < total; u += u_step) {
-      const Unit x = decode_unit(p, u, units0, units1, nt, rank);
+      // the next unit's tile-table loads overlap this unit's work
+      const Unit x = nx;
+      if (u + u_step < total) nx = decode_unit(p, u + u_step, units0, units1, nt, rank);
       const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
       // paired: this CTA's half of the tile's rows (rounded up to 16), as
       // 32-row boxes; the rows past the half that a box brings in are not
@@ -509,8 +515,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     int sa = 0, sb = 0;
     uint32_t pa = 0;
     int c = 0;
+    Unit nx = u_first < total ? decode_unit(p, u_first, units0, units1, nt, rank) : Unit{};
     for (int u = u_first; u < total; u += u_step) {
-      const Unit x = decode_unit(p, u, units0, units1, nt, rank);
+      // the next unit's tile-table loads overlap this unit's work
+      const Unit x = nx;
+      if (u + u_step < total) nx = decode_unit(p, u + u_step, units0, units1, nt, rank);
       const uint32_t n = static_cast<uint32_t>((x.n_rows + 15) & ~15);
       const Regions rg = regions_of(p, n, c);
       bool ok = mbar_wait_bounded<kPair>(tempty_bar(c & 1), region_phase(c) ^ 1u, abort_flag,
@@ -568,8 +577,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     const bool swiglu = p.mode == kModeSwiGLU;
     const bool single = p.a_per_unit == 1;
     int c = 0;
+    Unit nx = u_first < total ? decode_unit(p, u_first, units0, units1, nt, rank) : Unit{};
     for (int u = u_first; u < total; u += u_step) {
-      const Unit x = decode_unit(p, u, units0, units1, nt, rank);
+      // the next unit's tile-table loads overlap this unit's work
+      const Unit x = nx;
+      if (u + u_step < total) nx = decode_unit(p, u + u_step, units0, units1, nt, rank);
       const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
       // the segment's output description, once per unit, in registers
       __nv_bfloat16* const out = s->out;
