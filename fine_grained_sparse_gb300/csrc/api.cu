@@ -56,22 +56,28 @@ int d_expert(const moe_config* c) { return c->d_latent ? c->d_latent : c->d_mode
 // Parts of the router's K (= 3 d: the hi, mid and lo weight pieces) summed
 // separately: one per piece, and each piece cut further when T is small so
 // that the GEMM has enough independent units.
+int env_int(const char* name, int fallback) {
+  const char* v = getenv(name);
+  return (v && *v) ? atoi(v) : fallback;
+}
+
+// K parts of the router GEMM (a multiple of 3: the split weight's three
+// bf16 terms are separate parts): enough parts that small batches still
+// occupy the SMs.
 int router_ksplit(int64_t T, int d) {
-  int h = 1;
+  static const int forced = env_int("FGS_ROUTER_KSPLIT", 0);  // tuning override
   const int kd = d / 64;
+  if (forced >= 3 && forced % 3 == 0 && kd % (forced / 3) == 0) return forced;
+  int h = 1;
   for (int c = 1; c <= 16 && static_cast<int64_t>(c) * T <= 2048; ++c)
     if (kd % c == 0) h = c;
   return 3 * h;
 }
 
-int router_tile(int64_t T) { return T <= 256 ? 32 : 128; }
-
-// token tile of the tensor-core GEMMs: small batches (few rows per expert)
-// take 32-row tiles and the deepest weight ring; large ones 256-row tiles,
-// so that most experts are one tile and their weights are read once
-int env_int(const char* name, int fallback) {
-  const char* v = getenv(name);
-  return (v && *v) ? atoi(v) : fallback;
+int router_tile(int64_t T) {
+  static const int forced = env_int("FGS_ROUTER_TILE", 0);  // tuning override
+  if (forced == 32 || forced == 64 || forced == 128 || forced == 256) return forced;
+  return T <= 256 ? 32 : 128;
 }
 
 // Token tiles: 32 rows for small batches; otherwise 256, so most experts are
