@@ -10,32 +10,42 @@
 // every shared expert.  The K3 latent projections and the router logits use
 // the down-pass form (store mode) with one group.
 //
+// (The layer forward applies the routing weight w_r in its combine; the
+// down pass stores the unscaled product there.)
+//
 // Swap-AB tiling.  The MMA's M side is a block of WEIGHT rows and its N side
 // (16..256, a multiple of 16) a block of token rows of one expert, so an
 // expert with few tokens still streams its weights through full-height MMAs.
 // A unit is 256 weight rows -- two 128-row A tiles, two TMEM accumulators --
 // against one token tile, so each token tile in shared memory feeds twice
 // the MMA work.  Weights and tokens flow through separate rings with their
-// own producer warps: the weight ring is deep (5-6 stages of 32 KB, the HBM
-// stream), the token ring shallow (2-3 stages, mostly L2 hits).
+// own producer warps (the weight ring takes what shared memory the token
+// ring leaves: 4 stages of 32 KB beside 3 token stages of 256 rows), but
+// share one full and one empty barrier per k step, so the MMA issuer waits
+// once and commits once per k step.
 //   A tiles: 2 x (128 rows x 64 k) bf16, K-major, 128-byte swizzle (32 KB)
-//   B tile:  up to nt rows x 64 k, same layout, loaded as 32-row boxes
+//   B tile:  up to nt rows x 64 k, same layout (one bulk copy of packed
+//            activation rows, or 32-row TMA boxes)
 //   D:       2 accumulators x N fp32 columns in TMEM (regions below).
 // For the gate/up pass each A tile interleaves the two halves of W_gate_up
 // [E, 2F, d] in 16-row slices: rows 32q..32q+15 are gate features
 // 16q + (0..15) of the tile's 64 and rows 32q+16..32q+31 the up features with
 // the same indices.  TMEM lane quadrant q (the one warp q%4 may read) thus
 // holds both halves of 16 features, and the SwiGLU is one shuffle away.
+// The epilogue turns each lane's column of 16 tokens into 16-byte rows of
+// the output with 8 x 8 transposes inside lane octets.
 //
 // Units are ordered (segment, expert, output block, token tile) with the
 // token tile fastest, so the CTAs that share an expert's weight block run
-// side by side and the second reader finds the block in L2.
+// side by side and the second reader finds the block in L2; the second
+// segment (the shared experts) comes first.
 //
 // Warp roles (one CTA per SM, persistent over the units):
 //   warp 0 lane 0: weight producer (bulk copies of packed weights, or TMA);
-//   warp 1 lane 0: MMA issuer; warp 2 lane 0: token producer (TMA);
+//   warp 1 lane 0: MMA issuer; warp 2 lane 0: token producer;
 //   warps 3..10: epilogue, warp w reads lane quadrant w%4 of accumulator
-//   (w-3)/4 (TMEM -> registers -> global stores).
+//   (w-3)/4, or of the single accumulator's column chunks (w-3)/4, 2 + ...
+//   (TMEM -> registers -> global stores).
 // Every wait is bounded (%globaltimer); on expiry the CTA records
 // MOE_ERR_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
 #include <cudaTypedefs.h>
