@@ -186,10 +186,15 @@ def per_step_work(shape, counts):
 
 
 def kernel_source_hash():
+    """Hash of the GEMM kernel's sources with comments and blank space
+    removed, so that edits to comments keep a profile valid."""
     h = hashlib.sha256()
     for name in ("gemm_tc.cu", "common.cuh", "internal.h"):
-        with open(os.path.join(ROOT, "fine_grained_sparse_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "fine_grained_sparse_gb300", "csrc", name)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update("".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 
