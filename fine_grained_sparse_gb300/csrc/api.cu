@@ -12,6 +12,7 @@
 #include <cmath>
 #include <atomic>
 #include <mutex>
+#include <unordered_map>
 
 #include "common.cuh"
 #include "internal.h"
@@ -220,7 +221,7 @@ Layout layout(const moe_config* c, int64_t T) {
   o = round256(o + U_bytes + static_cast<size_t>(S) * T * c->d_model * eb);
   L.x_lat = take(c->d_latent ? static_cast<size_t>(T) * c->d_latent * eb : 0);
   L.r_lat = take(c->d_latent ? static_cast<size_t>(T) * c->d_latent * eb : 0);
-  L.x_stage = take(static_cast<size_t>(T) * c->d_model * eb);
+  L.x_stage = take(2 * round256(static_cast<size_t>(T) * c->d_model * eb));  // two, alternating
   L.y_stage = take(static_cast<size_t>(T) * c->d_model * eb);
   L.total = o;
   return L;
@@ -831,6 +832,24 @@ int32_t moe_layer_forward(const moe_config* cfg, int64_t T, const void* x, const
   return MOE_OK;
 }
 
+namespace {
+
+// Per-workspace state of the pipelined host-buffer forward: which staging
+// buffer the next call takes, and the events that order the copy stream and
+// the caller's stream around each buffer.
+struct HostPipe {
+  cudaEvent_t copied[2] = {nullptr, nullptr};  // x landed in staging buffer b
+  cudaEvent_t read[2] = {nullptr, nullptr};    // the forward that read buffer b finished
+  bool used[2] = {false, false};
+  int next = 0;
+};
+
+std::mutex g_pipe_mutex;
+std::unordered_map<void*, HostPipe> g_pipes;
+cudaStream_t g_copy_stream[64] = {nullptr};
+
+}  // namespace
+
 int32_t moe_layer_forward_host(const moe_config* cfg, int64_t T, const void* x_host,
                                const float* W_r, const float* bias, const void* W_gate_up,
                                const void* W_down, const void* Ws_gate_up, const void* Ws_down,
@@ -843,13 +862,38 @@ int32_t moe_layer_forward_host(const moe_config* cfg, int64_t T, const void* x_h
   if (!workspace || ws_bytes < L.total) return fail(MOE_ERR_WORKSPACE, "workspace too small");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t bytes = static_cast<size_t>(T) * cfg->d_model * elem_bytes(cfg);
-  void* xd = at<void>(workspace, L.x_stage);
+  int dev = 0;
+  MOE_CUDA(cudaGetDevice(&dev));
+  if (dev >= 64) return fail(MOE_ERR_INVALID_ARG, "device index above 63");
+  HostPipe* hp;
+  cudaStream_t cs;
+  int b;
+  {
+    std::lock_guard<std::mutex> lock(g_pipe_mutex);
+    if (!g_copy_stream[dev])
+      MOE_CUDA(cudaStreamCreateWithFlags(&g_copy_stream[dev], cudaStreamNonBlocking));
+    cs = g_copy_stream[dev];
+    hp = &g_pipes[workspace];
+    for (int i = 0; i < 2; ++i) {
+      if (!hp->copied[i]) MOE_CUDA(cudaEventCreateWithFlags(&hp->copied[i], cudaEventDisableTiming));
+      if (!hp->read[i]) MOE_CUDA(cudaEventCreateWithFlags(&hp->read[i], cudaEventDisableTiming));
+    }
+    b = hp->next;
+    hp->next ^= 1;
+  }
+  void* xd = at<void>(workspace, L.x_stage + b * round256(bytes));
   void* yd = at<void>(workspace, L.y_stage);
-  MOE_CUDA(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s));
+  // the buffer is free once the forward that last read it has finished
+  if (hp->used[b]) MOE_CUDA(cudaStreamWaitEvent(cs, hp->read[b], 0));
+  MOE_CUDA(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, cs));
+  MOE_CUDA(cudaEventRecord(hp->copied[b], cs));
+  MOE_CUDA(cudaStreamWaitEvent(s, hp->copied[b], 0));
   st = moe_layer_forward(cfg, T, xd, W_r, bias, W_gate_up, W_down, Ws_gate_up, Ws_down,
                          W_lat_down, W_lat_up, yd, nullptr, nullptr, nullptr, workspace, ws_bytes,
                          nullptr, stream);
   if (st != MOE_OK) return st;
+  MOE_CUDA(cudaEventRecord(hp->read[b], s));
+  hp->used[b] = true;
   MOE_CUDA(cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s));
   return MOE_OK;
 }

@@ -262,7 +262,13 @@ int32_t moe_layer_forward(const moe_config* cfg, int64_t T, const void* x, const
  * copies; pageable memory works but the copies then block).  The call
  * enqueues the host-to-device copy of x into the workspace, the forward and
  * the device-to-host copy of y, and returns without waiting: y_host is valid
- * after `stream` has been synchronised.  Weights stay device pointers. */
+ * after `stream` has been synchronised.  Weights stay device pointers.
+ * Successive calls on one workspace are pipelined: x is copied on a copy
+ * stream of the library into one of two staging buffers, alternating, so
+ * the copy for one call overlaps the forward of the call before it.  That
+ * copy therefore does not wait for work enqueued earlier on `stream`: x_host
+ * must hold its values when the call is made (host writes, or device work
+ * already synchronised). */
 int32_t moe_layer_forward_host(const moe_config* cfg, int64_t T, const void* x_host,
                                const float* W_r, const float* bias, const void* W_gate_up,
                                const void* W_down, const void* Ws_gate_up, const void* Ws_down,
