@@ -316,6 +316,29 @@ struct ExpertIO {
   void* Y_shared;        // [S, T, d] or null
 };
 
+// The shared experts' gate/up pass as a GEMM segment: every token of x
+// against each shared expert, SwiGLU outputs into the packed planes Hs.
+int32_t shared_gate_up_segment(GemmSegment& s, const moe_config* c, int64_t T, const void* x,
+                               const void* Ws_gate_up, const Layout& L, void* ws, bool packed) {
+  clear(s);
+  int32_t e;
+  if ((e = set_gate_up_A(s, Ws_gate_up, c->E_shared, c->d_ff_shared, c->d_model, packed)) != MOE_OK)
+    return e;
+  if ((e = set_B(s, x, T, c->d_model)) != MOE_OK) return e;
+  s.a128 = c->d_ff_shared / 64;
+  s.groups = c->E_shared;
+  s.rows = static_cast<int>(T);
+  s.b_group_stride = 0;
+  s.out_group_stride = L.Ts;
+  s.out = at<__nv_bfloat16>(ws, L.Hs);
+  s.out_packed = 1;
+  s.out_plane_rows = L.plane_rows_s;
+  s.own_mode = 1;
+  s.mode = kModeSwiGLU;
+  s.nt = token_tile(T);
+  return MOE_OK;
+}
+
 // weights_in_Y: scale the routed rows of Y by their routing weights (the
 // moe_grouped_swiglu contract); the layer forward leaves Y unscaled and
 // weights the rows in its combine instead, which keeps the scale out of the
@@ -377,27 +400,19 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
     r.out = static_cast<__nv_bfloat16*>(H);
     r.out_packed = 1;
     r.out_plane_rows = L.plane_rows;
-    if (S) {
-      GemmSegment& s = p.seg[1];
-      clear(s);
-      if ((e = set_gate_up_A(s, io.Ws_gate_up, S, Fs, d, packed)) != MOE_OK) return e;
-      if ((e = set_B(s, io.x_shared, T, d)) != MOE_OK) return e;
-      s.a128 = Fs / 64;
-      s.groups = S;
-      s.rows = static_cast<int>(T);
-      s.b_group_stride = 0;
-      s.out_group_stride = L.Ts;
-      s.out = static_cast<__nv_bfloat16*>(Hs);
-      s.out_packed = 1;
-      s.out_plane_rows = L.plane_rows_s;
-    }
+    if (p.nseg == 2 &&
+        (e = shared_gate_up_segment(p.seg[1], c, T, io.x_shared, io.Ws_gate_up, L, ws, packed)) !=
+            MOE_OK)
+      return e;
     p.pair = use_pairs(false);
     MOE_CUDA(launch_tc_gemm(p, num_sms(), st));
     if (ev_down) MOE_CUDA(cudaEventRecord(ev_down, st));
 
-    // down: routed rows scaled by their gate weight, shared rows unscaled
+    // down: routed rows (scaled by their gate weight when weights_in_Y) and
+    // the shared experts' rows, one launch
     p.mode = kModeStore;
     p.nt = nt_down;
+    p.nseg = S ? 2 : 1;
     p.a_per_unit = down_a_per_unit();
     GemmSegment& r2 = p.seg[0];
     clear(r2);

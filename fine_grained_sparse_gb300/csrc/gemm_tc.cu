@@ -94,7 +94,8 @@ __device__ __forceinline__ int out_blocks(const GemmParams& p, const GemmSegment
   return (p.a_per_unit == 2 || p.pair) ? (s->a128 + 1) / 2 : s->a128;
 }
 
-__device__ __forceinline__ int segment_units(const GemmParams& p, const GemmSegment* s, int nt) {
+__device__ __forceinline__ int segment_units(const GemmParams& p, const GemmSegment* s) {
+  const int nt = s->nt;
   const int ob = out_blocks(p, s);
   if (s->tiles) return *s->ntiles * ob;
   return s->groups * ((s->rows + nt - 1) / nt) * ob * ksplit_of(s);
@@ -104,11 +105,12 @@ __device__ __forceinline__ int segment_units(const GemmParams& p, const GemmSegm
 // weights shared by all token tiles) come first, the first segment's
 // weight-streaming units after them.
 __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int units0, int units1,
-                                            int nt, int rank) {
+                                            int rank) {
   Unit x;
   x.seg = u < units1 ? 1 : 0;
   int local = x.seg ? u : u - units1;
   const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
+  const int nt = s->nt;
   const int OB = out_blocks(p, s);
   const int ns = ksplit_of(s);
   const int kps = s->k_steps / ns;
@@ -368,8 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int units0 = segment_units(p, &p.seg[0], nt);
-  const int units1 = p.nseg > 1 ? segment_units(p, &p.seg[1], nt) : 0;
+  const int units0 = segment_units(p, &p.seg[0]);
+  const int units1 = p.nseg > 1 ? segment_units(p, &p.seg[1]) : 0;
   const int total = units0 + units1;
 
   if (warp == 0 && lane == 0) {
@@ -380,11 +382,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     int stage = 0;
     uint32_t phase = 0;
     int64_t issued = 0;
-    Unit nx = u_first < total ? decode_unit(p, u_first, units0, units1, nt, rank) : Unit{};
+    Unit nx = u_first < total ? decode_unit(p, u_first, units0, units1, rank) : Unit{};
     for (int u = u_first; u < total; u += u_step) {
       // the next unit's tile-table loads overlap this unit's work
       const Unit x = nx;
-      if (u + u_step < total) nx = decode_unit(p, u + u_step, units0, units1, nt, rank);
+      if (u + u_step < total) nx = decode_unit(p, u + u_step, units0, units1, rank);
       const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
       const uint32_t tx = kATileBytes * x.n_a;
       // a weight block read by one token tile is streamed; one shared by
@@ -419,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           for (int a = 0; a < x.n_a; ++a) {
             const int blk = x.blk0 + a;  // 128-row A tile index along O
             const uint32_t dst = a_dst + a * kATileBytes;
-            if (p.mode == kModeSwiGLU) {
+            if (s->mode == kModeSwiGLU) {
               if (s->a_boxes == 1) {
                 tma_load_5d(dst, &s->tmA, fb, kc, 0, 0, blk * 4, x.group, pol_w);
               } else {
@@ -457,11 +459,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     int estage = 0;             // weight stage of k step issued - Sb
     uint32_t ephase = 0;
     int64_t issued = 0;
-    Unit nx = u_first < total ? decode_unit(p, u_first, units0, units1, nt, rank) : Unit{};
+    Unit nx = u_first < total ? decode_unit(p, u_first, units0, units1, rank) : Unit{};
     for (int u = u_first; u < total; u += u_step) {
       // the next unit's tile-table loads overlap this unit's work
       const Unit x = nx;
-      if (u + u_step < total) nx = decode_unit(p, u + u_step, units0, units1, nt, rank);
+      if (u + u_step < total) nx = decode_unit(p, u + u_step, units0, units1, rank);
       const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
       // paired: this CTA's half of the tile's rows (rounded up to 16), as
       // 32-row boxes; the rows past the half that a box brings in are not
@@ -525,11 +527,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     int sa = 0, sb = 0;
     uint32_t pa = 0;
     int c = 0;
-    Unit nx = u_first < total ? decode_unit(p, u_first, units0, units1, nt, rank) : Unit{};
+    Unit nx = u_first < total ? decode_unit(p, u_first, units0, units1, rank) : Unit{};
     for (int u = u_first; u < total; u += u_step) {
       // the next unit's tile-table loads overlap this unit's work
       const Unit x = nx;
-      if (u + u_step < total) nx = decode_unit(p, u + u_step, units0, units1, nt, rank);
+      if (u + u_step < total) nx = decode_unit(p, u + u_step, units0, units1, rank);
       const uint32_t n = static_cast<uint32_t>((x.n_rows + 15) & ~15);
       const Regions rg = regions_of(p, n, c);
       bool ok = mbar_wait_bounded<kPair>(tempty_bar(c & 1), region_phase(c) ^ 1u, abort_flag,
@@ -584,15 +586,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     const int q = warp & 3;           // TMEM lane quadrant this warp may access
     const int grp = (warp - 3) >> 2;  // warp group: accumulator (two-tile units)
                                       // or column half (single-tile units)
-    const bool swiglu = p.mode == kModeSwiGLU;
+
     const bool single = p.a_per_unit == 1;
     int c = 0;
-    Unit nx = u_first < total ? decode_unit(p, u_first, units0, units1, nt, rank) : Unit{};
+    Unit nx = u_first < total ? decode_unit(p, u_first, units0, units1, rank) : Unit{};
     for (int u = u_first; u < total; u += u_step) {
       // the next unit's tile-table loads overlap this unit's work
       const Unit x = nx;
-      if (u + u_step < total) nx = decode_unit(p, u + u_step, units0, units1, nt, rank);
+      if (u + u_step < total) nx = decode_unit(p, u + u_step, units0, units1, rank);
       const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
+      const bool swiglu = s->mode == kModeSwiGLU;
       // the segment's output description, once per unit, in registers
       __nv_bfloat16* const out = s->out;
       float* const out_f32 = s->out_f32 ? s->out_f32 + x.split * s->out_split_stride : nullptr;
@@ -876,6 +879,14 @@ bool pair_capable(const GemmParams& p) {
 
 cudaError_t launch_tc_gemm(const GemmParams& params, int num_sms, cudaStream_t stream) {
   GemmParams p = params;
+  for (int i = 0; i < p.nseg; ++i) {
+    GemmSegment& g = p.seg[i];
+    if (!g.own_mode) {
+      g.mode = params.mode;
+      g.nt = params.nt;
+    }
+    if (g.nt > p.nt) p.nt = g.nt;  // the token ring holds the largest tile
+  }
   p.pair = (params.pair && pair_capable(params) && num_sms >= 2) ? 1 : 0;
   p.a_per_unit = (p.pair || params.a_per_unit == 1) ? 1 : 2;
   const GemmPlan plan = plan_gemm(p.nt, p.a_per_unit, p.pair != 0);

@@ -126,13 +126,19 @@ struct GemmSegment {
   int64_t b_plane_rows;
   int out_packed;
   int64_t out_plane_rows;
+  // the segment's own pass (kModeSwiGLU / kModeStore) and token tile, when
+  // own_mode is set; otherwise the launch's GemmParams::mode and ::nt
+  int own_mode;
+  int mode;
+  int nt;
 };
 
 struct GemmParams {
   GemmSegment seg[2];
   int nseg;
-  int mode;
-  int nt;        // token tile (MMA N upper bound): 32, 64, 128 or 256
+  int mode;      // pass of the segments without their own (GemmSegment::own_mode)
+  int nt;        // token tile (MMA N upper bound): 32, 64, 128 or 256; the
+                 // launch takes the largest of its segments
   int a_per_unit;  // 128-row weight tiles per unit: 2 (default) or 1
   // 1: run on CTA pairs (clusters of two) with MMAs of M = 256 over the pair;
   // each CTA takes one of a unit's two 128-row weight tiles and half of its
