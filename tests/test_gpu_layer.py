@@ -69,6 +69,14 @@ SMALL = [
     synth.custom(name="small_k3", T=200, d_model=512, d_latent=256, E_routed=16, K=4,
                  E_shared=2, d_ff=128, d_ff_shared=128),
     synth.custom(name="small_noshared", T=33, d_model=256, E_routed=8, K=2, d_ff=64),
+    # edge cases: one token; top-1 with no shared expert; one token past the
+    # small-batch tile switch, with an odd number of 128-row weight tiles in
+    # both passes (d_ff 192 -> 3 gate/up tiles, d_model 384 -> 3 down tiles)
+    synth.custom(name="one_token", T=1, d_model=256, E_routed=8, K=2, E_shared=1, d_ff=64,
+                 d_ff_shared=64),
+    synth.custom(name="top1", T=300, d_model=256, E_routed=16, K=1, d_ff=128),
+    synth.custom(name="tile_switch_odd_tiles", T=257, d_model=384, E_routed=12, K=3,
+                 E_shared=1, d_ff=192, d_ff_shared=128),
 ]
 
 
