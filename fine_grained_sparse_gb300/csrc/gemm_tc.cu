@@ -611,20 +611,32 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       const bool rows8 = !add && !out_f32 && o_limit % 8 == 0 && ld % 8 == 0;
       const uint32_t n = static_cast<uint32_t>((x.n_rows + 15) & ~15);
       const Regions rg = regions_of(p, n, c);
-      const int acc = single ? 0 : grp;
+      // A two-tile unit with both accumulators in one region: warp group g
+      // drains accumulator g.  A two-tile unit with one region per
+      // accumulator: all warps drain accumulator 0, release its region, then
+      // accumulator 1, so a following unit that needs one region starts
+      // half an epilogue earlier.  A single-tile unit: all warps, one pass.
+      // In the all-warps passes the warp groups split the 64-column chunks.
+      const bool all_warps = single || rg.big;
+      const int npass = rg.big ? 2 : 1;
+      bool aborted = false;
+      for (int pass = 0; pass < npass; ++pass) {
+      const int acc = rg.big ? pass : (single ? 0 : grp);
       const int use = rg.big ? c + acc : c;
       const int region = region_of(rg, acc);
-      if (!warp_wait(tfull_bar(region), region_phase(use), abort_flag, p.status)) break;
+      if (!warp_wait(tfull_bar(region), region_phase(use), abort_flag, p.status)) {
+        aborted = true;
+        break;
+      }
       tc_fence_after();
       if (acc < x.n_a) {
         const uint32_t taddr0 =
             tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc_column(rg, acc);
         const int blk = x.blk0 + acc;
-        // 64 columns per TMEM load (one wait each); a single accumulator is
-        // split between the two warp groups by 64-column chunk
+        // 64 columns per TMEM load (one wait each)
         const int nchunks = (x.n_rows + 63) / 64;
-        const int step = single ? 2 : 1;
-        for (int ch = single ? grp : 0; ch < nchunks; ch += step) {
+        const int step = all_warps ? 2 : 1;
+        for (int ch = all_warps ? grp : 0; ch < nchunks; ch += step) {
           uint32_t v64[64];
           tmem_ld_x64(taddr0 + static_cast<uint32_t>(ch * 64), v64);
           tmem_ld_wait(v64);
@@ -663,15 +675,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        // a region holding one accumulator of a two-tile unit gets both
-        // arrivals from its 4 warps; paired CTAs release CTA 0's region
-        if (kPair) {
+        // every epilogue warp arrives once per region it drained; paired
+        // CTAs release CTA 0's region
+        if (kPair)
           mbar_arrive_cluster(lead(tempty_bar(region)));
-        } else {
+        else
           mbar_arrive(tempty_bar(region));
-          if (rg.big) mbar_arrive(tempty_bar(region));
-        }
       }
+      }
+      if (aborted) break;
       c += rg.big ? 2 : 1;
     }
   }
