@@ -89,7 +89,7 @@ int token_tile(int64_t T, bool down_pass = false) {
   static const int forced = env_int("FGS_TOKEN_TILE", 0);  // tuning override
   static const int forced_down = env_int("FGS_DOWN_TILE", 0);
   const int f = down_pass ? forced_down : forced;
-  if (f == 32 || f == 64 || f == 128 || f == 256) return f;
+  if (f >= 32 && f <= 256 && f % 32 == 0) return f;
   return T <= 256 ? 32 : 256;
 }
 
