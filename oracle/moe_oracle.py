@@ -22,8 +22,8 @@ Sources (page title, then section / equation / listing):
             projection, their combined output is projected back to 7168, two
             shared experts stay at 7168).
 
-Readings of passages the pages leave open are listed in the design doc; the ones
-that shape this file are restated next to the code they shape.
+Where the pages leave a step open, the reading taken is stated next to the
+code it shapes.
 """
 from __future__ import annotations
 
