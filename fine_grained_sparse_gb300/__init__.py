@@ -24,7 +24,7 @@ __all__ = [
     "moe_get_device_status", "moe_router", "moe_router_from_logits", "moe_permute",
     "moe_grouped_swiglu", "moe_combine", "moe_linear", "moe_layer_forward",
     "moe_layer_forward_host", "moe_last_error_detail", "moe_pack_weights", "pack_layer_weights",
-    "moe_router_noalloc", "moe_launch_count",
+    "moe_router_noalloc", "moe_launch_count", "moe_dense_gates", "moe_update_bias",
     "MOE_WEIGHTS_NATURAL", "MOE_WEIGHTS_PACKED", "MOE_PACK_GATE_UP", "MOE_PACK_PLAIN",
 ]
 
@@ -78,6 +78,8 @@ _SIGS = {
     "moe_get_device_status": ([_P, _P], _I32),
     "moe_router": ([_CFG, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P], _I32),
     "moe_router_from_logits": ([_CFG, _I64, _P, _P, _P, _P, _P], _I32),
+    "moe_dense_gates": ([_CFG, _I64, _P, _P, _P, _P], _I32),
+    "moe_update_bias": ([_CFG, _I64, _P, _F, _P, _P], _I32),
     "moe_permute": ([_CFG, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P], _I32),
     "moe_grouped_swiglu": ([_CFG, _I64] + [_P] * 12 + [_SZ, _P], _I32),
     "moe_combine": ([_CFG, _I64, _P, _P, _P, _P, _P], _I32),
@@ -165,6 +167,18 @@ def moe_get_device_status(workspace, stream=None) -> int:
 def moe_router(cfg, T, x, W_r, bias, topk_idx, topk_w, workspace=None, ws_bytes=0, stream=None):
     _check(lib.moe_router(ctypes.byref(cfg), T, _ptr(x), _ptr(W_r), _ptr(bias), _ptr(topk_idx),
                           _ptr(topk_w), _ptr(workspace), ws_bytes, _stream(stream)), "moe_router")
+
+
+def moe_dense_gates(cfg, T, topk_idx, topk_w, G, stream=None):
+    """G [T, E] fp32: the routing weights at their experts, 0 elsewhere."""
+    _check(lib.moe_dense_gates(ctypes.byref(cfg), T, _ptr(topk_idx), _ptr(topk_w), _ptr(G),
+                               _stream(stream)), "moe_dense_gates")
+
+
+def moe_update_bias(cfg, T, counts, gamma, bias, stream=None):
+    """bias [E] fp32 in place: += gamma * sign(T K / E - counts)."""
+    _check(lib.moe_update_bias(ctypes.byref(cfg), T, _ptr(counts), float(gamma), _ptr(bias),
+                               _stream(stream)), "moe_update_bias")
 
 
 def moe_router_noalloc(cfg, T, x, W_r, bias, topk_idx, topk_w, stream=None):

@@ -669,6 +669,31 @@ int32_t moe_router(const moe_config* cfg, int64_t T, const void* x, const float*
   return MOE_OK;
 }
 
+int32_t moe_dense_gates(const moe_config* cfg, int64_t T, const int32_t* topk_idx,
+                        const float* topk_w, float* G, void* stream) {
+  int32_t st = check_router_cfg(cfg, T);
+  if (st != MOE_OK) return st;
+  if (!topk_idx || !topk_w || !G) return fail(MOE_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(topk_idx) || !aligned16(topk_w) || !aligned16(G))
+    return fail(MOE_ERR_ALIGNMENT, "pointer not 16-byte aligned");
+  MOE_CUDA(launch_dense_gates(topk_idx, topk_w, T, cfg->K, cfg->E_routed, G,
+                              static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int32_t moe_update_bias(const moe_config* cfg, int64_t T, const int32_t* counts, float gamma,
+                        float* bias, void* stream) {
+  int32_t st = check_router_cfg(cfg, T);
+  if (st != MOE_OK) return st;
+  if (!counts || !bias) return fail(MOE_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(counts) || !aligned16(bias))
+    return fail(MOE_ERR_ALIGNMENT, "pointer not 16-byte aligned");
+  if (!(gamma >= 0.0f) || !(gamma < 1.0f)) return fail(MOE_ERR_INVALID_ARG, "gamma not in [0, 1)");
+  MOE_CUDA(launch_bias_update(counts, T, cfg->K, cfg->E_routed, gamma, bias,
+                              static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
 int32_t moe_router_from_logits(const moe_config* cfg, int64_t T, const float* logits,
                                const float* bias, int32_t* topk_idx, float* topk_w,
                                void* stream) {

@@ -30,6 +30,12 @@ struct RouterArgs {
   float* topk_w = nullptr;
 };
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream);
+// G [T, E] from the routing (0 off the selected experts); K <= 32.
+cudaError_t launch_dense_gates(const int32_t* topk_idx, const float* topk_w, int64_t T, int K,
+                               int E, float* G, cudaStream_t stream);
+// bias[e] += gamma * sign(T K / E - counts[e]).
+cudaError_t launch_bias_update(const int32_t* counts, int64_t T, int K, int E, float gamma,
+                               float* bias, cudaStream_t stream);
 
 // --------------------------------------------------------------- dispatch
 // One row tile of a routed expert: rows [row_start, row_start + n_rows) of

@@ -470,7 +470,58 @@ cudaError_t launch_logits(const RouterArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// G [T, E]: each token's selected weights at their experts, 0 elsewhere.
+// One CTA per row (grid-stride); every entry is written once, by the thread
+// that owns it, after looking the expert up among the row's K indices.
+__global__ void __launch_bounds__(128) dense_gates_kernel(const int32_t* __restrict__ idx,
+                                                          const float* __restrict__ w, int64_t T,
+                                                          int K, int E, float* __restrict__ G) {
+  __shared__ int sidx[32];
+  __shared__ float sw[32];
+  for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+    if (threadIdx.x < K) {
+      sidx[threadIdx.x] = __ldg(idx + t * K + threadIdx.x);
+      sw[threadIdx.x] = __ldg(w + t * K + threadIdx.x);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      float v = 0.0f;
+      for (int k = 0; k < K; ++k)
+        if (sidx[k] == e) v = sw[k];
+      G[t * E + e] = v;
+    }
+    __syncthreads();
+  }
+}
+
+// bias[e] += gamma * sign(T K / E - counts[e]): the comparison with the mean
+// load in integers, then one fp32 addition.
+__global__ void bias_update_kernel(const int32_t* __restrict__ counts, int64_t pairs, int E,
+                                   float gamma, float* __restrict__ bias) {
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < E; e += gridDim.x * blockDim.x) {
+    const int64_t diff = pairs - static_cast<int64_t>(E) * __ldg(counts + e);
+    const float step = diff > 0 ? gamma : (diff < 0 ? -gamma : 0.0f);
+    bias[e] = bias[e] + step;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_dense_gates(const int32_t* topk_idx, const float* topk_w, int64_t T, int K,
+                               int E, float* G, cudaStream_t stream) {
+  if (T <= 0) return cudaSuccess;
+  const unsigned blocks = static_cast<unsigned>(T < 8192 ? T : 8192);
+  note_launch();
+  dense_gates_kernel<<<blocks, 128, 0, stream>>>(topk_idx, topk_w, T, K, E, G);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bias_update(const int32_t* counts, int64_t T, int K, int E, float gamma,
+                               float* bias, cudaStream_t stream) {
+  note_launch();
+  bias_update_kernel<<<(E + 255) / 256, 256, 0, stream>>>(counts, T * K, E, gamma, bias);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream) {
   if (a.logits) {

@@ -176,6 +176,28 @@ int32_t moe_router_from_logits(const moe_config* cfg, int64_t T, const float* lo
                                void* stream);
 
 /*
+ * Dense gate matrix ("Kimi K2 · Router · OpenModelAtlas": "out: G [B batch,
+ * T positions, 384 experts]"; its Explanation: G spreads each position's K
+ * weights over all experts, zero for the others):
+ *   G[t, e] = topk_w[t, k] where topk_idx[t, k] == e, else 0.
+ *   topk_idx [T, K] int32, topk_w [T, K] fp32 in (moe_router's outputs);
+ *   G [T, E] fp32 out, every entry written.  Indices outside [0, E) are
+ *   ignored.  Needs no workspace. */
+int32_t moe_dense_gates(const moe_config* cfg, int64_t T, const int32_t* topk_idx,
+                        const float* topk_w, float* G, void* stream);
+
+/*
+ * One aux-loss-free update of the selection bias ("Kimi K2 MoE",
+ * "Routing-distribution diagnostics": DeepSeek V3's schedule, gamma = 1e-3,
+ * sign-only) from one batch's per-expert loads:
+ *   bias[e] += gamma * sign(T*K/E - counts[e])
+ * the comparison with the mean load made in integers (E*counts[e] against
+ * T*K), the step one fp32 addition.  counts [E] int32 (moe_permute's output
+ * for that batch), bias [E] fp32 updated in place.  Needs no workspace. */
+int32_t moe_update_bias(const moe_config* cfg, int64_t T, const int32_t* counts, float gamma,
+                        float* bias, void* stream);
+
+/*
  * Dispatch: group the T*K (token, slot) pairs by expert ("Kimi K2 MoE",
  * section 3, dispatch_and_combine; its body is not given).  Order: expert
  * major, ascending token index within an expert.  Pair j = t * K + k.

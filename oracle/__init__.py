@@ -26,6 +26,8 @@ from .moe_oracle import (  # noqa: F401
     router_weights,
     router_from_logits,
     router_from_x,
+    dense_gates,
+    aux_free_bias_update,
     permute,
     swiglu_expert,
     moe_layer,

@@ -202,6 +202,41 @@ def router_from_x(x64, W_r64, bias32, K: int, n_group: int = 1, topk_group: int 
 
 
 # --------------------------------------------------------------------------
+# router: the dense gate matrix and the aux-loss-free bias update
+# --------------------------------------------------------------------------
+def dense_gates(idx, w, E: int) -> np.ndarray:
+    """G [T, E]: each token's selected weights at their experts, 0 elsewhere.
+
+    [Router] the "out: G [B batch, T positions, 384 experts]" shape and the
+    Explanation: the implementation returns the K weights with their expert
+    indices, and G spreads them over all E experts, zero for the others.
+    """
+    idx = np.asarray(idx)
+    T = idx.shape[0]
+    G = np.zeros((T, E))
+    G[np.arange(T)[:, None], idx] = np.asarray(w, dtype=np.float64)
+    return G
+
+
+def aux_free_bias_update(bias32, counts, T: int, K: int, gamma: float = 1e-3) -> np.ndarray:
+    """One sign-only update of the selection bias from one batch's loads.
+
+    [K2MoE] "Routing-distribution diagnostics": the aux-loss-free bias keeps
+    DeepSeek V3's schedule, gamma = 1e-3 and a sign-only update.  Reading:
+    an expert that received more pairs than the mean load T K / E has its
+    bias lowered by gamma, one that received fewer has it raised by gamma,
+    one at the mean keeps it.  The comparison with the mean is made in
+    integers (E * load against T * K); the bias is fp32 and the step is one
+    fp32 addition of the fp32 gamma.
+    """
+    counts = np.asarray(counts, dtype=np.int64)
+    E = counts.shape[0]
+    step = np.sign(np.int64(T) * K - E * counts).astype(np.float64)
+    g32 = np.float64(np.float32(gamma))
+    return round_f32(np.asarray(bias32, dtype=np.float64) + g32 * step).astype(np.float32)
+
+
+# --------------------------------------------------------------------------
 # dispatch (permute)
 # --------------------------------------------------------------------------
 def permute(idx, E: int) -> Dict[str, np.ndarray]:

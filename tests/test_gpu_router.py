@@ -101,3 +101,45 @@ def test_router_ragged_tokens_and_small_E(tensor_cores):
                              router_only=True)
         g = synth.generate(shape, device="cuda", seed=T + E)
         _check_router_from_x(shape, g["x"], g["W_r"], g["bias"], tensor_cores)
+
+
+def test_dense_gates_from_router_outputs():
+    """G [T, E] from the router's own outputs equals the oracle's spreading
+    of those outputs exactly (its entries are copies)."""
+    need_gpu()
+    fgs = lib()
+    shape = synth.custom(name="dense_g", T=300, d_model=512, E_routed=64, K=6, n_group=8,
+                         topk_group=3, router_only=True, x_dist="clusters32")
+    g = synth.generate(shape, device="cuda", weights=False)
+    cfg = fgs.config(shape, d_ff=0)
+    T = shape.T
+    ws, nws = workspace(cfg, T)
+    idx = torch.empty((T, shape.K), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, shape.K), dtype=torch.float32, device="cuda")
+    fgs.moe_router(cfg, T, g["x"], g["W_r"], g["bias"], idx, w, ws, nws)
+    G = torch.full((T, shape.E_routed), -1.0, dtype=torch.float32, device="cuda")
+    fgs.moe_dense_gates(cfg, T, idx, w, G)
+    torch.cuda.synchronize()
+    want = oracle.dense_gates(idx.cpu().numpy(), w.cpu().numpy().astype(np.float64),
+                              shape.E_routed)
+    np.testing.assert_array_equal(G.cpu().numpy().astype(np.float64), want)
+
+
+@pytest.mark.parametrize("T,K,E", [(4096, 8, 384), (7, 3, 16), (128, 16, 896)])
+def test_bias_update_bit_exact(T, K, E):
+    need_gpu()
+    fgs = lib()
+    gen = torch.Generator().manual_seed(T + K + E)
+    counts = torch.multinomial(torch.ones(E), T * K, replacement=True, generator=gen)
+    counts = torch.bincount(counts, minlength=E).to(torch.int32)
+    counts[: min(E, 4)] = T * K // E  # some experts exactly at the mean load
+    bias = (torch.rand(E, generator=gen) - 0.5).to(torch.float32)
+    cfg = fgs.config(d_model=128, E_routed=E, K=K)
+    b_dev = bias.cuda()
+    for _ in range(3):  # three batches with the same loads
+        fgs.moe_update_bias(cfg, T, counts.cuda(), 1e-3, b_dev)
+    torch.cuda.synchronize()
+    want = bias.numpy()
+    for _ in range(3):
+        want = oracle.aux_free_bias_update(want, counts.numpy(), T, K, 1e-3)
+    np.testing.assert_array_equal(b_dev.cpu().numpy(), want)

@@ -329,12 +329,60 @@ def check_gaps():
     assert oracle.selection_gaps(c, 4)[0] == np.inf
 
 
+def check_dense_gates():
+    """G [T, E] from a real routing: exactly K non-zero entries per row, at
+    the selected experts, holding their weights; each row sums to the
+    scaling factor when the weights are renormalised (the G equation's
+    numerator over its denominator sums to 1)."""
+    rng = np.random.default_rng(11)
+    T, E, K = 40, 32, 4
+    z = rng.normal(size=(T, E)).astype(np.float32)
+    b = rng.uniform(-0.1, 0.1, size=E).astype(np.float32)
+    r = oracle.router_from_logits(z, b, K)
+    G = oracle.dense_gates(r["idx"], r["w"], E)
+    assert G.shape == (T, E)
+    assert ((G != 0).sum(axis=1) == K).all()
+    for t in range(T):
+        for k in range(K):
+            assert G[t, r["idx"][t, k]] == r["w"][t, k]
+    np.testing.assert_allclose(G.sum(axis=1), oracle.ROUTED_SCALING_FACTOR, rtol=1e-12)
+    # without renormalisation a row holds scale * s of its selected experts
+    r1 = oracle.router_from_logits(z, b, K, norm_topk_prob=False)
+    G1 = oracle.dense_gates(r1["idx"], r1["w"], E)
+    s = oracle.sigmoid(z.astype(np.float64))
+    sel = G1 != 0
+    np.testing.assert_allclose(G1[sel], oracle.ROUTED_SCALING_FACTOR * s[sel], rtol=1e-12)
+
+
+def check_bias_update():
+    """Special cases of the sign-only update with gamma: a batch whose loads
+    all equal the mean leaves b unchanged bit for bit; when one expert takes
+    every pair, its bias drops by gamma and every other rises by gamma; an
+    expert's direction depends only on whether its load is above or below
+    T K / E (here the mean, 2, is met by experts 1 and 2)."""
+    g = np.float32(1e-3)
+    b = np.array([0.25, -0.5, 0.125, 0.0], dtype=np.float32)
+    T, K, E = 4, 2, 4                       # T K = 8 pairs, mean load 2
+    same = oracle.aux_free_bias_update(b, [2, 2, 2, 2], T, K)
+    assert same.dtype == np.float32 and (same == b).all()
+    one = oracle.aux_free_bias_update(b, [8, 0, 0, 0], T, K)
+    assert one[0] == np.float32(0.25) - g
+    assert (one[1:] == b[1:] + g).all()
+    mixed = oracle.aux_free_bias_update(b, [5, 2, 2, 0], T, K)
+    assert mixed[0] < b[0] and mixed[1] == b[1] and mixed[2] == b[2] and mixed[3] > b[3]
+    # many steps with a fixed imbalance move the biases linearly, in fp32
+    bb = b.copy()
+    for _ in range(10):
+        bb = oracle.aux_free_bias_update(bb, [8, 0, 0, 0], T, K)
+    assert abs(float(bb[0]) - (0.25 - 10e-3)) < 1e-6 and abs(float(bb[3]) - 10e-3) < 1e-6
+
+
 ALL_CHECKS = [
     check_sigmoid_closed_forms, check_silu, check_bf16_upcast, check_biased_scores_fp32,
     check_select_plain_bruteforce, check_select_grouped_bruteforce, check_group_special_cases,
     check_masked_fill_is_literal_zero, check_weights, check_router_from_x, check_permute,
     check_swiglu_expert, check_dense_reduction, check_layer_routing_weights,
-    check_k3_composition, check_page_figures, check_gaps,
+    check_k3_composition, check_page_figures, check_gaps, check_dense_gates, check_bias_update,
 ]
 
 
@@ -402,6 +450,16 @@ def _biased_weights_router(z32, bias32, K, n_group=1, topk_group=1, scale=2.827,
     return out
 
 
+def _dense_gates_transposed(idx, w, E):
+    G = np.zeros((np.asarray(idx).shape[0], E))
+    G[np.arange(G.shape[0])[:, None], np.asarray(idx)[:, ::-1]] = np.asarray(w)
+    return G
+
+
+def _bias_update_wrong_sign(bias32, counts, T, K, gamma=1e-3):
+    return mo._orig_bias_update(bias32, counts, T, K, -gamma)
+
+
 MUTANTS = {
     "sigmoid_not_logistic": ("sigmoid", _softmax_like),
     "gate_up_swapped": ("swiglu_expert", _swapped_swiglu),
@@ -411,6 +469,8 @@ MUTANTS = {
     "permute_not_stable": ("permute", _permute_token_major),
     "masked_fill_neg_inf": ("select_experts", _masked_neg_inf_select),
     "weights_from_biased_scores": ("router_from_logits", _biased_weights_router),
+    "dense_gates_misplaced": ("dense_gates", _dense_gates_transposed),
+    "bias_update_wrong_sign": ("aux_free_bias_update", _bias_update_wrong_sign),
 }
 
 
@@ -419,6 +479,7 @@ def test_planted_mistakes_are_caught(mutant, monkeypatch):
     name, fn = MUTANTS[mutant]
     monkeypatch.setattr(mo, "_orig_permute", mo.permute, raising=False)
     monkeypatch.setattr(mo, "_orig_router_from_logits", mo.router_from_logits, raising=False)
+    monkeypatch.setattr(mo, "_orig_bias_update", mo.aux_free_bias_update, raising=False)
     monkeypatch.setattr(mo, name, fn)
     # the package namespace re-exports the functions: patch it too
     if hasattr(oracle, name):
