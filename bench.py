@@ -73,6 +73,48 @@ def dist_env():
     return world, rank, local
 
 
+# Replica plumbing for N > 1.  The layer has no exchange step, so ranks meet
+# only at the barriers around the timed region and in the max-over-ranks
+# reduction of its duration; the helpers take the backend and the device of
+# the reduction buffer so that the same code runs over gloo on CPU.
+
+def init_ranks(torch, world, backend="nccl", device=None):
+    if world > 1:
+        import torch.distributed as dist
+        kw = {"device_id": device} if backend == "nccl" and device is not None else {}
+        dist.init_process_group(backend, **kw)
+
+
+def barrier(torch, world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(torch, ms, world, device):
+    """The slowest rank's duration: the job is done when its last rank is."""
+    if world == 1:
+        return float(ms)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world, tokens_per_rank, steps, ms_total):
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank * steps / (ms_total / 1e3)
+
+
+def replica_seed(seed, rank):
+    """Each replica draws its own batch; the weights keep the common seed."""
+    return seed + 7919 * rank
+
+
+def finish_ranks(torch, world):
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -289,9 +331,7 @@ def run_own(args):
 
     world, rank, local = dist_env()
     torch.cuda.set_device(local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    init_ranks(torch, world, "nccl", torch.device("cuda", local))
     try:
         import fine_grained_sparse_gb300 as fgs
     except ImportError:
@@ -304,7 +344,7 @@ def run_own(args):
     seed = synth.SEEDS[shape.name]
     g = synth.generate(shape, device="cuda", seed=seed)
     if rank:  # replicas: every rank its own batch, same weights
-        g["x"] = synth.activations(shape, "cuda", seed=seed + 7919 * rank)
+        g["x"] = synth.activations(shape, "cuda", seed=replica_seed(seed, rank))
     cfg = fgs.config(shape, weight_layout=fgs.MOE_WEIGHTS_PACKED)
     # one-time load step: weights rearranged into the order the tensor cores
     # stream (the natural copies stay for the CPU oracle leg)
@@ -338,8 +378,7 @@ def run_own(args):
     sampler = ClockSampler(device_id(torch, local)) if rank == 0 else None
     if sampler:
         sampler.start()
-    if world > 1:
-        torch.distributed.barrier()
+    barrier(torch, world)
     torch.cuda.synchronize()
     t0 = time.time()
     launches0 = fgs.moe_launch_count()
@@ -350,14 +389,9 @@ def run_own(args):
     launches = fgs.moe_launch_count() - launches0
     torch.cuda.synchronize()
     t1 = time.time()
-    if world > 1:
-        torch.distributed.barrier()
+    barrier(torch, world)
     clocks = sampler.stop(t0, t1) if sampler else None
-    ms_total = start.elapsed_time(end)
-    if world > 1:
-        tt = torch.tensor([ms_total], device="cuda")
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(torch, start.elapsed_time(end), world, "cuda")
     status = fgs.moe_get_device_status(ws, stream)
     if status:
         raise RuntimeError("device status after the timed steps: " + fgs.moe_status_string(status))
@@ -366,7 +400,7 @@ def run_own(args):
     stage_ms = [statistics.mean(ev[j].elapsed_time(ev[j + 1]) for ev in step_events)
                 for j in range(nev - 1)]
     ms_step = ms_total / args.steps
-    value = world * T * args.steps / (ms_total / 1e3)
+    value = job_tokens_per_s(world, T, args.steps, ms_total)
     counts_h = counts.cpu().numpy()
     work = per_step_work(shape, counts_h)
     peaks = load_peaks()
@@ -425,13 +459,9 @@ def run_own(args):
         step_host()
     ee.record(stream)
     ee.synchronize()
-    e_ms = es.elapsed_time(ee)
-    if world > 1:
-        tt = torch.tensor([e_ms], device="cuda")
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e_ms = float(tt.item())
+    e_ms = max_over_ranks(torch, es.elapsed_time(ee), world, "cuda")
     nbytes = T * shape.d_model * 2
-    line["e2e"] = {"value": round(world * T * e_steps / (e_ms / 1e3), 1), "unit": UNIT,
+    line["e2e"] = {"value": round(job_tokens_per_s(world, T, e_steps, e_ms), 1), "unit": UNIT,
                    "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes, "steps": e_steps,
                    "api": "moe_layer_forward_host (pinned host x and y)"}
 
@@ -440,9 +470,7 @@ def run_own(args):
                                                         args.cpu_sample_tokens)
     if rank == 0:
         print(json.dumps(line), flush=True)
-    if world > 1:
-        torch.distributed.barrier()
-        torch.distributed.destroy_process_group()
+    finish_ranks(torch, world)
 
 
 # ------------------------------------------------------------ reference arm
