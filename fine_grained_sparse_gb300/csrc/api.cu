@@ -81,6 +81,15 @@ int router_tile(int64_t T) {
   return T <= 256 ? 32 : 128;
 }
 
+// Unit order of a segment with implicit token tiles: token-tile-major when
+// the weights are small enough to stay in L2 (64 MB, half of it) and the
+// activation rows are the larger operand, so neither is fetched from HBM
+// twice.  FGS_B_MAJOR=0 keeps the output-block-major order everywhere.
+int prefer_b_major(int64_t a_bytes, int64_t b_bytes) {
+  static const int forced = env_int("FGS_B_MAJOR", 1);  // tuning override
+  return forced && a_bytes <= (64ll << 20) && b_bytes > a_bytes ? 1 : 0;
+}
+
 // Token tiles: 32 rows for small batches; otherwise 256, so most experts are
 // one tile and their weights stream once per pass.  A unit of two 128-row
 // weight tiles against a tile of more than 128 tokens fills both TMEM
@@ -336,6 +345,8 @@ int32_t shared_gate_up_segment(GemmSegment& s, const moe_config* c, int64_t T, c
   s.own_mode = 1;
   s.mode = kModeSwiGLU;
   s.nt = token_tile(T);
+  s.b_major = prefer_b_major(4ll * c->E_shared * c->d_ff_shared * c->d_model,
+                             2ll * T * c->d_model);
   return MOE_OK;
 }
 
@@ -438,6 +449,7 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
       s2.out_group_stride = T;
       s2.out = static_cast<__nv_bfloat16*>(io.Y_shared);
       s2.out_ld = d;
+      s2.b_major = prefer_b_major(2ll * S * d * Fs, 2ll * T * Fs);
     }
     p.pair = use_pairs(true);
     MOE_CUDA(launch_tc_gemm(p, num_sms(), st));
@@ -524,6 +536,7 @@ int32_t run_linear(int64_t T, int in_f, int out_f, const void* x, const void* W,
   s.out_ld = out_f;
   s.add = static_cast<const __nv_bfloat16*>(add);
   s.add_ld = out_f;
+  s.b_major = prefer_b_major(2ll * out_f * in_f, 2ll * T * in_f);
   MOE_CUDA(launch_tc_gemm(p, num_sms(), st));
   return MOE_OK;
 }
@@ -657,6 +670,7 @@ int32_t moe_router(const moe_config* cfg, int64_t T, const void* x, const float*
     g.out_f32 = logits;
     g.out_ld = E;
     g.ksplit = router_ksplit(T, d);
+    g.b_major = prefer_b_major(6ll * E * d, 2ll * T * d);
     g.out_split_stride = T * E;
     MOE_CUDA(launch_tc_gemm(p, num_sms(), s));
     a.logits = logits;
@@ -990,6 +1004,7 @@ int32_t moe_router_noalloc(const moe_config* cfg, int64_t T, const void* x, cons
   g.out_f32 = logits;
   g.out_ld = E;
   g.ksplit = ksplit;
+  g.b_major = prefer_b_major(6ll * E * d, 2ll * T * d);
   g.out_split_stride = T * E;
   MOE_CUDA(launch_tc_gemm(p, num_sms(), s));
   RouterArgs a;

@@ -115,14 +115,28 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int unit
   const int ns = ksplit_of(s);
   const int kps = s->k_steps / ns;
   x.split = 0;
-  if (ns > 1) {  // the K part is the outermost index of a split segment
+  if (ns > 1 && !s->b_major) {  // the K part is the outermost index of a split segment
     const int per = s->groups * ((s->rows + nt - 1) / nt) * OB;
     x.split = local / per;
     local -= x.split * per;
   }
-  x.k0 = x.split * kps;
-  x.k1 = x.k0 + kps;
-  if (s->tiles) {
+  if (s->b_major && !s->tiles) {
+    // (group, token tile) outermost, then the K part, the output block fastest
+    const int tpg = (s->rows + nt - 1) / nt;
+    const int inner = ns * OB;
+    const int gt = local / inner;
+    const int r = local - gt * inner;
+    x.split = r / OB;
+    x.ob = r - x.split * OB;
+    const int g = gt / tpg;
+    const int t0 = (gt - g * tpg) * nt;
+    x.group = g;
+    x.n_rows = min(nt, s->rows - t0);
+    x.b_row = static_cast<int>(g * s->b_group_stride + t0);
+    x.out_row = static_cast<int>(g * s->out_group_stride + t0);
+    x.scale_row = x.out_row;
+    x.ntiles = tpg;
+  } else if (s->tiles) {
     // the units of one expert are [first_tile * OB, (first_tile + ntiles) * OB)
     const RowTile& any = s->tiles[local / OB];
     const int r = local - any.first_tile * OB;
@@ -148,6 +162,8 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int unit
     x.scale_row = x.out_row;
     x.ntiles = tpg;
   }
+  x.k0 = x.split * kps;
+  x.k1 = x.k0 + kps;
   if (p.a_per_unit == 2) {
     x.blk0 = 2 * x.ob;
     x.n_a = min(2, s->a128 - 2 * x.ob);
@@ -379,6 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     for (int s = 0; s < p.nseg; ++s) prefetch_tensormap(&p.seg[s].tmA);
     const uint64_t pol_stream = l2_policy_evict_first();
     const uint64_t pol_normal = l2_policy_evict_normal();
+    const uint64_t pol_keep = l2_policy_evict_last();
     int stage = 0;
     uint32_t phase = 0;
     int64_t issued = 0;
@@ -390,8 +407,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
       const uint32_t tx = kATileBytes * x.n_a;
       // a weight block read by one token tile is streamed; one shared by
-      // several token tiles (running side by side) is kept for the others
-      const uint64_t pol_w = x.ntiles > 1 ? pol_normal : pol_stream;
+      // several token tiles (running side by side) is kept for the others;
+      // a token-tile-major segment's weights serve every token tile
+      const uint64_t pol_w = s->b_major ? pol_keep : x.ntiles > 1 ? pol_normal : pol_stream;
       bool ok = true;
       for (int ks = x.k0; ks < x.k1; ++ks) {
         if (!mbar_wait_bounded(a_empty(stage), phase ^ 1u, abort_flag, p.status)) {
@@ -455,6 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     for (int s = 0; s < p.nseg; ++s)
       if (kPair || !p.seg[s].b_packed) prefetch_tensormap(&p.seg[s].tmB);
     const uint64_t pol_keep = l2_policy_evict_last();
+    const uint64_t pol_normal = l2_policy_evict_normal();
     int stage = 0, fstage = 0;  // token stage, and the k step's full barrier
     int estage = 0;             // weight stage of k step issued - Sb
     uint32_t ephase = 0;
@@ -465,6 +484,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       const Unit x = nx;
       if (u + u_step < total) nx = decode_unit(p, u + u_step, units0, units1, rank);
       const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
+      // token rows are kept for the units that re-read them, except in a
+      // token-tile-major segment, whose readers of a tile run side by side
+      const uint64_t pol_b = s->b_major ? pol_normal : pol_keep;
       // paired: this CTA's half of the tile's rows (rounded up to 16), as
       // 32-row boxes; the rows past the half that a box brings in are not
       // read by the MMA
@@ -496,19 +518,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           for (int bx = 0; bx < nbox; ++bx) {
             if (s->b_packed)
               tma_load_3d_pair(b_dst + bx * kBBoxBytes, &s->tmB, lead(fb), 0,
-                               b_row + bx * kBBoxRows, kstep, pol_keep);
+                               b_row + bx * kBBoxRows, kstep, pol_b);
             else
               tma_load_2d_pair(b_dst + bx * kBBoxBytes, &s->tmB, lead(fb), kstep * kBK,
-                               b_row + bx * kBBoxRows, pol_keep);
+                               b_row + bx * kBBoxRows, pol_b);
           }
         } else if (s->b_packed) {
           const uint8_t* src =
               s->b_packed + (static_cast<int64_t>(kstep) * s->b_plane_rows + b_row) * 128;
-          bulk_load(b_dst, src, tx, fb, pol_keep);
+          bulk_load(b_dst, src, tx, fb, pol_b);
         } else {
           for (int bx = 0; bx < nbox; ++bx)
             tma_load_2d(b_dst + bx * kBBoxBytes, &s->tmB, fb, kstep * kBK,
-                        b_row + bx * kBBoxRows, pol_keep);
+                        b_row + bx * kBBoxRows, pol_b);
         }
         ++issued;
         if (++fstage == sa_n) fstage = 0;

@@ -137,6 +137,11 @@ struct GemmSegment {
   int own_mode;
   int mode;
   int nt;
+  // implicit tiles only: 1 = a token tile's units (all K parts and output
+  // blocks) run side by side, so the tile is fetched from HBM once while the
+  // weights, small enough to stay in L2, are re-read from there; 0 = the
+  // output blocks outermost (weights fetched once, token tiles re-read)
+  int b_major;
 };
 
 struct GemmParams {
