@@ -75,6 +75,14 @@ int router_ksplit(int64_t T, int d) {
   return 3 * h;
 }
 
+// Weight tiles per router GEMM unit: two (each token tile in shared memory
+// feeds two weight tiles), although a 384-expert router then has units of
+// two and of one tile.
+int router_a_per_unit() {
+  static const int forced = env_int("FGS_ROUTER_A", 2);  // tuning override
+  return forced == 1 ? 1 : 2;
+}
+
 int router_tile(int64_t T) {
   static const int forced = env_int("FGS_ROUTER_TILE", 0);  // tuning override
   if (forced == 32 || forced == 64 || forced == 128 || forced == 256) return forced;
@@ -653,6 +661,7 @@ int32_t moe_router(const moe_config* cfg, int64_t T, const void* x, const float*
     memset(&p, 0, sizeof(p));
     p.mode = kModeStore;
     p.nt = router_tile(T);
+    p.a_per_unit = router_a_per_unit();
     p.status = at<int>(workspace, L.status);
     p.nseg = 1;
     GemmSegment& g = p.seg[0];
@@ -988,6 +997,7 @@ int32_t moe_router_noalloc(const moe_config* cfg, int64_t T, const void* x, cons
   memset(&p, 0, sizeof(p));
   p.mode = kModeStore;
   p.nt = router_tile(T);
+  p.a_per_unit = router_a_per_unit();
   p.status = status;
   p.nseg = 1;
   GemmSegment& g = p.seg[0];

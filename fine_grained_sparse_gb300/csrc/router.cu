@@ -252,15 +252,17 @@ __device__ __forceinline__ void select_token(const float (&z)[PM], int lane, int
     refine_above(floor_v - kMargin, 0, E);
     rounds();
   }
-  // weights from the unbiased scores, in fp64, one lane per selected expert
-  const double sk = lane < K ? sigmoid_f64(sel_z) : 0.0;
-  double sum = sk;
+  // weights from the unbiased scores, one lane per selected expert, in
+  // fp32: the fast sigmoid's error (below 1e-6 relative) is far inside the
+  // weights' tolerance, and fp64 throughput is scarce on this part
+  const float sk = lane < K ? __frcp_rn(1.0f + expf(-sel_z)) : 0.0f;
+  float sum = sk;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(full, sum, off);
   if (lane < K) {
-    const double w = (K > 1 && norm) ? sk / (sum + 1e-20) : sk;
+    const float w = (K > 1 && norm) ? __fdiv_rn(sk, sum + 1e-20f) : sk;
     out_idx[lane] = sel_idx;
-    out_w[lane] = static_cast<float>(w * static_cast<double>(scale));
+    out_w[lane] = w * scale;
   }
 }
 

@@ -36,10 +36,14 @@ def main(argv=None):
     ap.add_argument("--x-dist", default="clusters32")
     ap.add_argument("--iters", type=int, default=2)
     ap.add_argument("--natural", action="store_true", help="natural (unpacked) weight layout")
+    ap.add_argument("--router-only", action="store_true",
+                    help="run moe_router alone (no expert weights are made)")
     a = ap.parse_args(argv)
     shape = synth.custom(name="profile_case", T=a.T, d_model=a.d, E_routed=a.E, K=a.K,
                          E_shared=a.S, d_ff=a.F, d_ff_shared=a.Fs or a.F, n_group=a.G,
                          topk_group=a.Gk, d_latent=a.L, x_dist=a.x_dist)
+    if a.router_only:
+        return run_router(shape, a)
     g = synth.generate(shape, device="cuda")
     cfg = fgs.config(shape)
     if not a.natural:
@@ -56,6 +60,22 @@ def main(argv=None):
     if status:
         raise SystemExit("device status: " + fgs.moe_status_string(status))
     print("ok", float(y.float().abs().mean()))
+
+
+def run_router(shape, a):
+    x = synth.activations(shape, "cuda")
+    W_r, bias = synth.router_params(shape, "cuda")
+    cfg = fgs.config(shape)
+    nws = fgs.moe_workspace_size(cfg, a.T)
+    ws = torch.zeros(nws, dtype=torch.uint8, device="cuda")
+    idx = torch.empty((a.T, a.K), dtype=torch.int32, device="cuda")
+    w = torch.empty((a.T, a.K), dtype=torch.float32, device="cuda")
+    for _ in range(a.iters):
+        fgs.moe_router(cfg, a.T, x, W_r, bias, idx, w, ws, nws)
+    status = fgs.moe_get_device_status(ws)
+    if status:
+        raise SystemExit("device status: " + fgs.moe_status_string(status))
+    print("ok", float(w.sum()) / a.T)
 
 
 if __name__ == "__main__":
