@@ -16,6 +16,9 @@ form (identity projections), which is stated in that test.
 from .moe_oracle import (  # noqa: F401
     ROUTED_SCALING_FACTOR,
     bf16_bits_to_f64,
+    e4m3_to_f64,
+    FP8_BLOCK,
+    dequant_fp8_blocks,
     sigmoid,
     silu,
     round_f32,
@@ -32,4 +35,5 @@ from .moe_oracle import (  # noqa: F401
     swiglu_expert,
     moe_layer,
     moe_layer_tokens,
+    moe_layer_tokens_fp8,
 )

@@ -21,6 +21,12 @@ Sources (page title, then section / equation / listing):
             Stable LatentMoE paragraph (routed experts see a 7168 -> 3584
             projection, their combined output is projected back to 7168, two
             shared experts stay at 7168).
+  [Params]  "Kimi K2 · Router · OpenModelAtlas", section "Parameters": the
+            note under the per-instance accounting says the checkpoint's
+            tensors carry FP8 block scales.  The pages name neither the FP8
+            encoding nor the block shape nor the scale's type; the reading
+            taken (``e4m3_to_f64``, ``dequant_fp8_blocks``) is the OCP E4M3
+            encoding with one fp32 multiplier per 128 x 128 block.
 
 Where the pages leave a step open, the reading taken is stated next to the
 code it shapes.
@@ -42,6 +48,39 @@ def bf16_bits_to_f64(bits) -> np.ndarray:
     """Exact value of bf16 numbers given as their 16-bit patterns."""
     u = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
     return u.view(np.float32).astype(np.float64)
+
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    """Value of FP8 E4M3 numbers given as their 8-bit codes.
+
+    [Params] reading: the OCP 8-bit floating-point E4M3 encoding -- bit 7
+    the sign, bits 6..3 the exponent with bias 7, bits 2..0 the mantissa;
+    exponent 0 is subnormal (m/8 * 2^-6); there are no infinities and
+    S.1111.111 is NaN, so the largest magnitude is 1.75 * 2^8 = 448.
+    """
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2((e - 7).astype(np.float64)))
+    mag = np.where((e == 15) & ((c & 0x7) == 7), np.nan, mag)
+    return sign * mag
+
+
+FP8_BLOCK = 128  # [Params] reading: one scale per 128 x 128 block
+
+
+def dequant_fp8_blocks(codes, scales, block: int = FP8_BLOCK) -> np.ndarray:
+    """W[..., r, c] = e4m3(codes[..., r, c]) * scales[..., r // block, c // block], fp64.
+
+    [Params] reading: a block-scaled FP8 matrix stores codes and one fp32
+    multiplier per block x block tile of it (rows and columns counted from
+    0); the weight is the code's value times its tile's multiplier.
+    """
+    q = e4m3_to_f64(codes)
+    sc = np.asarray(scales, dtype=np.float64)
+    full = np.repeat(np.repeat(sc, block, axis=-2), block, axis=-1)
+    return q * full[..., :q.shape[-2], :q.shape[-1]]
 
 
 def sigmoid(z) -> np.ndarray:
@@ -343,5 +382,32 @@ def moe_layer_tokens(x64, W_r64, bias32, W_gate_up, W_down, Ws_gate_up, Ws_down,
         x64, W_r64, bias32,
         routed=lambda e: split(W_gate_up, W_down, e),
         shared=(lambda s: split(Ws_gate_up, Ws_down, s)) if n_shared else None,
+        n_shared=n_shared, K=K, n_group=n_group, topk_group=topk_group, scale=scale,
+        norm_topk_prob=norm_topk_prob, W_lat_down64=W_lat_down64, W_lat_up64=W_lat_up64)
+
+
+def moe_layer_tokens_fp8(x64, W_r64, bias32, gu_q, gu_s, dn_q, dn_s, sgu_q=None, sgu_s=None,
+                         sdn_q=None, sdn_s=None, K: int = 8, n_group: int = 1,
+                         topk_group: int = 1, scale: float = ROUTED_SCALING_FACTOR,
+                         norm_topk_prob: bool = True, W_lat_down64=None,
+                         W_lat_up64=None) -> Dict[str, np.ndarray]:
+    """``moe_layer`` with FP8 block-scaled expert weights ([Params] reading).
+
+    gu_q [E, 2F, d] uint8 codes with gu_s [E, 2F/128, d/128] fp32 scales
+    (gate rows then up rows), dn_q [E, d, F] with dn_s [E, d/128, F/128]; the
+    shared experts' banks likewise (or None).  Each selected expert is
+    dequantised exactly in fp64 (``dequant_fp8_blocks``) and then runs the
+    same fp64 SwiGLU as the bf16 form.
+    """
+    def split(q_gu, s_gu, q_dn, s_dn, e):
+        gu = dequant_fp8_blocks(q_gu[e], s_gu[e])
+        F = gu.shape[0] // 2
+        return gu[:F], gu[F:], dequant_fp8_blocks(q_dn[e], s_dn[e])
+
+    n_shared = 0 if sgu_q is None else len(sgu_q)
+    return moe_layer(
+        x64, W_r64, bias32,
+        routed=lambda e: split(gu_q, gu_s, dn_q, dn_s, e),
+        shared=(lambda s_: split(sgu_q, sgu_s, sdn_q, sdn_s, s_)) if n_shared else None,
         n_shared=n_shared, K=K, n_group=n_group, topk_group=topk_group, scale=scale,
         norm_topk_prob=norm_topk_prob, W_lat_down64=W_lat_down64, W_lat_up64=W_lat_up64)

@@ -36,7 +36,8 @@ from typing import Dict, Optional
 import torch
 
 __all__ = ["LayerShape", "CONFIGS", "SEEDS", "shape", "generate", "custom", "activations",
-           "router_params", "routed_expert", "shared_expert", "latent_projections"]
+           "router_params", "routed_expert", "shared_expert", "latent_projections",
+           "routed_expert_fp8", "shared_expert_fp8", "FP8_BLOCK"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -58,6 +59,10 @@ class LayerShape:
     x_dist: str = "normal"       # "normal" or "clusters32"
     bias_range: float = 0.1
     router_only: bool = False
+    # "bf16", or "fp8": routed and shared expert weights as FP8 E4M3 codes
+    # with one fp32 multiplier per 128 x 128 block (the K3 latent
+    # projections stay bf16)
+    weights: str = "bf16"
 
     @property
     def d_expert(self) -> int:
@@ -81,7 +86,12 @@ CONFIGS: Dict[str, LayerShape] = {
                             bias_range=0.1),
 }
 
-SEEDS = {"tiny": 0, "k2_router": 1, "k2_decode": 2, "k2_prefill": 3, "k3_latent": 4}
+for _n in ("k2_decode", "k2_prefill", "k3_latent"):
+    CONFIGS[_n + "_fp8"] = dataclasses.replace(CONFIGS[_n], name=_n + "_fp8", weights="fp8")
+
+# the FP8 forms draw x, W_r and the bias from their bf16 forms' seeds
+SEEDS = {"tiny": 0, "k2_router": 1, "k2_decode": 2, "k2_prefill": 3, "k3_latent": 4,
+         "k2_decode_fp8": 2, "k2_prefill_fp8": 3, "k3_latent_fp8": 4}
 
 
 def shape(name: str) -> LayerShape:
@@ -101,6 +111,9 @@ def _wdtype(cfg: LayerShape) -> torch.dtype:
 # expert's weights can be drawn without drawing the others.
 _STREAM_X, _STREAM_WR, _STREAM_BIAS, _STREAM_LAT_DOWN, _STREAM_LAT_UP = 1, 2, 3, 4, 5
 _STREAM_SHARED, _STREAM_ROUTED = 100, 1000
+_STREAM_SHARED_FP8, _STREAM_ROUTED_FP8 = 500, 100000
+FP8_BLOCK = 128
+FP8_CODE_STD = 112.0  # codes ~ N(0, 112^2): the largest of a block's ~16k near 448
 
 
 def _gen(seed: int, stream: int, device) -> torch.Generator:
@@ -166,6 +179,33 @@ def shared_expert(cfg: LayerShape, s_idx: int, device="cpu", seed: Optional[int]
     return _normal(g, (2 * Fs, d), 0.02, device, dt), _normal(g, (d, Fs), 0.02, device, dt)
 
 
+def _fp8_matrix(gen, rows: int, cols: int, device):
+    """A block-scaled FP8 E4M3 matrix: (codes [rows, cols] uint8, scales
+    [ceil(rows/128), ceil(cols/128)] fp32).  Code values are drawn N(0, 112^2)
+    clamped to +-448 and rounded to E4M3 by torch's float8 cast; the block
+    multipliers U(0.5, 1.5) * 0.02 / 112, so the weights are about N(0, 0.02)."""
+    v = torch.randn((rows, cols), generator=gen, device=device, dtype=torch.float32)
+    codes = v.mul_(FP8_CODE_STD).clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    nb = ((rows + FP8_BLOCK - 1) // FP8_BLOCK, (cols + FP8_BLOCK - 1) // FP8_BLOCK)
+    scales = _uniform(gen, nb, 0.5, 1.5, device).mul_(0.02 / FP8_CODE_STD)
+    return codes, scales
+
+
+def routed_expert_fp8(cfg: LayerShape, e: int, device="cpu", seed: Optional[int] = None):
+    """(gu codes [2F, d_e], gu scales, down codes [d_e, F], down scales) of
+    routed expert e in the FP8 block-scaled form."""
+    g = _gen(_seed(cfg, seed), _STREAM_ROUTED_FP8 + e, device)
+    de, F = cfg.d_expert, cfg.d_ff
+    return (*_fp8_matrix(g, 2 * F, de, device), *_fp8_matrix(g, de, F, device))
+
+
+def shared_expert_fp8(cfg: LayerShape, s_idx: int, device="cpu", seed: Optional[int] = None):
+    """(gu codes [2Fs, d], gu scales, down codes [d, Fs], down scales)."""
+    g = _gen(_seed(cfg, seed), _STREAM_SHARED_FP8 + s_idx, device)
+    d, Fs = cfg.d_model, cfg.d_ff_shared
+    return (*_fp8_matrix(g, 2 * Fs, d, device), *_fp8_matrix(g, d, Fs, device))
+
+
 def latent_projections(cfg: LayerShape, device="cpu", seed: Optional[int] = None):
     """(W_lat_down [L, d], W_lat_up [d, L]), N(0, 0.02)."""
     s, dt, d, L = _seed(cfg, seed), _wdtype(cfg), cfg.d_model, cfg.d_latent
@@ -181,6 +221,11 @@ def generate(cfg: LayerShape, device="cpu", seed: Optional[int] = None,
     if cfg.router_only or not weights:
         return out
     dt, de, F, E = _wdtype(cfg), cfg.d_expert, cfg.d_ff, cfg.E_routed
+    if cfg.weights == "fp8":
+        _generate_fp8(cfg, device, seed, out)
+        if cfg.d_latent:
+            out["W_lat_down"], out["W_lat_up"] = latent_projections(cfg, device, seed)
+        return out
     W_gate_up = torch.empty((E, 2 * F, de), device=device, dtype=dt)
     W_down = torch.empty((E, de, F), device=device, dtype=dt)
     for e in range(E):
@@ -196,3 +241,27 @@ def generate(cfg: LayerShape, device="cpu", seed: Optional[int] = None,
     if cfg.d_latent:
         out["W_lat_down"], out["W_lat_up"] = latent_projections(cfg, device, seed)
     return out
+
+
+def _bank(n: int, rows: int, cols: int, device):
+    nb = ((rows + FP8_BLOCK - 1) // FP8_BLOCK, (cols + FP8_BLOCK - 1) // FP8_BLOCK)
+    return (torch.empty((n, rows, cols), device=device, dtype=torch.uint8),
+            torch.empty((n, *nb), device=device, dtype=torch.float32))
+
+
+def _generate_fp8(cfg: LayerShape, device, seed, out: Dict[str, torch.Tensor]) -> None:
+    """FP8 expert banks: W_gate_up_q/_s, W_down_q/_s and the shared experts'
+    Ws_gate_up_q/_s, Ws_down_q/_s (codes uint8, block scales fp32)."""
+    de, F, E = cfg.d_expert, cfg.d_ff, cfg.E_routed
+    gq, gs = _bank(E, 2 * F, de, device)
+    dq, ds = _bank(E, de, F, device)
+    for e in range(E):
+        gq[e], gs[e], dq[e], ds[e] = routed_expert_fp8(cfg, e, device, seed)
+    out.update(W_gate_up_q=gq, W_gate_up_s=gs, W_down_q=dq, W_down_s=ds)
+    S, Fs, d = cfg.E_shared, cfg.d_ff_shared, cfg.d_model
+    if S:
+        sgq, sgs = _bank(S, 2 * Fs, d, device)
+        sdq, sds = _bank(S, d, Fs, device)
+        for i in range(S):
+            sgq[i], sgs[i], sdq[i], sds[i] = shared_expert_fp8(cfg, i, device, seed)
+        out.update(Ws_gate_up_q=sgq, Ws_gate_up_s=sgs, Ws_down_q=sdq, Ws_down_s=sds)
