@@ -26,10 +26,12 @@ __all__ = [
     "moe_layer_forward_host", "moe_last_error_detail", "moe_pack_weights", "pack_layer_weights",
     "moe_router_noalloc", "moe_launch_count", "moe_dense_gates", "moe_update_bias",
     "MOE_WEIGHTS_NATURAL", "MOE_WEIGHTS_PACKED", "MOE_PACK_GATE_UP", "MOE_PACK_PLAIN",
+    "MOE_WEIGHTS_PACKED_FP8", "moe_packed_fp8_bytes", "moe_pack_weights_fp8",
+    "pack_layer_weights_fp8",
 ]
 
 MOE_F32, MOE_BF16 = 0, 1
-MOE_WEIGHTS_NATURAL, MOE_WEIGHTS_PACKED = 0, 1
+MOE_WEIGHTS_NATURAL, MOE_WEIGHTS_PACKED, MOE_WEIGHTS_PACKED_FP8 = 0, 1, 2
 MOE_PACK_GATE_UP, MOE_PACK_PLAIN = 0, 1
 MOE_STAGE_COUNT = 5
 STAGE_NAMES = ("router", "dispatch", "expert_gate_up", "expert_down", "combine")
@@ -85,6 +87,8 @@ _SIGS = {
     "moe_combine": ([_CFG, _I64, _P, _P, _P, _P, _P], _I32),
     "moe_linear": ([_I64, _I32, _I32, _P, _P, _P, _P, _P, _SZ, _P], _I32),
     "moe_pack_weights": ([_I32, _I64, _I64, _I64, _P, _P, _P], _I32),
+    "moe_packed_fp8_bytes": ([_I64, _I64, _I64], _I64),
+    "moe_pack_weights_fp8": ([_I32, _I64, _I64, _I64, _P, _P, _P, _P], _I32),
     "moe_router_noalloc": ([_CFG, _I64, _P, _P, _P, _P, _P, _P], _I32),
     "moe_layer_forward": ([_CFG, _I64] + [_P] * 14 + [_SZ, _P, _P], _I32),
     "moe_layer_forward_host": ([_CFG, _I64] + [_P] * 11 + [_SZ, _P], _I32),
@@ -130,6 +134,8 @@ def config(shape=None, **kw) -> MoeConfig:
             vals["dtype"] = MOE_F32 if shape.dtype == "f32" else MOE_BF16
         if getattr(shape, "router_only", False):
             vals["d_ff"] = 0
+        if getattr(shape, "weights", "bf16") == "fp8":
+            vals["weight_layout"] = MOE_WEIGHTS_PACKED_FP8
     vals.update(kw)
     vals["norm_topk_prob"] = int(bool(vals["norm_topk_prob"]))
     return MoeConfig(**vals)
@@ -257,6 +263,39 @@ def moe_layer_forward_host(cfg, T, x_host, W_r, bias, W_gate_up, W_down, Ws_gate
 def moe_pack_weights(kind, groups, rows, cols, src, dst, stream=None):
     _check(lib.moe_pack_weights(kind, groups, rows, cols, _ptr(src), _ptr(dst), _stream(stream)),
            "moe_pack_weights")
+
+
+def moe_packed_fp8_bytes(groups, rows, cols) -> int:
+    return int(lib.moe_packed_fp8_bytes(groups, rows, cols))
+
+
+def moe_pack_weights_fp8(kind, groups, rows, cols, codes, scales, dst, stream=None):
+    _check(lib.moe_pack_weights_fp8(kind, groups, rows, cols, _ptr(codes), _ptr(scales), _ptr(dst),
+                                    _stream(stream)), "moe_pack_weights_fp8")
+
+
+def pack_layer_weights_fp8(weights: dict, stream=None) -> dict:
+    """The weights of one layer for a config whose weight_layout is
+    MOE_WEIGHTS_PACKED_FP8: the FP8 banks (keys ``<bank>_q`` with codes and
+    ``<bank>_s`` with block scales, as produced by ``synth.generate`` for an
+    FP8 shape) packed into one uint8 buffer each under ``<bank>``, and the
+    bf16 latent projections packed as by ``pack_layer_weights``."""
+    import torch
+    out = {k: v for k, v in weights.items() if not (k.endswith("_q") or k.endswith("_s"))}
+    kinds = {"W_gate_up": MOE_PACK_GATE_UP, "Ws_gate_up": MOE_PACK_GATE_UP,
+             "W_down": MOE_PACK_PLAIN, "Ws_down": MOE_PACK_PLAIN}
+    for key, kind in kinds.items():
+        q, sc = weights.get(key + "_q"), weights.get(key + "_s")
+        if q is None:
+            continue
+        G, R, C = q.shape
+        dst = torch.empty(moe_packed_fp8_bytes(G, R, C), dtype=torch.uint8, device=q.device)
+        moe_pack_weights_fp8(kind, G, R, C, q.contiguous(), sc.contiguous(), dst, stream)
+        out[key] = dst
+    lat = {k: weights[k] for k in ("W_lat_down", "W_lat_up") if weights.get(k) is not None}
+    if lat:
+        out.update(pack_layer_weights(lat, stream))
+    return out
 
 
 def pack_layer_weights(weights: dict, stream=None) -> dict:

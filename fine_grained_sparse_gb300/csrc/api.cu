@@ -161,10 +161,15 @@ int32_t check_layer_cfg(const moe_config* c, int64_t T) {
   if (c->E_shared < 0 || c->E_shared > 8) return fail(MOE_ERR_INVALID_ARG, "E_shared not in [0, 8]");
   if (c->E_shared > 0 && c->d_ff_shared < 1) return fail(MOE_ERR_INVALID_ARG, "d_ff_shared < 1");
   if (c->d_latent < 0) return fail(MOE_ERR_INVALID_ARG, "d_latent < 0");
-  if (c->weight_layout != MOE_WEIGHTS_NATURAL && c->weight_layout != MOE_WEIGHTS_PACKED)
+  if (c->weight_layout != MOE_WEIGHTS_NATURAL && c->weight_layout != MOE_WEIGHTS_PACKED &&
+      c->weight_layout != MOE_WEIGHTS_PACKED_FP8)
     return fail(MOE_ERR_INVALID_ARG, "weight_layout");
-  if (c->weight_layout == MOE_WEIGHTS_PACKED && c->dtype != MOE_BF16)
-    return fail(MOE_ERR_UNSUPPORTED_SHAPE, "packed weights are bf16 only");
+  if (c->weight_layout != MOE_WEIGHTS_NATURAL && c->dtype != MOE_BF16)
+    return fail(MOE_ERR_UNSUPPORTED_SHAPE, "packed weights need bf16 activations");
+  if (c->weight_layout == MOE_WEIGHTS_PACKED_FP8 &&
+      (c->d_model % 128 || c->d_ff % 128 || (c->E_shared > 0 && c->d_ff_shared % 128) ||
+       c->d_latent % 128))
+    return fail(MOE_ERR_UNSUPPORTED_SHAPE, "FP8 weights: d_model, d_ff, d_ff_shared, d_latent % 128");
   if (c->dtype == MOE_BF16) {
     if (c->d_model % 128) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "bf16 path: d_model % 128 != 0");
     if (c->d_ff % 64) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "bf16 path: d_ff % 64 != 0");
@@ -265,9 +270,25 @@ int num_sms() {
 // Weights in MOE_WEIGHTS_PACKED order stream as one bulk copy per stage;
 // natural ones through tensor maps: for gate/up a 5-D map when the driver
 // accepts it, else eight 16-row boxes.
-int32_t set_gate_up_A(GemmSegment& s, const void* W, int groups, int F, int Kd, bool packed) {
+// Records of a packed FP8 bank: one per (group, pair of 128-row tiles,
+// 64-column k step), after the tiles.
+void set_fp8_records(GemmSegment& s, const void* W, int groups, int64_t rows, int Kd) {
+  s.a_fp8 = 1;
+  s.a_rec = static_cast<const uint8_t*>(W) + static_cast<int64_t>(groups) * rows * Kd;
+  s.a_rec_group = ((rows / 128 + 1) / 2) * (Kd / 64);
+}
+
+int32_t set_gate_up_A(GemmSegment& s, const void* W, int groups, int F, int Kd, int layout) {
   s.a_rows = F;
-  if (packed) {
+  if (layout == MOE_WEIGHTS_PACKED_FP8) {
+    s.a_packed = static_cast<const uint8_t*>(W);
+    s.a_group_bytes = 2ll * F * Kd;
+    s.a_groups = groups;
+    s.a_boxes = 1;
+    set_fp8_records(s, W, groups, 2ll * F, Kd);
+    return MOE_OK;
+  }
+  if (layout == MOE_WEIGHTS_PACKED) {
     s.a_packed = static_cast<const uint8_t*>(W);
     s.a_group_bytes = 2ll * F * Kd * 2;
     s.a_groups = groups;
@@ -300,8 +321,17 @@ void set_B_packed(GemmSegment& s, const void* B, int64_t plane_rows, int Kd) {
   s.k_steps = Kd / 64;
 }
 
-int32_t set_store_A(GemmSegment& s, const void* W, int groups, int O, int Kd, bool packed) {
-  if (packed) {
+int32_t set_store_A(GemmSegment& s, const void* W, int groups, int O, int Kd, int layout) {
+  if (layout == MOE_WEIGHTS_PACKED_FP8) {
+    s.a_packed = static_cast<const uint8_t*>(W);
+    s.a_group_bytes = static_cast<int64_t>(O) * Kd;
+    s.a_groups = groups;
+    s.a_boxes = 1;
+    s.a_rows = 0;
+    set_fp8_records(s, W, groups, O, Kd);
+    return MOE_OK;
+  }
+  if (layout == MOE_WEIGHTS_PACKED) {
     s.a_packed = static_cast<const uint8_t*>(W);
     s.a_group_bytes = static_cast<int64_t>(O) * Kd * 2;
     s.a_groups = groups;
@@ -336,7 +366,7 @@ struct ExpertIO {
 // The shared experts' gate/up pass as a GEMM segment: every token of x
 // against each shared expert, SwiGLU outputs into the packed planes Hs.
 int32_t shared_gate_up_segment(GemmSegment& s, const moe_config* c, int64_t T, const void* x,
-                               const void* Ws_gate_up, const Layout& L, void* ws, bool packed) {
+                               const void* Ws_gate_up, const Layout& L, void* ws, int packed) {
   clear(s);
   int32_t e;
   if ((e = set_gate_up_A(s, Ws_gate_up, c->E_shared, c->d_ff_shared, c->d_model, packed)) != MOE_OK)
@@ -377,7 +407,7 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
   void* H = at<void>(ws, L.H);
   void* Hs = at<void>(ws, L.Hs);
   const bool bf16 = c->dtype == MOE_BF16;
-  const bool packed = c->weight_layout == MOE_WEIGHTS_PACKED;
+  const int packed = c->weight_layout;  // moe_weight_layout of the expert banks
   const int nt = bf16 ? token_tile(T) : kSimtTile;
   const int nt_down = bf16 ? token_tile(T, true) : kSimtTile;
   RowTile* tiles_down = tiles;
@@ -523,8 +553,14 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
   return MOE_OK;
 }
 
+// The K3 latent projections are bf16 whatever the expert banks are: packed
+// when the banks are packed (bf16 or FP8), natural otherwise.
+int latent_layout(const moe_config* c) {
+  return c->weight_layout == MOE_WEIGHTS_NATURAL ? MOE_WEIGHTS_NATURAL : MOE_WEIGHTS_PACKED;
+}
+
 int32_t run_linear(int64_t T, int in_f, int out_f, const void* x, const void* W, const void* add,
-                   void* y, int* status, cudaStream_t st, bool packed = false) {
+                   void* y, int* status, cudaStream_t st, int packed = MOE_WEIGHTS_NATURAL) {
   GemmParams p;
   memset(&p, 0, sizeof(p));
   p.mode = kModeStore;
@@ -814,6 +850,29 @@ int32_t moe_pack_weights(int32_t kind, int64_t groups, int64_t rows, int64_t col
   return MOE_OK;
 }
 
+int64_t moe_packed_fp8_bytes(int64_t groups, int64_t rows, int64_t cols) {
+  if (groups < 1 || rows < 128 || cols < 128 || rows % 128 || cols % 128) return -1;
+  return packed_fp8_bytes(groups, rows, cols);
+}
+
+int32_t moe_pack_weights_fp8(int32_t kind, int64_t groups, int64_t rows, int64_t cols,
+                             const void* codes, const float* scales, void* dst, void* stream) {
+  if (kind != MOE_PACK_GATE_UP && kind != MOE_PACK_PLAIN) return fail(MOE_ERR_INVALID_ARG, "kind");
+  if (groups < 1 || rows < 128 || cols < 128) return fail(MOE_ERR_INVALID_ARG, "sizes");
+  if (rows % 128 || cols % 128) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "rows % 128 or cols % 128");
+  if (!codes || !scales || !dst) return fail(MOE_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(codes) || !aligned16(dst) || reinterpret_cast<uintptr_t>(scales) % 4)
+    return fail(MOE_ERR_ALIGNMENT, "codes or dst not 16-byte aligned, or scales not 4-byte aligned");
+  const char* a = static_cast<const char*>(codes);
+  const char* b = static_cast<const char*>(dst);
+  const size_t na = static_cast<size_t>(groups * rows * cols);
+  const size_t nb = static_cast<size_t>(packed_fp8_bytes(groups, rows, cols));
+  if (a < b + nb && b < a + na) return fail(MOE_ERR_INVALID_ARG, "codes and dst overlap");
+  MOE_CUDA(launch_pack_weights_fp8(kind, groups, rows, cols, codes, scales, dst,
+                                   static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
 int32_t moe_linear(int64_t T, int32_t in_features, int32_t out_features, const void* x,
                    const void* W, const void* add, void* y, void* workspace, size_t ws_bytes,
                    void* stream) {
@@ -869,7 +928,7 @@ int32_t moe_layer_forward(const moe_config* cfg, int64_t T, const void* x, const
   const void* x_e = x;
   if (cfg->d_latent) {
     st = run_linear(T, cfg->d_model, cfg->d_latent, x, W_lat_down, nullptr, at<void>(ws, L.x_lat),
-                    status, s, cfg->weight_layout == MOE_WEIGHTS_PACKED);
+                    status, s, latent_layout(cfg));
     if (st != MOE_OK) return st;
     x_e = at<void>(ws, L.x_lat);
   }
@@ -886,7 +945,7 @@ int32_t moe_layer_forward(const moe_config* cfg, int64_t T, const void* x, const
     MOE_CUDA(launch_combine(at<void>(ws, L.Y), inv, w, T, cfg->K, cfg->d_latent, nullptr, 0, 0,
                             at<void>(ws, L.r_lat), bf16, s));
     st = run_linear(T, cfg->d_latent, cfg->d_model, at<void>(ws, L.r_lat), W_lat_up, nullptr,
-                    at<void>(ws, L.U), status, s, cfg->weight_layout == MOE_WEIGHTS_PACKED);
+                    at<void>(ws, L.U), status, s, latent_layout(cfg));
     if (st != MOE_OK) return st;
     MOE_CUDA(launch_combine(nullptr, nullptr, nullptr, T, 0, cfg->d_model, at<void>(ws, L.U), 1 + S,
                             T, y, bf16, s));

@@ -158,6 +158,12 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// Orders this thread's earlier generic-proxy writes to shared memory before
+// later async-proxy reads of it (the tensor cores reading an operand).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- cluster
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -378,6 +384,22 @@ __device__ __forceinline__ float silu_f(float v) { return __fdividef(v, 1.0f + _
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&p);
+}
+
+// Two FP8 E4M3 codes (bits 0..7 and 8..15 of `two`) times `scale`, as a
+// bf16 pair (the low code in the low half).  E4M3 -> f16 is exact (one
+// hardware conversion for the pair), f16 -> f32 is exact, the product is
+// rounded to fp32 and then to bf16.
+__device__ __forceinline__ uint32_t e4m3x2_scaled_bf16x2(uint32_t two, float scale) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
+      : "=r"(h2)
+      : "r"(two));
+  float lo, hi;
+  asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h2));
+  return pack_bf16x2(lo * scale, hi * scale);
 }
 
 // 8 x 8 transpose of 16-bit values within each octet of lanes: before, lane

@@ -67,6 +67,11 @@ constexpr int kBBoxRows = 32;
 constexpr uint32_t kBBoxBytes = kBBoxRows * 128;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (3 + kEpiWarps);
+// FP8 weights: four more warps convert each landed FP8 stage into the bf16
+// weight ring (one warp per SM sub-partition)
+constexpr int kConvWarps = 4;
+constexpr int kThreadsFp8 = kThreads + 32 * kConvWarps;
+constexpr uint32_t kF8TileBytes = 128 * 64;  // one 128-row x 64-k FP8 tile
 constexpr int kMaxStages = 12;
 constexpr size_t kSmemBudget = 229376;  // pipeline bytes per CTA (224 KB)
 constexpr int kSmemMax = 232448;        // the per-block limit (227 KB)
@@ -317,8 +322,16 @@ __device__ __forceinline__ uint32_t acc_column(const Regions& r, int acc) {
 //     across the pair.  Both CTAs' copies complete on CTA 0's full barriers;
 //     CTA 0's commits release both CTAs' stages and signal both epilogues;
 //     both epilogues release TMEM on CTA 0's barrier.
-template <bool kPair>
-__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ GemmParams p) {
+//
+// kFp8 (never with kPair): the weight producer's bulk copies bring FP8 tiles
+// and their 16-byte block-scale record into a ring of f8_stages stages; the
+// converter warps wait for a stage and for a free bf16 weight stage, write
+// code x scale as bf16 in the same swizzled layout (FP8 byte offset o of a
+// tile becomes bf16 byte offset 2 o), fence for the tensor cores' proxy and
+// arrive on the k step's full barrier in place of the weight producer.
+template <bool kPair, bool kFp8>
+__global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -327,9 +340,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   const int nt = p.nt;
   const uint32_t b_stage_bytes = b_stage_bytes_of(nt, kPair);
   const uint32_t a_stage_bytes = kATileBytes * static_cast<uint32_t>(p.a_per_unit);
+  const int s8_n = kFp8 ? p.f8_stages : 0;
   uint8_t* smem_b = smem + sa_n * a_stage_bytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_b + sb_n * b_stage_bytes);
-  // bars: full[Sa] | empty[Sa] | tfull[2] | tempty[2] | drain
+  uint8_t* smem_f8 = smem_b + sb_n * b_stage_bytes;          // FP8 ring: s8 x 2 tiles
+  uint8_t* smem_rec = smem_f8 + s8_n * (2 * kF8TileBytes);  // s8 x 16-byte records
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_rec + 16 * s8_n);
+  // bars: full[Sa] | empty[Sa] | tfull[2] | tempty[2] | drain | f8full[S8] | f8empty[S8]
   // k step i of the CTA's sequence uses weight stage i % Sa and token stage
   // i % Sb.  full[i % Sa] counts the bytes of both (one wait per k step for
   // the MMA issuer) and empty[i % Sa] frees both (one commit per k step):
@@ -337,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   // completes k step i's phase.  With Sb <= Sa that phase is never
   // ambiguous, and no token copy reaches a full barrier before the
   // barrier's previous phase completed.
-  const int nbars = 2 * sa_n + 5;
+  const int nbars = 2 * sa_n + 5 + 2 * s8_n;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + nbars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -356,6 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   auto tfull_bar = [&](int r) { return bar_base + 8u * (2 * sa_n + r); };
   auto tempty_bar = [&](int r) { return bar_base + 8u * (2 * sa_n + 2 + r); };
   const uint32_t drain_bar = bar_base + 8u * (2 * sa_n + 4);
+  auto f8full = [&](int s) { return bar_base + 8u * (2 * sa_n + 5 + s); };
+  auto f8empty = [&](int s) { return bar_base + 8u * (2 * sa_n + 5 + s8_n + s); };
   // the same barrier in CTA 0 of the pair (the MMA issuer's)
   auto lead = [&](uint32_t bar) { return kPair ? cluster_map(bar, 0) : bar; };
   constexpr uint32_t kTmemCols = 512;
@@ -366,8 +384,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   }
   if (warp == 1 && lane == 0) {
     for (int s = 0; s < sa_n; ++s) {
-      mbar_init(a_full(s), 2);  // the two producers' arrivals (CTA 0's in a pair)
+      // the two producers' arrivals (CTA 0's in a pair), or the token
+      // producer's and the converter warps'
+      mbar_init(a_full(s), kFp8 ? 1 + kConvWarps : 2);
       mbar_init(a_empty(s), 1);
+    }
+    for (int s = 0; s < s8_n; ++s) {
+      mbar_init(f8full(s), 1);
+      mbar_init(f8empty(s), kConvWarps);
     }
     for (int r = 0; r < 2; ++r) {
       mbar_init(tfull_bar(r), 1);
@@ -396,6 +420,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     const uint64_t pol_stream = l2_policy_evict_first();
     const uint64_t pol_normal = l2_policy_evict_normal();
     const uint64_t pol_keep = l2_policy_evict_last();
+    // the producer's ring: the bf16 weight stages, or the FP8 stages
+    const int ring = kFp8 ? s8_n : sa_n;
+    auto slot_free = [&](int st) { return kFp8 ? f8empty(st) : a_empty(st); };
     int stage = 0;
     uint32_t phase = 0;
     int64_t issued = 0;
@@ -405,18 +432,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       const Unit x = nx;
       if (u + u_step < total) nx = decode_unit(p, u + u_step, units0, units1, rank);
       const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
-      const uint32_t tx = kATileBytes * x.n_a;
+      const uint32_t tx = (kFp8 ? kF8TileBytes : kATileBytes) * x.n_a;
       // a weight block read by one token tile is streamed; one shared by
       // several token tiles (running side by side) is kept for the others;
       // a token-tile-major segment's weights serve every token tile
       const uint64_t pol_w = s->b_major ? pol_keep : x.ntiles > 1 ? pol_normal : pol_stream;
       bool ok = true;
       for (int ks = x.k0; ks < x.k1; ++ks) {
-        if (!mbar_wait_bounded(a_empty(stage), phase ^ 1u, abort_flag, p.status)) {
+        if (!mbar_wait_bounded(slot_free(stage), phase ^ 1u, abort_flag, p.status)) {
           ok = false;
           break;
         }
-        const uint32_t fb = a_full(stage);
+        const uint32_t fb = kFp8 ? f8full(stage) : a_full(stage);
         const uint32_t a_dst = a_base + stage * a_stage_bytes;
         const int kc = ks * kBK;
         // packed weights: the unit's tiles at k step ks (a pair, or the
@@ -425,7 +452,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         const int in_pair = min(2, s->a128 - 2 * pair_idx);
         const int64_t tile = 2ll * pair_idx * s->k_steps + static_cast<int64_t>(ks) * in_pair +
                              (x.blk0 & 1);
-        if (kPair) {
+        if (kFp8) {
+          // the FP8 tiles and the pair's block-scale record for this k step
+          mbar_arrive_expect_tx(fb, tx + 16);
+          bulk_load(smem_u32(smem_f8) + stage * (2 * kF8TileBytes),
+                    s->a_packed + x.group * s->a_group_bytes + tile * kF8TileBytes, tx, fb, pol_w);
+          bulk_load(smem_u32(smem_rec) + stage * 16,
+                    s->a_rec + ((x.group * s->a_rec_group) + pair_idx * s->k_steps + ks) * 16, 16,
+                    fb, pol_w);
+        } else if (kPair) {
           // CTA 0 expects both CTAs' tiles on its barrier
           if (rank == 0) mbar_arrive_expect_tx(fb, 2 * kATileBytes);
           tma_load_2d_pair(a_dst, &s->tmA, lead(fb), 0,
@@ -453,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           }
         }
         ++issued;
-        if (++stage == sa_n) {
+        if (++stage == ring) {
           stage = 0;
           phase ^= 1u;
         }
@@ -462,11 +497,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     }
     // drain: wait until the last stages issued were consumed (so every copy
     // into them, of either producer and either CTA, has landed)
-    const int64_t first = issued > sa_n ? issued - sa_n : 0;
+    const int64_t first = issued > ring ? issued - ring : 0;
     for (int64_t q = first; q < issued; ++q) {
-      const int st = static_cast<int>(q % sa_n);
-      const uint32_t par = static_cast<uint32_t>((q / sa_n) & 1);
-      if (!drain_wait(a_empty(st), par, p.status)) break;
+      const int st = static_cast<int>(q % ring);
+      const uint32_t par = static_cast<uint32_t>((q / ring) & 1);
+      if (!drain_wait(slot_free(st), par, p.status)) break;
     }
   } else if (warp == 2 && lane == 0) {
     // ------------------------------------------------- token (B) producer
@@ -603,6 +638,67 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     else
       tc_commit(drain_bar);
     drain_wait(drain_bar, 0, p.status);
+  } else if (kFp8 && warp >= 3 + kEpiWarps) {
+    // ---------------------------------------------- FP8 -> bf16 converters
+    // Thread ct handles the 8-byte FP8 pieces ct + 128 i of a stage: piece
+    // pc is row pc / 8 of the stage's 256 rows (tile pc / 1024), so piece i
+    // of every thread lies in tile i / 8 and in its gate half (rows with bit
+    // 4 clear) for even i, its up half for odd i -- the record's scale
+    // 2 (i / 8) + (i % 2).  A plain store-mode tile has one scale, written
+    // twice in its record.
+    const int ct = threadIdx.x - 32 * (3 + kEpiWarps);
+    int sa = 0, s8 = 0;
+    uint32_t pa = 0, p8 = 0;
+    Unit nx = u_first < total ? decode_unit(p, u_first, units0, units1, rank) : Unit{};
+    for (int u = u_first; u < total; u += u_step) {
+      const Unit x = nx;
+      if (u + u_step < total) nx = decode_unit(p, u + u_step, units0, units1, rank);
+      bool ok = true;
+      for (int ks = x.k0; ks < x.k1; ++ks) {
+        if (!warp_wait(f8full(s8), p8, abort_flag, p.status) ||
+            !warp_wait(a_empty(sa), pa ^ 1u, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        const float* rec = reinterpret_cast<const float*>(smem_rec + 16 * s8);
+        float sc[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sc[j] = rec[j];
+        const uint8_t* src = smem_f8 + s8 * (2 * kF8TileBytes);
+        uint8_t* dst = smem + sa * a_stage_bytes;
+        const int n_i = 8 * x.n_a;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          if (i < n_i) {
+            const int pc = ct + 128 * i;
+            const float scale = sc[2 * (i >> 3) + (i & 1)];
+            const uint2 v = *reinterpret_cast<const uint2*>(src + 8 * pc);
+            uint4 o;
+            o.x = e4m3x2_scaled_bf16x2(v.x & 0xffffu, scale);
+            o.y = e4m3x2_scaled_bf16x2(v.x >> 16, scale);
+            o.z = e4m3x2_scaled_bf16x2(v.y & 0xffffu, scale);
+            o.w = e4m3x2_scaled_bf16x2(v.y >> 16, scale);
+            *reinterpret_cast<uint4*>(dst + 16 * pc) = o;
+          }
+        }
+        // the stage is read next by the tensor cores (async proxy)
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(f8empty(s8));
+          mbar_arrive(a_full(sa));
+        }
+        if (++s8 == s8_n) {
+          s8 = 0;
+          p8 ^= 1u;
+        }
+        if (++sa == sa_n) {
+          sa = 0;
+          pa ^= 1u;
+        }
+      }
+      if (!ok) break;
+    }
   } else if (warp >= 3) {
     // ---------------------------------------------------------- epilogue
     const int q = warp & 3;           // TMEM lane quadrant this warp may access
@@ -744,10 +840,13 @@ __global__ void __launch_bounds__(256) split_router_weight_kernel(const float* _
 
 // One 16-byte chunk of the packed bank per thread step: dst is written in
 // order, src gathered (a one-time load step).
+// V carries 8 consecutive elements: uint4 for bf16, uint2 for FP8 (whose
+// tiles are 8 KB and whose rows are 64 bytes; the same chunk swizzle).
+template <typename V>
 __global__ void __launch_bounds__(256) pack_weights_kernel(int kind, int64_t groups, int64_t rows,
                                                            int64_t cols,
-                                                           const uint4* __restrict__ src,
-                                                           uint4* __restrict__ dst) {
+                                                           const V* __restrict__ src,
+                                                           V* __restrict__ dst) {
   const int64_t ksteps = cols / kBK;
   const int64_t a128 = rows / 128;
   const int64_t per_group = a128 * ksteps;  // 16 KB tiles per group
@@ -781,6 +880,43 @@ __global__ void __launch_bounds__(256) pack_weights_kernel(int kind, int64_t gro
       row = blk * 128 + r;
     }
     dst[i] = src[((g * rows + row) * cols + ks * kBK + chunk * 8) >> 3];
+  }
+}
+
+// One 16-byte record per (group, tile pair, k step): the block scales of
+// the pair's two tiles at that k step, (tile 0 gate or plain, tile 0 up or
+// plain, tile 1 ..., tile 1 ...); 0 for a missing second tile.
+__global__ void __launch_bounds__(256) pack_scale_records_kernel(int kind, int64_t groups,
+                                                                 int64_t rows, int64_t cols,
+                                                                 const float* __restrict__ scales,
+                                                                 float4* __restrict__ rec) {
+  const int64_t ksteps = cols / kBK;
+  const int64_t a128 = rows / 128;
+  const int64_t npairs = (a128 + 1) / 2;
+  const int64_t nbr = (rows + 127) / 128, nbc = (cols + 127) / 128;
+  const int64_t n = groups * npairs * ksteps;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t g = i / (npairs * ksteps);
+    const int64_t rem = i - g * npairs * ksteps;
+    const int64_t pair = rem / ksteps;
+    const int64_t cb = ((rem - pair * ksteps) * kBK) / 128;  // column block of the k step
+    float v[4];
+#pragma unroll
+    for (int a = 0; a < 2; ++a) {
+      const int64_t blk = 2 * pair + a;
+      if (blk >= a128) {
+        v[2 * a] = v[2 * a + 1] = 0.0f;
+        continue;
+      }
+      // row blocks of the tile's rows: gate/up tile blk holds rows
+      // 64 blk.. of the gate half and F + 64 blk.. of the up half
+      const int64_t rb0 = kind == 0 ? (64 * blk) / 128 : blk;
+      const int64_t rb1 = kind == 0 ? (rows / 2 + 64 * blk) / 128 : blk;
+      v[2 * a] = scales[(g * nbr + rb0) * nbc + cb];
+      v[2 * a + 1] = scales[(g * nbr + rb1) * nbc + cb];
+    }
+    rec[i] = make_float4(v[0], v[1], v[2], v[3]);
   }
 }
 
@@ -868,7 +1004,39 @@ GemmPlan plan_gemm(int nt, int a_per_unit, bool pair) {
   }
   if (g.b_stages > sa) g.b_stages = sa;  // see the barrier layout in the kernel
   g.a_stages = sa;
+  g.f8_stages = 0;
   g.smem_bytes = 1024 + a_stage * sa + b_stage * g.b_stages + 8 * (2 * sa + 5) + 16;
+  return g;
+}
+
+// FP8 weights: two bf16 weight stages (the converters stay one stage ahead
+// of the MMAs), two token stages, and every remaining byte as FP8 stages
+// (the copies in flight from HBM), at most kMaxStages.
+GemmPlan plan_gemm_fp8(int nt) {
+  static const int forced_a = [] {  // tuning override: bf16 weight stages
+    const char* v = getenv("FGS_FP8_A_STAGES");
+    return (v && *v) ? atoi(v) : 0;
+  }();
+  static const int forced_8 = [] {  // tuning override: cap on the FP8 stages
+    const char* v = getenv("FGS_F8_STAGES");
+    return (v && *v) ? atoi(v) : 0;
+  }();
+  GemmPlan g;
+  g.nt = nt;
+  const size_t b_stage = b_stage_bytes_of(nt, false);
+  const size_t a_stage = 2ull * kATileBytes;
+  g.a_stages = (forced_a >= 2 && forced_a <= 4) ? forced_a : 2;
+  g.b_stages = 2;
+  const size_t f8_stage = 2ull * kF8TileBytes + 16 + 16;  // tiles, record, two barriers
+  const size_t fixed = 1024 + a_stage * g.a_stages + b_stage * g.b_stages +
+                       8 * (2 * g.a_stages + 5) + 16;
+  int s8 = fixed < static_cast<size_t>(kSmemMax)
+               ? static_cast<int>((static_cast<size_t>(kSmemMax) - fixed) / f8_stage)
+               : 0;
+  if (s8 > kMaxStages) s8 = kMaxStages;
+  if (forced_8 >= 2 && s8 > forced_8) s8 = forced_8;
+  g.f8_stages = s8;
+  g.smem_bytes = fixed + f8_stage * s8;
   return g;
 }
 
@@ -906,7 +1074,8 @@ CUresult encode_pair_maps(GemmSegment& s) {
 bool pair_capable(const GemmParams& p) {
   for (int i = 0; i < p.nseg; ++i) {
     const GemmSegment& s = p.seg[i];
-    if (!s.a_packed || s.a_groups < 1 || s.a128 % 2 || s.ksplit > 1 || s.b_k_period) return false;
+    if (!s.a_packed || s.a_fp8 || s.a_groups < 1 || s.a128 % 2 || s.ksplit > 1 || s.b_k_period)
+      return false;
   }
   return p.nseg > 0;
 }
@@ -921,11 +1090,18 @@ cudaError_t launch_tc_gemm(const GemmParams& params, int num_sms, cudaStream_t s
     }
     if (g.nt > p.nt) p.nt = g.nt;  // the token ring holds the largest tile
   }
-  p.pair = (params.pair && pair_capable(params) && num_sms >= 2) ? 1 : 0;
-  p.a_per_unit = (p.pair || params.a_per_unit == 1) ? 1 : 2;
-  const GemmPlan plan = plan_gemm(p.nt, p.a_per_unit, p.pair != 0);
+  // FP8 weights: every segment packed FP8, two weight tiles per unit, no pairs
+  p.fp8 = p.seg[0].a_fp8 ? 1 : 0;
+  for (int i = 0; i < p.nseg; ++i)
+    if ((p.seg[i].a_fp8 != 0) != (p.fp8 != 0) || (p.seg[i].a_fp8 && !p.seg[i].a_packed))
+      return cudaErrorInvalidValue;
+  p.pair = (!p.fp8 && params.pair && pair_capable(params) && num_sms >= 2) ? 1 : 0;
+  p.a_per_unit = (p.fp8 || !(p.pair || params.a_per_unit == 1)) ? 2 : 1;
+  const GemmPlan plan = p.fp8 ? plan_gemm_fp8(p.nt) : plan_gemm(p.nt, p.a_per_unit, p.pair != 0);
+  if (p.fp8 && plan.f8_stages < 2) return cudaErrorInvalidValue;
   p.a_stages = plan.a_stages;
   p.b_stages = plan.b_stages;
+  p.f8_stages = plan.f8_stages;
   if (p.pair)
     for (int i = 0; i < p.nseg; ++i)
       if (encode_pair_maps(p.seg[i]) != CUDA_SUCCESS) return cudaErrorInvalidValue;
@@ -934,10 +1110,13 @@ cudaError_t launch_tc_gemm(const GemmParams& params, int num_sms, cudaStream_t s
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev >= 64 || !configured[dev]) {
-    err = cudaFuncSetAttribute(tc_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kSmemMax);
+    err = cudaFuncSetAttribute(tc_gemm_kernel<false, false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
     if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(tc_gemm_kernel<true>,
+      err = cudaFuncSetAttribute(tc_gemm_kernel<true, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(tc_gemm_kernel<false, true>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
     if (err != cudaSuccess) return err;
     if (dev < 64) configured[dev] = 1;
@@ -956,10 +1135,13 @@ cudaError_t launch_tc_gemm(const GemmParams& params, int num_sms, cudaStream_t s
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     note_launch();
-    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<true>, p);
+    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<true, false>, p);
   }
   note_launch();
-  tc_gemm_kernel<false><<<num_sms, kThreads, plan.smem_bytes, stream>>>(p);
+  if (p.fp8)
+    tc_gemm_kernel<false, true><<<num_sms, kThreadsFp8, plan.smem_bytes, stream>>>(p);
+  else
+    tc_gemm_kernel<false, false><<<num_sms, kThreads, plan.smem_bytes, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -970,8 +1152,35 @@ cudaError_t launch_pack_weights(int kind, int64_t groups, int64_t rows, int64_t 
   if (blocks > 65536) blocks = 65536;
   if (blocks < 1) return cudaSuccess;
   note_launch();
-  pack_weights_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+  pack_weights_kernel<uint4><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
       kind, groups, rows, cols, static_cast<const uint4*>(src), static_cast<uint4*>(dst));
+  return cudaGetLastError();
+}
+
+int64_t packed_fp8_bytes(int64_t groups, int64_t rows, int64_t cols) {
+  const int64_t npairs = (rows / 128 + 1) / 2;
+  return groups * rows * cols + groups * npairs * (cols / kBK) * 16;
+}
+
+cudaError_t launch_pack_weights_fp8(int kind, int64_t groups, int64_t rows, int64_t cols,
+                                    const void* codes, const float* scales, void* dst,
+                                    cudaStream_t stream) {
+  const int64_t n = groups * rows * cols / 8;
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 65536) blocks = 65536;
+  if (blocks < 1) return cudaSuccess;
+  note_launch();
+  pack_weights_kernel<uint2><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      kind, groups, rows, cols, static_cast<const uint2*>(codes), static_cast<uint2*>(dst));
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const int64_t nrec = groups * ((rows / 128 + 1) / 2) * (cols / kBK);
+  int64_t rblocks = (nrec + 255) / 256;
+  if (rblocks > 65536) rblocks = 65536;
+  note_launch();
+  pack_scale_records_kernel<<<static_cast<unsigned>(rblocks), 256, 0, stream>>>(
+      kind, groups, rows, cols, scales,
+      reinterpret_cast<float4*>(static_cast<uint8_t*>(dst) + groups * rows * cols));
   return cudaGetLastError();
 }
 

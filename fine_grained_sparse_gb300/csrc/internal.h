@@ -111,6 +111,12 @@ struct GemmSegment {
   const uint8_t* a_packed;
   int64_t a_group_bytes;
   int a_groups;  // groups in the packed bank
+  // FP8 E4M3 packed weights (see moe_pack_weights_fp8): a_packed holds 8 KB
+  // tiles, a_rec the 16-byte block-scale record of each (tile pair, k step),
+  // a_rec_group records per group
+  int a_fp8;
+  const uint8_t* a_rec;
+  int64_t a_rec_group;
   // explicit tiles (routed experts) or implicit ones (groups x rows)
   const RowTile* tiles;
   const int* ntiles;
@@ -156,21 +162,33 @@ struct GemmParams {
   // token tile.  Applied only when pair_capable(); implies one weight tile
   // per CTA.
   int pair;
-  int a_stages;  // weight ring depth
+  int a_stages;  // weight ring depth (bf16 weight tiles the MMAs read)
   int b_stages;  // token ring depth
+  // 1: the segments' weights are FP8 (a_fp8): their tiles land in a ring of
+  // f8_stages FP8 stages and converter warps write the bf16 weight ring
+  int fp8;
+  int f8_stages;
   int* status;
 };
 
 struct GemmPlan {
-  int nt, a_stages, b_stages;
+  int nt, a_stages, b_stages, f8_stages;
   size_t smem_bytes;
 };
 GemmPlan plan_gemm(int nt, int a_per_unit, bool pair);
+GemmPlan plan_gemm_fp8(int nt);
 // Whether a launch can run on CTA pairs (packed weights with an even number
 // of 128-row tiles in every segment, no K split).
 bool pair_capable(const GemmParams& p);
 
 cudaError_t launch_tc_gemm(const GemmParams& p, int num_sms, cudaStream_t stream);
+
+// Rearrange an FP8 bank and its block scales into the packed FP8 order (see
+// moe_pack_weights_fp8); packed_fp8_bytes is its size.
+int64_t packed_fp8_bytes(int64_t groups, int64_t rows, int64_t cols);
+cudaError_t launch_pack_weights_fp8(int kind, int64_t groups, int64_t rows, int64_t cols,
+                                    const void* codes, const float* scales, void* dst,
+                                    cudaStream_t stream);
 
 // Rearrange a bf16 weight bank into the packed order (see moe_pack_weights).
 cudaError_t launch_pack_weights(int kind, int64_t groups, int64_t rows, int64_t cols,

@@ -74,16 +74,31 @@ typedef struct moe_config {
   int32_t norm_topk_prob;      /* renormalise the K weights when K > 1 (1)      */
   int32_t d_latent;     /* K3 latent width L (3584); 0 = K2 form (no projection)*/
   int32_t dtype;        /* moe_dtype of activations, expert weights, outputs    */
-  int32_t weight_layout;/* moe_weight_layout of the bf16 expert, shared-expert
-                           and latent-projection weights                       */
+  int32_t weight_layout;/* moe_weight_layout of the expert, shared-expert and
+                           latent-projection weights                           */
 } moe_config;
 
-/* Layouts of the bf16 weight matrices the expert GEMMs stream.
- *   MOE_WEIGHTS_NATURAL: row-major [G, O, K] as documented per argument.
+/* Layouts of the weight matrices the expert GEMMs stream.
+ *   MOE_WEIGHTS_NATURAL: bf16, row-major [G, O, K] as documented per argument.
  *   MOE_WEIGHTS_PACKED:  the same values rearranged by moe_pack_weights()
  *     into the order the tensor cores consume them, so that every pipeline
- *     stage of a GEMM is one contiguous bulk copy (see moe_pack_weights). */
-typedef enum moe_weight_layout { MOE_WEIGHTS_NATURAL = 0, MOE_WEIGHTS_PACKED = 1 } moe_weight_layout;
+ *     stage of a GEMM is one contiguous bulk copy (see moe_pack_weights).
+ *   MOE_WEIGHTS_PACKED_FP8: the routed and shared experts' W_gate_up and
+ *     W_down are FP8 E4M3 with one fp32 multiplier per 128 x 128 block,
+ *     packed by moe_pack_weights_fp8 (each bank one buffer: tiles, then the
+ *     block-scale records); the latent projections stay bf16, packed by
+ *     moe_pack_weights.  Needs bf16 activations and d_model, d_ff,
+ *     d_ff_shared, d_latent multiples of 128.  ("Kimi K2 · Router ·
+ *     OpenModelAtlas", Parameters: the checkpoint's tensors carry FP8 block
+ *     scales.  The encoding, the block shape and the scale's type are not on
+ *     the page; E4M3, 128 x 128 and an fp32 multiplier are this library's
+ *     reading.)  Activations, H and the accumulation stay as in the bf16
+ *     form; each weight enters the tensor cores as bf16(code value x scale). */
+typedef enum moe_weight_layout {
+  MOE_WEIGHTS_NATURAL = 0,
+  MOE_WEIGHTS_PACKED = 1,
+  MOE_WEIGHTS_PACKED_FP8 = 2
+} moe_weight_layout;
 
 /* Kinds of packed matrices. */
 typedef enum moe_pack_kind {
@@ -109,6 +124,34 @@ typedef enum moe_pack_kind {
  * side by side. */
 int32_t moe_pack_weights(int32_t kind, int64_t groups, int64_t rows, int64_t cols,
                          const void* src, void* dst, void* stream);
+
+/* Bytes of a bank packed by moe_pack_weights_fp8:
+ * groups * rows * cols (the codes) + groups * ceil(rows / 256) * (cols / 64)
+ * * 16 (the records); -1 for sizes moe_pack_weights_fp8 rejects. */
+int64_t moe_packed_fp8_bytes(int64_t groups, int64_t rows, int64_t cols);
+
+/*
+ * Rearrange an FP8 E4M3 weight bank and its block scales into
+ * MOE_WEIGHTS_PACKED_FP8 order (a one-time load step, like
+ * moe_pack_weights).
+ *   codes  [groups, rows, cols] uint8, device, E4M3 codes (row-major)
+ *   scales [groups, rows / 128, cols / 128] fp32, device: weight (g, r, c) =
+ *          value(codes[g][r][c]) * scales[g][r / 128][c / 128]
+ *   dst    device buffer of moe_packed_fp8_bytes(groups, rows, cols) bytes,
+ *          not overlapping codes
+ * rows % 128 == 0 and cols % 128 == 0 (MOE_PACK_GATE_UP: rows = 2 F, the
+ * gate rows then the up rows).  codes and dst 16-byte aligned, scales 4-byte
+ * aligned.  The tiles take the order and row interleave of moe_pack_weights
+ * with one byte per element: a tile is 128 rows x 64 columns = 8 KB, row r
+ * at bytes [64 r, 64 r + 64), its 8-byte chunk c (columns 8c..8c+7) at
+ * chunk position c XOR (r mod 8).  After all tiles, one 16-byte record per
+ * (group, tile pair u, k step), in that order: four fp32 scales, those of
+ * tile 2u's rows (its gate rows, then its up rows; for MOE_PACK_PLAIN its one
+ * row block twice) and of tile 2u + 1's (zero when the pair has one tile),
+ * each at the k step's 128-column block.  Asynchronous on `stream`;
+ * MOE_ERR_INVALID_ARG / UNSUPPORTED_SHAPE / ALIGNMENT before any launch. */
+int32_t moe_pack_weights_fp8(int32_t kind, int64_t groups, int64_t rows, int64_t cols,
+                             const void* codes, const float* scales, void* dst, void* stream);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int32_t moe_version(void);
