@@ -51,6 +51,10 @@ WORKLOADS = {
                  "experts (intermediate 3072), top-16, 2 shared experts at 7168 (intermediate "
                  "3072), scale 2.827, bf16 experts, fp32 router",
 }
+_FP8_NOTE = (" -- expert weights FP8 E4M3 with one fp32 scale per 128 x 128 block (dequantised "
+             "to bf16 in shared memory; bf16 activations, fp32 accumulation)")
+for _n in ("k2_decode", "k2_prefill", "k3_latent"):
+    WORKLOADS[_n + "_fp8"] = WORKLOADS[_n].replace(", bf16 experts", "") + _FP8_NOTE
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 
 
@@ -61,7 +65,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="k2_prefill", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="own", choices=["own", "reference"])
-    ap.add_argument("--cpu-sample-tokens", type=int, default=64)
+    ap.add_argument("--cpu-sample-tokens", type=int, default=0,
+                    help="tokens of the CPU oracle sample (default 64; 8 with FP8 weights, "
+                         "whose per-expert dequantisation dominates the oracle's time)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -205,10 +211,13 @@ def per_step_work(shape, counts):
     de = L if L else d
     U = int((counts > 0).sum())
     b16 = 2
-    w_gu = 2 * F * de * b16
-    w_dn = de * F * b16
-    ws_gu = 2 * Fs * d * b16
-    ws_dn = d * Fs * b16
+    # expert weight bytes per element: bf16, or an FP8 code plus its share of
+    # the block's fp32 scale
+    bw = 1 + 4 / (128 * 128) if getattr(shape, "weights", "bf16") == "fp8" else b16
+    w_gu = 2 * F * de * bw
+    w_dn = de * F * bw
+    ws_gu = 2 * Fs * d * bw
+    ws_dn = d * Fs * bw
     xbytes = T * d * b16
     router_bytes = E * d * 4 + E * 4 + xbytes + T * K * 8
     # x is read once; with the latent form the routed experts read x_lat instead
@@ -221,8 +230,8 @@ def per_step_work(shape, counts):
     flops_gate_up = 2 * T * K * de * 2 * F + 2 * T * S * d * 2 * Fs
     flops_down = 2 * T * K * F * de + 2 * T * S * Fs * d
     flops_proj = 2 * 2 * T * d * L if L else 0
-    return {"U": U, "gate_up_bytes": gate_up_bytes, "down_bytes": down_bytes,
-            "router_bytes": router_bytes, "layer_bytes": layer_bytes,
+    return {"U": U, "gate_up_bytes": int(gate_up_bytes), "down_bytes": int(down_bytes),
+            "router_bytes": router_bytes, "layer_bytes": int(layer_bytes),
             "flops_router": flops_router, "flops_gate_up": flops_gate_up, "flops_down": flops_down,
             "flops_layer": flops_router + flops_gate_up + flops_down + flops_proj}
 
@@ -256,25 +265,48 @@ def profiled_traffic(config):
 
 
 # ------------------------------------------------------------ CPU oracle leg
+def is_fp8(shape):
+    return getattr(shape, "weights", "bf16") == "fp8"
+
+
+def expert_f64(shape, rec):
+    """(W_gate, W_up, W_down) in fp64 from an expert's host tensors: (gate_up,
+    down) bf16, or FP8 (gate_up codes, scales, down codes, scales), which the
+    oracle dequantises."""
+    import oracle
+    if is_fp8(shape):
+        gu = oracle.dequant_fp8_blocks(rec[0].numpy(), rec[1].numpy())
+        dn = oracle.dequant_fp8_blocks(rec[2].numpy(), rec[3].numpy())
+    else:
+        gu, dn = (t.to(__import__("torch").float64).numpy() for t in rec)
+    F = gu.shape[0] // 2
+    return gu[:F], gu[F:], dn
+
+
+def expert_record(shape, g, bank, e):
+    """One expert's weights of a generated layer, copied to the host."""
+    if is_fp8(shape):
+        return tuple(g[f"{bank}_{m}_{k}"][e].cpu() for m in ("gate_up", "down") for k in "qs")
+    return g[f"{bank}_gate_up"][e].cpu(), g[f"{bank}_down"][e].cpu()
+
+
 def oracle_sample(shape, x_rows, W_r, bias, routed, shared, lat):
-    """Run the oracle on the given token rows; returns (seconds, result)."""
-    import numpy as np
+    """Run the oracle on the given token rows; returns (seconds, result).
+    routed(e) / shared(s) give an expert's host tensors (see expert_f64); the
+    conversion to fp64 (and the FP8 dequantisation) is part of the timed
+    oracle work."""
     import torch
     import oracle
     f64 = lambda t: t.to(torch.float64).numpy()  # noqa: E731
     t0 = time.perf_counter()
     res = oracle.moe_layer(
         f64(x_rows), f64(W_r), bias.numpy(),
-        routed=lambda e: tuple(f64(w) for w in routed(e)),
-        shared=(lambda s: tuple(f64(w) for w in shared(s))) if shape.E_shared else None,
+        routed=lambda e: expert_f64(shape, routed(e)),
+        shared=(lambda s: expert_f64(shape, shared(s))) if shape.E_shared else None,
         n_shared=shape.E_shared, K=shape.K, n_group=shape.n_group, topk_group=shape.topk_group,
         scale=shape.routed_scaling_factor, norm_topk_prob=shape.norm_topk_prob,
         W_lat_down64=f64(lat[0]) if lat else None, W_lat_up64=f64(lat[1]) if lat else None)
     return time.perf_counter() - t0, res
-
-
-def split_gu(gu, F):
-    return gu[:F], gu[F:]
 
 
 def cpu_baseline_from_device(shape, g, idx, n_tokens):
@@ -285,20 +317,18 @@ def cpu_baseline_from_device(shape, g, idx, n_tokens):
     T = shape.T
     rows = np.unique(np.linspace(0, T - 1, n_tokens).astype(int))
     experts = sorted(set(int(e) for e in idx[rows].reshape(-1)))
-    F, Fs = shape.d_ff, shape.d_ff_shared
-    host = {e: (g["W_gate_up"][e].cpu(), g["W_down"][e].cpu()) for e in experts}
+    host = {e: expert_record(shape, g, "W", e) for e in experts}
 
     def routed(e):
         if e not in host:  # the oracle chose an expert the device did not
-            host[e] = (g["W_gate_up"][e].cpu(), g["W_down"][e].cpu())
-        gu, dn = host[e]
-        return (*split_gu(gu, F), dn)
+            host[e] = expert_record(shape, g, "W", e)
+        return host[e]
 
-    sh = [(g["Ws_gate_up"][s].cpu(), g["Ws_down"][s].cpu()) for s in range(shape.E_shared)]
+    sh = [expert_record(shape, g, "Ws", s) for s in range(shape.E_shared)]
     lat = (g["W_lat_down"].cpu(), g["W_lat_up"].cpu()) if shape.d_latent else None
     x_rows = g["x"][torch.as_tensor(rows, device=g["x"].device)].cpu()
     secs, _ = oracle_sample(shape, x_rows, g["W_r"].cpu(), g["bias"].cpu(), routed,
-                            lambda s: (*split_gu(sh[s][0], Fs), sh[s][1]), lat)
+                            lambda s: sh[s], lat)
     cores = len(os.sched_getaffinity(0))
     return {"value": len(rows) / secs, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{len(rows)} of the {T} tokens of the benchmarked batch, full layer "
@@ -345,10 +375,12 @@ def run_own(args):
     g = synth.generate(shape, device="cuda", seed=seed)
     if rank:  # replicas: every rank its own batch, same weights
         g["x"] = synth.activations(shape, "cuda", seed=replica_seed(seed, rank))
-    cfg = fgs.config(shape, weight_layout=fgs.MOE_WEIGHTS_PACKED)
+    # bf16 banks packed, or FP8 banks (config(shape) picks MOE_WEIGHTS_PACKED_FP8)
+    cfg = fgs.config(shape) if is_fp8(shape) else fgs.config(shape,
+                                                             weight_layout=fgs.MOE_WEIGHTS_PACKED)
     # one-time load step: weights rearranged into the order the tensor cores
     # stream (the natural copies stay for the CPU oracle leg)
-    gp = fgs.pack_layer_weights(g)
+    gp = fgs.pack_layer_weights_fp8(g) if is_fp8(shape) else fgs.pack_layer_weights(g)
     torch.cuda.synchronize()
     nws = fgs.moe_workspace_size(cfg, T)
     ws = torch.zeros(nws, dtype=torch.uint8, device="cuda")
@@ -418,10 +450,16 @@ def run_own(args):
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded; bf16 expert weights N(0,0.02), fp32 router weight "
-                "kaiming-uniform, bias uniform; shapes of the pages' K2/K3 layers)",
+        "data": ("synthetic (seeded; FP8 E4M3 expert weights, codes N(0,112^2) rounded by "
+                 "torch's float8 cast, 128x128 block scales U(0.5,1.5)*0.02/112"
+                 if is_fp8(shape) else
+                 "synthetic (seeded; bf16 expert weights N(0,0.02)")
+                + ", fp32 router weight kaiming-uniform, bias uniform; shapes of the pages' "
+                  "K2/K3 layers)",
         "config": {"workload": WORKLOADS[args.config], "name": args.config, "tokens_per_step": T,
-                   "weights": "bf16, packed once before timing (moe_pack_weights)",
+                   "weights": ("FP8 E4M3 + fp32 128x128 block scales, packed once before "
+                               "timing (moe_pack_weights_fp8)" if is_fp8(shape) else
+                               "bf16, packed once before timing (moe_pack_weights)"),
                    "l2": "inputs larger than L2: the selected experts' weights (tens of GB) "
                          "stream from HBM every step",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -467,7 +505,8 @@ def run_own(args):
 
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_from_device(shape, g, idx.cpu().numpy(),
-                                                        args.cpu_sample_tokens)
+                                                        args.cpu_sample_tokens or
+                                                        (8 if is_fp8(shape) else 64))
     if rank == 0:
         print(json.dumps(line), flush=True)
     finish_ranks(torch, world)
@@ -489,15 +528,15 @@ def run_reference(args):
     x = synth.activations(shape, "cpu", seed)
     W_r, bias = synth.router_params(shape, "cpu", seed)
     lat = synth.latent_projections(shape, "cpu", seed) if shape.d_latent else None
-    sh = [synth.shared_expert(shape, s, "cpu", seed) for s in range(shape.E_shared)]
-    F, Fs = shape.d_ff, shape.d_ff_shared
+    draw_routed = synth.routed_expert_fp8 if is_fp8(shape) else synth.routed_expert
+    draw_shared = synth.shared_expert_fp8 if is_fp8(shape) else synth.shared_expert
+    sh = [draw_shared(shape, s, "cpu", seed) for s in range(shape.E_shared)]
     cache = {}
 
     def routed(e):
         if e not in cache:
-            cache[e] = synth.routed_expert(shape, e, "cpu", seed)
-        gu, dn = cache[e]
-        return (*split_gu(gu, F), dn)
+            cache[e] = draw_routed(shape, e, "cpu", seed)
+        return cache[e]
 
     # a pool of tokens whose experts are drawn once (drawing weights is not the
     # oracle's work); each step runs the oracle on the next token of the pool
@@ -513,7 +552,7 @@ def run_reference(args):
     for i in range(total):
         rows = pool[i % len(pool): i % len(pool) + tokens_per_step]
         secs, _ = oracle_sample(shape, x[torch.as_tensor(rows)], W_r, bias, routed,
-                                lambda s: (*split_gu(sh[s][0], Fs), sh[s][1]), lat)
+                                lambda s: sh[s], lat)
         if i >= args.warmup:
             times.append(secs)
     secs = sum(times)

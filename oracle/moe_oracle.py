@@ -58,13 +58,22 @@ def e4m3_to_f64(codes) -> np.ndarray:
     exponent 0 is subnormal (m/8 * 2^-6); there are no infinities and
     S.1111.111 is NaN, so the largest magnitude is 1.75 * 2^8 = 448.
     """
-    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    return _E4M3_TABLE[np.asarray(codes, dtype=np.uint8)]
+
+
+def _e4m3_values() -> np.ndarray:
+    """The value of every code 0..255, from the field definitions above (a
+    table, so that decoding a large bank is one lookup per code)."""
+    c = np.arange(256, dtype=np.int64)
     sign = np.where(c & 0x80, -1.0, 1.0)
     e = (c >> 3) & 0xF
     m = (c & 0x7).astype(np.float64)
     mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2((e - 7).astype(np.float64)))
     mag = np.where((e == 15) & ((c & 0x7) == 7), np.nan, mag)
     return sign * mag
+
+
+_E4M3_TABLE = _e4m3_values()
 
 
 FP8_BLOCK = 128  # [Params] reading: one scale per 128 x 128 block
@@ -79,8 +88,13 @@ def dequant_fp8_blocks(codes, scales, block: int = FP8_BLOCK) -> np.ndarray:
     """
     q = e4m3_to_f64(codes)
     sc = np.asarray(scales, dtype=np.float64)
+    R, C = q.shape[-2], q.shape[-1]
+    if R % block == 0 and C % block == 0:  # each block times its scale, by broadcasting
+        lead = q.shape[:-2]
+        qb = q.reshape(*lead, R // block, block, C // block, block)
+        return (qb * sc[..., :, None, :, None]).reshape(q.shape)
     full = np.repeat(np.repeat(sc, block, axis=-2), block, axis=-1)
-    return q * full[..., :q.shape[-2], :q.shape[-1]]
+    return q * full[..., :R, :C]
 
 
 def sigmoid(z) -> np.ndarray:

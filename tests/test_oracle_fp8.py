@@ -66,12 +66,13 @@ def _small_bank(seed=0, G=2, R=256, C=384):
     rng = np.random.default_rng(seed)
     q = rng.integers(0, 256, size=(G, R, C), dtype=np.uint8)
     q[(q & 0x7F) == 0x7F] = 0x3C  # no NaN codes
-    s = rng.uniform(0.5, 2.0, size=(G, R // 128, C // 128))
+    s = rng.uniform(0.5, 2.0, size=(G, -(-R // 128), -(-C // 128)))
     return q, s
 
 
-def test_dequant_blocks_brute_force():
-    q, s = _small_bank()
+@pytest.mark.parametrize("R,C", [(256, 384), (200, 136)], ids=["whole_blocks", "ragged_blocks"])
+def test_dequant_blocks_brute_force(R, C):
+    q, s = _small_bank(R=R, C=C)
     np.testing.assert_array_equal(oracle.dequant_fp8_blocks(q, s), _brute_dequant(q, s))
 
 
