@@ -1004,7 +1004,22 @@ int32_t moe_layer_forward_host(const moe_config* cfg, int64_t T, const void* x_h
     hp->next ^= 1;
   }
   void* xd = at<void>(workspace, L.x_stage + b * round256(bytes));
+  // y_host pinned and mapped into this device's address space: the layer's
+  // last kernel writes y there itself (over the host link), so no staging
+  // copy delays the next call's forward on `stream`
   void* yd = at<void>(workspace, L.y_stage);
+  bool y_direct = false;
+  static const int direct_ok = env_int("FGS_Y_DIRECT", 1);  // 0: always stage and copy
+  if (direct_ok) {
+    cudaPointerAttributes pa;
+    if (cudaPointerGetAttributes(&pa, y_host) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
+        pa.devicePointer && aligned16(pa.devicePointer) && pa.device == dev) {
+      yd = pa.devicePointer;
+      y_direct = true;
+    } else {
+      cudaGetLastError();  // an unregistered pointer leaves an error to clear
+    }
+  }
   // the buffer is free once the forward that last read it has finished
   if (hp->used[b]) MOE_CUDA(cudaStreamWaitEvent(cs, hp->read[b], 0));
   MOE_CUDA(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, cs));
@@ -1016,7 +1031,7 @@ int32_t moe_layer_forward_host(const moe_config* cfg, int64_t T, const void* x_h
   if (st != MOE_OK) return st;
   MOE_CUDA(cudaEventRecord(hp->read[b], s));
   hp->used[b] = true;
-  MOE_CUDA(cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s));
+  if (!y_direct) MOE_CUDA(cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s));
   return MOE_OK;
 }
 

@@ -333,7 +333,12 @@ int32_t moe_layer_forward(const moe_config* cfg, int64_t T, const void* x, const
  * the copy for one call overlaps the forward of the call before it.  That
  * copy therefore does not wait for work enqueued earlier on `stream`: x_host
  * must hold its values when the call is made (host writes, or device work
- * already synchronised). */
+ * already synchronised).  When y_host is pinned host memory mapped into the
+ * current device's address space (cudaHostAlloc / cudaHostRegister on a
+ * unified-addressing system) and 16-byte aligned, the layer's last kernel
+ * writes y straight into it over the host link instead of staging y in the
+ * workspace and copying it, so no copy stands between this call's forward and
+ * the next one on `stream`; y_host is valid at the same point either way. */
 int32_t moe_layer_forward_host(const moe_config* cfg, int64_t T, const void* x_host,
                                const float* W_r, const float* bias, const void* W_gate_up,
                                const void* W_down, const void* Ws_gate_up, const void* Ws_down,

@@ -115,30 +115,37 @@ def test_layer_full_size_sampled(name):
         torch.cuda.empty_cache()
 
 
-def test_layer_forward_host_pipelined_calls():
+@pytest.mark.parametrize("y_pinned", [True, False], ids=["y_pinned", "y_pageable"])
+@pytest.mark.parametrize("shape", [SMALL[1], SMALL[2]], ids=lambda s: s.name)
+def test_layer_forward_host_pipelined_calls(shape, y_pinned):
     """Three host-buffer calls in a row on one workspace (their x copies go
     through alternating staging buffers, overlapping the previous forward)
-    each return what the device-buffer forward returns for the same x."""
+    each return what the device-buffer forward returns for the same x.  A
+    pinned y is written by the layer's last kernel directly (the combine for
+    the K2 form, the latent up-projection for K3); a pageable one is staged
+    and copied."""
     need_gpu()
     fgs = lib()
-    shape = SMALL[1]  # bf16, grouped routing, one shared expert
     g = synth.generate(shape, device="cuda")
     cfg = fgs.config(shape)
     T = shape.T
     ws, nws = workspace(cfg, T)
     xs = [synth.generate(shape, device="cuda", seed=s, weights=False)["x"] for s in (1, 2, 3)]
-    ys_host = [torch.empty((T, shape.d_model), dtype=xs[0].dtype).pin_memory() for _ in xs]
+    ys_host = [torch.full((T, shape.d_model), float("nan"), dtype=xs[0].dtype) for _ in xs]
+    if y_pinned:
+        ys_host = [y.pin_memory() for y in ys_host]
     xs_host = [x.cpu().pin_memory() for x in xs]
     for xh, yh in zip(xs_host, ys_host):  # enqueued back to back, no synchronisation
         fgs.moe_layer_forward_host(cfg, T, xh, g["W_r"], g["bias"], g["W_gate_up"], g["W_down"],
-                                   g.get("Ws_gate_up"), g.get("Ws_down"), None, None, yh, ws, nws)
+                                   g.get("Ws_gate_up"), g.get("Ws_down"), g.get("W_lat_down"),
+                                   g.get("W_lat_up"), yh, ws, nws)
     torch.cuda.synchronize()
     assert fgs.moe_get_device_status(ws) == 0
     for x, yh in zip(xs, ys_host):
         ws2, nws2 = workspace(cfg, T)
         y = torch.empty((T, shape.d_model), dtype=x.dtype, device="cuda")
         fgs.moe_layer_forward(cfg, T, x, g["W_r"], g["bias"], g["W_gate_up"], g["W_down"],
-                              g.get("Ws_gate_up"), g.get("Ws_down"), None, None, y, None, None,
-                              None, ws2, nws2)
+                              g.get("Ws_gate_up"), g.get("Ws_down"), g.get("W_lat_down"),
+                              g.get("W_lat_up"), y, None, None, None, ws2, nws2)
         torch.cuda.synchronize()
         assert torch.equal(yh, y.cpu())
