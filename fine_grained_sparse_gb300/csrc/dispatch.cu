@@ -189,6 +189,10 @@ __global__ void __launch_bounds__(256) gather_packed_kernel(
   const int lane = threadIdx.x & 31;
   const int64_t warp_global = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  // each token row is read K times: keep x in L2, and let the gathered copy
+  // (K times larger, read again only by the next GEMM) leave it first
+  const uint64_t keep = l2_policy_evict_last();
+  const uint64_t pass = l2_policy_evict_first();
   for (int64_t r = warp_global; r < rows; r += nwarps) {
     int lo = 0, hi = E;  // offsets[lo] <= r < offsets[hi]
     while (hi - lo > 1) {
@@ -204,11 +208,12 @@ __global__ void __launch_bounds__(256) gather_packed_kernel(
       uint4 t[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u)
-        if (v0 + 32 * u < vec_per_row) t[u] = __ldg(src + v0 + 32 * u);
+        if (v0 + 32 * u < vec_per_row) t[u] = ld_global_hint(src + v0 + 32 * u, keep);
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int v = v0 + 32 * u;
-        if (v < vec_per_row) Xp[((v >> 3) * plane_rows + R) * 8 + ((v & 7) ^ sw)] = t[u];
+        if (v < vec_per_row)
+          st_global_hint(Xp + ((v >> 3) * plane_rows + R) * 8 + ((v & 7) ^ sw), t[u], pass);
       }
     }
     if (lane == 0 && w_perm) w_perm[r] = topk_w ? __ldg(topk_w + j) : 1.0f;
