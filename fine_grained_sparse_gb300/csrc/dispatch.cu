@@ -30,6 +30,21 @@ namespace fgs {
 
 namespace {
 
+// 16-byte global load / store with an L2 eviction-priority hint.
+__device__ __forceinline__ uint4 ld_global_hint(const uint4* p, uint64_t policy) {
+  uint4 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(policy));
+  return v;
+}
+__device__ __forceinline__ void st_global_hint(uint4* p, uint4 v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w), "l"(policy)
+               : "memory");
+}
+
+
 constexpr int kChunkThreads = 256;
 constexpr int kScatterWarps = 8;       // chunks per CTA of the scatter
 
