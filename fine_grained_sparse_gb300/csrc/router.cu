@@ -426,17 +426,30 @@ __global__ void __launch_bounds__(256) router_logits_kernel(
   const int lane = threadIdx.x % 32;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
   if (t >= T) return;
+  // z = the parts summed in order 0, 1, ..., parts - 1 for every expert;
+  // the loads of four parts of all the lane's experts are in flight at once
+  // (small batches split the GEMM's K into dozens of parts)
   float z[PM];
+  const float* pz = logits + t * E + lane;
 #pragma unroll
-  for (int j = 0; j < PM; ++j) {
-    const int e = lane + 32 * j;
-    float v = 0.0f;
-    if (e < E) {
-      v = __ldg(logits + t * E + e);
-      for (int q = 1; q < parts; ++q) v += __ldg(logits + q * part_stride + t * E + e);
-    }
-    z[j] = v;
+  for (int j = 0; j < PM; ++j) z[j] = lane + 32 * j < E ? __ldg(pz + 32 * j) : 0.0f;
+  int q = 1;
+  for (; q + 4 <= parts; q += 4) {
+    float b[4][PM];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < PM; ++j)
+        b[i][j] = lane + 32 * j < E ? __ldg(pz + (q + i) * part_stride + 32 * j) : 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < PM; ++j) z[j] += b[i][j];
   }
+  for (; q < parts; ++q)
+#pragma unroll
+    for (int j = 0; j < PM; ++j)
+      if (lane + 32 * j < E) z[j] += __ldg(pz + q * part_stride + 32 * j);
   select_token<PM>(z, lane, E, bias, K, G, Gk, scale, norm, topk_idx + t * K, topk_w + t * K);
 }
 
