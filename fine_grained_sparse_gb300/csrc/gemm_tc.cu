@@ -821,20 +821,35 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
 __global__ void __launch_bounds__(256) split_router_weight_kernel(const float* __restrict__ W,
                                                                   int E, int d,
                                                                   __nv_bfloat16* __restrict__ out) {
-  const int64_t n = static_cast<int64_t>(E) * d;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+  // eight consecutive weights per thread step (d % 8 == 0): two 16-byte
+  // loads, one 16-byte store into each of the three pieces
+  const int64_t n8 = static_cast<int64_t>(E) * d / 8;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t e = i / d, k = i - e * d;
-    const float w = __ldg(W + i);
-    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
-    const float r1 = w - __bfloat162float(hi);
-    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
-    const float r2 = r1 - __bfloat162float(mid);
-    const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
-    __nv_bfloat16* row = out + e * 3 * d;
-    row[k] = hi;
-    row[d + k] = mid;
-    row[2 * d + k] = lo;
+    const int64_t e = (8 * i) / d, k = 8 * i - e * d;
+    const float4 a = __ldg(reinterpret_cast<const float4*>(W) + 2 * i);
+    const float4 b = __ldg(reinterpret_cast<const float4*>(W) + 2 * i + 1);
+    const float w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t hi[4], mid[4], lo[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float h[2], m[2], l[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const float v = w[2 * j + q];
+        h[q] = __bfloat162float(__float2bfloat16_rn(v));
+        const float r1 = v - h[q];
+        m[q] = __bfloat162float(__float2bfloat16_rn(r1));
+        l[q] = r1 - m[q];
+      }
+      hi[j] = pack_bf16x2(h[0], h[1]);
+      mid[j] = pack_bf16x2(m[0], m[1]);
+      lo[j] = pack_bf16x2(l[0], l[1]);
+    }
+    __nv_bfloat16* row = out + e * 3 * d + k;
+    *reinterpret_cast<uint4*>(row) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(row + d) = make_uint4(mid[0], mid[1], mid[2], mid[3]);
+    *reinterpret_cast<uint4*>(row + 2 * d) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
   }
 }
 
@@ -1186,7 +1201,7 @@ cudaError_t launch_pack_weights_fp8(int kind, int64_t groups, int64_t rows, int6
 
 cudaError_t launch_split_router_weight(const float* W_r, int E, int d, __nv_bfloat16* W_split,
                                        cudaStream_t stream) {
-  const int64_t n = static_cast<int64_t>(E) * d;
+  const int64_t n = static_cast<int64_t>(E) * d / 8;
   int64_t blocks = (n + 255) / 256;
   if (blocks > 4096) blocks = 4096;
   note_launch();
