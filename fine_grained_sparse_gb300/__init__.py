@@ -233,7 +233,9 @@ def moe_layer_forward(cfg, T, x, W_r, bias, W_gate_up, W_down, Ws_gate_up, Ws_do
     if stage_events is not None:
         handles = []
         for e in stage_events:
-            if hasattr(e, "cuda_event"):
+            if e is None:  # this stage boundary is not recorded
+                handles.append(None)
+            elif hasattr(e, "cuda_event"):
                 if not e.cuda_event:  # torch creates its events lazily, on first record
                     import torch
                     e.record(torch.cuda.current_stream() if stream is None else stream)

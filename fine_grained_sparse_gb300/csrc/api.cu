@@ -24,6 +24,13 @@ namespace {
 std::atomic<uint64_t> g_launches{0};
 }  // namespace
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("FGS_PDL");  // tuning override: 0 = plain launches
+    return !(v && *v == '0');
+  }();
+  return on;
+}
 }  // namespace fgs
 
 namespace {

@@ -158,6 +158,20 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// Programmatic dependent launch.  pdl_release lets the next kernel of the
+// stream (launched with programmatic stream serialization) start launching
+// once every CTA of this grid has released or exited; the persistent GEMM
+// releases when its work is done, before its teardown (released at the
+// start, waiting CTAs of the next kernel sat beside the running ones and
+// cost time), the other kernels release by exiting.  pdl_wait blocks until
+// the previous kernel of the stream has completed and its writes are
+// visible; every kernel calls it before its first global memory access.
+// Both are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_release() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Orders this thread's earlier generic-proxy writes to shared memory before
 // later async-proxy reads of it (the tensor cores reading an operand).
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -51,6 +51,7 @@ constexpr int kScatterWarps = 8;       // chunks per CTA of the scatter
 __global__ void __launch_bounds__(kChunkThreads) chunk_count_kernel(
     const int32_t* __restrict__ idx, int64_t n, int chunk, int E, int32_t* __restrict__ ccount,
     int* status) {
+  pdl_wait();
   extern __shared__ int hist[];
   for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
@@ -76,6 +77,7 @@ __global__ void __launch_bounds__(1024) chunk_scan_kernel(int32_t* __restrict__ 
                                                           int nchunks, int E,
                                                           int32_t* __restrict__ counts,
                                                           int32_t* __restrict__ offsets) {
+  pdl_wait();
   __shared__ int scan[1024];
   const int e = threadIdx.x;
   int total = 0;
@@ -110,6 +112,7 @@ __global__ void __launch_bounds__(32 * kScatterWarps) chunk_scatter_kernel(
     const int32_t* __restrict__ idx, int64_t n, int chunk, int E,
     const int32_t* __restrict__ ccount, const int32_t* __restrict__ offsets, int nchunks,
     int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+  pdl_wait();
   extern __shared__ int cnt_all[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int c = blockIdx.x * kScatterWarps + warp;
@@ -144,6 +147,7 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __rest
                                                            RowTile* __restrict__ tiles,
                                                            int* __restrict__ ntiles,
                                                            int32_t* __restrict__ poffsets) {
+  pdl_wait();
   __shared__ int scan[1024];
   __shared__ int pscan[1024];
   const int e = threadIdx.x;
@@ -200,6 +204,7 @@ __global__ void __launch_bounds__(256) gather_packed_kernel(
     const int32_t* __restrict__ offsets, const int32_t* __restrict__ poffsets, int E,
     const float* __restrict__ topk_w, uint4* __restrict__ Xp, int64_t plane_rows,
     float* __restrict__ w_perm) {
+  pdl_wait();
   const int rows = offsets[E];
   const int lane = threadIdx.x & 31;
   const int64_t warp_global = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -243,6 +248,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x
                                                      const float* __restrict__ topk_w,
                                                      uint4* __restrict__ Xp,
                                                      float* __restrict__ w_perm) {
+  pdl_wait();
   const int rows = offsets[E];
   const int lane = threadIdx.x & 31;
   const int64_t warp_global = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -303,6 +309,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const void* __restrict__ Y
                                                       int D, const void* __restrict__ adds,
                                                       int n_add, int64_t add_stride_rows,
                                                       void* __restrict__ y) {
+  pdl_wait();
   using V = Vec8<BF16>;
   const int64_t t = blockIdx.x;
   const int nvec = D / 8;
@@ -351,30 +358,26 @@ cudaError_t launch_permute(const int32_t* topk_idx, int64_t T, int K, int E, int
   const int chunk = permute_chunk(n);
   const int64_t nchunks = permute_chunks(n);
   if (nchunks < 1) return cudaSuccess;
-  note_launch();
-  chunk_count_kernel<<<static_cast<unsigned>(nchunks), kChunkThreads, sizeof(int) * E, stream>>>(
-      topk_idx, n, chunk, E, ccount, status);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_pdl(chunk_count_kernel, dim3(static_cast<unsigned>(nchunks)),
+                               dim3(kChunkThreads), sizeof(int) * E, stream, topk_idx, n, chunk, E,
+                               ccount, status);
   if (err != cudaSuccess) return err;
-  note_launch();
-  chunk_scan_kernel<<<1, 1024, 0, stream>>>(ccount, static_cast<int>(nchunks), E, counts,
-                                            offsets);
-  err = cudaGetLastError();
+  err = launch_pdl(chunk_scan_kernel, dim3(1), dim3(1024), 0, stream, ccount,
+                   static_cast<int>(nchunks), E, counts, offsets);
   if (err != cudaSuccess) return err;
   const unsigned blocks = static_cast<unsigned>((nchunks + kScatterWarps - 1) / kScatterWarps);
-  note_launch();
-  chunk_scatter_kernel<<<blocks, 32 * kScatterWarps, sizeof(int) * E * kScatterWarps, stream>>>(
-      topk_idx, n, chunk, E, ccount, offsets, static_cast<int>(nchunks), perm, inv);
-  return cudaGetLastError();
+  return launch_pdl(chunk_scatter_kernel, dim3(blocks), dim3(32 * kScatterWarps),
+                    sizeof(int) * E * kScatterWarps, stream, topk_idx, n, chunk, E,
+                    static_cast<const int32_t*>(ccount), static_cast<const int32_t*>(offsets),
+                    static_cast<int>(nchunks), perm, inv);
 }
 
 int64_t max_tiles(int64_t rows, int E, int nt) { return rows / nt + E; }
 
 cudaError_t launch_build_tiles(const int32_t* offsets, int E, int nt, RowTile* tiles, int* ntiles,
                                int32_t* poffsets, cudaStream_t stream) {
-  note_launch();
-  build_tiles_kernel<<<1, 1024, 0, stream>>>(offsets, E, nt, tiles, ntiles, poffsets);
-  return cudaGetLastError();
+  return launch_pdl(build_tiles_kernel, dim3(1), dim3(1024), 0, stream, offsets, E, nt, tiles,
+                    ntiles, poffsets);
 }
 
 cudaError_t launch_gather_packed(const void* x, int K, int width, const int32_t* perm,
@@ -384,11 +387,9 @@ cudaError_t launch_gather_packed(const void* x, int K, int width, const int32_t*
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  note_launch();
-  gather_packed_kernel<<<sms * 8, 256, 0, stream>>>(
-      static_cast<const uint4*>(x), K, width / 8, perm, offsets, poffsets, E, topk_w,
-      static_cast<uint4*>(Xp), plane_rows, w_perm);
-  return cudaGetLastError();
+  return launch_pdl(gather_packed_kernel, dim3(sms * 8), dim3(256), 0, stream,
+                    static_cast<const uint4*>(x), K, width / 8, perm, offsets, poffsets, E, topk_w,
+                    static_cast<uint4*>(Xp), plane_rows, w_perm);
 }
 
 cudaError_t launch_gather(const void* x, int64_t T, int K, int width, int elem_bytes,
@@ -409,16 +410,11 @@ cudaError_t launch_combine(const void* Y, const int32_t* inv, const float* w, in
                            int D, const void* adds, int n_add, int64_t add_stride_rows, void* y,
                            bool bf16, cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
-  if (bf16) {
-    note_launch();
-    combine_kernel<true><<<static_cast<unsigned>(T), 128, 0, stream>>>(Y, inv, w, K, D, adds,
-                                                                       n_add, add_stride_rows, y);
-  } else {
-    note_launch();
-    combine_kernel<false><<<static_cast<unsigned>(T), 128, 0, stream>>>(Y, inv, w, K, D, adds,
-                                                                        n_add, add_stride_rows, y);
-  }
-  return cudaGetLastError();
+  if (bf16)
+    return launch_pdl(combine_kernel<true>, dim3(static_cast<unsigned>(T)), dim3(128), 0, stream,
+                      Y, inv, w, K, D, adds, n_add, add_stride_rows, y);
+  return launch_pdl(combine_kernel<false>, dim3(static_cast<unsigned>(T)), dim3(128), 0, stream, Y,
+                    inv, w, K, D, adds, n_add, add_stride_rows, y);
 }
 
 }  // namespace fgs

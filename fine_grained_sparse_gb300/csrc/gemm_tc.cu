@@ -409,6 +409,8 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
   if (kPair) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // the set-up above overlaps the previous kernel; global memory only after it
+  pdl_wait();
 
   const int units0 = segment_units(p, &p.seg[0]);
   const int units1 = p.nseg > 1 ? segment_units(p, &p.seg[1]) : 0;
@@ -807,6 +809,9 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
   }
 
   __syncthreads();
+  // this CTA's work is done: the next kernel of the stream may start
+  // launching (it still waits for this grid's completion before it reads)
+  pdl_release();
   // neither CTA of a pair leaves (or frees TMEM) while the other may still
   // reach its shared memory, barriers or accumulators
   if (kPair) cluster_sync_all();
@@ -821,6 +826,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
 __global__ void __launch_bounds__(256) split_router_weight_kernel(const float* __restrict__ W,
                                                                   int E, int d,
                                                                   __nv_bfloat16* __restrict__ out) {
+  pdl_wait();
   // eight consecutive weights per thread step (d % 8 == 0): two 16-byte
   // loads, one 16-byte store into each of the three pieces
   const int64_t n8 = static_cast<int64_t>(E) * d / 8;
@@ -1152,12 +1158,11 @@ cudaError_t launch_tc_gemm(const GemmParams& params, int num_sms, cudaStream_t s
     note_launch();
     return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<true, false>, p);
   }
-  note_launch();
   if (p.fp8)
-    tc_gemm_kernel<false, true><<<num_sms, kThreadsFp8, plan.smem_bytes, stream>>>(p);
-  else
-    tc_gemm_kernel<false, false><<<num_sms, kThreads, plan.smem_bytes, stream>>>(p);
-  return cudaGetLastError();
+    return launch_pdl(tc_gemm_kernel<false, true>, dim3(num_sms), dim3(kThreadsFp8),
+                      plan.smem_bytes, stream, p);
+  return launch_pdl(tc_gemm_kernel<false, false>, dim3(num_sms), dim3(kThreads), plan.smem_bytes,
+                    stream, p);
 }
 
 cudaError_t launch_pack_weights(int kind, int64_t groups, int64_t rows, int64_t cols,
@@ -1204,10 +1209,8 @@ cudaError_t launch_split_router_weight(const float* W_r, int E, int d, __nv_bflo
   const int64_t n = static_cast<int64_t>(E) * d / 8;
   int64_t blocks = (n + 255) / 256;
   if (blocks > 4096) blocks = 4096;
-  note_launch();
-  split_router_weight_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(W_r, E, d,
-                                                                                W_split);
-  return cudaGetLastError();
+  return launch_pdl(split_router_weight_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                    stream, W_r, E, d, W_split);
 }
 
 }  // namespace fgs

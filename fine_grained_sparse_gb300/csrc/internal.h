@@ -12,6 +12,27 @@ namespace fgs {
 // enqueued (read through moe_launch_count).
 void note_launch();
 
+// Launch a hot-path kernel with programmatic stream serialization (the
+// kernel calls pdl_release / pdl_wait, see common.cuh), so that it starts
+// while the previous kernel of the stream drains; FGS_PDL=0 launches plainly.
+bool pdl_enabled();
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  note_launch();
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
+
 
 // ----------------------------------------------------------------- router
 struct RouterArgs {

@@ -423,6 +423,7 @@ __global__ void __launch_bounds__(256) router_logits_kernel(
     const float* __restrict__ logits, int parts, int64_t part_stride,
     const float* __restrict__ bias, int T, int E, int K, int G, int Gk, float scale, int norm,
     int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+  pdl_wait();
   const int lane = threadIdx.x % 32;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
   if (t >= T) return;
@@ -478,11 +479,9 @@ template <int PM>
 cudaError_t launch_logits(const RouterArgs& a, cudaStream_t stream) {
   const int warps = 8;
   const unsigned blocks = static_cast<unsigned>((a.T + warps - 1) / warps);
-  note_launch();
-  router_logits_kernel<PM><<<blocks, warps * 32, 0, stream>>>(
-      a.logits, a.logit_parts, a.logit_part_stride, a.bias, static_cast<int>(a.T), a.E, a.K, a.G,
-      a.Gk, a.scale, a.norm, a.topk_idx, a.topk_w);
-  return cudaGetLastError();
+  return launch_pdl(router_logits_kernel<PM>, dim3(blocks), dim3(warps * 32), 0, stream, a.logits,
+                    a.logit_parts, a.logit_part_stride, a.bias, static_cast<int>(a.T), a.E, a.K,
+                    a.G, a.Gk, a.scale, a.norm, a.topk_idx, a.topk_w);
 }
 
 // G [T, E]: each token's selected weights at their experts, 0 elsewhere.

@@ -313,7 +313,10 @@ int32_t moe_linear(int64_t T, int32_t in_features, int32_t out_features, const v
  *   of the routing (NULL to skip).
  *   stage_events: NULL, or MOE_STAGE_COUNT + 1 cudaEvent_t handles recorded
  *   on `stream` before each stage and after the last (router, dispatch,
- *   expert gate/up, expert down, combine and projections). */
+ *   expert gate/up, expert down, combine and projections); a NULL entry is
+ *   not recorded.  A recorded event keeps the kernels on its two sides from
+ *   overlapping (the library launches successive kernels so that the next
+ *   one's set-up runs while the previous one drains). */
 #define MOE_STAGE_COUNT 5
 int32_t moe_layer_forward(const moe_config* cfg, int64_t T, const void* x, const float* W_r,
                           const float* bias, const void* W_gate_up, const void* W_down,
