@@ -109,3 +109,33 @@ def test_python_binding_raises(fgs):
     with pytest.raises(fgs.MoeError) as ei:
         fgs.moe_router(cfg, 16, None, None, None, None, None, stream=0)
     assert ei.value.status == 1
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({}, 0),
+    ({"d_ff": 2048 - 64}, 2),       # FP8 blocks: d_ff % 128
+    ({"d_ff_shared": 192}, 2),
+    ({"d_model": 7168 + 64}, 2),    # d_model % 128 fails the bf16 rule first, also FP8's
+    ({"d_latent": 3584}, 0),
+    ({"d_latent": 3584 - 64}, 2),
+    ({"dtype": 0}, 2),              # FP8 weights need bf16 activations
+])
+def test_validate_config_fp8_layout(fgs, kw, status):
+    cfg = _k2(fgs, weight_layout=fgs.MOE_WEIGHTS_PACKED_FP8, **kw)
+    assert fgs.moe_validate_config(cfg, 8192) == status
+
+
+def test_packed_fp8_bytes(fgs):
+    # codes, then one 16-byte record per (group, pair of 128-row tiles, 64-column k step)
+    assert fgs.moe_packed_fp8_bytes(384, 4096, 7168) == 384 * 4096 * 7168 + 384 * 16 * 112 * 16
+    assert fgs.moe_packed_fp8_bytes(2, 384, 256) == 2 * 384 * 256 + 2 * 2 * 4 * 16  # odd pair
+    for bad in [(0, 128, 128), (1, 192, 128), (1, 128, 192), (1, 64, 128)]:
+        assert fgs.moe_packed_fp8_bytes(*bad) == -1
+
+
+def test_pack_fp8_argument_errors(fgs):
+    lib = fgs.lib
+    assert lib.moe_pack_weights_fp8(5, 1, 128, 128, 0x1000, 0x1000, 0x100000, None) == 1  # kind
+    assert lib.moe_pack_weights_fp8(1, 1, 192, 128, 0x1000, 0x1000, 0x100000, None) == 2  # rows
+    assert lib.moe_pack_weights_fp8(1, 1, 128, 128, 0x1001, 0x1000, 0x100000, None) == 3  # align
+    assert lib.moe_pack_weights_fp8(1, 1, 128, 128, 0x1000, 0x1000, 0x1000, None) == 1  # overlap
