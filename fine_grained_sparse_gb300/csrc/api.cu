@@ -69,17 +69,26 @@ int env_int(const char* name, int fallback) {
   return (v && *v) ? atoi(v) : fallback;
 }
 
+int router_tile(int64_t T);
+
 // K parts of the router GEMM (a multiple of 3: the split weight's three
-// bf16 terms are separate parts): enough parts that small batches still
-// occupy the SMs.
-int router_ksplit(int64_t T, int d) {
+// bf16 terms are separate parts): the fewest parts that give the GEMM about
+// 2.4 waves of units on a 152-SM GB300 (a fixed count, so that a workspace
+// sized on one device fits the call on another), at most 48.  One wave or
+// less leaves SMs idle at the end; more parts cost partial-logit traffic.
+int router_ksplit(int64_t T, int d, int E) {
   static const int forced = env_int("FGS_ROUTER_KSPLIT", 0);  // tuning override
   const int kd = d / 64;
   if (forced >= 3 && forced % 3 == 0 && kd % (forced / 3) == 0) return forced;
-  int h = 1;
-  for (int c = 1; c <= 16 && static_cast<int64_t>(c) * T <= 2048; ++c)
-    if (kd % c == 0) h = c;
-  return 3 * h;
+  const int64_t nt = router_tile(T);
+  const int64_t per_part = ((T + nt - 1) / nt) * (((E + 127) / 128 + 1) / 2);
+  int best = 1;
+  for (int c = 1; c <= 16; ++c) {
+    if (kd % c) continue;
+    best = c;
+    if (per_part * 3 * c * 10 >= 24 * 152) break;
+  }
+  return 3 * best;
 }
 
 // Weight tiles per router GEMM unit: two (each token tile in shared memory
@@ -227,7 +236,7 @@ Layout layout(const moe_config* c, int64_t T) {
   L.w_perm = take(4 * TK);
   L.w_split = take(c->dtype == MOE_BF16 ? 3ull * c->E_routed * c->d_model * 2 : 0);
   L.logits = take(c->dtype == MOE_BF16 && c->d_model % 64 == 0
-                      ? 4ull * router_ksplit(T, c->d_model) * T * c->E_routed
+                      ? 4ull * router_ksplit(T, c->d_model, c->E_routed) * T * c->E_routed
                       : 0);
   // bf16: gathered rows and SwiGLU outputs in the packed activation layout
   // (64-column planes of 128-byte rows, experts 8-row aligned); fp32: plain
@@ -721,7 +730,7 @@ int32_t moe_router(const moe_config* cfg, int64_t T, const void* x, const float*
     g.rows = static_cast<int>(T);
     g.out_f32 = logits;
     g.out_ld = E;
-    g.ksplit = router_ksplit(T, d);
+    g.ksplit = router_ksplit(T, d, E);
     g.b_major = prefer_b_major(6ll * E * d, 2ll * T * d);
     g.out_split_stride = T * E;
     MOE_CUDA(launch_tc_gemm(p, num_sms(), s));
@@ -1053,7 +1062,7 @@ int32_t moe_router_noalloc(const moe_config* cfg, int64_t T, const void* x, cons
       !aligned16(topk_w))
     return fail(MOE_ERR_ALIGNMENT, "pointer not 16-byte aligned");
   const int d = cfg->d_model, E = cfg->E_routed;
-  const int ksplit = router_ksplit(T, d);
+  const int ksplit = router_ksplit(T, d, E);
   // scratch: status word | split router weight | partial logits
   const size_t split_off = kWsHeader;
   const size_t logits_off = split_off + round256(3ull * E * d * 2);
