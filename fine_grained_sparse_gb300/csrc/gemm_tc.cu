@@ -45,7 +45,10 @@
 //   warp 1 lane 0: MMA issuer; warp 2 lane 0: token producer;
 //   warps 3..10: epilogue, warp w reads lane quadrant w%4 of accumulator
 //   (w-3)/4, or of the single accumulator's column chunks (w-3)/4, 2 + ...
-//   (TMEM -> registers -> global stores).
+//   (TMEM -> registers -> global stores);
+//   FP8 weights only, warps 11..14: converters (FP8 stage -> bf16 stage).
+// A segment with implicit token tiles whose weights fit in L2 may instead
+// take its units token-tile-major (GemmSegment::b_major).
 // Every wait is bounded (%globaltimer); on expiry the CTA records
 // MOE_ERR_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
 #include <cudaTypedefs.h>
