@@ -176,3 +176,55 @@ def test_grouped_swiglu_packed_equals_natural(case):
     assert torch.equal(Y, Y2)
     if S:
         assert torch.equal(Ys, Ys2)
+
+
+@pytest.mark.parametrize("case", [(100, 256, 8, 2, 128, 1, 128, False),
+                                  (600, 384, 4, 2, 256, 1, 128, False),
+                                  (33, 512, 16, 4, 128, 2, 128, True)],
+                         ids=lambda c: "T%d_d%d_E%d_K%d_F%d_S%d" % c[:6])
+def test_grouped_swiglu_fp8(case):
+    """moe_grouped_swiglu with FP8 block-scaled banks: the routed rows of Y
+    carry their routing weight (applied in the FP8 down pass's epilogue)."""
+    need_gpu()
+    fgs = lib()
+    T, d, E, K, F, S, Fs, skew = case
+    shape = synth.custom(T=T, d_model=d, E_routed=E, K=K, E_shared=S, d_ff=F, d_ff_shared=Fs,
+                         weights="fp8")
+    g = synth.generate(shape, device="cuda", seed=T + E)
+    gen = torch.Generator().manual_seed(T + E)
+    wts = torch.ones(E)
+    if skew:
+        wts[:K] = 50.0
+    idx = torch.stack([torch.multinomial(wts, K, replacement=False, generator=gen)
+                       for _ in range(T)]).numpy()
+    topk_w = torch.rand((T, K), generator=gen) + 0.1
+    cfg = fgs.config(shape)
+    assert cfg.weight_layout == fgs.MOE_WEIGHTS_PACKED_FP8
+    gp = fgs.pack_layer_weights_fp8(g)
+    p = oracle.permute(idx, E)
+    ws, nws = workspace(cfg, T)
+    Y = torch.empty((T * K, d), dtype=torch.bfloat16, device="cuda")
+    Ys = torch.empty((S, T, d), dtype=torch.bfloat16, device="cuda") if S else None
+    fgs.moe_grouped_swiglu(
+        cfg, T, g["x"], torch.from_numpy(p["offsets"].astype(np.int32)).cuda(),
+        torch.from_numpy(p["perm"].astype(np.int32)).cuda(), topk_w.cuda(), gp["W_gate_up"],
+        gp["W_down"], g["x"] if S else None, gp.get("Ws_gate_up"), gp.get("Ws_down"), Y, Ys, ws,
+        nws)
+    assert fgs.moe_get_device_status(ws) == 0
+    x = np64(g["x"])
+    host = {k: v.cpu().numpy() for k, v in g.items() if k.endswith(("_q", "_s"))}
+    Yref = np.zeros((T * K, d))
+    for e in range(E):
+        slots = np.arange(p["offsets"][e], p["offsets"][e + 1])
+        if slots.size == 0:
+            continue
+        j = p["perm"][slots]
+        t, k = j // K, j % K
+        gu = oracle.dequant_fp8_blocks(host["W_gate_up_q"][e], host["W_gate_up_s"][e])
+        dn = oracle.dequant_fp8_blocks(host["W_down_q"][e], host["W_down_s"][e])
+        Yref[slots] = topk_w.numpy()[t, k][:, None] * oracle.swiglu_expert(x[t], gu[:F], gu[F:], dn)
+    assert rel_max_err(np64(Y), Yref) <= TOL_BF16
+    for s in range(S):
+        gu = oracle.dequant_fp8_blocks(host["Ws_gate_up_q"][s], host["Ws_gate_up_s"][s])
+        dn = oracle.dequant_fp8_blocks(host["Ws_down_q"][s], host["Ws_down_s"][s])
+        assert rel_max_err(np64(Ys[s]), oracle.swiglu_expert(x, gu[:Fs], gu[Fs:], dn)) <= TOL_BF16
