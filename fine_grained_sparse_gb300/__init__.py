@@ -27,7 +27,7 @@ __all__ = [
     "moe_router_noalloc", "moe_launch_count", "moe_dense_gates", "moe_update_bias",
     "MOE_WEIGHTS_NATURAL", "MOE_WEIGHTS_PACKED", "MOE_PACK_GATE_UP", "MOE_PACK_PLAIN",
     "MOE_WEIGHTS_PACKED_FP8", "moe_packed_fp8_bytes", "moe_pack_weights_fp8",
-    "pack_layer_weights_fp8",
+    "pack_layer_weights_fp8", "moe_selftest_bounded_wait",
 ]
 
 MOE_F32, MOE_BF16 = 0, 1
@@ -88,6 +88,7 @@ _SIGS = {
     "moe_linear": ([_I64, _I32, _I32, _P, _P, _P, _P, _P, _SZ, _P], _I32),
     "moe_pack_weights": ([_I32, _I64, _I64, _I64, _P, _P, _P], _I32),
     "moe_packed_fp8_bytes": ([_I64, _I64, _I64], _I64),
+    "moe_selftest_bounded_wait": ([_P, _P], _I32),
     "moe_pack_weights_fp8": ([_I32, _I64, _I64, _I64, _P, _P, _P, _P], _I32),
     "moe_router_noalloc": ([_CFG, _I64, _P, _P, _P, _P, _P, _P], _I32),
     "moe_layer_forward": ([_CFG, _I64] + [_P] * 14 + [_SZ, _P, _P], _I32),
@@ -265,6 +266,13 @@ def moe_layer_forward_host(cfg, T, x_host, W_r, bias, W_gate_up, W_down, Ws_gate
 def moe_pack_weights(kind, groups, rows, cols, src, dst, stream=None):
     _check(lib.moe_pack_weights(kind, groups, rows, cols, _ptr(src), _ptr(dst), _stream(stream)),
            "moe_pack_weights")
+
+
+def moe_selftest_bounded_wait(workspace, stream=None):
+    """Enqueue one bounded device wait that runs out (about 2 s); the
+    workspace status word then reads MOE_ERR_TIMEOUT."""
+    _check(lib.moe_selftest_bounded_wait(_ptr(workspace), _stream(stream)),
+           "moe_selftest_bounded_wait")
 
 
 def moe_packed_fp8_bytes(groups, rows, cols) -> int:

@@ -667,6 +667,39 @@ size_t moe_workspace_size(const moe_config* cfg, int64_t T) {
   return layout(cfg, T).total;
 }
 
+namespace fgs {
+namespace {
+
+// One thread waits, through the library's bounded mbarrier wait, on a
+// barrier that nothing arrives at: the wait gives up after its time limit,
+// records MOE_ERR_TIMEOUT in the status word and the kernel returns.
+__global__ void bounded_wait_probe_kernel(int* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const bool ok = mbar_wait_bounded(smem_u32(&bar), 0u, &abort_flag, status);
+    if (ok) record_status(status, MOE_ERR_INVALID_ARG);  // cannot happen: nothing arrives
+  }
+}
+
+}  // namespace
+}  // namespace fgs
+
+int32_t moe_selftest_bounded_wait(void* workspace, void* stream) {
+  if (!workspace) return fail(MOE_ERR_WORKSPACE, "workspace is null");
+  fgs::note_launch();
+  fgs::bounded_wait_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<int*>(workspace));
+  MOE_CUDA(cudaGetLastError());
+  return MOE_OK;
+}
+
 int32_t moe_get_device_status(void* workspace, void* stream) {
   if (!workspace) return fail(MOE_ERR_WORKSPACE, "workspace is null");
   cudaStream_t st = static_cast<cudaStream_t>(stream);

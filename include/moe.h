@@ -153,6 +153,16 @@ int64_t moe_packed_fp8_bytes(int64_t groups, int64_t rows, int64_t cols);
 int32_t moe_pack_weights_fp8(int32_t kind, int64_t groups, int64_t rows, int64_t cols,
                              const void* codes, const float* scales, void* dst, void* stream);
 
+/*
+ * Self-test of the library's failure detection, with no counterpart on the
+ * pages: every device wait of the library is a bounded mbarrier wait that
+ * gives up after 2 s of %globaltimer, records MOE_ERR_TIMEOUT in the
+ * workspace status word and lets its kernel return.  This enqueues one
+ * such wait on a barrier that nothing arrives at (about 2 s on `stream`);
+ * moe_get_device_status(workspace) then reads MOE_ERR_TIMEOUT, and the
+ * context stays usable.  Returns MOE_ERR_WORKSPACE for a null workspace. */
+int32_t moe_selftest_bounded_wait(void* workspace, void* stream);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 int32_t moe_version(void);
 
