@@ -20,9 +20,14 @@
 //                       in the chunk plus its rank among the lanes of the
 //                       same expert (match_any) -> perm / inv
 //   build_tiles_kernel  row tiles for the grouped GEMMs (one CTA, E <= 1024)
-//   gather_kernel     Xp[r] = x[perm[r] / K], w_perm[r] = topk_w[perm[r]]
+//   gather_packed_kernel  Xp[r] = x[perm[r] / K] in the packed plane layout
+//                     the tensor cores read (x read with an L2 evict-last
+//                     hint, Xp written evict-first), w_perm[r] = topk_w[perm[r]]
+//   gather_kernel     the same in plain rows (fp32 layers)
 //   combine_kernel    y[t] = sum_k w[t, k] Y[inv[t K + k]] + dense addends, fp32
 //                     sums in that order (w = 1 when absent)
+// All are launched with programmatic stream serialization and wait for the
+// previous kernel (pdl_wait) before touching global memory.
 #include "common.cuh"
 #include "internal.h"
 
