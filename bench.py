@@ -51,6 +51,9 @@ WORKLOADS = {
                  "experts (intermediate 3072), top-16, 2 shared experts at 7168 (intermediate "
                  "3072), scale 2.827, bf16 experts, fp32 router",
 }
+WORKLOADS["tiny"] = ("Tiny MoE layer, all fp32: T=64 tokens, d_model=256, 16 routed + 1 shared "
+                     "SwiGLU expert (intermediate 64), top-4, n_group 1, scale 2.827 "
+                     "(launch-bound; reported for its time per step)")
 WORKLOADS["k2_router"] = ("K2 router alone: T=4096 tokens, x bf16 N(0,1), fp32 W_r [384 x 7168] "
                           "kaiming-uniform, bias U(-0.05,0.05), sigmoid + bias top-8 of 384, "
                           "n_group 1, weights renormalised x 2.827")
@@ -213,7 +216,7 @@ def per_step_work(shape, counts):
     F, S, Fs, L = shape.d_ff, shape.E_shared, shape.d_ff_shared, shape.d_latent
     de = L if L else d
     U = int((counts > 0).sum())
-    b16 = 2
+    b16 = 4 if getattr(shape, "dtype", "bf16") == "f32" else 2  # activations and bf16 weights
     # expert weight bytes per element: bf16, or an FP8 code plus its share of
     # the block's fp32 scale
     bw = 1 + 4 / (128 * 128) if getattr(shape, "weights", "bf16") == "fp8" else b16
@@ -501,16 +504,19 @@ def run_own(args):
     g = synth.generate(shape, device="cuda", seed=seed)
     if rank:  # replicas: every rank its own batch, same weights
         g["x"] = synth.activations(shape, "cuda", seed=replica_seed(seed, rank))
-    # bf16 banks packed, or FP8 banks (config(shape) picks MOE_WEIGHTS_PACKED_FP8)
-    cfg = fgs.config(shape) if is_fp8(shape) else fgs.config(shape,
-                                                             weight_layout=fgs.MOE_WEIGHTS_PACKED)
+    # bf16 banks packed, FP8 banks (config(shape) picks MOE_WEIGHTS_PACKED_FP8),
+    # fp32 layers in the natural layout (their experts run on CUDA cores)
+    fp32 = shape.dtype == "f32"
+    cfg = (fgs.config(shape) if (is_fp8(shape) or fp32) else
+           fgs.config(shape, weight_layout=fgs.MOE_WEIGHTS_PACKED))
     # one-time load step: weights rearranged into the order the tensor cores
     # stream (the natural copies stay for the CPU oracle leg)
-    gp = fgs.pack_layer_weights_fp8(g) if is_fp8(shape) else fgs.pack_layer_weights(g)
+    gp = (g if fp32 else fgs.pack_layer_weights_fp8(g) if is_fp8(shape) else
+          fgs.pack_layer_weights(g))
     torch.cuda.synchronize()
     nws = fgs.moe_workspace_size(cfg, T)
     ws = torch.zeros(nws, dtype=torch.uint8, device="cuda")
-    y = torch.empty((T, shape.d_model), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((T, shape.d_model), dtype=g["x"].dtype, device="cuda")
     idx = torch.empty((T, shape.K), dtype=torch.int32, device="cuda")
     counts = torch.empty(shape.E_routed, dtype=torch.int32, device="cuda")
     stream = torch.cuda.Stream()
@@ -540,20 +546,35 @@ def run_own(args):
     sampler = ClockSampler(device_id(torch, local)) if rank == 0 else None
     if sampler:
         sampler.start()
+    # a layer whose weights fit in L2 (the tiny configuration) gets an L2
+    # flush between steps, outside per-step intervals; the K2/K3 weights
+    # (tens of GB) stream from HBM whatever the order
+    small = fp32 or sum(t.numel() * t.element_size() for k, t in g.items() if k != "x") < (256 << 20)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if small else None
+    step_iv = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)] if small else None
     barrier(torch, world)
     torch.cuda.synchronize()
     t0 = time.time()
     launches0 = fgs.moe_launch_count()
     start.record(stream)
-    for i in range(args.steps):
-        step(gu_events[i])
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            if small:
+                flush.zero_()
+                step_iv[i][0].record(stream)
+            step(gu_events[i])
+            if small:
+                step_iv[i][1].record(stream)
     end.record(stream)
     launches = fgs.moe_launch_count() - launches0
     torch.cuda.synchronize()
     t1 = time.time()
     barrier(torch, world)
     clocks = sampler.stop(t0, t1) if sampler else None
-    ms_total = max_over_ranks(torch, start.elapsed_time(end), world, "cuda")
+    ms_local = (sum(a.elapsed_time(b) for a, b in step_iv) if small
+                else start.elapsed_time(end))
+    ms_total = max_over_ranks(torch, ms_local, world, "cuda")
     status = fgs.moe_get_device_status(ws, stream)
     if status:
         raise RuntimeError("device status after the timed steps: " + fgs.moe_status_string(status))
@@ -576,7 +597,10 @@ def run_own(args):
     gu_ms = gu_live_ms  # the gate/up launch inside the timed region
     achieved = work["gate_up_bytes"] / (gu_ms / 1e3) / 1e9
     traffic = profiled_traffic(args.config)
-    roofline = {"bound": "hbm", "kernel": "tc_gemm_kernel (expert gate/up + SwiGLU, routed + shared)",
+    kernel = ("simt_gemm_kernel (expert gate/up + SwiGLU on CUDA cores, fp32; launch-bound at "
+              "this size)" if fp32 else
+              "tc_gemm_kernel (expert gate/up + SwiGLU, routed + shared)")
+    roofline = {"bound": "hbm", "kernel": kernel,
                 "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
                 "peak_source": peaks["source"],
@@ -586,19 +610,24 @@ def run_own(args):
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if fp32 else "bf16",
         "data": ("synthetic (seeded; FP8 E4M3 expert weights, codes N(0,112^2) rounded by "
                  "torch's float8 cast, 128x128 block scales U(0.5,1.5)*0.02/112"
                  if is_fp8(shape) else
+                 "synthetic (seeded; fp32 expert weights N(0,0.02)" if fp32 else
                  "synthetic (seeded; bf16 expert weights N(0,0.02)")
                 + ", fp32 router weight kaiming-uniform, bias uniform; shapes of the pages' "
                   "K2/K3 layers)",
         "config": {"workload": WORKLOADS[args.config], "name": args.config, "tokens_per_step": T,
                    "weights": ("FP8 E4M3 + fp32 128x128 block scales, packed once before "
                                "timing (moe_pack_weights_fp8)" if is_fp8(shape) else
+                               "fp32, natural layout" if fp32 else
                                "bf16, packed once before timing (moe_pack_weights)"),
-                   "l2": "inputs larger than L2: the selected experts' weights (tens of GB) "
-                         "stream from HBM every step",
+                   "l2": ("inputs fit in L2: a 256 MB buffer is written between steps, outside "
+                          "the timed per-step intervals" if small else
+                          "inputs larger than L2: the selected experts' weights (tens of GB) "
+                          "stream from HBM every step"),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": roofline,
         "layer": {"hbm_frac": round(work["layer_bytes"] / (ms_step / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
@@ -618,7 +647,7 @@ def run_own(args):
 
     # end to end through the C ABI with host buffers (copies inside the region)
     x_host = g["x"].cpu().pin_memory()
-    y_host = torch.empty((T, shape.d_model), dtype=torch.bfloat16).pin_memory()
+    y_host = torch.empty((T, shape.d_model), dtype=g["x"].dtype).pin_memory()
 
     def step_host():
         fgs.moe_layer_forward_host(cfg, T, x_host, gp["W_r"], gp["bias"], gp["W_gate_up"],
@@ -637,7 +666,7 @@ def run_own(args):
     ee.record(stream)
     ee.synchronize()
     e_ms = max_over_ranks(torch, es.elapsed_time(ee), world, "cuda")
-    nbytes = T * shape.d_model * 2
+    nbytes = T * shape.d_model * g["x"].element_size()
     line["e2e"] = {"value": round(job_tokens_per_s(world, T, e_steps, e_ms), 1), "unit": UNIT,
                    "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes, "steps": e_steps,
                    "api": "moe_layer_forward_host (pinned host x and y)"}
