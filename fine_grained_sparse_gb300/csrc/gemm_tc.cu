@@ -270,7 +270,7 @@ __device__ __forceinline__ void store_rows8_chunk(const uint32_t (&v)[64], const
   }
 }
 
-// Wait on a barrier for a whole warp: lane 0 polls (bounded) and the verdict
+// Wait on a barrier for a whole warp: lane 0 polls (bounded) and the outcome
 // is broadcast, so the warp stays converged for the .sync.aligned tcgen05 ops.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           int* status) {
