@@ -184,3 +184,26 @@ def test_fp8_layout_rejects_unaligned_widths():
                          weights="fp8")
     cfg = fgs.config(shape)
     assert fgs.moe_validate_config(cfg, 8) == 2  # MOE_ERR_UNSUPPORTED_SHAPE
+
+
+def test_layer_fp8_host_buffers():
+    """moe_layer_forward_host with FP8 banks returns what the device-buffer
+    forward returns (pinned x and y; y written by the combine directly)."""
+    need_gpu()
+    fgs = lib()
+    shape = SMALL[0]
+    g = synth.generate(shape, device="cuda")
+    cfg = fgs.config(shape)
+    gp = fgs.pack_layer_weights_fp8(g)
+    T = shape.T
+    ws, nws = workspace(cfg, T)
+    x_host = g["x"].cpu().pin_memory()
+    y_host = torch.full((T, shape.d_model), float("nan"), dtype=torch.bfloat16).pin_memory()
+    fgs.moe_layer_forward_host(cfg, T, x_host, gp["W_r"], gp["bias"], gp["W_gate_up"],
+                               gp["W_down"], gp.get("Ws_gate_up"), gp.get("Ws_down"), None, None,
+                               y_host, ws, nws)
+    torch.cuda.synchronize()
+    assert fgs.moe_get_device_status(ws) == 0
+    y, idx, w, counts = _forward(shape, g)
+    torch.cuda.synchronize()
+    assert torch.equal(y_host, y.cpu())
