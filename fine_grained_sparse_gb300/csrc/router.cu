@@ -119,6 +119,50 @@ __device__ __forceinline__ void warp_best(float& bv, int& bi) {
   }
 }
 
+// A 64-bit key whose unsigned order is the selection order: the value's
+// bits mapped to an order-preserving unsigned integer (with -0 read as +0,
+// which compares equal to it), then the complement of the index, so that
+// equal values put the smaller index first.
+__device__ __forceinline__ uint64_t order_key(float v, int idx) {
+  uint32_t u = __float_as_uint(v);
+  if (u == 0x80000000u) u = 0u;
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(~idx);
+}
+
+__device__ __forceinline__ float key_value(uint64_t k) {
+  const uint32_t o = static_cast<uint32_t>(k >> 32);
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+
+__device__ __forceinline__ int key_index(uint64_t k) {
+  return static_cast<int>(~static_cast<uint32_t>(k));
+}
+
+// Bitonic sort of one key per lane into descending order across the warp
+// (lane 0 the largest), moving `z` with its key when kCarry.
+template <bool kCarry>
+__device__ __forceinline__ void warp_sort_desc(uint64_t& key, float& z, int lane) {
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const uint32_t ohi = __shfl_xor_sync(0xffffffffu, static_cast<uint32_t>(key >> 32), stride);
+      const uint32_t olo = __shfl_xor_sync(0xffffffffu, static_cast<uint32_t>(key), stride);
+      const float oz = kCarry ? __shfl_xor_sync(0xffffffffu, z, stride) : 0.0f;
+      const uint64_t other = (static_cast<uint64_t>(ohi) << 32) | olo;
+      // a descending block keeps the larger key in its lower lane
+      const bool desc = (lane & size) == 0;
+      const bool lower = (lane & stride) == 0;
+      const bool take = (lower == desc) ? other > key : other < key;
+      if (take) {
+        key = other;
+        if (kCarry) z = oz;
+      }
+    }
+  }
+}
+
 // Selection for one token by one warp.  Lane `lane` holds the logits of
 // experts e = lane + 32 j, j < PM.  Writes topk_idx[0..K) and topk_w[0..K).
 template <int PM>
@@ -126,7 +170,9 @@ __device__ __forceinline__ void select_token(const float (&z)[PM], int lane, int
                                              const float* __restrict__ bias, int K, int G,
                                              int Gk, float scale, int norm,
                                              int32_t* __restrict__ out_idx,
-                                             float* __restrict__ out_w) {
+                                             float* __restrict__ out_w,
+                                             uint64_t* cand_key = nullptr,
+                                             float* cand_z = nullptr) {
   const unsigned full = 0xffffffffu;
   float c[PM];
   unsigned exact = 0u;  // bit j: c[j] holds the exact value
@@ -243,7 +289,67 @@ __device__ __forceinline__ void select_token(const float (&z)[PM], int lane, int
       }
     }
   };
-  rounds();
+  // The same K (+1) winners in one pass when the warp has 32 words of
+  // shared scratch: the R-th best of the lanes' own bests is at or after
+  // the R-th best overall in the selection order, so the R best are among
+  // the experts at or before it; when those candidates fit in the 32 lanes,
+  // one sort across the warp orders them.  Otherwise the rounds run.
+  auto one_pass = [&]() -> bool {
+    const int R = K < E ? K + 1 : K;
+    if (cand_key == nullptr || R > 32) return false;
+    float lv = -CUDART_INF_F;
+    int li = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < PM; ++j) {
+      const int e = lane + 32 * j;
+      if (e < E && before(c[j], e, lv, li)) {
+        lv = c[j];
+        li = e;
+      }
+    }
+    uint64_t key = order_key(lv, li);
+    float unused = 0.0f;
+    warp_sort_desc<false>(key, unused, lane);
+    const uint64_t floor_key =
+        (static_cast<uint64_t>(__shfl_sync(full, static_cast<uint32_t>(key >> 32), R - 1)) << 32) |
+        __shfl_sync(full, static_cast<uint32_t>(key), R - 1);
+    unsigned mine = 0u;
+#pragma unroll
+    for (int j = 0; j < PM; ++j) {
+      const int e = lane + 32 * j;
+      if (e < E && order_key(c[j], e) >= floor_key) mine |= 1u << j;
+    }
+    const int n = __popc(mine);
+    int incl = n;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(full, incl, off);
+      if (lane >= off) incl += o;
+    }
+    const int total = __shfl_sync(full, incl, 31);
+    if (total > 32) return false;
+    int pos = incl - n;
+#pragma unroll
+    for (int j = 0; j < PM; ++j) {
+      if ((mine >> j) & 1u) {
+        cand_key[pos] = order_key(c[j], lane + 32 * j);
+        cand_z[pos] = z[j];
+        ++pos;
+      }
+    }
+    __syncwarp();
+    uint64_t ck = lane < total ? cand_key[lane] : 0ull;
+    float cz = lane < total ? cand_z[lane] : 0.0f;
+    __syncwarp();
+    warp_sort_desc<true>(ck, cz, lane);
+    if (lane < R) {
+      sel_idx = key_index(ck);
+      sel_v = key_value(ck);
+      sel_z = cz;
+    }
+    return true;
+  };
+  if (!one_pass()) rounds();
   // a near-tie among the K+1 best (order or boundary) -> exact values there
   const float next_v = __shfl_down_sync(full, sel_v, 1);
   const bool near = lane + 1 < (K < E ? K + 1 : K) && sel_v - next_v <= kMargin;
@@ -428,22 +534,25 @@ __global__ void __launch_bounds__(256) router_logits_kernel(
   const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
   if (t >= T) return;
   // z = the parts summed in order 0, 1, ..., parts - 1 for every expert;
-  // the loads of four parts of all the lane's experts are in flight at once
-  // (small batches split the GEMM's K into dozens of parts)
+  // the loads of a batch of parts of all the lane's experts are in flight
+  // at once (small batches split the GEMM's K into dozens of parts)
   float z[PM];
   const float* pz = logits + t * E + lane;
 #pragma unroll
   for (int j = 0; j < PM; ++j) z[j] = lane + 32 * j < E ? __ldg(pz + 32 * j) : 0.0f;
+  // (two parts at a time for the widest rows, whose registers would
+  // otherwise cap the kernel at one block per SM)
+  constexpr int kBatch = PM > 16 ? 2 : 4;
   int q = 1;
-  for (; q + 4 <= parts; q += 4) {
-    float b[4][PM];
+  for (; q + kBatch <= parts; q += kBatch) {
+    float b[kBatch][PM];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < kBatch; ++i)
 #pragma unroll
       for (int j = 0; j < PM; ++j)
         b[i][j] = lane + 32 * j < E ? __ldg(pz + (q + i) * part_stride + 32 * j) : 0.0f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < kBatch; ++i)
 #pragma unroll
       for (int j = 0; j < PM; ++j) z[j] += b[i][j];
   }
@@ -451,7 +560,11 @@ __global__ void __launch_bounds__(256) router_logits_kernel(
 #pragma unroll
     for (int j = 0; j < PM; ++j)
       if (lane + 32 * j < E) z[j] += __ldg(pz + q * part_stride + 32 * j);
-  select_token<PM>(z, lane, E, bias, K, G, Gk, scale, norm, topk_idx + t * K, topk_w + t * K);
+  __shared__ uint64_t cand_key[8][32];
+  __shared__ float cand_z[8][32];
+  const int w = threadIdx.x / 32;
+  select_token<PM>(z, lane, E, bias, K, G, Gk, scale, norm, topk_idx + t * K, topk_w + t * K,
+                   cand_key[w], cand_z[w]);
 }
 
 template <typename XT, int PM>
