@@ -567,6 +567,65 @@ __global__ void __launch_bounds__(256) router_logits_kernel(
                    cand_key[w], cand_z[w]);
 }
 
+// Small batches whose GEMM split K into many parts: one block per token,
+// so that the loads of all parts are in flight across eight warps instead of
+// queued behind one.  Warp w sums its contiguous share of the parts in
+// order, warp 0 adds the eight shares in warp order and selects.
+constexpr int kSplitWarps = 8;
+
+template <int PM>
+__global__ void __launch_bounds__(kSplitWarps * 32) router_logits_split_kernel(
+    const float* __restrict__ logits, int parts, int64_t part_stride,
+    const float* __restrict__ bias, int T, int E, int K, int G, int Gk, float scale, int norm,
+    int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+  pdl_wait();
+  __shared__ float share[kSplitWarps][32 * PM];
+  __shared__ uint64_t cand_key[32];
+  __shared__ float cand_z[32];
+  const int lane = threadIdx.x % 32;
+  const int w = threadIdx.x / 32;
+  const int64_t t = blockIdx.x;
+  const int per = (parts + kSplitWarps - 1) / kSplitWarps;
+  const int p0 = min(parts, w * per), p1 = min(parts, p0 + per);
+  const float* pz = logits + t * E + lane;
+  constexpr int kBatch = PM > 16 ? 2 : 4;
+  float acc[PM];
+  if (p0 < p1) {
+#pragma unroll
+    for (int j = 0; j < PM; ++j) acc[j] = lane + 32 * j < E ? __ldg(pz + p0 * part_stride + 32 * j) : 0.0f;
+    int q = p0 + 1;
+    for (; q + kBatch <= p1; q += kBatch) {
+      float b[kBatch][PM];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i)
+#pragma unroll
+        for (int j = 0; j < PM; ++j)
+          b[i][j] = lane + 32 * j < E ? __ldg(pz + (q + i) * part_stride + 32 * j) : 0.0f;
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i)
+#pragma unroll
+        for (int j = 0; j < PM; ++j) acc[j] += b[i][j];
+    }
+    for (; q < p1; ++q)
+#pragma unroll
+      for (int j = 0; j < PM; ++j)
+        if (lane + 32 * j < E) acc[j] += __ldg(pz + q * part_stride + 32 * j);
+#pragma unroll
+    for (int j = 0; j < PM; ++j) share[w][lane + 32 * j] = acc[j];
+  }
+  __syncthreads();
+  if (w != 0) return;
+  const int nw = (parts + per - 1) / per;  // warps that had parts
+  float z[PM];
+#pragma unroll
+  for (int j = 0; j < PM; ++j) z[j] = share[0][lane + 32 * j];
+  for (int v = 1; v < nw; ++v)
+#pragma unroll
+    for (int j = 0; j < PM; ++j) z[j] += share[v][lane + 32 * j];
+  select_token<PM>(z, lane, E, bias, K, G, Gk, scale, norm, topk_idx + t * K, topk_w + t * K,
+                   cand_key, cand_z);
+}
+
 template <typename XT, int PM>
 cudaError_t launch_fused(const RouterArgs& a, cudaStream_t stream) {
   const int CS = (a.E + kEC - 1) / kEC;
@@ -590,6 +649,13 @@ cudaError_t launch_fused(const RouterArgs& a, cudaStream_t stream) {
 
 template <int PM>
 cudaError_t launch_logits(const RouterArgs& a, cudaStream_t stream) {
+  // a token per block when the token-per-warp grid would leave most SMs
+  // idle while each warp walks many parts
+  if (a.logit_parts >= kSplitWarps && a.T <= 1024)
+    return launch_pdl(router_logits_split_kernel<PM>, dim3(static_cast<unsigned>(a.T)),
+                      dim3(kSplitWarps * 32), 0, stream, a.logits, a.logit_parts,
+                      a.logit_part_stride, a.bias, static_cast<int>(a.T), a.E, a.K, a.G, a.Gk,
+                      a.scale, a.norm, a.topk_idx, a.topk_w);
   const int warps = 8;
   const unsigned blocks = static_cast<unsigned>((a.T + warps - 1) / warps);
   return launch_pdl(router_logits_kernel<PM>, dim3(blocks), dim3(warps * 32), 0, stream, a.logits,
