@@ -524,8 +524,10 @@ __global__ void __launch_bounds__(kThreads) router_fused_kernel(
 
 // Logits given as `parts` partial arrays (a split reduction) are summed in
 // ascending part order, so the result does not depend on scheduling.
+constexpr int kSelWarps = 8;  // tokens (warps) per block of router_logits_kernel
+
 template <int PM>
-__global__ void __launch_bounds__(256) router_logits_kernel(
+__global__ void __launch_bounds__(kSelWarps * 32) router_logits_kernel(
     const float* __restrict__ logits, int parts, int64_t part_stride,
     const float* __restrict__ bias, int T, int E, int K, int G, int Gk, float scale, int norm,
     int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
@@ -560,8 +562,8 @@ __global__ void __launch_bounds__(256) router_logits_kernel(
 #pragma unroll
     for (int j = 0; j < PM; ++j)
       if (lane + 32 * j < E) z[j] += __ldg(pz + q * part_stride + 32 * j);
-  __shared__ uint64_t cand_key[8][32];
-  __shared__ float cand_z[8][32];
+  __shared__ uint64_t cand_key[kSelWarps][32];
+  __shared__ float cand_z[kSelWarps][32];
   const int w = threadIdx.x / 32;
   select_token<PM>(z, lane, E, bias, K, G, Gk, scale, norm, topk_idx + t * K, topk_w + t * K,
                    cand_key[w], cand_z[w]);
@@ -656,7 +658,7 @@ cudaError_t launch_logits(const RouterArgs& a, cudaStream_t stream) {
                       dim3(kSplitWarps * 32), 0, stream, a.logits, a.logit_parts,
                       a.logit_part_stride, a.bias, static_cast<int>(a.T), a.E, a.K, a.G, a.Gk,
                       a.scale, a.norm, a.topk_idx, a.topk_w);
-  const int warps = 8;
+  const int warps = kSelWarps;
   const unsigned blocks = static_cast<unsigned>((a.T + warps - 1) / warps);
   return launch_pdl(router_logits_kernel<PM>, dim3(blocks), dim3(warps * 32), 0, stream, a.logits,
                     a.logit_parts, a.logit_part_stride, a.bias, static_cast<int>(a.T), a.E, a.K,
