@@ -273,9 +273,14 @@ struct Vec8;
 
 template <>
 struct Vec8<true> {
-  static __device__ __forceinline__ void load(const void* p, int64_t i, float (&v)[8]) {
-    const uint4 u = __ldg(reinterpret_cast<const uint4*>(p) + i);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+  struct Raw {
+    uint4 u;
+  };
+  static __device__ __forceinline__ Raw load_raw(const void* p, int64_t i) {
+    return Raw{__ldg(reinterpret_cast<const uint4*>(p) + i)};
+  }
+  static __device__ __forceinline__ void unpack(const Raw& r, float (&v)[8]) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r.u);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const float2 f = __bfloat1622float2(h[q]);
@@ -294,11 +299,16 @@ struct Vec8<true> {
 
 template <>
 struct Vec8<false> {
-  static __device__ __forceinline__ void load(const void* p, int64_t i, float (&v)[8]) {
-    const float4 a = __ldg(reinterpret_cast<const float4*>(p) + 2 * i);
-    const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 2 * i + 1);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  struct Raw {
+    float4 a, b;
+  };
+  static __device__ __forceinline__ Raw load_raw(const void* p, int64_t i) {
+    return Raw{__ldg(reinterpret_cast<const float4*>(p) + 2 * i),
+               __ldg(reinterpret_cast<const float4*>(p) + 2 * i + 1)};
+  }
+  static __device__ __forceinline__ void unpack(const Raw& r, float (&v)[8]) {
+    v[0] = r.a.x; v[1] = r.a.y; v[2] = r.a.z; v[3] = r.a.w;
+    v[4] = r.b.x; v[5] = r.b.y; v[6] = r.b.z; v[7] = r.b.w;
   }
   static __device__ __forceinline__ void store(void* p, int64_t i, const float (&v)[8]) {
     reinterpret_cast<float4*>(p)[2 * i] = make_float4(v[0], v[1], v[2], v[3]);
@@ -306,7 +316,10 @@ struct Vec8<false> {
   }
 };
 
-// One CTA per token row; D must be a multiple of 8.
+// One CTA per token row, or per (row, slice of 128 vectors) for small
+// batches (gridDim.y slices); D must be a multiple of 8.  The rows of a
+// batch of eight k are loaded before any is added, so their loads are in
+// flight together; the sum still runs over k in order, then the addends.
 template <bool BF16>
 __global__ void __launch_bounds__(128) combine_kernel(const void* __restrict__ Y,
                                                       const int32_t* __restrict__ inv,
@@ -325,19 +338,39 @@ __global__ void __launch_bounds__(128) combine_kernel(const void* __restrict__ Y
     wts[threadIdx.x] = w ? __ldg(w + t * K + threadIdx.x) : 1.0f;
   }
   __syncthreads();
-  for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+  constexpr int kB = 8;
+  for (int v = blockIdx.y * blockDim.x + threadIdx.x; v < nvec; v += gridDim.y * blockDim.x) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     float tmp[8];
-    for (int k = 0; k < K; ++k) {
-      V::load(Y, static_cast<int64_t>(slots[k]) * nvec + v, tmp);
-      const float wk = wts[k];
+    for (int k0 = 0; k0 < K; k0 += kB) {
+      typename V::Raw raw[kB];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] = fmaf(wk, tmp[q], acc[q]);
+      for (int i = 0; i < kB; ++i)
+        if (k0 + i < K) raw[i] = V::load_raw(Y, static_cast<int64_t>(slots[k0 + i]) * nvec + v);
+#pragma unroll
+      for (int i = 0; i < kB; ++i) {
+        if (k0 + i < K) {
+          V::unpack(raw[i], tmp);
+          const float wk = wts[k0 + i];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] = fmaf(wk, tmp[q], acc[q]);
+        }
+      }
     }
-    for (int a = 0; a < n_add; ++a) {
-      V::load(adds, (a * add_stride_rows + t) * nvec + v, tmp);
+    constexpr int kA = 2;  // addends per batch (the shared experts: one or two)
+    for (int a0 = 0; a0 < n_add; a0 += kA) {
+      typename V::Raw raw[kA];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] += tmp[q];
+      for (int i = 0; i < kA; ++i)
+        if (a0 + i < n_add) raw[i] = V::load_raw(adds, ((a0 + i) * add_stride_rows + t) * nvec + v);
+#pragma unroll
+      for (int i = 0; i < kA; ++i) {
+        if (a0 + i < n_add) {
+          V::unpack(raw[i], tmp);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] += tmp[q];
+        }
+      }
     }
     V::store(y, t * nvec + v, acc);
   }
@@ -415,11 +448,14 @@ cudaError_t launch_combine(const void* Y, const int32_t* inv, const float* w, in
                            int D, const void* adds, int n_add, int64_t add_stride_rows, void* y,
                            bool bf16, cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
+  // small batches: several CTAs per row, one 8-element vector per thread
+  const unsigned slices = T < 1024 ? static_cast<unsigned>((D / 8 + 127) / 128) : 1u;
+  const dim3 grid(static_cast<unsigned>(T), slices);
   if (bf16)
-    return launch_pdl(combine_kernel<true>, dim3(static_cast<unsigned>(T)), dim3(128), 0, stream,
-                      Y, inv, w, K, D, adds, n_add, add_stride_rows, y);
-  return launch_pdl(combine_kernel<false>, dim3(static_cast<unsigned>(T)), dim3(128), 0, stream, Y,
-                    inv, w, K, D, adds, n_add, add_stride_rows, y);
+    return launch_pdl(combine_kernel<true>, grid, dim3(128), 0, stream, Y, inv, w, K, D, adds,
+                      n_add, add_stride_rows, y);
+  return launch_pdl(combine_kernel<false>, grid, dim3(128), 0, stream, Y, inv, w, K, D, adds,
+                    n_add, add_stride_rows, y);
 }
 
 }  // namespace fgs
