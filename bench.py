@@ -371,7 +371,9 @@ def run_router_only(args, fgs, torch, synth, shape, world, rank, local):
     g = synth.generate(shape, device="cuda", seed=seed)
     if rank:
         g["x"] = synth.activations(shape, "cuda", seed=replica_seed(seed, rank))
-    cfg = fgs.config(shape)
+    # the fp32 router weight split once into its three bf16 terms (a load step)
+    cfg = fgs.config(shape, router_weight=fgs.MOE_ROUTER_WEIGHT_SPLIT)
+    W_s = fgs.split_router_weight(cfg, g["W_r"])
     nws = fgs.moe_workspace_size(cfg, T)
     ws = torch.zeros(nws, dtype=torch.uint8, device="cuda")
     idx = torch.empty((T, K), dtype=torch.int32, device="cuda")
@@ -380,7 +382,7 @@ def run_router_only(args, fgs, torch, synth, shape, world, rank, local):
     stream = torch.cuda.Stream()
 
     def step():
-        fgs.moe_router(cfg, T, g["x"], g["W_r"], g["bias"], idx, w, ws, nws, stream=stream)
+        fgs.moe_router(cfg, T, g["x"], W_s, g["bias"], idx, w, ws, nws, stream=stream)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -427,10 +429,12 @@ def run_router_only(args, fgs, torch, synth, shape, world, rank, local):
         "config": {"workload": WORKLOADS[args.config], "name": args.config, "tokens_per_step": T,
                    "l2": "inputs (70 MB) fit in L2: a 256 MB buffer is written between steps, "
                          "outside the timed intervals",
+                   "router_weight": "fp32 W_r split once before timing into three bf16 terms "
+                                    "(moe_split_router_weight)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         # the dominant kernel is the split-bf16 logits GEMM; the interval is
-        # the whole moe_router call (weight split, GEMM, selection)
-        "roofline": {"bound": "tensor", "kernel": "moe_router (weight split + tensor-core logits "
+        # the whole moe_router call (logits GEMM and selection)
+        "roofline": {"bound": "tensor", "kernel": "moe_router (tensor-core logits "
                      "GEMM + selection)", "achieved": round(tflops, 2),
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": round(tflops / peaks["bf16_tflops"], 4), "traffic": None,
@@ -453,7 +457,7 @@ def run_router_only(args, fgs, torch, synth, shape, world, rank, local):
         es.record(stream)
         for _ in range(e_steps):
             xd.copy_(x_host, non_blocking=True)
-            fgs.moe_router(cfg, T, xd, g["W_r"], g["bias"], idx, w, ws, nws, stream=stream)
+            fgs.moe_router(cfg, T, xd, W_s, g["bias"], idx, w, ws, nws, stream=stream)
             idx_h.copy_(idx, non_blocking=True)
             w_h.copy_(w, non_blocking=True)
         ee.record(stream)
@@ -513,6 +517,12 @@ def run_own(args):
     # stream (the natural copies stay for the CPU oracle leg)
     gp = (g if fp32 else fgs.pack_layer_weights_fp8(g) if is_fp8(shape) else
           fgs.pack_layer_weights(g))
+    if not fp32:
+        # the fp32 router weight split once into its three bf16 terms (the
+        # form its tensor-core GEMM reads), also a load step
+        cfg.router_weight = fgs.MOE_ROUTER_WEIGHT_SPLIT
+        gp = dict(gp)
+        gp["W_r"] = fgs.split_router_weight(cfg, g["W_r"])
     torch.cuda.synchronize()
     nws = fgs.moe_workspace_size(cfg, T)
     ws = torch.zeros(nws, dtype=torch.uint8, device="cuda")
@@ -624,6 +634,9 @@ def run_own(args):
                                "timing (moe_pack_weights_fp8)" if is_fp8(shape) else
                                "fp32, natural layout" if fp32 else
                                "bf16, packed once before timing (moe_pack_weights)"),
+                   "router_weight": ("fp32, natural" if fp32 else
+                                     "fp32 W_r split once before timing into three bf16 terms "
+                                     "(moe_split_router_weight)"),
                    "l2": ("inputs fit in L2: a 256 MB buffer is written between steps, outside "
                           "the timed per-step intervals" if small else
                           "inputs larger than L2: the selected experts' weights (tens of GB) "

@@ -27,12 +27,15 @@ __all__ = [
     "moe_router_noalloc", "moe_launch_count", "moe_dense_gates", "moe_update_bias",
     "MOE_WEIGHTS_NATURAL", "MOE_WEIGHTS_PACKED", "MOE_PACK_GATE_UP", "MOE_PACK_PLAIN",
     "MOE_WEIGHTS_PACKED_FP8", "moe_packed_fp8_bytes", "moe_pack_weights_fp8",
-    "pack_layer_weights_fp8", "moe_selftest_bounded_wait",
+    "pack_layer_weights_fp8", "moe_selftest_bounded_wait", "MOE_ROUTER_WEIGHT_F32",
+    "MOE_ROUTER_WEIGHT_SPLIT", "moe_router_weight_split_bytes", "moe_split_router_weight",
+    "split_router_weight",
 ]
 
 MOE_F32, MOE_BF16 = 0, 1
 MOE_WEIGHTS_NATURAL, MOE_WEIGHTS_PACKED, MOE_WEIGHTS_PACKED_FP8 = 0, 1, 2
 MOE_PACK_GATE_UP, MOE_PACK_PLAIN = 0, 1
+MOE_ROUTER_WEIGHT_F32, MOE_ROUTER_WEIGHT_SPLIT = 0, 1
 MOE_STAGE_COUNT = 5
 STAGE_NAMES = ("router", "dispatch", "expert_gate_up", "expert_down", "combine")
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
@@ -53,7 +56,7 @@ class MoeConfig(ctypes.Structure):
         ("n_group", ctypes.c_int32), ("topk_group", ctypes.c_int32),
         ("routed_scaling_factor", ctypes.c_float), ("norm_topk_prob", ctypes.c_int32),
         ("d_latent", ctypes.c_int32), ("dtype", ctypes.c_int32),
-        ("weight_layout", ctypes.c_int32),
+        ("weight_layout", ctypes.c_int32), ("router_weight", ctypes.c_int32),
     ]
 
 
@@ -91,6 +94,8 @@ _SIGS = {
     "moe_selftest_bounded_wait": ([_P, _P], _I32),
     "moe_pack_weights_fp8": ([_I32, _I64, _I64, _I64, _P, _P, _P, _P], _I32),
     "moe_router_noalloc": ([_CFG, _I64, _P, _P, _P, _P, _P, _P], _I32),
+    "moe_router_weight_split_bytes": ([_CFG], _SZ),
+    "moe_split_router_weight": ([_CFG, _P, _P, _P], _I32),
     "moe_layer_forward": ([_CFG, _I64] + [_P] * 14 + [_SZ, _P, _P], _I32),
     "moe_layer_forward_host": ([_CFG, _I64] + [_P] * 11 + [_SZ, _P], _I32),
 }
@@ -126,7 +131,8 @@ def config(shape=None, **kw) -> MoeConfig:
     """MoeConfig from a ``synth.LayerShape``-like object and/or keywords."""
     vals = dict(d_model=0, d_ff=0, E_routed=0, E_shared=0, d_ff_shared=0, K=1, n_group=1,
                 topk_group=1, routed_scaling_factor=2.827, norm_topk_prob=1, d_latent=0,
-                dtype=MOE_BF16, weight_layout=MOE_WEIGHTS_NATURAL)
+                dtype=MOE_BF16, weight_layout=MOE_WEIGHTS_NATURAL,
+                router_weight=MOE_ROUTER_WEIGHT_F32)
     if shape is not None:
         for k in vals:
             if hasattr(shape, k):
@@ -266,6 +272,25 @@ def moe_layer_forward_host(cfg, T, x_host, W_r, bias, W_gate_up, W_down, Ws_gate
 def moe_pack_weights(kind, groups, rows, cols, src, dst, stream=None):
     _check(lib.moe_pack_weights(kind, groups, rows, cols, _ptr(src), _ptr(dst), _stream(stream)),
            "moe_pack_weights")
+
+
+def moe_router_weight_split_bytes(cfg) -> int:
+    return int(lib.moe_router_weight_split_bytes(ctypes.byref(cfg)))
+
+
+def moe_split_router_weight(cfg, W_r, W_split, stream=None):
+    _check(lib.moe_split_router_weight(ctypes.byref(cfg), _ptr(W_r), _ptr(W_split),
+                                       _stream(stream)), "moe_split_router_weight")
+
+
+def split_router_weight(cfg, W_r, stream=None):
+    """The MOE_ROUTER_WEIGHT_SPLIT form of an fp32 router weight on W_r's
+    device: a new bf16 [E, 3 d] tensor, for a config whose router_weight is
+    MOE_ROUTER_WEIGHT_SPLIT (a one-time load step)."""
+    import torch
+    out = torch.empty((cfg.E_routed, 3 * cfg.d_model), dtype=torch.bfloat16, device=W_r.device)
+    moe_split_router_weight(cfg, W_r, out, stream)
+    return out
 
 
 def moe_selftest_bounded_wait(workspace, stream=None):

@@ -167,6 +167,8 @@ int32_t check_router_cfg(const moe_config* c, int64_t T) {
     return fail(MOE_ERR_INVALID_ARG, "K > topk_group * E / n_group");
   if (!std::isfinite(c->routed_scaling_factor)) return fail(MOE_ERR_INVALID_ARG, "scale not finite");
   if (c->d_model < 32 || c->d_model % 32) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "d_model % 32 != 0");
+  if (c->router_weight != MOE_ROUTER_WEIGHT_F32 && c->router_weight != MOE_ROUTER_WEIGHT_SPLIT)
+    return fail(MOE_ERR_INVALID_ARG, "router_weight not a moe_router_weight_form");
   return MOE_OK;
 }
 
@@ -719,6 +721,10 @@ int32_t moe_router(const moe_config* cfg, int64_t T, const void* x, const float*
   if (!aligned16(x) || !aligned16(W_r) || !aligned16(bias) || !aligned16(topk_idx) ||
       !aligned16(topk_w) || (workspace && !aligned16(workspace)))
     return fail(MOE_ERR_ALIGNMENT, "pointer not 16-byte aligned");
+  const bool presplit = cfg->router_weight == MOE_ROUTER_WEIGHT_SPLIT;
+  if (presplit && !(workspace && cfg->dtype == MOE_BF16 && cfg->d_model % 64 == 0))
+    return fail(MOE_ERR_UNSUPPORTED_SHAPE,
+                "a split router weight needs bf16 x, d_model % 64 == 0 and a workspace");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   RouterArgs a;
   a.W_r = W_r;
@@ -738,10 +744,12 @@ int32_t moe_router(const moe_config* cfg, int64_t T, const void* x, const float*
     const Layout L = layout(cfg, T);
     if (ws_bytes < L.total) return fail(MOE_ERR_WORKSPACE, "workspace too small");
     // logits = x (W_hi + W_mid + W_lo)^T on the tensor cores
-    __nv_bfloat16* w_split = at<__nv_bfloat16>(workspace, L.w_split);
+    const void* w_split = presplit ? static_cast<const void*>(W_r)
+                                   : at<__nv_bfloat16>(workspace, L.w_split);
     float* logits = at<float>(workspace, L.logits);
     const int d = cfg->d_model, E = cfg->E_routed;
-    MOE_CUDA(launch_split_router_weight(W_r, E, d, w_split, s));
+    if (!presplit)
+      MOE_CUDA(launch_split_router_weight(W_r, E, d, at<__nv_bfloat16>(workspace, L.w_split), s));
     GemmParams p;
     memset(&p, 0, sizeof(p));
     p.mode = kModeStore;
@@ -1084,6 +1092,32 @@ int32_t moe_layer_forward_host(const moe_config* cfg, int64_t T, const void* x_h
   return MOE_OK;
 }
 
+size_t moe_router_weight_split_bytes(const moe_config* cfg) {
+  if (!cfg || cfg->E_routed < 1 || cfg->E_routed > 1024 || cfg->d_model < 64 ||
+      cfg->d_model % 64)
+    return 0;
+  return 6ull * cfg->E_routed * cfg->d_model;
+}
+
+int32_t moe_split_router_weight(const moe_config* cfg, const float* W_r, void* W_split,
+                                void* stream) {
+  if (!cfg) return fail(MOE_ERR_INVALID_ARG, "cfg is null");
+  if (cfg->E_routed < 1 || cfg->E_routed > 1024)
+    return fail(MOE_ERR_INVALID_ARG, "E_routed not in [1, 1024]");
+  if (cfg->d_model < 64 || cfg->d_model % 64)
+    return fail(MOE_ERR_UNSUPPORTED_SHAPE, "d_model % 64 != 0");
+  if (!W_r || !W_split) return fail(MOE_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(W_r) || !aligned16(W_split)) return fail(MOE_ERR_ALIGNMENT, "pointer not 16-byte aligned");
+  const uint8_t* a = reinterpret_cast<const uint8_t*>(W_r);
+  const uint8_t* b = static_cast<const uint8_t*>(W_split);
+  const size_t na = 4ull * cfg->E_routed * cfg->d_model, nb = 6ull * cfg->E_routed * cfg->d_model;
+  if (a < b + nb && b < a + na) return fail(MOE_ERR_INVALID_ARG, "W_r and W_split overlap");
+  MOE_CUDA(launch_split_router_weight(W_r, cfg->E_routed, cfg->d_model,
+                                      static_cast<__nv_bfloat16*>(W_split),
+                                      static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
 int32_t moe_router_noalloc(const moe_config* cfg, int64_t T, const void* x, const float* W_r,
                            const float* bias, int32_t* topk_idx, float* topk_w, void* stream) {
   int32_t st = check_router_cfg(cfg, T);
@@ -1110,12 +1144,14 @@ int32_t moe_router_noalloc(const moe_config* cfg, int64_t T, const void* x, cons
   if ((st = noalloc_scratch(&scratch)) != MOE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* status = at<int>(scratch, 0);
-  __nv_bfloat16* w_split = at<__nv_bfloat16>(scratch, split_off);
+  const bool presplit = cfg->router_weight == MOE_ROUTER_WEIGHT_SPLIT;
+  __nv_bfloat16* w_scratch = at<__nv_bfloat16>(scratch, split_off);
+  const void* w_split = presplit ? static_cast<const void*>(W_r) : w_scratch;
   float* logits = at<float>(scratch, logits_off);
   // the array keeps the previous call's contents: only the status word must
   // start at zero (the split weight and every partial logit are rewritten)
   MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int), s));
-  MOE_CUDA(launch_split_router_weight(W_r, E, d, w_split, s));
+  if (!presplit) MOE_CUDA(launch_split_router_weight(W_r, E, d, w_scratch, s));
   GemmParams p;
   memset(&p, 0, sizeof(p));
   p.mode = kModeStore;

@@ -76,7 +76,23 @@ typedef struct moe_config {
   int32_t dtype;        /* moe_dtype of activations, expert weights, outputs    */
   int32_t weight_layout;/* moe_weight_layout of the expert, shared-expert and
                            latent-projection weights                           */
+  int32_t router_weight;/* moe_router_weight_form of the W_r argument          */
 } moe_config;
+
+/* Forms of the router weight W_r passed to moe_router and the layer forwards.
+ *   MOE_ROUTER_WEIGHT_F32: fp32 [E, d_model], as the model stores gate.weight.
+ *   MOE_ROUTER_WEIGHT_SPLIT: the same weight as three bf16 terms, written
+ *     once by moe_split_router_weight() (a load step, like the packing of the
+ *     expert weights): bf16 [E, 3 d_model], row e = hi | mid | lo with
+ *     hi = bf16(W_r[e]), mid = bf16(W_r[e] - hi), lo = bf16(W_r[e] - hi - mid)
+ *     elementwise.  The tensor-core router GEMM reads it as it is instead of
+ *     splitting W_r on every call; the logits are bit-identical.  Needs bf16
+ *     x, d_model % 64 == 0 and a workspace (the CUDA-core path reads fp32);
+ *     the pointer is still passed as the W_r argument. */
+typedef enum moe_router_weight_form {
+  MOE_ROUTER_WEIGHT_F32 = 0,
+  MOE_ROUTER_WEIGHT_SPLIT = 1
+} moe_router_weight_form;
 
 /* Layouts of the weight matrices the expert GEMMs stream.
  *   MOE_WEIGHTS_NATURAL: bf16, row-major [G, O, K] as documented per argument.
@@ -196,6 +212,18 @@ size_t moe_workspace_size(const moe_config* cfg, int64_t T);
  * since the last read. */
 int32_t moe_get_device_status(void* workspace, void* stream);
 
+/* Bytes of the split router weight: 6 * E_routed * d_model; 0 for a NULL
+ * cfg or sizes moe_split_router_weight rejects. */
+size_t moe_router_weight_split_bytes(const moe_config* cfg);
+
+/*
+ * Write the MOE_ROUTER_WEIGHT_SPLIT form of an fp32 router weight (see
+ * moe_router_weight_form): W_r fp32 [E, d_model] in, W_split bf16
+ * [E, 3 d_model] out, both device buffers, 16-byte aligned, not overlapping.
+ * Needs 1 <= E_routed <= 1024 and d_model % 64 == 0.  Asynchronous on stream. */
+int32_t moe_split_router_weight(const moe_config* cfg, const float* W_r, void* W_split,
+                                void* stream);
+
 /*
  * Router, all four steps ("Kimi K2 · Router", "All 4 steps"; MoEGate):
  *   z = x W_r^T in fp32 (x upcast from cfg->dtype), s = sigmoid(z),
@@ -203,7 +231,8 @@ int32_t moe_get_device_status(void* workspace, void* stream);
  *   with the largest sum of their two best c, set c of every other expert to
  *   0.0), then the K largest c.
  *   x        [T, d_model]  cfg->dtype
- *   W_r      [E, d_model]  fp32 (gate.weight)
+ *   W_r      [E, d_model]  fp32 (gate.weight), or [E, 3 d_model] bf16 when
+ *                          cfg->router_weight is MOE_ROUTER_WEIGHT_SPLIT
  *   bias     [E]           fp32 (e_score_correction_bias)
  *   topk_idx [T, K] int32  out: selected experts, ordered by c descending,
  *                          equal c by smaller expert index first

@@ -139,3 +139,26 @@ def test_pack_fp8_argument_errors(fgs):
     assert lib.moe_pack_weights_fp8(1, 1, 192, 128, 0x1000, 0x1000, 0x100000, None) == 2  # rows
     assert lib.moe_pack_weights_fp8(1, 1, 128, 128, 0x1001, 0x1000, 0x100000, None) == 3  # align
     assert lib.moe_pack_weights_fp8(1, 1, 128, 128, 0x1000, 0x1000, 0x1000, None) == 1  # overlap
+
+
+def test_router_weight_split_form_argument_errors(fgs):
+    lib = fgs.lib
+    cfg = fgs.config(d_model=7168, E_routed=384, K=8)
+    assert fgs.moe_router_weight_split_bytes(cfg) == 6 * 384 * 7168
+    assert fgs.moe_router_weight_split_bytes(fgs.config(d_model=96, E_routed=16, K=4)) == 0
+    split = fgs.config(d_model=256, E_routed=16, K=4, router_weight=fgs.MOE_ROUTER_WEIGHT_SPLIT)
+    assert fgs.moe_validate_config(split, 64) == 0
+    assert fgs.moe_validate_config(fgs.config(d_model=256, E_routed=16, K=4, router_weight=2), 64) == 1
+    # moe_split_router_weight: shape, alignment and overlap checks
+    bad_d = fgs.config(d_model=96, E_routed=16, K=4)
+    assert lib.moe_split_router_weight(ctypes.byref(bad_d), 0x1000, 0x100000, None) == 2
+    assert lib.moe_split_router_weight(ctypes.byref(split), 0x1004, 0x100000, None) == 3
+    assert lib.moe_split_router_weight(ctypes.byref(split), 0x1000, 0x2000, None) == 1
+    assert lib.moe_split_router_weight(ctypes.byref(split), None, 0x100000, None) == 1
+    # the split form needs the tensor-core path: a workspace and bf16 x
+    assert lib.moe_router(ctypes.byref(split), 64, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000,
+                          None, 0, None) == 2
+    split_f32 = fgs.config(d_model=256, E_routed=16, K=4, dtype=fgs.MOE_F32,
+                           router_weight=fgs.MOE_ROUTER_WEIGHT_SPLIT)
+    assert lib.moe_router(ctypes.byref(split_f32), 64, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000,
+                          0x100000, 1 << 30, None) == 2

@@ -149,3 +149,27 @@ def test_layer_forward_host_pipelined_calls(shape, y_pinned):
                               g.get("W_lat_up"), y, None, None, None, ws2, nws2)
         torch.cuda.synchronize()
         assert torch.equal(yh, y.cpu())
+
+
+@pytest.mark.parametrize("shape", SMALL[1:3], ids=lambda s: s.name)
+def test_layer_with_presplit_router_weight(shape):
+    """The layer forward with the router weight split once
+    (MOE_ROUTER_WEIGHT_SPLIT) returns exactly what it returns with fp32 W_r."""
+    need_gpu()
+    fgs = lib()
+    g = synth.generate(shape, device="cuda")
+    y0, idx0, w0, c0 = _forward(shape, g)
+    cfg = fgs.config(shape, router_weight=fgs.MOE_ROUTER_WEIGHT_SPLIT)
+    g_s = dict(g)
+    g_s["W_r"] = fgs.split_router_weight(cfg, g["W_r"])
+    T = g["x"].shape[0]
+    ws, nws = workspace(cfg, T)
+    y = torch.empty_like(y0)
+    idx, w, counts = torch.empty_like(idx0), torch.empty_like(w0), torch.empty_like(c0)
+    fgs.moe_layer_forward(cfg, T, g_s["x"], g_s["W_r"], g_s["bias"], g_s["W_gate_up"],
+                          g_s["W_down"], g_s.get("Ws_gate_up"), g_s.get("Ws_down"),
+                          g_s.get("W_lat_down"), g_s.get("W_lat_up"), y, idx, w, counts, ws, nws)
+    torch.cuda.synchronize()
+    assert fgs.moe_get_device_status(ws) == 0
+    for a, b in ((y, y0), (idx, idx0), (w, w0), (counts, c0)):
+        assert torch.equal(a, b)

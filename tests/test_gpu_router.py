@@ -143,3 +143,33 @@ def test_bias_update_bit_exact(T, K, E):
     for _ in range(3):
         want = oracle.aux_free_bias_update(want, counts.numpy(), T, K, 1e-3)
     np.testing.assert_array_equal(b_dev.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("name,T", [("k2_router", 700), ("k3_latent", 300), ("k2_decode", None)])
+def test_presplit_router_weight_is_bit_identical(name, T):
+    """A router weight split once (MOE_ROUTER_WEIGHT_SPLIT) gives the same
+    indices and weights, bit for bit, as the fp32 weight split per call;
+    through moe_router, moe_router_noalloc and the layer forward."""
+    need_gpu()
+    fgs = lib()
+    shape = synth.shape(name)
+    T = T or shape.T
+    g = synth.generate(shape, device="cuda", T=T, weights=False)
+    cfg = fgs.config(shape, d_ff=0)
+    cfg_s = fgs.config(shape, d_ff=0, router_weight=fgs.MOE_ROUTER_WEIGHT_SPLIT)
+    W_s = fgs.split_router_weight(cfg_s, g["W_r"])
+    ws, nws = workspace(cfg, T)
+    outs = []
+    for c, W in ((cfg, g["W_r"]), (cfg_s, W_s)):
+        idx = torch.empty((T, c.K), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, c.K), dtype=torch.float32, device="cuda")
+        fgs.moe_router(c, T, g["x"], W, g["bias"], idx, w, ws, nws)
+        idx2, w2 = idx.clone(), w.clone()
+        if c.E_routed <= 384:  # the static scratch holds up to a 384-expert router
+            fgs.moe_router_noalloc(c, T, g["x"], W, g["bias"], idx2, w2)
+        torch.cuda.synchronize()
+        assert fgs.moe_get_device_status(ws) == 0
+        outs.append((idx.cpu(), w.cpu(), idx2.cpu(), w2.cpu()))
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a, b)
+    assert torch.equal(outs[0][0], outs[0][2]) and torch.equal(outs[0][1], outs[0][3])
