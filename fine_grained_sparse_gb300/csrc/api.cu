@@ -1130,9 +1130,11 @@ int32_t moe_router_noalloc(const moe_config* cfg, int64_t T, const void* x, cons
     return fail(MOE_ERR_ALIGNMENT, "pointer not 16-byte aligned");
   const int d = cfg->d_model, E = cfg->E_routed;
   const int ksplit = router_ksplit(T, d, E);
-  // scratch: status word | split router weight | partial logits
+  // scratch: status word | split router weight (unless the caller passes
+  // it) | partial logits
+  const bool presplit = cfg->router_weight == MOE_ROUTER_WEIGHT_SPLIT;
   const size_t split_off = kWsHeader;
-  const size_t logits_off = split_off + round256(3ull * E * d * 2);
+  const size_t logits_off = split_off + (presplit ? 0 : round256(3ull * E * d * 2));
   const size_t need = logits_off + round256(4ull * ksplit * T * E);
   if (need > kNoAllocScratchBytes) {
     snprintf(g_detail, sizeof(g_detail),
@@ -1144,7 +1146,6 @@ int32_t moe_router_noalloc(const moe_config* cfg, int64_t T, const void* x, cons
   if ((st = noalloc_scratch(&scratch)) != MOE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* status = at<int>(scratch, 0);
-  const bool presplit = cfg->router_weight == MOE_ROUTER_WEIGHT_SPLIT;
   __nv_bfloat16* w_scratch = at<__nv_bfloat16>(scratch, split_off);
   const void* w_split = presplit ? static_cast<const void*>(W_r) : w_scratch;
   float* logits = at<float>(scratch, logits_off);

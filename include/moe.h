@@ -400,7 +400,8 @@ int32_t moe_layer_forward_host(const moe_config* cfg, int64_t T, const void* x_h
  *   Arguments as moe_router.  cfg->dtype must be MOE_BF16 and d_model a
  *   multiple of 64 (MOE_ERR_UNSUPPORTED_SHAPE otherwise).
  *   Scratch needed: 256 + 6 E d + 4 T E P bytes (each term rounded up to
- *   256), P = 3 for T >= 2048 and up to 48 for small T; more than 64 MiB is
+ *   256; no 6 E d term when cfg->router_weight is MOE_ROUTER_WEIGHT_SPLIT),
+ *   P = 3 for T >= 2048 and up to 48 for small T; more than 64 MiB is
  *   rejected with MOE_ERR_WORKSPACE before anything is enqueued (the K2
  *   router fits up to T = 8192; the K3 router up to T = 2048).
  *   The first call on a device looks up the array's device address; make
