@@ -23,7 +23,8 @@ __all__ = [
     "config", "moe_version", "moe_status_string", "moe_validate_config", "moe_workspace_size",
     "moe_get_device_status", "moe_router", "moe_router_from_logits", "moe_permute",
     "moe_grouped_swiglu", "moe_combine", "moe_linear", "moe_layer_forward",
-    "moe_layer_forward_host", "moe_last_error_detail", "moe_pack_weights", "pack_layer_weights",
+    "moe_layer_forward_host", "moe_layer_forward_host_release", "moe_last_error_detail",
+    "moe_pack_weights", "pack_layer_weights",
     "moe_router_noalloc", "moe_launch_count", "moe_dense_gates", "moe_update_bias",
     "MOE_WEIGHTS_NATURAL", "MOE_WEIGHTS_PACKED", "MOE_PACK_GATE_UP", "MOE_PACK_PLAIN",
     "MOE_WEIGHTS_PACKED_FP8", "moe_packed_fp8_bytes", "moe_pack_weights_fp8",
@@ -87,7 +88,7 @@ _SIGS = {
     "moe_update_bias": ([_CFG, _I64, _P, _F, _P, _P], _I32),
     "moe_permute": ([_CFG, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P], _I32),
     "moe_grouped_swiglu": ([_CFG, _I64] + [_P] * 12 + [_SZ, _P], _I32),
-    "moe_combine": ([_CFG, _I64, _P, _P, _P, _P, _P], _I32),
+    "moe_combine": ([_CFG, _I64, _P, _P, _P, _P, _P, _P], _I32),
     "moe_linear": ([_I64, _I32, _I32, _P, _P, _P, _P, _P, _SZ, _P], _I32),
     "moe_pack_weights": ([_I32, _I64, _I64, _I64, _P, _P, _P], _I32),
     "moe_packed_fp8_bytes": ([_I64, _I64, _I64], _I64),
@@ -98,6 +99,7 @@ _SIGS = {
     "moe_split_router_weight": ([_CFG, _P, _P, _P], _I32),
     "moe_layer_forward": ([_CFG, _I64] + [_P] * 14 + [_SZ, _P, _P], _I32),
     "moe_layer_forward_host": ([_CFG, _I64] + [_P] * 11 + [_SZ, _P], _I32),
+    "moe_layer_forward_host_release": ([_P], _I32),
 }
 for _name, (_args, _res) in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -222,9 +224,11 @@ def moe_grouped_swiglu(cfg, T, x_e, offsets, perm, topk_w, W_gate_up, W_down, x_
            "moe_grouped_swiglu")
 
 
-def moe_combine(cfg, T, Y, inv, Y_shared, y, stream=None):
-    _check(lib.moe_combine(ctypes.byref(cfg), T, _ptr(Y), _ptr(inv), _ptr(Y_shared), _ptr(y),
-                           _stream(stream)), "moe_combine")
+def moe_combine(cfg, T, Y, inv, topk_w, Y_shared, y, stream=None):
+    """y = sum_k w_k Y[inv] + sum_s Y_shared; topk_w None means weight 1 (the
+    weights already in Y)."""
+    _check(lib.moe_combine(ctypes.byref(cfg), T, _ptr(Y), _ptr(inv), _ptr(topk_w), _ptr(Y_shared),
+                           _ptr(y), _stream(stream)), "moe_combine")
 
 
 def moe_linear(T, in_features, out_features, x, W, add, y, workspace, ws_bytes, stream=None):
@@ -267,6 +271,11 @@ def moe_layer_forward_host(cfg, T, x_host, W_r, bias, W_gate_up, W_down, Ws_gate
                                       _ptr(Ws_down), _ptr(W_lat_down), _ptr(W_lat_up),
                                       _ptr(y_host), _ptr(workspace), ws_bytes, _stream(stream)),
            "moe_layer_forward_host")
+
+
+def moe_layer_forward_host_release(workspace):
+    """Drop the library's per-workspace state of moe_layer_forward_host."""
+    _check(lib.moe_layer_forward_host_release(_ptr(workspace)), "moe_layer_forward_host_release")
 
 
 def moe_pack_weights(kind, groups, rows, cols, src, dst, stream=None):

@@ -616,23 +616,85 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 namespace {
 
 std::mutex g_noalloc_mutex;
-void* g_noalloc_ptr[64] = {nullptr};
+// Per device: the context the address was looked up in, and the address.
+struct NoAllocSlot {
+  unsigned long long ctx_id = 0;
+  void* ptr = nullptr;
+};
+NoAllocSlot g_noalloc_slot[64];
 
-// Device address of g_noalloc_scratch for the current device, looked up once
-// per device.  In host code the array's name is only a stand-in for the
-// device object, so kernels must be given this address instead.
+// Identity of the calling thread's current CUDA context (0 when there is
+// none yet, or when the driver entry points are unavailable).  A context
+// that is torn down (cudaDeviceReset) and created again gets a new id.
+unsigned long long current_context_id() {
+  typedef CUresult (*GetCurrent)(CUcontext*);
+  typedef CUresult (*GetId)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* a = nullptr;
+    void* b = nullptr;
+    cudaDriverEntryPointQueryResult qa, qb;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) ==
+            cudaSuccess &&
+        qa == cudaDriverEntryPointSuccess &&
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) ==
+            cudaSuccess &&
+        qb == cudaDriverEntryPointSuccess) {
+      get_current = reinterpret_cast<GetCurrent>(a);
+      get_id = reinterpret_cast<GetId>(b);
+    }
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of g_noalloc_scratch in the current device's context.  In
+// host code the array's name is only a stand-in for the device object, so
+// kernels must be given this address instead.  It is looked up once per
+// device and context: again after the context was torn down and created
+// anew, and on every call when the context cannot be identified.
 int32_t noalloc_scratch(void** out) {
   int dev = 0;
   MOE_CUDA(cudaGetDevice(&dev));
   if (dev < 0 || dev >= 64) return fail(MOE_ERR_CUDA, "device ordinal beyond 63");
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (!g_noalloc_ptr[dev]) {
+  NoAllocSlot& slot = g_noalloc_slot[dev];
+  unsigned long long id = current_context_id();
+  if (id == 0 || id != slot.ctx_id || !slot.ptr) {
     void* p = nullptr;
     MOE_CUDA(cudaGetSymbolAddress(&p, g_noalloc_scratch));
-    g_noalloc_ptr[dev] = p;
+    if (id == 0) id = current_context_id();  // the lookup made the context current
+    slot.ctx_id = id;
+    slot.ptr = p;
   }
-  *out = g_noalloc_ptr[dev];
+  *out = slot.ptr;
   return MOE_OK;
+}
+
+// Scratch bytes moe_router_noalloc needs with P K parts: the status word,
+// the split router weight (unless the caller passes it) and P partial
+// logit arrays.
+size_t noalloc_need(int64_t T, int d, int E, bool presplit, int parts) {
+  return kWsHeader + (presplit ? 0 : round256(3ull * E * d * 2)) +
+         round256(4ull * parts * T * E);
+}
+
+// K parts of the allocation-free router GEMM: moe_router's own count when
+// that fits the static scratch, else the largest smaller count (a multiple
+// of 3 whose third divides d / 64) that fits; 0 when none does.
+int noalloc_ksplit(int64_t T, int d, int E, bool presplit) {
+  const int p0 = router_ksplit(T, d, E);
+  const int kd = d / 64;
+  for (int c = p0 / 3; c >= 1; --c) {
+    if (kd % c) continue;
+    if (noalloc_need(T, d, E, presplit, 3 * c) <= kNoAllocScratchBytes) return 3 * c;
+  }
+  return 0;
 }
 
 }  // namespace
@@ -878,17 +940,18 @@ int32_t moe_grouped_swiglu(const moe_config* cfg, int64_t T, const void* x_e,
 }
 
 int32_t moe_combine(const moe_config* cfg, int64_t T, const void* Y, const int32_t* inv,
-                    const void* Y_shared, void* y, void* stream) {
+                    const float* topk_w, const void* Y_shared, void* y, void* stream) {
   int32_t st = check_layer_cfg(cfg, T);
   if (st != MOE_OK) return st;
   if (!Y || !inv || !y) return fail(MOE_ERR_INVALID_ARG, "null pointer");
   if (Y_shared && cfg->d_latent) return fail(MOE_ERR_INVALID_ARG, "Y_shared with d_latent");
-  if (!aligned16(Y) || !aligned16(inv) || !aligned16(y) || (Y_shared && !aligned16(Y_shared)))
+  if (!aligned16(Y) || !aligned16(inv) || !aligned16(y) || (Y_shared && !aligned16(Y_shared)) ||
+      (topk_w && !aligned16(topk_w)))
     return fail(MOE_ERR_ALIGNMENT, "pointer not 16-byte aligned");
   const int D = d_expert(cfg);
   if (D % 8) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "width % 8 != 0");
-  MOE_CUDA(launch_combine(Y, inv, nullptr, T, cfg->K, D, Y_shared, Y_shared ? cfg->E_shared : 0, T, y,
-                          cfg->dtype == MOE_BF16, static_cast<cudaStream_t>(stream)));
+  MOE_CUDA(launch_combine(Y, inv, topk_w, T, cfg->K, D, Y_shared, Y_shared ? cfg->E_shared : 0, T,
+                          y, cfg->dtype == MOE_BF16, static_cast<cudaStream_t>(stream)));
   return MOE_OK;
 }
 
@@ -1092,6 +1155,26 @@ int32_t moe_layer_forward_host(const moe_config* cfg, int64_t T, const void* x_h
   return MOE_OK;
 }
 
+int32_t moe_layer_forward_host_release(void* workspace) {
+  if (!workspace) return fail(MOE_ERR_INVALID_ARG, "workspace is null");
+  std::lock_guard<std::mutex> lock(g_pipe_mutex);
+  auto it = g_pipes.find(workspace);
+  if (it == g_pipes.end()) return MOE_OK;
+  // an event whose recorded work is still pending is released once that
+  // work completes; waits already enqueued on it are unaffected
+  cudaError_t first = cudaSuccess;
+  for (int i = 0; i < 2; ++i) {
+    for (cudaEvent_t e : {it->second.copied[i], it->second.read[i]}) {
+      if (!e) continue;
+      const cudaError_t r = cudaEventDestroy(e);
+      if (first == cudaSuccess) first = r;
+    }
+  }
+  g_pipes.erase(it);
+  if (first != cudaSuccess) return cuda_fail(first, "cudaEventDestroy");
+  return MOE_OK;
+}
+
 size_t moe_router_weight_split_bytes(const moe_config* cfg) {
   if (!cfg || cfg->E_routed < 1 || cfg->E_routed > 1024 || cfg->d_model < 64 ||
       cfg->d_model % 64)
@@ -1129,19 +1212,18 @@ int32_t moe_router_noalloc(const moe_config* cfg, int64_t T, const void* x, cons
       !aligned16(topk_w))
     return fail(MOE_ERR_ALIGNMENT, "pointer not 16-byte aligned");
   const int d = cfg->d_model, E = cfg->E_routed;
-  const int ksplit = router_ksplit(T, d, E);
   // scratch: status word | split router weight (unless the caller passes
   // it) | partial logits
   const bool presplit = cfg->router_weight == MOE_ROUTER_WEIGHT_SPLIT;
-  const size_t split_off = kWsHeader;
-  const size_t logits_off = split_off + (presplit ? 0 : round256(3ull * E * d * 2));
-  const size_t need = logits_off + round256(4ull * ksplit * T * E);
-  if (need > kNoAllocScratchBytes) {
+  const int ksplit = noalloc_ksplit(T, d, E, presplit);
+  if (ksplit == 0) {
     snprintf(g_detail, sizeof(g_detail),
              "moe_router_noalloc needs %zu bytes of scratch; its static scratch holds %zu",
-             need, kNoAllocScratchBytes);
+             noalloc_need(T, d, E, presplit, 3), kNoAllocScratchBytes);
     return MOE_ERR_WORKSPACE;
   }
+  const size_t split_off = kWsHeader;
+  const size_t logits_off = split_off + (presplit ? 0 : round256(3ull * E * d * 2));
   void* scratch = nullptr;
   if ((st = noalloc_scratch(&scratch)) != MOE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

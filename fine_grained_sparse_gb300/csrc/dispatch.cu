@@ -25,7 +25,9 @@
 //                     hint, Xp written evict-first), w_perm[r] = topk_w[perm[r]]
 //   gather_kernel     the same in plain rows (fp32 layers)
 //   combine_kernel    y[t] = sum_k w[t, k] Y[inv[t K + k]] + dense addends, fp32
-//                     sums in that order (w = 1 when absent)
+//                     sums in that order (w = 1 when absent); a slot outside
+//                     [0, T K) (inv = -1: a pair the permute rejected) adds
+//                     nothing
 // All are launched with programmatic stream serialization and wait for the
 // previous kernel (pdl_wait) before touching global memory.
 #include "common.cuh"
@@ -142,6 +144,8 @@ __global__ void __launch_bounds__(32 * kScatterWarps) chunk_scatter_kernel(
       perm[slot] = static_cast<int32_t>(j);
       inv[j] = slot;
       if ((mask & lt_mask) == 0) cnt[e] = base + __popc(mask);  // the group's first lane
+    } else if (j < n) {
+      inv[j] = -1;  // a pair whose expert index was rejected holds no slot
     }
     __syncwarp();
   }
@@ -334,8 +338,13 @@ __global__ void __launch_bounds__(128) combine_kernel(const void* __restrict__ Y
   __shared__ int slots[64];
   __shared__ float wts[64];
   if (threadIdx.x < K) {
-    slots[threadIdx.x] = __ldg(inv + t * K + threadIdx.x);
-    wts[threadIdx.x] = w ? __ldg(w + t * K + threadIdx.x) : 1.0f;
+    // a slot outside the T K rows of Y (a rejected pair) is read as row 0
+    // with weight 0, so that every load stays inside Y
+    const int64_t rows = static_cast<int64_t>(gridDim.x) * K;
+    const int sl = __ldg(inv + t * K + threadIdx.x);
+    const bool in = sl >= 0 && sl < rows;
+    slots[threadIdx.x] = in ? sl : 0;
+    wts[threadIdx.x] = !in ? 0.0f : w ? __ldg(w + t * K + threadIdx.x) : 1.0f;
   }
   __syncthreads();
   constexpr int kB = 8;

@@ -289,7 +289,7 @@ int32_t moe_update_bias(const moe_config* cfg, int64_t T, const int32_t* counts,
  *   perm     [T*K]  int32  out: perm[offsets[e] + r] = j of the r-th pair of e
  *   inv      [T*K]  int32  out: inv[j] = the slot of pair j
  * An index outside [0, E) records MOE_ERR_DEVICE_INDEX in the workspace
- * status and its pair is left out of counts, perm and inv. */
+ * status; its pair is left out of counts and perm, and its inv entry is -1. */
 int32_t moe_permute(const moe_config* cfg, int64_t T, const int32_t* topk_idx,
                     int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
                     void* workspace, size_t ws_bytes, void* stream);
@@ -319,15 +319,22 @@ int32_t moe_grouped_swiglu(const moe_config* cfg, int64_t T, const void* x_e,
                            void* workspace, size_t ws_bytes, void* stream);
 
 /*
- * Weighted combine ("Kimi K2 MoE", section 3: shared_expert(x) + routed):
- *   y[t] = sum_{k=0..K-1} Y[inv[t*K + k]] + sum_s Y_shared[s, t]
- * summed in fp32 in that fixed order.  The gate weights are already in Y
- * when moe_grouped_swiglu was given topk_w.
- *   Y        [T*K, D], inv [T*K], Y_shared [S, T, D] or NULL, y [T, D] out;
- *   D = d_e.  For the K3 form (d_latent != 0) Y_shared must be NULL: the
- *   routed sum is in latent space. */
+ * Weighted combine ("Kimi K2 MoE", section 3: shared_expert(x) + routed;
+ * the routed part is the gate-weighted sum of the selected experts):
+ *   y[t] = sum_{k=0..K-1} w[t, k] Y[inv[t*K + k]] + sum_s Y_shared[s, t]
+ * summed in fp32 in that fixed order, w[t, k] = topk_w[t*K + k], or 1 when
+ * topk_w is NULL (the weights are already in Y: moe_grouped_swiglu was
+ * given topk_w).  Passing topk_w here and NULL to moe_grouped_swiglu is
+ * what moe_layer_forward does: the weight is applied in fp32 after Y was
+ * rounded to cfg->dtype, instead of before.
+ *   Y        [T*K, D], inv [T*K], topk_w [T, K] fp32 or NULL,
+ *   Y_shared [S, T, D] or NULL, y [T, D] out; D = d_e.  For the K3 form
+ *   (d_latent != 0) Y_shared must be NULL: the routed sum is in latent space.
+ * An inv entry outside [0, T*K) -- moe_permute writes -1 for a pair whose
+ * expert index it rejected, and reports MOE_ERR_DEVICE_INDEX itself --
+ * adds nothing to y[t]; no read leaves Y. */
 int32_t moe_combine(const moe_config* cfg, int64_t T, const void* Y, const int32_t* inv,
-                    const void* Y_shared, void* y, void* stream);
+                    const float* topk_w, const void* Y_shared, void* y, void* stream);
 
 /*
  * Plain projection y = x W^T (+ add) for the K3 latent maps ("Kimi K3's
@@ -388,28 +395,49 @@ int32_t moe_layer_forward_host(const moe_config* cfg, int64_t T, const void* x_h
                                void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Release the library's per-workspace state of moe_layer_forward_host: the
+ * four CUDA events that order its staging copies, kept from the first
+ * host-buffer call on `workspace` until this call (the paper has no
+ * counterpart; it bounds what a caller that cycles through workspaces
+ * holds).  Work already enqueued is not waited for.  A later host-buffer
+ * call on the same workspace starts afresh; it must not be enqueued before
+ * the earlier calls on that workspace have completed (their staging buffers
+ * are no longer tracked).  A workspace without such state is accepted.
+ * MOE_ERR_INVALID_ARG for a NULL workspace. */
+int32_t moe_layer_forward_host_release(void* workspace);
+
+/*
  * moe_router without a caller-provided workspace.  This entry point has no
  * counterpart on the pages: it exists for callers that cannot allocate
  * device memory when they route tokens -- for example code running inside
  * an allocator-free runtime or a plugin interface that hands over only its
- * input and output buffers.  It computes exactly what moe_router computes
- * with a workspace and bf16 x (the split-bf16 tensor-core router), taking
- * its scratch (the three-way split of W_r and the partial logits) from a
- * static device array of 64 MiB that every GPU loading this library holds
- * until the process exits; it calls no allocating routine.
+ * input and output buffers.  It computes what moe_router computes with a
+ * workspace and bf16 x (the split-bf16 tensor-core router), taking its
+ * scratch (the three-way split of W_r and the partial logits) from a static
+ * device array of 64 MiB that every GPU loading this library holds until
+ * the process exits; it calls no allocating routine.
  *   Arguments as moe_router.  cfg->dtype must be MOE_BF16 and d_model a
  *   multiple of 64 (MOE_ERR_UNSUPPORTED_SHAPE otherwise).
- *   Scratch needed: 256 + 6 E d + 4 T E P bytes (each term rounded up to
- *   256; no 6 E d term when cfg->router_weight is MOE_ROUTER_WEIGHT_SPLIT),
- *   P = 3 for T >= 2048 and up to 48 for small T; more than 64 MiB is
- *   rejected with MOE_ERR_WORKSPACE before anything is enqueued (the K2
- *   router fits up to T = 8192; the K3 router up to T = 2048).
- *   The first call on a device looks up the array's device address; make
- *   that first call before any stream capture.  All calls on a device share
- *   the array, which keeps the previous call's contents: calls whose work
- *   overlaps on the GPU (other streams, other threads) race and must be
- *   serialised by the caller.  A bounded device wait that expires leaves the
- *   outputs incomplete and is not reported by this entry point. */
+ *   Scratch for P K parts: 256 + S + 4 T E P bytes (each term rounded up
+ *   to 256), S = 6 E d, or 0 when cfg->router_weight is
+ *   MOE_ROUTER_WEIGHT_SPLIT.  P is moe_router's own count of K parts when
+ *   that fits the array; otherwise the largest smaller count that fits (a
+ *   multiple of 3 whose third divides d_model / 64), and the logits are then
+ *   summed in a different grouping than moe_router's: they may differ from
+ *   it in the last bit, and so may a selection whose deciding margin is of
+ *   that size.  The call is rejected with MOE_ERR_WORKSPACE, before anything
+ *   is enqueued, only when even P = 3 does not fit: 256 + S + 12 T E > 64 MiB,
+ *   which holds for every T above a bound (K2 router, E = 384, d = 7168:
+ *   T > 10979, or T > 14563 with the split weight; K3, E = 896: T > 2657, or
+ *   T > 6241 with the split weight).
+ *   The call looks up the array's device address in the current context
+ *   the first time it runs in that context (again after the context was
+ *   destroyed and created anew); make that first call before any stream
+ *   capture.  All calls on a device share the array, which keeps the
+ *   previous call's contents: calls whose work overlaps on the GPU (other
+ *   streams, other threads) race and must be serialised by the caller.  A
+ *   bounded device wait that expires leaves the outputs incomplete and is
+ *   not reported by this entry point. */
 int32_t moe_router_noalloc(const moe_config* cfg, int64_t T, const void* x, const float* W_r,
                            const float* bias, int32_t* topk_idx, float* topk_w, void* stream);
 

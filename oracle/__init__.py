@@ -32,6 +32,7 @@ from .moe_oracle import (  # noqa: F401
     dense_gates,
     aux_free_bias_update,
     permute,
+    combine,
     swiglu_expert,
     moe_layer,
     moe_layer_tokens,

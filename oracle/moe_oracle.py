@@ -313,6 +313,28 @@ def permute(idx, E: int) -> Dict[str, np.ndarray]:
     return {"counts": counts, "offsets": offsets, "perm": perm, "inv": inv}
 
 
+def combine(Y, inv, w, Y_shared=None) -> np.ndarray:
+    """y[t] = sum_k w[t, k] Y[inv[t K + k]] + sum_s Y_shared[s, t], in fp64.
+
+    [K2MoE] section 3: the routed output is the gate-weighted sum of the
+    selected experts' outputs, and the layer adds the shared expert's output
+    (shared(x) + routed).  Y holds one expert output per slot (the dispatch
+    order of ``permute``), inv maps pair t K + k to its slot, w [T, K] are the
+    gate weights (ones when the rows of Y already carry them).
+    """
+    Y = np.asarray(Y, dtype=np.float64)
+    inv = np.asarray(inv, dtype=np.int64)
+    w = np.asarray(w, dtype=np.float64)
+    T, K = w.shape
+    y = np.zeros((T, Y.shape[1]))
+    for t in range(T):
+        for k in range(K):
+            y[t] += w[t, k] * Y[inv[t * K + k]]
+    if Y_shared is not None:
+        y = y + np.asarray(Y_shared, dtype=np.float64).sum(axis=0)
+    return y
+
+
 # --------------------------------------------------------------------------
 # experts and the layer
 # --------------------------------------------------------------------------

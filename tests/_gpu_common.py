@@ -70,3 +70,25 @@ def by_expert(idx, w=None):
     if w is None:
         return sidx
     return sidx, np.take_along_axis(np.asarray(w), order, axis=1)
+
+
+def rows_covering_experts(idx, E, K, largest=None, step=128):
+    """Token rows that reach the row tiles of the expert GEMMs at full size:
+    for each expert that received pairs (or only the ``largest`` ones by
+    pair count), the tokens in its first and last slot and in every
+    ``step``-th slot between them, so that each of its row tiles (at most 256
+    rows) and its ragged tail are compared.  Slots follow the dispatch order
+    (the oracle's permute of the device's expert indices, which the permute
+    tests pin bit for bit)."""
+    import oracle
+    p = oracle.permute(np.asarray(idx), E)
+    live = [e for e in range(E) if p["counts"][e] > 0]
+    if largest is not None:
+        live = sorted(live, key=lambda e: -int(p["counts"][e]))[:largest]
+    rows = set()
+    for e in live:
+        m = int(p["counts"][e])
+        o = int(p["offsets"][e])
+        for r in sorted(set(list(range(0, m, step)) + [m - 1])):
+            rows.add(int(p["perm"][o + r]) // K)
+    return np.array(sorted(rows), dtype=np.int64)

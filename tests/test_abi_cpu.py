@@ -162,3 +162,45 @@ def test_router_weight_split_form_argument_errors(fgs):
                            router_weight=fgs.MOE_ROUTER_WEIGHT_SPLIT)
     assert lib.moe_router(ctypes.byref(split_f32), 64, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000,
                           0x100000, 1 << 30, None) == 2
+
+
+def test_combine_argument_errors(fgs):
+    lib = fgs.lib
+    cfg = _k2(fgs)
+    # Y, inv, topk_w, Y_shared, y: null Y, then a misaligned topk_w
+    assert lib.moe_combine(ctypes.byref(cfg), 16, None, 0x1000, None, None, 0x1000, None) == 1
+    assert lib.moe_combine(ctypes.byref(cfg), 16, 0x1000, 0x1000, 0x1004, None, 0x1000, None) == 3
+    # Y_shared with the latent form
+    k3 = _k2(fgs, d_latent=3584, n_group=1, topk_group=1)
+    assert lib.moe_combine(ctypes.byref(k3), 16, 0x1000, 0x1000, None, 0x2000, 0x3000, None) == 1
+
+
+def test_host_pipeline_release_without_state(fgs):
+    lib = fgs.lib
+    assert lib.moe_layer_forward_host_release(None) == 1
+    # a workspace that never went through moe_layer_forward_host: nothing to release
+    assert lib.moe_layer_forward_host_release(0x1000) == 0
+
+
+@pytest.mark.parametrize("E,T,split,ok", [
+    (384, 10979, False, True), (384, 10980, False, False),
+    (384, 14563, True, True), (384, 14564, True, False),
+    (896, 2657, False, True), (896, 2658, False, False),
+    (896, 6241, True, True), (896, 6242, True, False),
+])
+def test_noalloc_router_size_bound(fgs, E, T, split, ok):
+    """moe_router_noalloc rejects a problem, before any CUDA call, exactly when
+    even three K parts overflow its 64 MiB scratch (the bound its header
+    states); larger problems are rejected, smaller ones get past the check."""
+    cfg = fgs.config(d_model=7168, E_routed=E, K=8,
+                     router_weight=fgs.MOE_ROUTER_WEIGHT_SPLIT if split else 0)
+    if ok:
+        # accepted sizes would go on to the GPU: check the bound arithmetic only
+        need = 256 + (0 if split else (6 * E * 7168 + 255) // 256 * 256) + \
+            (12 * T * E + 255) // 256 * 256
+        assert need <= 64 << 20
+        return
+    st = fgs.lib.moe_router_noalloc(ctypes.byref(cfg), T, 0x1000, 0x1000, 0x1000, 0x1000,
+                                    0x1000, None)
+    assert st == 4
+    assert "static scratch" in fgs.moe_last_error_detail()

@@ -15,7 +15,8 @@ import torch
 
 import oracle
 import synth
-from _gpu_common import GAP_MIN, TOL_BF16, by_expert, lib, need_gpu, np64, rel_max_err, workspace
+from _gpu_common import (GAP_MIN, TOL_BF16, by_expert, lib, need_gpu, np64, rel_max_err,
+                         rows_covering_experts, workspace)
 
 pytestmark = pytest.mark.gpu
 
@@ -168,7 +169,13 @@ def test_layer_fp8_full_size_sampled(name):
     try:
         y, idx, w, counts = _forward(shape, g)
         torch.cuda.synchronize()
-        rows = np.unique(np.linspace(0, shape.T - 1, 4).astype(int))
+        # the oracle dequantises every expert the compared tokens select, in
+        # fp64 (seconds each): four evenly spaced tokens, and the tokens at
+        # the first, last and every 128th slot of the two largest experts
+        # (both of their row tiles and their ragged tails)
+        rows = np.unique(np.concatenate([
+            np.linspace(0, shape.T - 1, 4).astype(np.int64),
+            rows_covering_experts(idx.cpu().numpy(), shape.E_routed, shape.K, largest=2)]))
         _compare(shape, g, y, idx, w, counts, rows)
         assert np.isfinite(np64(y)).all()
     finally:

@@ -13,7 +13,7 @@ import torch
 import oracle
 import synth
 from _gpu_common import (GAP_MIN, TOL_BF16, TOL_F32, by_expert, lib, need_gpu, np64,
-                         rel_max_err, to_f64_cpu, workspace)
+                         rel_max_err, rows_covering_experts, to_f64_cpu, workspace)
 
 pytestmark = pytest.mark.gpu
 
@@ -94,6 +94,11 @@ def test_layer_small_every_token(shape, packed):
 
 @pytest.mark.parametrize("name", ["k2_decode", "k2_prefill", "k3_latent"])
 def test_layer_full_size_sampled(name):
+    """Full-size layers in the benchmark's launch configuration.  The output
+    is compared element by element with the oracle on every token at decode
+    size, and otherwise on the tokens that reach every expert's every row
+    tile (first, last and every 128th slot of each expert), so that each
+    expert's weights, each token tile and each ragged tail is checked."""
     need_gpu()
     shape = synth.shape(name)
     g = synth.generate(shape, device="cuda")
@@ -101,7 +106,8 @@ def test_layer_full_size_sampled(name):
         y, idx, w, counts = _forward(shape, g, packed=True)
         torch.cuda.synchronize()
         T = shape.T
-        rows = np.unique(np.linspace(0, T - 1, 6).astype(int))
+        rows = (np.arange(T) if T <= 256 else
+                rows_covering_experts(idx.cpu().numpy(), shape.E_routed, shape.K))
         _compare(shape, g, y, idx, w, counts, rows, TOL_BF16)
         # the routing of every token on the gap criterion
         r = oracle.router_from_x(np64(g["x"]), np64(g["W_r"]), g["bias"].cpu().numpy(), shape.K,
@@ -173,3 +179,69 @@ def test_layer_with_presplit_router_weight(shape):
     assert fgs.moe_get_device_status(ws) == 0
     for a, b in ((y, y0), (idx, idx0), (w, w0), (counts, c0)):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("weights_in", ["combine", "experts"])
+@pytest.mark.parametrize("shape", [SMALL[1], SMALL[5]], ids=lambda s: s.name)
+def test_layer_composed_from_the_public_calls(shape, weights_in):
+    """moe_router -> moe_permute -> moe_grouped_swiglu -> moe_combine, each
+    through the C ABI, equals the oracle layer.  With the gate weights applied
+    in the combine (NULL to the experts) the result is the layer forward's,
+    bit for bit; applied in the experts' epilogue (NULL to the combine) they
+    scale each expert row before it is rounded to bf16."""
+    need_gpu()
+    fgs = lib()
+    g = synth.generate(shape, device="cuda")
+    cfg = fgs.config(shape)
+    T, K, E, d, S = shape.T, shape.K, shape.E_routed, shape.d_model, shape.E_shared
+    ws, nws = workspace(cfg, T)
+    dev = dict(device="cuda")
+    idx = torch.empty((T, K), dtype=torch.int32, **dev)
+    w = torch.empty((T, K), dtype=torch.float32, **dev)
+    fgs.moe_router(cfg, T, g["x"], g["W_r"], g["bias"], idx, w, ws, nws)
+    counts = torch.empty(E, dtype=torch.int32, **dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, **dev)
+    perm = torch.empty(T * K, dtype=torch.int32, **dev)
+    inv = torch.empty(T * K, dtype=torch.int32, **dev)
+    fgs.moe_permute(cfg, T, idx, counts, offsets, perm, inv, ws, nws)
+    Y = torch.empty((T * K, d), dtype=g["x"].dtype, **dev)
+    Ysh = torch.empty((S, T, d), dtype=g["x"].dtype, **dev) if S else None
+    in_experts = weights_in == "experts"
+    fgs.moe_grouped_swiglu(cfg, T, g["x"], offsets, perm, w if in_experts else None,
+                           g["W_gate_up"], g["W_down"], g["x"] if S else None,
+                           g.get("Ws_gate_up"), g.get("Ws_down"), Y, Ysh, ws, nws)
+    y = torch.empty((T, d), dtype=g["x"].dtype, **dev)
+    fgs.moe_combine(cfg, T, Y, inv, None if in_experts else w, Ysh, y)
+    torch.cuda.synchronize()
+    assert fgs.moe_get_device_status(ws) == 0
+    _compare(shape, g, y, idx, w, counts, np.arange(T), TOL_BF16)
+    if not in_experts:
+        y_layer, idx_l, w_l, counts_l = _forward(shape, g)
+        torch.cuda.synchronize()
+        assert torch.equal(idx, idx_l) and torch.equal(w, w_l)
+        assert torch.equal(y, y_layer)
+
+
+def test_layer_forward_host_release_starts_afresh():
+    """After moe_layer_forward_host_release, host-buffer calls on the same
+    workspace run again (on new state) and still return the device-buffer
+    forward's result."""
+    need_gpu()
+    fgs = lib()
+    shape = SMALL[1]
+    g = synth.generate(shape, device="cuda")
+    cfg = fgs.config(shape)
+    T = shape.T
+    ws, nws = workspace(cfg, T)
+    x_host = g["x"].cpu().pin_memory()
+    y_ref, _, _, _ = _forward(shape, g)
+    for _ in range(2):
+        y_host = torch.full((T, shape.d_model), float("nan"), dtype=g["x"].dtype).pin_memory()
+        for _ in range(3):
+            fgs.moe_layer_forward_host(cfg, T, x_host, g["W_r"], g["bias"], g["W_gate_up"],
+                                       g["W_down"], g.get("Ws_gate_up"), g.get("Ws_down"), None,
+                                       None, y_host, ws, nws)
+        torch.cuda.synchronize()
+        assert torch.equal(y_host, y_ref.cpu())
+        fgs.moe_layer_forward_host_release(ws)
+    fgs.moe_layer_forward_host_release(ws)  # releasing twice is harmless

@@ -322,11 +322,94 @@ def check_page_figures():
     assert g["W_r"].numel() + g["bias"].numel() == vals["router_params_per_instance"]
 
 
+def _brute_gap(c32, K, G, Gk):
+    """Smallest margin of a token's decisions, by enumerating pairs: every
+    selected vs every unselected masked score, and (G > 1, Gk < G) every kept
+    vs every dropped group score (group scores by enumerating member pairs)."""
+    E = len(c32)
+    gs = E // G
+    gscore = []
+    for j in range(G):
+        members = range(j * gs, (j + 1) * gs)
+        gscore.append(max(np.float32(c32[a]) + np.float32(c32[b])
+                          for a, b in itertools.permutations(members, 2)))
+    kept = _brute_topk(gscore, Gk) if G > 1 else {0}
+    masked = [c32[e] if (G == 1 or (e // gs) in kept) else np.float32(0.0) for e in range(E)]
+    sel = _brute_topk(masked, K)
+    gap = math.inf
+    for a in sel:
+        for b in set(range(E)) - sel:
+            gap = min(gap, float(masked[a]) - float(masked[b]))
+    if G > 1:
+        for a in kept:
+            for b in set(range(G)) - kept:
+                gap = min(gap, float(gscore[a]) - float(gscore[b]))
+    return gap
+
+
 def check_gaps():
     c = np.array([[0.9, 0.5, 0.5 + 2 ** -20, 0.1]], dtype=np.float32)
     gap = oracle.selection_gaps(c, 2)
     assert gap[0] == pytest.approx(2 ** -20, rel=1e-6)
     assert oracle.selection_gaps(c, 4)[0] == np.inf
+    # group limiting where the group decision binds: E = 8 in 4 groups of 2,
+    # keep 2 groups, K = 2.  Group scores (both members summed) are 1.0,
+    # 0.9375, 0.921875, 0.4375: groups 0 and 1 are kept with a margin of
+    # 0.9375 - 0.921875 = 1/64; the masked scores 0.875, 0.125, 0.5, 0.4375,
+    # 0, 0, 0, 0 select experts 0 and 2 with a margin of 0.5 - 0.4375 = 1/16.
+    # The token's gap is the smaller one, exactly 1/64 (all values are exact
+    # in fp32).
+    cg = np.array([[0.875, 0.125, 0.5, 0.4375, 0.625, 0.296875, 0.25, 0.1875]],
+                  dtype=np.float32)
+    assert set(oracle.select_experts(cg, 2, 4, 2)[0][0].tolist()) == {0, 2}
+    assert oracle.selection_gaps(cg, 2, 4, 2)[0] == 1.0 / 64
+    # without group limiting the same scores decide only the expert top-2:
+    # experts 0 and 4 (0.875, 0.625) against 0.5, margin 1/8
+    assert oracle.selection_gaps(cg, 2)[0] == 0.125
+    # the pairwise brute force on random tiny tokens, plain and grouped,
+    # with many exact ties (values on a coarse grid)
+    rng = _rng(21)
+    for case in range(300):
+        G = int(rng.choice([1, 2, 3, 4]))
+        gs = int(rng.integers(2, 4))
+        E = G * gs
+        Gk = int(rng.integers(1, G + 1))
+        K = int(rng.integers(1, min(E, Gk * gs) + 1)) if G > 1 else int(rng.integers(1, E + 1))
+        c32 = (rng.integers(0, 24, E) / 16.0 - 0.25).astype(np.float32)
+        got = oracle.selection_gaps(c32[None, :], K, G, Gk)[0]
+        want = _brute_gap(list(c32), K, G, Gk)
+        assert got == want, (case, c32, K, G, Gk, got, want)
+
+
+def check_combine():
+    """The combine of per-slot expert outputs equals the layer's routed sum:
+    evaluating every expert on its dispatched rows (slot order of permute),
+    combining them with the gate weights and adding the shared experts gives
+    the y of moe_layer; and a hand case with K = 2."""
+    Y = np.array([[1.0, 2.0], [3.0, 4.0], [5.0, 6.0], [7.0, 8.0]])
+    inv = np.array([2, 0, 3, 1])  # token 0: slots 2, 0; token 1: slots 3, 1
+    w = np.array([[0.5, 0.25], [1.0, 2.0]])
+    Ys = np.array([[[10.0, 20.0], [30.0, 40.0]]])
+    y = oracle.combine(Y, inv, w, Ys)
+    np.testing.assert_array_equal(y, [[0.5 * 5 + 0.25 * 1 + 10, 0.5 * 6 + 0.25 * 2 + 20],
+                                      [7 + 2 * 3 + 30, 8 + 2 * 4 + 40]])
+    rng = _rng(22)
+    T, d, E, K, F = 12, 16, 6, 3, 8
+    gu, dn = _small_bank(rng, E, F, d)
+    sgu, sdn = _small_bank(rng, 1, F, d)
+    x = rng.normal(size=(T, d))
+    Wr = rng.normal(size=(E, d)) * 0.3
+    b = rng.uniform(-0.1, 0.1, E).astype(np.float32)
+    ref = oracle.moe_layer_tokens(x, Wr, b, gu, dn, sgu, sdn, K)
+    p = oracle.permute(ref["idx"], E)
+    Yslot = np.zeros((T * K, d))
+    for e in range(E):
+        for r in range(p["offsets"][e], p["offsets"][e + 1]):
+            t = p["perm"][r] // K
+            Yslot[r] = oracle.swiglu_expert(x[t:t + 1], gu[e, :F], gu[e, F:], dn[e])[0]
+    Ysh = oracle.swiglu_expert(x, sgu[0, :F], sgu[0, F:], sdn[0])[None]
+    np.testing.assert_allclose(oracle.combine(Yslot, p["inv"], ref["w"], Ysh), ref["y"],
+                               rtol=1e-12, atol=1e-12)
 
 
 def check_dense_gates():
@@ -382,7 +465,8 @@ ALL_CHECKS = [
     check_select_plain_bruteforce, check_select_grouped_bruteforce, check_group_special_cases,
     check_masked_fill_is_literal_zero, check_weights, check_router_from_x, check_permute,
     check_swiglu_expert, check_dense_reduction, check_layer_routing_weights,
-    check_k3_composition, check_page_figures, check_gaps, check_dense_gates, check_bias_update,
+    check_k3_composition, check_page_figures, check_gaps, check_combine, check_dense_gates,
+    check_bias_update,
 ]
 
 
@@ -460,6 +544,33 @@ def _bias_update_wrong_sign(bias32, counts, T, K, gamma=1e-3):
     return mo._orig_bias_update(bias32, counts, T, K, -gamma)
 
 
+def _gaps_without_groups(c32, K, n_group=1, topk_group=1):
+    return mo._orig_selection_gaps(c32, K, 1, 1) if n_group == 1 else \
+        _expert_gap_only(c32, K, n_group, topk_group)
+
+
+def _expert_gap_only(c32, K, n_group, topk_group):
+    _, masked = mo.select_experts(np.asarray(c32, np.float32), K, n_group, topk_group)
+    srt = -np.sort(-masked.astype(np.float64), axis=-1)
+    return srt[:, K - 1] - srt[:, K] if K < masked.shape[1] else np.full(masked.shape[0], np.inf)
+
+
+def _gaps_group_rank_shifted(c32, K, n_group=1, topk_group=1):
+    gap = _expert_gap_only(c32, K, n_group, topk_group)
+    if n_group > 1 and topk_group + 1 < n_group:  # one rank too far down
+        g = -np.sort(-mo.group_scores_f32(np.asarray(c32, np.float32), n_group).astype(np.float64), -1)
+        gap = np.minimum(gap, g[:, topk_group] - g[:, topk_group + 1])
+    return gap
+
+
+def _combine_by_perm(Y, inv, w, Y_shared=None):
+    # reads Y through the inverse map's inverse (perm) instead of inv
+    inv = np.asarray(inv)
+    perm = np.empty_like(inv)
+    perm[inv] = np.arange(inv.size)
+    return mo._orig_combine(Y, perm, w, Y_shared)
+
+
 MUTANTS = {
     "sigmoid_not_logistic": ("sigmoid", _softmax_like),
     "gate_up_swapped": ("swiglu_expert", _swapped_swiglu),
@@ -471,6 +582,9 @@ MUTANTS = {
     "weights_from_biased_scores": ("router_from_logits", _biased_weights_router),
     "dense_gates_misplaced": ("dense_gates", _dense_gates_transposed),
     "bias_update_wrong_sign": ("aux_free_bias_update", _bias_update_wrong_sign),
+    "gaps_ignore_group_decision": ("selection_gaps", _gaps_without_groups),
+    "gaps_group_rank_shifted": ("selection_gaps", _gaps_group_rank_shifted),
+    "combine_reads_perm": ("combine", _combine_by_perm),
 }
 
 
@@ -480,6 +594,8 @@ def test_planted_mistakes_are_caught(mutant, monkeypatch):
     monkeypatch.setattr(mo, "_orig_permute", mo.permute, raising=False)
     monkeypatch.setattr(mo, "_orig_router_from_logits", mo.router_from_logits, raising=False)
     monkeypatch.setattr(mo, "_orig_bias_update", mo.aux_free_bias_update, raising=False)
+    monkeypatch.setattr(mo, "_orig_selection_gaps", mo.selection_gaps, raising=False)
+    monkeypatch.setattr(mo, "_orig_combine", mo.combine, raising=False)
     monkeypatch.setattr(mo, name, fn)
     # the package namespace re-exports the functions: patch it too
     if hasattr(oracle, name):
