@@ -75,6 +75,10 @@ def parse_args():
                     help="tokens of the CPU oracle sample (default 64; 8 with FP8 weights, "
                          "whose per-expert dequantisation dominates the oracle's time)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-configs", action="store_true",
+                    help="skip the companion workloads measured after the headline one")
+    ap.add_argument("--extra-steps", type=int, default=30,
+                    help="timed steps of each companion workload")
     return ap.parse_args()
 
 
@@ -360,7 +364,8 @@ def time_router(fgs, torch, cfg, T, gp, ws, nws, stream, reps=20):
     return a.elapsed_time(b) / reps
 
 
-def run_router_only(args, fgs, torch, synth, shape, world, rank, local):
+def run_router_only(args, fgs, torch, synth, shape, world, rank, local, steps, warmup,
+                    full=True):
     """One step = one moe_router call (x, W_r and the bias resident).  The
     inputs (70 MB) fit in L2, so a 256 MB buffer is written between steps,
     outside the timed intervals, and the step time is the sum of the
@@ -385,12 +390,12 @@ def run_router_only(args, fgs, torch, synth, shape, world, rank, local):
         fgs.moe_router(cfg, T, g["x"], W_s, g["bias"], idx, w, ws, nws, stream=stream)
 
     with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             flush.zero_()
             step()
     stream.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
+           for _ in range(steps)]
     sampler = ClockSampler(device_id(torch, local)) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -413,7 +418,7 @@ def run_router_only(args, fgs, torch, synth, shape, world, rank, local):
     status = fgs.moe_get_device_status(ws, stream)
     if status:
         raise RuntimeError("device status after the timed steps: " + fgs.moe_status_string(status))
-    ms_step = ms_total / args.steps
+    ms_step = ms_total / steps
     peaks = load_peaks()
     d, E = shape.d_model, shape.E_routed
     flops_fp32 = 2 * T * d * E            # the method's fp32 GEMM
@@ -421,12 +426,12 @@ def run_router_only(args, fgs, torch, synth, shape, world, rank, local):
     tflops = flops_bf16 / (ms_step / 1e3) / 1e12
     bytes_alg = T * d * 2 + E * d * 4 + E * 4 + T * K * 8
     line = {
-        "metric": METRIC, "value": round(job_tokens_per_s(world, T, args.steps, ms_total), 1),
-        "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "metric": METRIC, "value": round(job_tokens_per_s(world, T, steps, ms_total), 1),
+        "unit": UNIT, "n_gpus": world, "steps": steps, "warmup": warmup,
         "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16x3 (fp32-exact products)",
         "data": "synthetic (seeded; x N(0,1) bf16, W_r kaiming-uniform fp32, bias U(-0.05,0.05))",
-        "config": {"workload": WORKLOADS[args.config], "name": args.config, "tokens_per_step": T,
+        "config": {"workload": WORKLOADS[shape.name], "name": shape.name, "tokens_per_step": T,
                    "l2": "inputs (70 MB) fit in L2: a 256 MB buffer is written between steps, "
                          "outside the timed intervals",
                    "router_weight": "fp32 W_r split once before timing into three bf16 terms "
@@ -446,12 +451,14 @@ def run_router_only(args, fgs, torch, synth, shape, world, rank, local):
         "gpu_launches": launches,
         "clocks": clocks,
     }
+    if not full:
+        return line
     # end to end: pinned host x in, routing (indices and weights) out
     x_host = g["x"].cpu().pin_memory()
     xd = torch.empty_like(g["x"])
     idx_h = torch.empty((T, K), dtype=torch.int32).pin_memory()
     w_h = torch.empty((T, K), dtype=torch.float32).pin_memory()
-    e_steps = max(3, min(args.steps, 50))
+    e_steps = max(3, min(steps, 50))
     es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         es.record(stream)
@@ -466,7 +473,7 @@ def run_router_only(args, fgs, torch, synth, shape, world, rank, local):
     line["e2e"] = {"value": round(job_tokens_per_s(world, T, e_steps, e_ms), 1), "unit": UNIT,
                    "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * K * 8,
                    "steps": e_steps, "api": "moe_router (pinned host x in, idx and w out)"}
-    if rank == 0 and not args.no_cpu_baseline:
+    if full and rank == 0 and not args.no_cpu_baseline:
         import oracle
         n = args.cpu_sample_tokens or T  # the oracle router takes seconds for the batch
         rows = torch.as_tensor(np.unique(np.linspace(0, T - 1, n).astype(int)), device="cuda")
@@ -480,29 +487,17 @@ def run_router_only(args, fgs, torch, synth, shape, world, rank, local):
                                 "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
                                 "sample": f"{len(rows)} of the {T} tokens, fp64 router "
                                           f"(logits, sigmoid, selection, weights); {secs:.2f} s"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    finish_ranks(torch, world)
+    return line
 
 
-def run_own(args):
+def run_layer(args, fgs, torch, synth, name, steps, warmup, world, rank, local, full=True):
+    """One workload: its JSON fields (full: with the end-to-end and CPU legs)."""
     import numpy as np
-    import torch
-    import synth
 
-    world, rank, local = dist_env()
-    torch.cuda.set_device(local)
-    init_ranks(torch, world, "nccl", torch.device("cuda", local))
-    try:
-        import fine_grained_sparse_gb300 as fgs
-    except ImportError:
-        import __graft_entry__
-        __graft_entry__.build()
-        import fine_grained_sparse_gb300 as fgs
-
-    shape = synth.shape(args.config)
+    shape = synth.shape(name)
     if shape.router_only:
-        return run_router_only(args, fgs, torch, synth, shape, world, rank, local)
+        return run_router_only(args, fgs, torch, synth, shape, world, rank, local, steps, warmup,
+                               full)
     T = shape.T
     seed = synth.SEEDS[shape.name]
     g = synth.generate(shape, device="cuda", seed=seed)
@@ -539,7 +534,7 @@ def run_own(args):
                               nws, stage_events=events, stream=stream)
 
     with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             step()
     stream.synchronize()
     status = fgs.moe_get_device_status(ws, stream)
@@ -551,7 +546,7 @@ def run_own(args):
     # overlapping); the other stage times come from an instrumented pass
     # after it
     gu_events = [[None, None, torch.cuda.Event(enable_timing=True),
-                  torch.cuda.Event(enable_timing=True), None, None] for _ in range(args.steps)]
+                  torch.cuda.Event(enable_timing=True), None, None] for _ in range(steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(device_id(torch, local)) if rank == 0 else None
     if sampler:
@@ -562,14 +557,14 @@ def run_own(args):
     small = fp32 or sum(t.numel() * t.element_size() for k, t in g.items() if k != "x") < (256 << 20)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if small else None
     step_iv = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)] if small else None
+               for _ in range(steps)] if small else None
     barrier(torch, world)
     torch.cuda.synchronize()
     t0 = time.time()
     launches0 = fgs.moe_launch_count()
     start.record(stream)
     with torch.cuda.stream(stream):
-        for i in range(args.steps):
+        for i in range(steps):
             if small:
                 flush.zero_()
                 step_iv[i][0].record(stream)
@@ -592,21 +587,21 @@ def run_own(args):
     gu_live_ms = statistics.mean(ev[2].elapsed_time(ev[3]) for ev in gu_events)
     # stage breakdown: a few steps with every stage boundary recorded
     step_events = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)]
-                   for _ in range(min(args.steps, 10))]
+                   for _ in range(min(steps, 10))]
     with torch.cuda.stream(stream):
         for evs in step_events:
             step(evs)
     stream.synchronize()
     stage_ms = [statistics.mean(ev[j].elapsed_time(ev[j + 1]) for ev in step_events)
                 for j in range(nev - 1)]
-    ms_step = ms_total / args.steps
-    value = job_tokens_per_s(world, T, args.steps, ms_total)
+    ms_step = ms_total / steps
+    value = job_tokens_per_s(world, T, steps, ms_total)
     counts_h = counts.cpu().numpy()
     work = per_step_work(shape, counts_h)
     peaks = load_peaks()
     gu_ms = gu_live_ms  # the gate/up launch inside the timed region
     achieved = work["gate_up_bytes"] / (gu_ms / 1e3) / 1e9
-    traffic = profiled_traffic(args.config)
+    traffic = profiled_traffic(name)
     kernel = ("simt_gemm_kernel (expert gate/up + SwiGLU on CUDA cores, fp32; launch-bound at "
               "this size)" if fp32 else
               "tc_gemm_kernel (expert gate/up + SwiGLU, routed + shared)")
@@ -619,7 +614,7 @@ def run_own(args):
                                                   / peaks["bf16_tflops_sustained"], 4)}
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "steps": steps, "warmup": warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32" if fp32 else "bf16",
         "data": ("synthetic (seeded; FP8 E4M3 expert weights, codes N(0,112^2) rounded by "
@@ -629,7 +624,7 @@ def run_own(args):
                  "synthetic (seeded; bf16 expert weights N(0,0.02)")
                 + ", fp32 router weight kaiming-uniform, bias uniform; shapes of the pages' "
                   "K2/K3 layers)",
-        "config": {"workload": WORKLOADS[args.config], "name": args.config, "tokens_per_step": T,
+        "config": {"workload": WORKLOADS[name], "name": name, "tokens_per_step": T,
                    "weights": ("FP8 E4M3 + fp32 128x128 block scales, packed once before "
                                "timing (moe_pack_weights_fp8)" if is_fp8(shape) else
                                "fp32, natural layout" if fp32 else
@@ -658,6 +653,8 @@ def run_own(args):
         "clocks": clocks,
     }
 
+    if not full:
+        return line
     # end to end through the C ABI with host buffers (copies inside the region)
     x_host = g["x"].cpu().pin_memory()
     y_host = torch.empty((T, shape.d_model), dtype=g["x"].dtype).pin_memory()
@@ -671,7 +668,7 @@ def run_own(args):
     for _ in range(2):
         step_host()
     stream.synchronize()
-    e_steps = max(3, min(args.steps, 50))
+    e_steps = max(3, min(steps, 50))
     es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     es.record(stream)
     for _ in range(e_steps):
@@ -684,10 +681,49 @@ def run_own(args):
                    "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes, "steps": e_steps,
                    "api": "moe_layer_forward_host (pinned host x and y)"}
 
+    fgs.moe_layer_forward_host_release(ws)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_from_device(shape, g, idx.cpu().numpy(),
                                                         args.cpu_sample_tokens or
                                                         (8 if is_fp8(shape) else 64))
+    return line
+
+
+
+
+# Companion workloads measured in the same run as the headline one (each a
+# short timed run of its own, with its own clocks): the other configurations
+# of the benchmark set.
+EXTRA = ["k2_decode", "k3_latent", "k2_router", "tiny"]
+EXTRA_KEYS = ("value", "unit", "ms_per_step", "steps", "warmup", "dtype", "roofline", "layer",
+              "router", "stages_ms", "gpu_launches", "clocks", "config")
+
+
+def run_own(args):
+    import torch
+    import synth
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    init_ranks(torch, world, "nccl", torch.device("cuda", local))
+    try:
+        import fine_grained_sparse_gb300 as fgs
+    except ImportError:
+        import __graft_entry__
+        __graft_entry__.build()
+        import fine_grained_sparse_gb300 as fgs
+
+    line = run_layer(args, fgs, torch, synth, args.config, args.steps, args.warmup, world, rank,
+                     local, full=True)
+    torch.cuda.empty_cache()  # the workload's tensors died with its call
+    if not args.no_extra_configs and args.config == "k2_prefill":
+        extras = {}
+        for name in EXTRA:
+            sub = run_layer(args, fgs, torch, synth, name, args.extra_steps, 3, world, rank, local,
+                            full=False)
+            torch.cuda.empty_cache()
+            extras[name] = {k: sub[k] for k in EXTRA_KEYS if k in sub}
+        line["configs"] = extras
     if rank == 0:
         print(json.dumps(line), flush=True)
     finish_ranks(torch, world)

@@ -26,6 +26,7 @@ __all__ = [
     "moe_layer_forward_host", "moe_layer_forward_host_release", "moe_last_error_detail",
     "moe_pack_weights", "pack_layer_weights",
     "moe_router_noalloc", "moe_launch_count", "moe_dense_gates", "moe_update_bias",
+    "moe_quantile_bias_update",
     "MOE_WEIGHTS_NATURAL", "MOE_WEIGHTS_PACKED", "MOE_PACK_GATE_UP", "MOE_PACK_PLAIN",
     "MOE_WEIGHTS_PACKED_FP8", "moe_packed_fp8_bytes", "moe_pack_weights_fp8",
     "pack_layer_weights_fp8", "moe_selftest_bounded_wait", "MOE_ROUTER_WEIGHT_F32",
@@ -86,6 +87,7 @@ _SIGS = {
     "moe_router_from_logits": ([_CFG, _I64, _P, _P, _P, _P, _P], _I32),
     "moe_dense_gates": ([_CFG, _I64, _P, _P, _P, _P], _I32),
     "moe_update_bias": ([_CFG, _I64, _P, _F, _P, _P], _I32),
+    "moe_quantile_bias_update": ([_CFG, _I64, _P, _F, _P, _P, _P], _I32),
     "moe_permute": ([_CFG, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P], _I32),
     "moe_grouped_swiglu": ([_CFG, _I64] + [_P] * 12 + [_SZ, _P], _I32),
     "moe_combine": ([_CFG, _I64, _P, _P, _P, _P, _P, _P], _I32),
@@ -194,6 +196,13 @@ def moe_update_bias(cfg, T, counts, gamma, bias, stream=None):
     """bias [E] fp32 in place: += gamma * sign(T K / E - counts)."""
     _check(lib.moe_update_bias(ctypes.byref(cfg), T, _ptr(counts), float(gamma), _ptr(bias),
                                _stream(stream)), "moe_update_bias")
+
+
+def moe_quantile_bias_update(cfg, T, logits, rate, theta, bias, stream=None):
+    """Quantile Balancing: theta [E] out, bias [E] fp32 updated in place."""
+    _check(lib.moe_quantile_bias_update(ctypes.byref(cfg), T, _ptr(logits), float(rate),
+                                        _ptr(theta), _ptr(bias), _stream(stream)),
+           "moe_quantile_bias_update")
 
 
 def moe_router_noalloc(cfg, T, x, W_r, bias, topk_idx, topk_w, stream=None):

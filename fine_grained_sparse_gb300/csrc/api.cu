@@ -325,9 +325,12 @@ int32_t set_gate_up_A(GemmSegment& s, const void* W, int groups, int F, int Kd, 
   return MOE_OK;
 }
 
-int32_t set_B(GemmSegment& s, const void* B, int64_t rows, int Kd) {
-  if (encode_tmap_2d_rows(&s.tmB, B, rows, Kd, 32) != CUDA_SUCCESS)
+// Activation rows through a tensor map whose box is a whole token tile of
+// `tile` rows, so that each k step of a unit is one copy.
+int32_t set_B(GemmSegment& s, const void* B, int64_t rows, int Kd, int tile) {
+  if (encode_tmap_2d_rows(&s.tmB, B, rows, Kd, tile) != CUDA_SUCCESS)
     return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for activations");
+  s.b_box_rows = tile;
   s.k_steps = Kd / 64;
   return MOE_OK;
 }
@@ -389,7 +392,7 @@ int32_t shared_gate_up_segment(GemmSegment& s, const moe_config* c, int64_t T, c
   int32_t e;
   if ((e = set_gate_up_A(s, Ws_gate_up, c->E_shared, c->d_ff_shared, c->d_model, packed)) != MOE_OK)
     return e;
-  if ((e = set_B(s, x, T, c->d_model)) != MOE_OK) return e;
+  if ((e = set_B(s, x, T, c->d_model, token_tile(T))) != MOE_OK) return e;
   s.a128 = c->d_ff_shared / 64;
   s.groups = c->E_shared;
   s.rows = static_cast<int>(T);
@@ -589,7 +592,7 @@ int32_t run_linear(int64_t T, int in_f, int out_f, const void* x, const void* W,
   clear(s);
   int32_t e;
   if ((e = set_store_A(s, W, 1, out_f, in_f, packed)) != MOE_OK) return e;
-  if ((e = set_B(s, x, T, in_f)) != MOE_OK) return e;
+  if ((e = set_B(s, x, T, in_f, p.nt)) != MOE_OK) return e;
   s.a128 = out_f / 128;
   s.o_limit = out_f;
   s.groups = 1;
@@ -821,10 +824,12 @@ int32_t moe_router(const moe_config* cfg, int64_t T, const void* x, const float*
     p.nseg = 1;
     GemmSegment& g = p.seg[0];
     clear(g);
-    if (encode_tmap_weights_3d(&g.tmA, w_split, 1, E, 3ll * d, 128) != CUDA_SUCCESS)
+    // a unit's weight tiles in one box, its token tile in another
+    g.a_box_rows = 128 * p.a_per_unit;
+    if (encode_tmap_weights_3d(&g.tmA, w_split, 1, E, 3ll * d, g.a_box_rows) != CUDA_SUCCESS)
       return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for the split router weight");
     int32_t e;
-    if ((e = set_B(g, x, T, d)) != MOE_OK) return e;
+    if ((e = set_B(g, x, T, d, p.nt)) != MOE_OK) return e;
     g.k_steps = 3 * d / 64;
     g.b_k_period = d / 64;
     g.a128 = (E + 127) / 128;
@@ -869,6 +874,19 @@ int32_t moe_update_bias(const moe_config* cfg, int64_t T, const int32_t* counts,
   if (!(gamma >= 0.0f) || !(gamma < 1.0f)) return fail(MOE_ERR_INVALID_ARG, "gamma not in [0, 1)");
   MOE_CUDA(launch_bias_update(counts, T, cfg->K, cfg->E_routed, gamma, bias,
                               static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int32_t moe_quantile_bias_update(const moe_config* cfg, int64_t T, const float* logits, float rate,
+                                 float* theta, float* bias, void* stream) {
+  int32_t st = check_router_cfg(cfg, T);
+  if (st != MOE_OK) return st;
+  if (!logits || !theta || !bias) return fail(MOE_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(logits) || !aligned16(theta) || !aligned16(bias))
+    return fail(MOE_ERR_ALIGNMENT, "pointer not 16-byte aligned");
+  if (!(rate >= 0.0f) || !(rate <= 1.0f)) return fail(MOE_ERR_INVALID_ARG, "rate not in [0, 1]");
+  MOE_CUDA(launch_quantile_bias(logits, T, cfg->K, cfg->E_routed, rate, theta, bias,
+                                static_cast<cudaStream_t>(stream)));
   return MOE_OK;
 }
 
@@ -1244,9 +1262,10 @@ int32_t moe_router_noalloc(const moe_config* cfg, int64_t T, const void* x, cons
   p.nseg = 1;
   GemmSegment& g = p.seg[0];
   clear(g);
-  if (encode_tmap_weights_3d(&g.tmA, w_split, 1, E, 3ll * d, 128) != CUDA_SUCCESS)
+  g.a_box_rows = 128 * p.a_per_unit;
+  if (encode_tmap_weights_3d(&g.tmA, w_split, 1, E, 3ll * d, g.a_box_rows) != CUDA_SUCCESS)
     return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for the split router weight");
-  if ((st = set_B(g, x, T, d)) != MOE_OK) return st;
+  if ((st = set_B(g, x, T, d, p.nt)) != MOE_OK) return st;
   g.k_steps = 3 * d / 64;
   g.b_k_period = d / 64;
   g.a128 = (E + 127) / 128;

@@ -474,6 +474,10 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
           mbar_arrive_expect_tx(fb, tx);
           bulk_load(a_dst, s->a_packed + x.group * s->a_group_bytes + tile * kATileBytes, tx, fb,
                     pol_w);
+        } else if (s->mode != kModeSwiGLU && s->a_box_rows == 256) {
+          // both 128-row tiles of the unit in one box (rows past O read as 0)
+          mbar_arrive_expect_tx(fb, 2 * kATileBytes);
+          tma_load_3d(a_dst, &s->tmA, fb, kc, x.blk0 * 128, x.group, pol_w);
         } else {
           mbar_arrive_expect_tx(fb, tx);
           for (int a = 0; a < x.n_a; ++a) {
@@ -532,12 +536,14 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
       // read by the MMA
       const int half = ((x.n_rows + 15) & ~15) >> 1;
       const int b_row = kPair ? x.b_row + rank * half : x.b_row;
-      const int nbox = kPair ? (half + kBBoxRows - 1) / kBBoxRows
-                             : (x.n_rows + kBBoxRows - 1) / kBBoxRows;
+      // tensor-map tiles: boxes of the segment's box height (its whole token
+      // tile: one copy per k step), 32 rows for pairs
+      const int br = (!kPair && s->b_box_rows) ? s->b_box_rows : kBBoxRows;
+      const int nbox = kPair ? (half + kBBoxRows - 1) / kBBoxRows : (x.n_rows + br - 1) / br;
       // packed: the tile's rows (rounded up to 16) are one contiguous run
       const uint32_t tx = kPair ? 2u * static_cast<uint32_t>(nbox) * kBBoxBytes
                           : s->b_packed ? static_cast<uint32_t>((x.n_rows + 15) & ~15) * 128u
-                                        : static_cast<uint32_t>(nbox) * kBBoxBytes;
+                                        : static_cast<uint32_t>(nbox * br) * 128u;
       bool ok = true;
       for (int ks = x.k0; ks < x.k1; ++ks) {
         if (issued >= sb_n) {  // token stage free once k step issued - Sb was consumed
@@ -569,8 +575,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
           bulk_load(b_dst, src, tx, fb, pol_b);
         } else {
           for (int bx = 0; bx < nbox; ++bx)
-            tma_load_2d(b_dst + bx * kBBoxBytes, &s->tmB, fb, kstep * kBK,
-                        b_row + bx * kBBoxRows, pol_b);
+            tma_load_2d(b_dst + bx * br * 128u, &s->tmB, fb, kstep * kBK, b_row + bx * br, pol_b);
         }
         ++issued;
         if (++fstage == sa_n) fstage = 0;

@@ -57,6 +57,10 @@ cudaError_t launch_dense_gates(const int32_t* topk_idx, const float* topk_w, int
 // bias[e] += gamma * sign(T K / E - counts[e]).
 cudaError_t launch_bias_update(const int32_t* counts, int64_t T, int K, int E, float gamma,
                                float* bias, cudaStream_t stream);
+// Quantile Balancing: theta[e] = the ceil(T K / E)-th largest fp32 score of
+// expert e in logits [T, E]; bias[e] += rate (mean(theta) - theta[e] - bias[e]).
+cudaError_t launch_quantile_bias(const float* logits, int64_t T, int K, int E, float rate,
+                                 float* theta, float* bias, cudaStream_t stream);
 
 // --------------------------------------------------------------- dispatch
 // One row tile of a routed expert: rows [row_start, row_start + n_rows) of
@@ -118,7 +122,10 @@ enum GemmMode : int { kModeSwiGLU = 0, kModeStore = 1 };
 // at the tail of O) times one row tile of at most nt activation rows.
 struct GemmSegment {
   CUtensorMap tmA;  // weights (see gemm_tc.cu for the layouts)
-  CUtensorMap tmB;  // activation rows [rows, K] bf16, box 64 x 32
+  CUtensorMap tmB;  // activation rows [rows, K] bf16, box 64 x b_box_rows
+  int b_box_rows;   // rows of one tmB box: a whole token tile in one copy
+  int a_box_rows;   // store-mode weights read through tmA: 128 (a box per
+                    // tile) or 256 (both tiles of a unit in one copy)
   int k_steps;      // A's K / 64
   int b_k_period;   // B's k coordinate wraps every b_k_period steps (0: never)
   int a128;         // 128-row A tiles along O (SwiGLU: F/64, store: O/128)

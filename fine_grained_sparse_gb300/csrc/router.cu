@@ -700,7 +700,99 @@ __global__ void bias_update_kernel(const int32_t* __restrict__ counts, int64_t p
   }
 }
 
+// ------------------------------------------------------ Quantile Balancing
+// ("Kimi K3's router picks 16 of 896 experts", "The router trains inside the
+// main run": per expert, the score threshold at which it receives its target
+// number of tokens, from a quantile of the router scores, updates the
+// selection bias.)  theta_e is the r-th largest fp32 score s = sigmoid(z) of
+// expert e over the batch, r = ceil(T K / E).  The sigmoid rounded to fp32
+// is non-decreasing in z, so theta_e is the score of the r-th largest logit:
+// the kernel selects that logit exactly (radix select on an order-preserving
+// integer key of the fp32 bits, four 8-bit digits from the top) and takes
+// one fp64 sigmoid of it.
+
+// Unsigned key whose order is the order of the fp32 values (-0 below +0).
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// One CTA per expert: theta[e] from column e of z [T, E].
+__global__ void __launch_bounds__(256) quantile_threshold_kernel(const float* __restrict__ z,
+                                                                 int64_t T, int E, int64_t r,
+                                                                 float* __restrict__ theta) {
+  pdl_wait();
+  __shared__ unsigned hist[256];
+  __shared__ uint32_t s_prefix;
+  __shared__ int64_t s_rank;
+  const int e = blockIdx.x;
+  uint32_t prefix = 0, mask = 0;
+  int64_t rank = r;  // rank still to find among the keys matching prefix, from the top
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int64_t t = threadIdx.x; t < T; t += blockDim.x) {
+      const uint32_t k = order_key(__ldg(z + t * E + e));
+      if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      // the digit whose bin holds the rank-th largest key, counting from 255
+      int64_t above = 0;
+      int d = 255;
+      for (; d > 0; --d) {
+        if (above + hist[d] >= rank) break;
+        above += hist[d];
+      }
+      s_prefix = prefix | (static_cast<uint32_t>(d) << shift);
+      s_rank = rank - above;
+    }
+    __syncthreads();
+    prefix = s_prefix;
+    rank = s_rank;
+    mask |= 255u << shift;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) theta[e] = static_cast<float>(sigmoid_f64(key_value(prefix)));
+}
+
+// tau = (sum_e theta_e) / E, summed in fp64 in expert order by one thread;
+// bias[e] = fp32(b + rate (tau - theta_e - b)) with every operation an fp64
+// operation rounded on its own (no fused multiply-add), in the order written.
+__global__ void __launch_bounds__(256) quantile_bias_kernel(const float* __restrict__ theta, int E,
+                                                            float rate, float* __restrict__ bias) {
+  pdl_wait();
+  __shared__ double s_tau;
+  if (threadIdx.x == 0) {
+    double total = 0.0;
+    for (int e = 0; e < E; ++e) total = __dadd_rn(total, static_cast<double>(theta[e]));
+    s_tau = __ddiv_rn(total, static_cast<double>(E));
+  }
+  __syncthreads();
+  const double tau = s_tau;
+  const double rd = static_cast<double>(rate);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const double b = static_cast<double>(bias[e]);
+    const double target = __dsub_rn(tau, static_cast<double>(theta[e]));
+    const double step = __dmul_rn(rd, __dsub_rn(target, b));
+    bias[e] = __double2float_rn(__dadd_rn(b, step));
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_quantile_bias(const float* logits, int64_t T, int K, int E, float rate,
+                                 float* theta, float* bias, cudaStream_t stream) {
+  const int64_t r = (T * K + E - 1) / E;
+  cudaError_t err = launch_pdl(quantile_threshold_kernel, dim3(static_cast<unsigned>(E)),
+                               dim3(256), 0, stream, logits, T, E, r, theta);
+  if (err != cudaSuccess) return err;
+  return launch_pdl(quantile_bias_kernel, dim3(1), dim3(256), 0, stream,
+                    static_cast<const float*>(theta), E, rate, bias);
+}
 
 cudaError_t launch_dense_gates(const int32_t* topk_idx, const float* topk_w, int64_t T, int K,
                                int E, float* G, cudaStream_t stream) {

@@ -280,6 +280,25 @@ int32_t moe_update_bias(const moe_config* cfg, int64_t T, const int32_t* counts,
                         float* bias, void* stream);
 
 /*
+ * One Quantile Balancing update of the selection bias ("Kimi K3's router
+ * picks 16 of 896 experts", "The router trains inside the main run": a
+ * per-expert threshold at which the expert receives its target number of
+ * tokens, from a quantile of the router scores, updates the bias; training
+ * only).  The page gives no formula; this library's reading:
+ *   target load n* = T K / E; s = sigmoid(z) rounded once to fp32;
+ *   theta[e] = the ceil(n*)-th largest s[t, e] over the batch (an order
+ *     statistic: the (1 - K/E) quantile of expert e's scores);
+ *   tau = (sum_e theta[e]) / E, summed in fp64 in expert order;
+ *   bias[e] = fp32(b + rate ((tau - theta[e]) - b)), b = bias[e], each step
+ *     an fp64 operation in that order, so that rate = 1 puts every expert's
+ *     biased score at its threshold on the common cut-off tau.
+ *   logits [T, E] fp32 in (the router GEMM's z for the batch), rate in
+ *   [0, 1], theta [E] fp32 out, bias [E] fp32 updated in place.  Needs no
+ *   workspace. */
+int32_t moe_quantile_bias_update(const moe_config* cfg, int64_t T, const float* logits, float rate,
+                                 float* theta, float* bias, void* stream);
+
+/*
  * Dispatch: group the T*K (token, slot) pairs by expert ("Kimi K2 MoE",
  * section 3, dispatch_and_combine; its body is not given).  Order: expert
  * major, ascending token index within an expert.  Pair j = t * K + k.

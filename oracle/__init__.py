@@ -31,6 +31,7 @@ from .moe_oracle import (  # noqa: F401
     router_from_x,
     dense_gates,
     aux_free_bias_update,
+    quantile_bias_update,
     permute,
     combine,
     swiglu_expert,

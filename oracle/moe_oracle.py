@@ -289,6 +289,45 @@ def aux_free_bias_update(bias32, counts, T: int, K: int, gamma: float = 1e-3) ->
     return round_f32(np.asarray(bias32, dtype=np.float64) + g32 * step).astype(np.float32)
 
 
+def quantile_bias_update(z32, bias32, K: int, rate: float = 1.0) -> Tuple[np.ndarray, np.ndarray]:
+    """One Quantile Balancing update of the selection bias from one batch.
+
+    [K3] "The router trains inside the main run": Quantile Balancing takes,
+    per expert, the threshold at which that expert receives its target
+    number of tokens from a quantile of the router scores, and updates the
+    selection bias from it (training only; at inference the bias is fixed).
+    The update rule is not printed; the reading taken:
+      * target load n* = T K / E tokens per expert (every expert equal);
+      * threshold theta_e = the ceil(n*)-th largest router score s_e(t) of
+        the batch (the (1 - K/E) quantile of expert e's scores, taken as an
+        order statistic), s = sigmoid(z) rounded once to fp32 (the scores the
+        selection compares);
+      * common cut-off tau = the mean of theta over the experts, summed in
+        fp64 in expert order;
+      * target bias b*_e = tau - theta_e, so that an expert's biased score
+        at its threshold, theta_e + b*_e, is the common cut-off and its top
+        n* tokens are the ones that reach tau;
+      * b_e <- b_e + rate (b*_e - b_e), in fp64, rounded once to fp32
+        (rate 1 sets the target bias).
+    Returns (theta [E] fp32, new bias [E] fp32).
+    """
+    z32 = np.asarray(z32, dtype=np.float32)
+    T, E = z32.shape
+    s32 = round_f32(sigmoid(z32.astype(np.float64)))
+    r = -(-(T * K) // E)  # ceil(T K / E), 1 <= r <= T
+    theta = np.empty(E, dtype=np.float32)
+    for e in range(E):
+        theta[e] = np.sort(s32[:, e])[::-1][r - 1]
+    total = 0.0
+    for e in range(E):  # fixed order, fp64
+        total += float(theta[e])
+    tau = total / E
+    b = np.asarray(bias32, dtype=np.float32).astype(np.float64)
+    target = tau - theta.astype(np.float64)
+    new = b + float(np.float32(rate)) * (target - b)
+    return theta, round_f32(new)
+
+
 # --------------------------------------------------------------------------
 # dispatch (permute)
 # --------------------------------------------------------------------------

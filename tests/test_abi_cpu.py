@@ -204,3 +204,11 @@ def test_noalloc_router_size_bound(fgs, E, T, split, ok):
                                     0x1000, None)
     assert st == 4
     assert "static scratch" in fgs.moe_last_error_detail()
+
+
+def test_quantile_bias_argument_errors(fgs):
+    lib = fgs.lib
+    cfg = fgs.config(d_model=128, E_routed=16, K=4)
+    assert lib.moe_quantile_bias_update(ctypes.byref(cfg), 8, None, 1.0, 0x1000, 0x1000, None) == 1
+    assert lib.moe_quantile_bias_update(ctypes.byref(cfg), 8, 0x1000, 1.5, 0x1000, 0x1000, None) == 1
+    assert lib.moe_quantile_bias_update(ctypes.byref(cfg), 8, 0x1000, 1.0, 0x1004, 0x1000, None) == 3

@@ -145,6 +145,33 @@ def test_bias_update_bit_exact(T, K, E):
     np.testing.assert_array_equal(b_dev.cpu().numpy(), want)
 
 
+@pytest.mark.parametrize("T,E,K,grid", [(4096, 896, 16, False), (8192, 384, 8, False),
+                                        (37, 12, 3, True), (1, 16, 4, False), (300, 32, 32, True)])
+def test_quantile_bias_update_bit_exact(T, E, K, grid):
+    """Quantile Balancing on the GPU equals the oracle bit for bit: the
+    thresholds (order statistics of each expert's fp32 scores) and the
+    updated bias, over two batches in a row with rates 1 and 0.3; a coarse
+    logit grid makes many scores tie."""
+    need_gpu()
+    fgs = lib()
+    gen = torch.Generator().manual_seed(T * 7 + E)
+    z = torch.randn((T, E), generator=gen) * 1.5 + torch.linspace(-1, 1, E)
+    if grid:
+        z = torch.round(z * 4) / 4
+    z = z.to(torch.float32)
+    bias = ((torch.rand(E, generator=gen) - 0.5) * 0.2).to(torch.float32)
+    cfg = fgs.config(d_model=128, E_routed=E, K=K)
+    b_dev = bias.cuda()
+    theta = torch.empty(E, dtype=torch.float32, device="cuda")
+    want_b = bias.numpy()
+    for rate in (1.0, 0.3):
+        fgs.moe_quantile_bias_update(cfg, T, z.cuda(), rate, theta, b_dev)
+        torch.cuda.synchronize()
+        want_theta, want_b = oracle.quantile_bias_update(z.numpy(), want_b, K, rate)
+        np.testing.assert_array_equal(theta.cpu().numpy(), want_theta)
+        np.testing.assert_array_equal(b_dev.cpu().numpy(), want_b)
+
+
 @pytest.mark.parametrize("name,T", [("k2_router", 700), ("k3_latent", 300), ("k2_decode", None)])
 def test_presplit_router_weight_is_bit_identical(name, T):
     """A router weight split once (MOE_ROUTER_WEIGHT_SPLIT) gives the same

@@ -460,13 +460,77 @@ def check_bias_update():
     assert abs(float(bb[0]) - (0.25 - 10e-3)) < 1e-6 and abs(float(bb[3]) - 10e-3) < 1e-6
 
 
+def _scores_f32(z32):
+    """fp32 router scores written out element by element: the fp64 logistic
+    function of each logit, rounded once to fp32."""
+    z32 = np.asarray(z32, dtype=np.float32)
+    out = np.empty(z32.shape, dtype=np.float32)
+    for idx in np.ndindex(z32.shape):
+        out[idx] = np.float32(1.0 / (1.0 + math.exp(-float(z32[idx]))))
+    return out
+
+
+def check_quantile_bias():
+    """Quantile Balancing (the K3 page's training-side bias update, read as
+    documented in the oracle): the threshold is an order statistic of each
+    expert's scores; equal score distributions need no correction; rate 0
+    keeps the bias, rate 1 sets it to the common cut-off minus the
+    threshold; one update makes a skewed batch's loads more even."""
+    # thresholds against a counting definition: theta is a score of the
+    # column with at least r scores >= theta and fewer than r scores > theta
+    rng = _rng(31)
+    for case in range(60):
+        T = int(rng.integers(1, 40))
+        E = int(rng.integers(1, 9))
+        K = int(rng.integers(1, E + 1))
+        z = (rng.integers(-8, 8, (T, E)) / 4.0).astype(np.float32)  # many ties
+        b = rng.uniform(-0.1, 0.1, E).astype(np.float32)
+        theta, nb = oracle.quantile_bias_update(z, b, K, rate=0.0)
+        assert (nb == b).all()
+        sc = _scores_f32(z)
+        r = -(-(T * K) // E)
+        for e in range(E):
+            col = sc[:, e]
+            assert theta[e] in col
+            assert (col >= theta[e]).sum() >= r and (col > theta[e]).sum() < r
+    # hand case: T = 4, E = 2, K = 1, so each expert's target is 2 tokens and
+    # its threshold the 2nd largest score; the cut-off is their mean
+    z = np.array([[2.0, -1.0], [1.5, -0.5], [-2.0, 0.5], [-1.0, 0.25]], dtype=np.float32)
+    sc = _scores_f32(z)
+    theta, nb = oracle.quantile_bias_update(z, np.zeros(2, np.float32), 1, rate=1.0)
+    assert theta[0] == sc[1, 0] and theta[1] == sc[3, 1]
+    tau = (float(theta[0]) + float(theta[1])) / 2
+    assert nb[0] == np.float32(tau - float(theta[0])) and nb[1] == np.float32(tau - float(theta[1]))
+    assert nb[0] < 0 < nb[1]  # the expert with the higher threshold is pushed down
+    # columns that hold the same scores in other orders: one threshold, no
+    # correction -- whatever the previous bias, rate 1 takes it to zero
+    base = rng.normal(size=24).astype(np.float32)
+    zc = np.stack([rng.permutation(base) for _ in range(6)], axis=1)
+    b = rng.uniform(-0.1, 0.1, 6).astype(np.float32)
+    theta, nb = oracle.quantile_bias_update(zc, b, 2, rate=1.0)
+    assert (theta == theta[0]).all() and (nb == 0).all()
+    _, half = oracle.quantile_bias_update(zc, b, 2, rate=0.5)
+    np.testing.assert_array_equal(half, (b.astype(np.float64) * 0.5).astype(np.float32))
+    # a batch routed unevenly (per-expert offsets in the logits): after one
+    # rate-1 update the selection with the new bias spreads the same tokens
+    # more evenly
+    T, E, K = 512, 16, 2
+    z = (rng.normal(size=(T, E)) + np.linspace(-1.5, 1.5, E)).astype(np.float32)
+    c0 = oracle.biased_scores_f32(z, np.zeros(E, np.float32))
+    load0 = np.bincount(oracle.select_experts(c0, K)[0].reshape(-1), minlength=E)
+    _, nb = oracle.quantile_bias_update(z, np.zeros(E, np.float32), K, rate=1.0)
+    load1 = np.bincount(oracle.select_experts(oracle.biased_scores_f32(z, nb), K)[0].reshape(-1),
+                        minlength=E)
+    assert load1.max() < 0.6 * load0.max() and load1.min() > 2 * max(load0.min(), 1)
+
+
 ALL_CHECKS = [
     check_sigmoid_closed_forms, check_silu, check_bf16_upcast, check_biased_scores_fp32,
     check_select_plain_bruteforce, check_select_grouped_bruteforce, check_group_special_cases,
     check_masked_fill_is_literal_zero, check_weights, check_router_from_x, check_permute,
     check_swiglu_expert, check_dense_reduction, check_layer_routing_weights,
     check_k3_composition, check_page_figures, check_gaps, check_combine, check_dense_gates,
-    check_bias_update,
+    check_bias_update, check_quantile_bias,
 ]
 
 
@@ -571,6 +635,21 @@ def _combine_by_perm(Y, inv, w, Y_shared=None):
     return mo._orig_combine(Y, perm, w, Y_shared)
 
 
+def _qb_variant(z32, bias32, K, rate=1.0, rank_shift=0, sign=1, biased=False, smallest=False):
+    z32 = np.asarray(z32, dtype=np.float32)
+    T, E = z32.shape
+    s32 = mo.round_f32(mo.sigmoid(z32.astype(np.float64)))
+    if biased:
+        s32 = s32 + np.asarray(bias32, np.float32)[None, :]
+    r = min(T, -(-(T * K) // E) + rank_shift)
+    srt = np.sort(s32, axis=0) if smallest else -np.sort(-s32, axis=0)
+    theta = srt[r - 1].astype(np.float32)
+    tau = sum(float(v) for v in theta) / E
+    b = np.asarray(bias32, np.float32).astype(np.float64)
+    new = b + float(np.float32(rate)) * (sign * (tau - theta.astype(np.float64)) - b)
+    return theta, mo.round_f32(new)
+
+
 MUTANTS = {
     "sigmoid_not_logistic": ("sigmoid", _softmax_like),
     "gate_up_swapped": ("swiglu_expert", _swapped_swiglu),
@@ -585,6 +664,15 @@ MUTANTS = {
     "gaps_ignore_group_decision": ("selection_gaps", _gaps_without_groups),
     "gaps_group_rank_shifted": ("selection_gaps", _gaps_group_rank_shifted),
     "combine_reads_perm": ("combine", _combine_by_perm),
+    "qb_rank_off_by_one": ("quantile_bias_update",
+                           lambda z, b, K, rate=1.0: _qb_variant(z, b, K, rate, rank_shift=1)),
+    "qb_sign_flipped": ("quantile_bias_update",
+                        lambda z, b, K, rate=1.0: _qb_variant(z, b, K, rate, sign=-1)),
+    "qb_quantile_of_biased_scores": ("quantile_bias_update",
+                                     lambda z, b, K, rate=1.0: _qb_variant(z, b, K, rate,
+                                                                           biased=True)),
+    "qb_smallest_scores": ("quantile_bias_update",
+                           lambda z, b, K, rate=1.0: _qb_variant(z, b, K, rate, smallest=True)),
 }
 
 
