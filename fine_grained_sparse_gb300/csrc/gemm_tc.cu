@@ -46,6 +46,9 @@
 //   warps 3..10: epilogue, warp w reads lane quadrant w%4 of accumulator
 //   (w-3)/4, or of the single accumulator's column chunks (w-3)/4, 2 + ...
 //   (TMEM -> registers -> global stores);
+//   bf16 single-CTA form, warp 11 lane 0: with token tiles of 128 rows or
+//   more, the MMA issuer of the second accumulator (warp 1 then issues the
+//   first's only; see the MMA issuers);
 //   FP8 weights only, warps 11..14: converters (FP8 stage -> bf16 stage).
 // A segment with implicit token tiles whose weights fit in L2 may instead
 // take its units token-tile-major (GemmSegment::b_major).
@@ -70,6 +73,9 @@ constexpr int kBBoxRows = 32;
 constexpr uint32_t kBBoxBytes = kBBoxRows * 128;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (3 + kEpiWarps);
+// bf16 single-CTA form: a twelfth warp issues the MMAs of the second
+// accumulator (see the kernel's MMA issuers)
+constexpr int kThreadsTwo = kThreads + 32;
 // FP8 weights: four more warps convert each landed FP8 stage into the bf16
 // weight ring (one warp per SM sub-partition)
 constexpr int kConvWarps = 4;
@@ -333,8 +339,11 @@ __device__ __forceinline__ uint32_t acc_column(const Regions& r, int acc) {
 // tile becomes bf16 byte offset 2 o), fence for the tensor cores' proxy and
 // arrive on the k step's full barrier in place of the weight producer.
 template <bool kPair, bool kFp8>
-__global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
+__global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : (kPair ? kThreads : kThreadsTwo), 1)
     tc_gemm_kernel(const __grid_constant__ GemmParams p) {
+  // two MMA issuers, one per accumulator (single-CTA bf16 form, large token
+  // tiles: GemmParams::two)
+  const bool two_issuers = !kPair && !kFp8 && p.two;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -390,18 +399,18 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
       // the two producers' arrivals (CTA 0's in a pair), or the token
       // producer's and the converter warps'
       mbar_init(a_full(s), kFp8 ? 1 + kConvWarps : 2);
-      mbar_init(a_empty(s), 1);
+      mbar_init(a_empty(s), two_issuers ? 2 : 1);  // each MMA issuer's commit
     }
     for (int s = 0; s < s8_n; ++s) {
       mbar_init(f8full(s), 1);
       mbar_init(f8empty(s), kConvWarps);
     }
     for (int r = 0; r < 2; ++r) {
-      mbar_init(tfull_bar(r), 1);
+      mbar_init(tfull_bar(r), two_issuers ? 2 : 1);
       // paired: both CTAs' epilogue warps release CTA 0's regions
       mbar_init(tempty_bar(r), kPair ? 2 * kEpiWarps : kEpiWarps);
     }
-    mbar_init(drain_bar, 1);
+    mbar_init(drain_bar, two_issuers ? 2 : 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -589,8 +598,17 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
       const uint32_t par = static_cast<uint32_t>((q / sa_n) & 1);
       if (!drain_wait(a_empty(st), par, p.status)) break;
     }
-  } else if (warp == 1 && lane == 0 && rank == 0) {
-    // ------------------------------------------------------- MMA issuer
+  } else if ((warp == 1 || (two_issuers && warp == 3 + kEpiWarps)) && lane == 0 && rank == 0) {
+    // ------------------------------------------------------- MMA issuers
+    // With two_issuers warp 1 issues the MMAs of accumulator 0 and the last
+    // warp those of accumulator 1, each followed by its own commit: one
+    // thread issuing a k step's 8 MMAs and its commit takes about twice the
+    // tensor time of an N <= 176 k step, two threads issuing 4 each keep up
+    // with it.  Both wait for every stage and both commits free it (a_empty
+    // counts 2); the accumulation order of each accumulator is unchanged.
+    // Each issuer also commits to every TMEM region the unit fills, so those
+    // count 2 as well.
+    const int my_acc = warp == 1 ? 0 : 1;
     int sa = 0, sb = 0;
     uint32_t pa = 0;
     int c = 0;
@@ -601,11 +619,17 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
       if (u + u_step < total) nx = decode_unit(p, u + u_step, units0, units1, rank);
       const uint32_t n = static_cast<uint32_t>((x.n_rows + 15) & ~15);
       const Regions rg = regions_of(p, n, c);
-      bool ok = mbar_wait_bounded<kPair>(tempty_bar(c & 1), region_phase(c) ^ 1u, abort_flag,
-                                         p.status);
-      if (ok && rg.big)
-        ok = mbar_wait_bounded(tempty_bar((c + 1) & 1), region_phase(c + 1) ^ 1u, abort_flag,
-                               p.status);
+      bool ok;
+      if (two_issuers) {  // the region this issuer's accumulator lives in
+        const int use = rg.big ? c + my_acc : c;
+        ok = mbar_wait_bounded(tempty_bar(use & 1), region_phase(use) ^ 1u, abort_flag, p.status);
+      } else {
+        ok = mbar_wait_bounded<kPair>(tempty_bar(c & 1), region_phase(c) ^ 1u, abort_flag,
+                                      p.status);
+        if (ok && rg.big)
+          ok = mbar_wait_bounded(tempty_bar((c + 1) & 1), region_phase(c + 1) ^ 1u, abort_flag,
+                                 p.status);
+      }
       if (!ok) break;
       tc_fence_after();
       const uint32_t idesc = idesc_bf16_f32(kPair ? 256 : 128, n);
@@ -616,7 +640,9 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
         }
         tc_fence_after();
         const uint64_t bdesc = smem_desc_sw128(b_base + sb * b_stage_bytes);
-        for (int a = 0; a < (kPair ? 1 : x.n_a); ++a) {
+        const int a_lo = two_issuers ? my_acc : 0;
+        const int a_hi = two_issuers ? min(my_acc + 1, x.n_a) : (kPair ? 1 : x.n_a);
+        for (int a = a_lo; a < a_hi; ++a) {
           const uint64_t adesc = smem_desc_sw128(a_base + sa * a_stage_bytes + a * kATileBytes);
           const uint32_t d = tmem_base + acc_column(rg, a);
 #pragma unroll
@@ -709,7 +735,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
       }
       if (!ok) break;
     }
-  } else if (warp >= 3) {
+  } else if (warp >= 3 && warp < 3 + kEpiWarps) {
     // ---------------------------------------------------------- epilogue
     const int q = warp & 3;           // TMEM lane quadrant this warp may access
     const int grp = (warp - 3) >> 2;  // warp group: accumulator (two-tile units)
@@ -1130,6 +1156,10 @@ cudaError_t launch_tc_gemm(const GemmParams& params, int num_sms, cudaStream_t s
   if (p.fp8 && plan.f8_stages < 2) return cudaErrorInvalidValue;
   p.a_stages = plan.a_stages;
   p.b_stages = plan.b_stages;
+  // two MMA issuers where token tiles are large enough for the single
+  // issuer's per-k-step cost to show (with 32-token tiles the weight stream
+  // sets the pace and the second commit per stage only delays its release)
+  p.two = (!p.pair && !p.fp8 && p.nt >= 128) ? 1 : 0;
   p.f8_stages = plan.f8_stages;
   if (p.pair)
     for (int i = 0; i < p.nseg; ++i)
@@ -1169,7 +1199,7 @@ cudaError_t launch_tc_gemm(const GemmParams& params, int num_sms, cudaStream_t s
   if (p.fp8)
     return launch_pdl(tc_gemm_kernel<false, true>, dim3(num_sms), dim3(kThreadsFp8),
                       plan.smem_bytes, stream, p);
-  return launch_pdl(tc_gemm_kernel<false, false>, dim3(num_sms), dim3(kThreads), plan.smem_bytes,
+  return launch_pdl(tc_gemm_kernel<false, false>, dim3(num_sms), dim3(kThreadsTwo), plan.smem_bytes,
                     stream, p);
 }
 

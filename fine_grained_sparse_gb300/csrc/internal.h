@@ -196,6 +196,9 @@ struct GemmParams {
   // f8_stages FP8 stages and converter warps write the bf16 weight ring
   int fp8;
   int f8_stages;
+  // 1: the MMAs of the two accumulators are issued by two threads, each
+  // committing its own (set by launch_tc_gemm for large token tiles)
+  int two;
   int* status;
 };
 
