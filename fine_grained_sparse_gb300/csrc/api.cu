@@ -331,6 +331,8 @@ int32_t set_B(GemmSegment& s, const void* B, int64_t rows, int Kd, int tile) {
   if (encode_tmap_2d_rows(&s.tmB, B, rows, Kd, tile) != CUDA_SUCCESS)
     return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for activations");
   s.b_box_rows = tile;
+  s.b_src = B;
+  s.b_src_rows = rows;
   s.k_steps = Kd / 64;
   return MOE_OK;
 }

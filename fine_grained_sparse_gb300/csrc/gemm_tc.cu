@@ -105,6 +105,7 @@ __device__ __forceinline__ int ksplit_of(const GemmSegment* s) { return s->kspli
 // output blocks of a segment: pairs of A tiles (one unit, or one unit of a
 // CTA pair), or single tiles
 __device__ __forceinline__ int out_blocks(const GemmParams& p, const GemmSegment* s) {
+  if (p.pair && p.a_per_unit == 2) return (s->a128 + 3) / 4;  // four tiles over a CTA pair
   return (p.a_per_unit == 2 || p.pair) ? (s->a128 + 1) / 2 : s->a128;
 }
 
@@ -178,7 +179,10 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int unit
   }
   x.k0 = x.split * kps;
   x.k1 = x.k0 + kps;
-  if (p.a_per_unit == 2) {
+  if (p.pair && p.a_per_unit == 2) {  // CTA `rank` of the pair takes tiles 4 ob + 2 rank, + 1
+    x.blk0 = 4 * x.ob + 2 * rank;
+    x.n_a = max(0, min(2, s->a128 - x.blk0));
+  } else if (p.a_per_unit == 2) {
     x.blk0 = 2 * x.ob;
     x.n_a = min(2, s->a128 - 2 * x.ob);
   } else if (p.pair) {  // CTA `rank` of the pair takes tile 2 ob + rank
@@ -339,11 +343,11 @@ __device__ __forceinline__ uint32_t acc_column(const Regions& r, int acc) {
 // tile becomes bf16 byte offset 2 o), fence for the tensor cores' proxy and
 // arrive on the k step's full barrier in place of the weight producer.
 template <bool kPair, bool kFp8>
-__global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : (kPair ? kThreads : kThreadsTwo), 1)
+__global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreadsTwo, 1)
     tc_gemm_kernel(const __grid_constant__ GemmParams p) {
-  // two MMA issuers, one per accumulator (single-CTA bf16 form, large token
-  // tiles: GemmParams::two)
-  const bool two_issuers = !kPair && !kFp8 && p.two;
+  // two MMA issuers, one per accumulator (bf16 forms, large token tiles:
+  // GemmParams::two)
+  const bool two_issuers = !kFp8 && p.two;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -475,8 +479,9 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : (kPair ? kThreads : kThre
                     s->a_rec + ((x.group * s->a_rec_group) + pair_idx * s->k_steps + ks) * 16, 16,
                     fb, pol_w);
         } else if (kPair) {
-          // CTA 0 expects both CTAs' tiles on its barrier
-          if (rank == 0) mbar_arrive_expect_tx(fb, 2 * kATileBytes);
+          // CTA 0 expects both CTAs' tiles on its barrier (one box: this
+          // CTA's one tile, or its pair of tiles, contiguous at k step ks)
+          if (rank == 0) mbar_arrive_expect_tx(fb, 2 * a_stage_bytes);
           tma_load_2d_pair(a_dst, &s->tmA, lead(fb), 0,
                            static_cast<int>(x.group * (s->a_group_bytes >> 7) + tile * 128), pol_w);
         } else if (s->a_packed) {
@@ -622,7 +627,8 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : (kPair ? kThreads : kThre
       bool ok;
       if (two_issuers) {  // the region this issuer's accumulator lives in
         const int use = rg.big ? c + my_acc : c;
-        ok = mbar_wait_bounded(tempty_bar(use & 1), region_phase(use) ^ 1u, abort_flag, p.status);
+        ok = mbar_wait_bounded<kPair>(tempty_bar(use & 1), region_phase(use) ^ 1u, abort_flag,
+                                      p.status);
       } else {
         ok = mbar_wait_bounded<kPair>(tempty_bar(c & 1), region_phase(c) ^ 1u, abort_flag,
                                       p.status);
@@ -640,8 +646,10 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : (kPair ? kThreads : kThre
         }
         tc_fence_after();
         const uint64_t bdesc = smem_desc_sw128(b_base + sb * b_stage_bytes);
+        // accumulators of this CTA (of each CTA of a pair): its weight tiles
+        const int n_acc = (kPair && p.a_per_unit == 1) ? 1 : x.n_a;
         const int a_lo = two_issuers ? my_acc : 0;
-        const int a_hi = two_issuers ? min(my_acc + 1, x.n_a) : (kPair ? 1 : x.n_a);
+        const int a_hi = two_issuers ? min(my_acc + 1, n_acc) : n_acc;
         for (int a = a_lo; a < a_hi; ++a) {
           const uint64_t adesc = smem_desc_sw128(a_base + sa * a_stage_bytes + a * kATileBytes);
           const uint32_t d = tmem_base + acc_column(rg, a);
@@ -663,6 +671,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : (kPair ? kThreads : kThre
       if (!ok) break;
       if (kPair) {  // both CTAs' accumulators are ready
         tc_commit_pair(tfull_bar(c & 1), kPairMask);
+        if (rg.big) tc_commit_pair(tfull_bar((c + 1) & 1), kPairMask);
       } else {
         tc_commit(tfull_bar(c & 1));
         if (rg.big) tc_commit(tfull_bar((c + 1) & 1));
@@ -1102,19 +1111,30 @@ namespace {
 // copies can do): weights as rows of 128 bytes, one 128-row tile per box;
 // activation planes as (64 columns, plane rows, planes), 32-row boxes.  The
 // data are stored pre-swizzled, so the maps do not swizzle again.
-CUresult encode_pair_maps(GemmSegment& s) {
+CUresult encode_pair_maps(GemmSegment& s, int a_per_unit) {
   auto fn = encode_fn();
   if (!fn) return CUDA_ERROR_NOT_INITIALIZED;
   cuuint32_t estr[3] = {1, 1, 1};
+  // one box per k step: the CTA's weight tile, or its pair of tiles (the
+  // packed bank keeps a pair's tiles of one k step together)
   const cuuint64_t a_dims[2] = {kBK, static_cast<cuuint64_t>(s.a_groups) *
                                          static_cast<cuuint64_t>(s.a_group_bytes / 128)};
   const cuuint64_t a_strides[1] = {128};
-  const cuuint32_t a_box[2] = {kBK, 128};
+  const cuuint32_t a_box[2] = {kBK, static_cast<cuuint32_t>(128 * a_per_unit)};
   CUresult r = fn(&s.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint8_t*>(s.a_packed),
                   a_dims, a_strides, a_box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS || !s.b_packed) return r;
+  if (r != CUDA_SUCCESS) return r;
+  if (!s.b_packed) {
+    // activation rows of a plain tensor map: 32-row boxes for the pair's
+    // halves of a token tile (128-byte swizzle, as the MMA reads them)
+    if (!s.b_src) return CUDA_ERROR_INVALID_VALUE;
+    return encode_tmap_2d_rows(&s.tmB, s.b_src, s.b_src_rows, 64ll * s.k_steps, kBBoxRows) ==
+                   CUDA_SUCCESS
+               ? CUDA_SUCCESS
+               : CUDA_ERROR_INVALID_VALUE;
+  }
   const cuuint64_t b_dims[3] = {kBK, static_cast<cuuint64_t>(s.b_plane_rows),
                                 static_cast<cuuint64_t>(s.k_steps)};
   const cuuint64_t b_strides[2] = {128, static_cast<cuuint64_t>(s.b_plane_rows) * 128};
@@ -1151,7 +1171,12 @@ cudaError_t launch_tc_gemm(const GemmParams& params, int num_sms, cudaStream_t s
     if ((p.seg[i].a_fp8 != 0) != (p.fp8 != 0) || (p.seg[i].a_fp8 && !p.seg[i].a_packed))
       return cudaErrorInvalidValue;
   p.pair = (!p.fp8 && params.pair && pair_capable(params) && num_sms >= 2) ? 1 : 0;
-  p.a_per_unit = (p.fp8 || !(p.pair || params.a_per_unit == 1)) ? 2 : 1;
+  // pairs take two weight tiles per CTA (four per unit) when every segment
+  // has a multiple of four 128-row tiles, else one
+  bool pair_two = p.pair != 0;
+  for (int i = 0; i < p.nseg; ++i)
+    if (p.seg[i].a128 % 4) pair_two = false;
+  p.a_per_unit = p.fp8 ? 2 : p.pair ? (pair_two ? 2 : 1) : (params.a_per_unit == 1 ? 1 : 2);
   const GemmPlan plan = p.fp8 ? plan_gemm_fp8(p.nt) : plan_gemm(p.nt, p.a_per_unit, p.pair != 0);
   if (p.fp8 && plan.f8_stages < 2) return cudaErrorInvalidValue;
   p.a_stages = plan.a_stages;
@@ -1159,11 +1184,11 @@ cudaError_t launch_tc_gemm(const GemmParams& params, int num_sms, cudaStream_t s
   // two MMA issuers where token tiles are large enough for the single
   // issuer's per-k-step cost to show (with 32-token tiles the weight stream
   // sets the pace and the second commit per stage only delays its release)
-  p.two = (!p.pair && !p.fp8 && p.nt >= 128) ? 1 : 0;
+  p.two = (!p.fp8 && p.nt >= 128) ? 1 : 0;
   p.f8_stages = plan.f8_stages;
   if (p.pair)
     for (int i = 0; i < p.nseg; ++i)
-      if (encode_pair_maps(p.seg[i]) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+      if (encode_pair_maps(p.seg[i], p.a_per_unit) != CUDA_SUCCESS) return cudaErrorInvalidValue;
   static int configured[64] = {0};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -1183,16 +1208,31 @@ cudaError_t launch_tc_gemm(const GemmParams& params, int num_sms, cudaStream_t s
   if (p.pair) {  // clusters of two CTAs, one CTA per SM
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(num_sms / 2 * 2));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kThreadsTwo);
     cfg.dynamicSmemBytes = plan.smem_bytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    // as many pairs as can be resident at once (a pair's SMs share a GPC):
+    // the units are dealt to the launched pairs in turn, so every pair of the
+    // grid must run from the start
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, tc_gemm_kernel<true, false>, &cfg) !=
+            cudaSuccess ||
+        clusters < 1) {
+      cudaGetLastError();
+      clusters = num_sms / 2;
+    }
+    if (clusters > num_sms / 2) clusters = num_sms / 2;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
     note_launch();
     return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<true, false>, p);
   }

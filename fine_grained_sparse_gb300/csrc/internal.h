@@ -124,6 +124,8 @@ struct GemmSegment {
   CUtensorMap tmA;  // weights (see gemm_tc.cu for the layouts)
   CUtensorMap tmB;  // activation rows [rows, K] bf16, box 64 x b_box_rows
   int b_box_rows;   // rows of one tmB box: a whole token tile in one copy
+  const void* b_src;   // the rows tmB maps (re-encoded with 32-row boxes for
+  int64_t b_src_rows;  // CTA pairs, which load half tiles)
   int a_box_rows;   // store-mode weights read through tmA: 128 (a box per
                     // tile) or 256 (both tiles of a unit in one copy)
   int k_steps;      // A's K / 64
