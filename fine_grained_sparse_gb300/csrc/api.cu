@@ -384,6 +384,10 @@ struct ExpertIO {
   const void* Ws_down;
   void* Y;               // [T*K, d_e]
   void* Y_shared;        // [S, T, d] or null
+  // the routing in token order (both or neither): lets the bf16 gather read
+  // each token row once and write its K copies
+  const int32_t* topk_idx = nullptr;
+  const int32_t* inv = nullptr;
 };
 
 // The shared experts' gate/up pass as a GEMM segment: every token of x
@@ -443,7 +447,10 @@ int32_t run_experts(const moe_config* c, int64_t T, const ExpertIO& io, void* ws
     ntiles_down = ntiles + 1;
     MOE_CUDA(launch_build_tiles(io.offsets, E, nt_down, tiles_down, ntiles_down, nullptr, st));
   }
-  if (bf16) {
+  if (bf16 && io.topk_idx && io.inv) {
+    MOE_CUDA(launch_gather_tokens_packed(io.x_e, T, K, de, io.topk_idx, io.inv, io.offsets,
+                                         poffsets, E, io.topk_w, Xp, L.plane_rows, w_perm, st));
+  } else if (bf16) {
     MOE_CUDA(launch_gather_packed(io.x_e, K, de, io.perm, io.offsets, poffsets, E, io.topk_w, Xp,
                                   L.plane_rows, w_perm, st));
   } else {
@@ -1074,6 +1081,8 @@ int32_t moe_layer_forward(const moe_config* cfg, int64_t T, const void* x, const
   }
   ExpertIO io = {x_e, offsets, perm, w, W_gate_up, W_down, S ? x : nullptr, Ws_gate_up, Ws_down,
                  at<void>(ws, L.Y), S ? at<void>(ws, L.Ysh) : nullptr};
+  io.topk_idx = idx;
+  io.inv = inv;
   st = run_experts(cfg, T, io, ws, ev(2), ev(3), s, false);
   if (st != MOE_OK) return st;
   if (ev(4)) MOE_CUDA(cudaEventRecord(ev(4), s));

@@ -23,6 +23,9 @@
 //   gather_packed_kernel  Xp[r] = x[perm[r] / K] in the packed plane layout
 //                     the tensor cores read (x read with an L2 evict-last
 //                     hint, Xp written evict-first), w_perm[r] = topk_w[perm[r]]
+//   gather_tokens_packed_kernel  the same rows written in token order: x[t]
+//                     read once, stored to the padded rows of its K pairs
+//                     (the layer forward, which has topk_idx and inv)
 //   gather_kernel     the same in plain rows (fp32 layers)
 //   combine_kernel    y[t] = sum_k w[t, k] Y[inv[t K + k]] + dense addends, fp32
 //                     sums in that order (w = 1 when absent); a slot outside
@@ -249,6 +252,59 @@ __global__ void __launch_bounds__(256) gather_packed_kernel(
   }
 }
 
+// Packed gather in token order: one warp per token t reads x[t] once and
+// writes it to the padded rows of its K pairs (the pair of slot
+// s = inv[t K + k] and expert e = topk_idx[t K + k] sits in padded row
+// poffsets[e] + s - offsets[e]), seven 16-byte vectors per lane at a time.
+// Pairs whose expert index was rejected (inv = -1) are skipped.  Same layout
+// as gather_packed_kernel; each x row is read from memory once instead of
+// once per pair.
+__global__ void __launch_bounds__(256) gather_tokens_packed_kernel(
+    const uint4* __restrict__ x, int64_t T, int K, int vec_per_row,
+    const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ inv,
+    const int32_t* __restrict__ offsets, const int32_t* __restrict__ poffsets, int E,
+    const float* __restrict__ topk_w, uint4* __restrict__ Xp, int64_t plane_rows,
+    float* __restrict__ w_perm) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t warp_global = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int64_t rows = static_cast<int64_t>(T) * K;
+  constexpr int kV = 7;  // vectors per lane per round (16 B each)
+  const uint64_t pass = l2_policy_evict_first();
+  for (int64_t t = warp_global; t < T; t += nwarps) {
+    // lane k (< K) finds its pair's padded row; the warp shares them
+    int64_t myR = -1;
+    if (lane < K) {
+      const int64_t j = t * K + lane;
+      const int s = __ldg(inv + j);
+      const int e = __ldg(topk_idx + j);
+      if (s >= 0 && s < rows && e >= 0 && e < E) {
+        myR = __ldg(poffsets + e) + (s - __ldg(offsets + e));
+        if (w_perm) w_perm[s] = topk_w ? __ldg(topk_w + j) : 1.0f;
+      }
+    }
+    const uint4* src = x + t * vec_per_row;
+    for (int v0 = lane; v0 < vec_per_row; v0 += 32 * kV) {
+      uint4 d[kV];
+#pragma unroll
+      for (int u = 0; u < kV; ++u)
+        if (v0 + 32 * u < vec_per_row) d[u] = __ldg(src + v0 + 32 * u);
+      for (int k = 0; k < K; ++k) {
+        const int64_t R = __shfl_sync(0xffffffffu, myR, k);
+        if (R < 0) continue;
+        const int sw = static_cast<int>(R & 7);
+#pragma unroll
+        for (int u = 0; u < kV; ++u) {
+          const int v = v0 + 32 * u;
+          if (v < vec_per_row)
+            st_global_hint(Xp + ((v >> 3) * plane_rows + R) * 8 + ((v & 7) ^ sw), d[u], pass);
+        }
+      }
+    }
+  }
+}
+
 // One warp per row, 16-byte vectors.
 __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x, int K,
                                                      int vec_per_row,
@@ -437,6 +493,20 @@ cudaError_t launch_gather_packed(const void* x, int K, int width, const int32_t*
   return launch_pdl(gather_packed_kernel, dim3(sms * 8), dim3(256), 0, stream,
                     static_cast<const uint4*>(x), K, width / 8, perm, offsets, poffsets, E, topk_w,
                     static_cast<uint4*>(Xp), plane_rows, w_perm);
+}
+
+cudaError_t launch_gather_tokens_packed(const void* x, int64_t T, int K, int width,
+                                        const int32_t* topk_idx, const int32_t* inv,
+                                        const int32_t* offsets, const int32_t* poffsets, int E,
+                                        const float* topk_w, void* Xp, int64_t plane_rows,
+                                        float* w_perm, cudaStream_t stream) {
+  if (T <= 0) return cudaSuccess;
+  const int64_t blocks = (T + 7) / 8;  // a warp per token
+  return launch_pdl(gather_tokens_packed_kernel,
+                    dim3(static_cast<unsigned>(blocks < 65535 * 16 ? blocks : 65535 * 16)),
+                    dim3(256), 0, stream, static_cast<const uint4*>(x), T, K, width / 8, topk_idx,
+                    inv, offsets, poffsets, E, topk_w, static_cast<uint4*>(Xp), plane_rows,
+                    w_perm);
 }
 
 cudaError_t launch_gather(const void* x, int64_t T, int K, int width, int elem_bytes,

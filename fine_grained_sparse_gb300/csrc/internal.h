@@ -99,6 +99,13 @@ cudaError_t launch_gather_packed(const void* x, int K, int width, const int32_t*
                                  const float* topk_w, void* Xp, int64_t plane_rows,
                                  float* w_perm, cudaStream_t stream);
 int64_t max_tiles(int64_t rows, int E, int nt);
+// The same packed rows written in token order: each x row is read once and
+// stored to the padded rows of its K pairs (from topk_idx and inv).
+cudaError_t launch_gather_tokens_packed(const void* x, int64_t T, int K, int width,
+                                        const int32_t* topk_idx, const int32_t* inv,
+                                        const int32_t* offsets, const int32_t* poffsets, int E,
+                                        const float* topk_w, void* Xp, int64_t plane_rows,
+                                        float* w_perm, cudaStream_t stream);
 
 // Xp[r] = x[perm[r] / K] and w_perm[r] = topk_w[perm[r]] (1 if topk_w null)
 // for r < rows (rows = offsets[E] read on the device).
