@@ -71,38 +71,41 @@ int env_int(const char* name, int fallback) {
 
 int router_tile(int64_t T);
 
-// K parts of the router GEMM (a multiple of 3: the split weight's three
-// bf16 terms are separate parts): the fewest parts that give the GEMM about
-// 2.4 waves of units on a 152-SM GB300 (a fixed count, so that a workspace
-// sized on one device fits the call on another), at most 48.  One wave or
-// less leaves SMs idle at the end; more parts cost partial-logit traffic.
+// K parts of the router GEMM: the count (at most 48, at most d / 64) that
+// minimises an estimate of its time on a 152-SM GB300 (a fixed count, so
+// that a workspace sized on one device fits the call on another): the waves
+// of units times the k steps of the longest part at 12 MMAs of N = tile per
+// k step (one per weight piece and 16-wide k slice; about max(N/2, 59)
+// cycles each), plus the partial logits written and read back at the HBM
+// rate (about 3.6 KB per cycle).  One wave with all SMs busy and few parts
+// wins; each extra part costs T E 8 bytes of traffic.
 int router_ksplit(int64_t T, int d, int E) {
   static const int forced = env_int("FGS_ROUTER_KSPLIT", 0);  // tuning override
   const int kd = d / 64;
-  if (forced >= 3 && forced % 3 == 0 && kd % (forced / 3) == 0) return forced;
+  const int pmax = kd < 48 ? kd : 48;
+  if (forced >= 1 && forced <= pmax) return forced;
   const int64_t nt = router_tile(T);
-  const int64_t per_part = ((T + nt - 1) / nt) * (((E + 127) / 128 + 1) / 2);
+  const int64_t per_part = ((T + nt - 1) / nt) * ((E + 127) / 128);
+  const double kstep_clk = 12.0 * (nt / 2 > 59 ? nt / 2 : 59);
   int best = 1;
-  for (int c = 1; c <= 16; ++c) {
-    if (kd % c) continue;
-    best = c;
-    if (per_part * 3 * c * 10 >= 24 * 152) break;
+  double best_cost = 0.0;
+  for (int P = 1; P <= pmax; ++P) {
+    const int64_t rounds = (per_part * P + 151) / 152;
+    const int64_t steps = (kd + P - 1) / P;
+    const double cost = static_cast<double>(rounds * steps) * kstep_clk +
+                        8.0 * P * static_cast<double>(T) * E / 3571.0;
+    if (P == 1 || cost < best_cost) {
+      best = P;
+      best_cost = cost;
+    }
   }
-  return 3 * best;
-}
-
-// Weight tiles per router GEMM unit: two (each token tile in shared memory
-// feeds two weight tiles), although a 384-expert router then has units of
-// two and of one tile.
-int router_a_per_unit() {
-  static const int forced = env_int("FGS_ROUTER_A", 2);  // tuning override
-  return forced == 1 ? 1 : 2;
+  return best;
 }
 
 int router_tile(int64_t T) {
   static const int forced = env_int("FGS_ROUTER_TILE", 0);  // tuning override
   if (forced == 32 || forced == 64 || forced == 128 || forced == 256) return forced;
-  return T <= 256 ? 32 : 128;
+  return T <= 256 ? 32 : 256;
 }
 
 // Unit order of a segment with implicit token tiles: token-tile-major when
@@ -615,6 +618,42 @@ int32_t run_linear(int64_t T, int in_f, int out_f, const void* x, const void* W,
   return MOE_OK;
 }
 
+// The router logits GEMM: partial logits part j = x W_split^T over k steps
+// [j K / P, (j + 1) K / P) of K = d / 64, where W_split [E, 3 d] holds the
+// hi, mid and lo bf16 pieces of W_r side by side; the three pieces of a
+// k step accumulate into the unit's one accumulator, so each token tile in
+// shared memory feeds all three.
+int32_t router_gemm(const void* x, const void* w_split, int64_t T, int d, int E, int parts,
+                    float* logits, int* status, cudaStream_t st) {
+  GemmParams p;
+  memset(&p, 0, sizeof(p));
+  p.mode = kModeStore;
+  p.nt = router_tile(T);
+  p.a_per_unit = 1;
+  p.pieces = 3;
+  p.status = status;
+  p.nseg = 1;
+  GemmSegment& g = p.seg[0];
+  clear(g);
+  if (encode_tmap_weights_3d(&g.tmA, w_split, 1, E, 3ll * d, 128) != CUDA_SUCCESS)
+    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for the split router weight");
+  int32_t e;
+  if ((e = set_B(g, x, T, d, p.nt)) != MOE_OK) return e;
+  g.k_steps = d / 64;
+  g.a_piece_cols = d;
+  g.a128 = (E + 127) / 128;
+  g.o_limit = E;
+  g.groups = 1;
+  g.rows = static_cast<int>(T);
+  g.out_f32 = logits;
+  g.out_ld = E;
+  g.ksplit = parts;
+  g.b_major = prefer_b_major(6ll * E * d, 2ll * T * d);
+  g.out_split_stride = T * E;
+  MOE_CUDA(launch_tc_gemm(p, num_sms(), st));
+  return MOE_OK;
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -697,15 +736,11 @@ size_t noalloc_need(int64_t T, int d, int E, bool presplit, int parts) {
 }
 
 // K parts of the allocation-free router GEMM: moe_router's own count when
-// that fits the static scratch, else the largest smaller count (a multiple
-// of 3 whose third divides d / 64) that fits; 0 when none does.
+// that fits the static scratch, else the largest smaller count that fits;
+// 0 when none does.
 int noalloc_ksplit(int64_t T, int d, int E, bool presplit) {
-  const int p0 = router_ksplit(T, d, E);
-  const int kd = d / 64;
-  for (int c = p0 / 3; c >= 1; --c) {
-    if (kd % c) continue;
-    if (noalloc_need(T, d, E, presplit, 3 * c) <= kNoAllocScratchBytes) return 3 * c;
-  }
+  for (int c = router_ksplit(T, d, E); c >= 1; --c)
+    if (noalloc_need(T, d, E, presplit, c) <= kNoAllocScratchBytes) return c;
   return 0;
 }
 
@@ -824,35 +859,12 @@ int32_t moe_router(const moe_config* cfg, int64_t T, const void* x, const float*
     const int d = cfg->d_model, E = cfg->E_routed;
     if (!presplit)
       MOE_CUDA(launch_split_router_weight(W_r, E, d, at<__nv_bfloat16>(workspace, L.w_split), s));
-    GemmParams p;
-    memset(&p, 0, sizeof(p));
-    p.mode = kModeStore;
-    p.nt = router_tile(T);
-    p.a_per_unit = router_a_per_unit();
-    p.status = at<int>(workspace, L.status);
-    p.nseg = 1;
-    GemmSegment& g = p.seg[0];
-    clear(g);
-    // a unit's weight tiles in one box, its token tile in another
-    g.a_box_rows = 128 * p.a_per_unit;
-    if (encode_tmap_weights_3d(&g.tmA, w_split, 1, E, 3ll * d, g.a_box_rows) != CUDA_SUCCESS)
-      return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for the split router weight");
-    int32_t e;
-    if ((e = set_B(g, x, T, d, p.nt)) != MOE_OK) return e;
-    g.k_steps = 3 * d / 64;
-    g.b_k_period = d / 64;
-    g.a128 = (E + 127) / 128;
-    g.o_limit = E;
-    g.groups = 1;
-    g.rows = static_cast<int>(T);
-    g.out_f32 = logits;
-    g.out_ld = E;
-    g.ksplit = router_ksplit(T, d, E);
-    g.b_major = prefer_b_major(6ll * E * d, 2ll * T * d);
-    g.out_split_stride = T * E;
-    MOE_CUDA(launch_tc_gemm(p, num_sms(), s));
+    const int parts = router_ksplit(T, d, E);
+    const int32_t e =
+        router_gemm(x, w_split, T, d, E, parts, logits, at<int>(workspace, L.status), s);
+    if (e != MOE_OK) return e;
     a.logits = logits;
-    a.logit_parts = g.ksplit;
+    a.logit_parts = parts;
     a.logit_part_stride = T * E;
   } else {
     a.x = x;
@@ -1248,7 +1260,7 @@ int32_t moe_router_noalloc(const moe_config* cfg, int64_t T, const void* x, cons
   if (ksplit == 0) {
     snprintf(g_detail, sizeof(g_detail),
              "moe_router_noalloc needs %zu bytes of scratch; its static scratch holds %zu",
-             noalloc_need(T, d, E, presplit, 3), kNoAllocScratchBytes);
+             noalloc_need(T, d, E, presplit, 1), kNoAllocScratchBytes);
     return MOE_ERR_WORKSPACE;
   }
   const size_t split_off = kWsHeader;
@@ -1264,31 +1276,7 @@ int32_t moe_router_noalloc(const moe_config* cfg, int64_t T, const void* x, cons
   // start at zero (the split weight and every partial logit are rewritten)
   MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(int), s));
   if (!presplit) MOE_CUDA(launch_split_router_weight(W_r, E, d, w_scratch, s));
-  GemmParams p;
-  memset(&p, 0, sizeof(p));
-  p.mode = kModeStore;
-  p.nt = router_tile(T);
-  p.a_per_unit = router_a_per_unit();
-  p.status = status;
-  p.nseg = 1;
-  GemmSegment& g = p.seg[0];
-  clear(g);
-  g.a_box_rows = 128 * p.a_per_unit;
-  if (encode_tmap_weights_3d(&g.tmA, w_split, 1, E, 3ll * d, g.a_box_rows) != CUDA_SUCCESS)
-    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for the split router weight");
-  if ((st = set_B(g, x, T, d, p.nt)) != MOE_OK) return st;
-  g.k_steps = 3 * d / 64;
-  g.b_k_period = d / 64;
-  g.a128 = (E + 127) / 128;
-  g.o_limit = E;
-  g.groups = 1;
-  g.rows = static_cast<int>(T);
-  g.out_f32 = logits;
-  g.out_ld = E;
-  g.ksplit = ksplit;
-  g.b_major = prefer_b_major(6ll * E * d, 2ll * T * d);
-  g.out_split_stride = T * E;
-  MOE_CUDA(launch_tc_gemm(p, num_sms(), s));
+  if ((st = router_gemm(x, w_split, T, d, E, ksplit, logits, status, s)) != MOE_OK) return st;
   RouterArgs a;
   a.logits = logits;
   a.logit_parts = ksplit;

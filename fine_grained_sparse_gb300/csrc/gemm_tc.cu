@@ -52,6 +52,13 @@
 //   FP8 weights only, warps 11..14: converters (FP8 stage -> bf16 stage).
 // A segment with implicit token tiles whose weights fit in L2 may instead
 // take its units token-tile-major (GemmSegment::b_major).
+// Split weights (GemmParams::pieces = R > 1; the router, whose fp32 weight is
+// held as three bf16 pieces side by side along K): units of one weight tile,
+// and each k step is R weight steps -- the unit's tile of piece 0, 1, ... at
+// that k step, each a 16 KB stage -- against one token stage, all
+// accumulated into the unit's one accumulator.  The token tile is thus read
+// into shared memory once for the R pieces; the weight producer arrives for
+// the token producer on the full barriers of pieces 1 .. R-1.
 // Every wait is bounded (%globaltimer); on expiry the CTA records
 // MOE_ERR_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
 #include <cudaTypedefs.h>
@@ -128,7 +135,6 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int unit
   const int nt = s->nt;
   const int OB = out_blocks(p, s);
   const int ns = ksplit_of(s);
-  const int kps = s->k_steps / ns;
   x.split = 0;
   if (ns > 1 && !s->b_major) {  // the K part is the outermost index of a split segment
     const int per = s->groups * ((s->rows + nt - 1) / nt) * OB;
@@ -177,8 +183,14 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int unit
     x.scale_row = x.out_row;
     x.ntiles = tpg;
   }
-  x.k0 = x.split * kps;
-  x.k1 = x.k0 + kps;
+  // part j of a split K: k steps [j K / ns, (j + 1) K / ns)
+  if (ns > 1) {
+    x.k0 = static_cast<int>(static_cast<int64_t>(x.split) * s->k_steps / ns);
+    x.k1 = static_cast<int>(static_cast<int64_t>(x.split + 1) * s->k_steps / ns);
+  } else {
+    x.k0 = 0;
+    x.k1 = s->k_steps;
+  }
   if (p.pair && p.a_per_unit == 2) {  // CTA `rank` of the pair takes tiles 4 ob + 2 rank, + 1
     x.blk0 = 4 * x.ob + 2 * rank;
     x.n_a = max(0, min(2, s->a128 - x.blk0));
@@ -354,6 +366,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreadsTwo, 1)
   const int sa_n = p.a_stages;
   const int sb_n = p.b_stages;
   const int nt = p.nt;
+  const int R = p.pieces > 1 ? p.pieces : 1;  // weight steps per k step
   const uint32_t b_stage_bytes = b_stage_bytes_of(nt, kPair);
   const uint32_t a_stage_bytes = kATileBytes * static_cast<uint32_t>(p.a_per_unit);
   const int s8_n = kFp8 ? p.f8_stages : 0;
@@ -456,7 +469,8 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreadsTwo, 1)
       // a token-tile-major segment's weights serve every token tile
       const uint64_t pol_w = s->b_major ? pol_keep : x.ntiles > 1 ? pol_normal : pol_stream;
       bool ok = true;
-      for (int ks = x.k0; ks < x.k1; ++ks) {
+      // weight steps: k step ks, piece pc (pc fastest)
+      for (int ks = x.k0, pc = 0; ks < x.k1; pc + 1 < R ? ++pc : (pc = 0, ++ks)) {
         if (!mbar_wait_bounded(slot_free(stage), phase ^ 1u, abort_flag, p.status)) {
           ok = false;
           break;
@@ -488,10 +502,14 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreadsTwo, 1)
           mbar_arrive_expect_tx(fb, tx);
           bulk_load(a_dst, s->a_packed + x.group * s->a_group_bytes + tile * kATileBytes, tx, fb,
                     pol_w);
-        } else if (s->mode != kModeSwiGLU && s->a_box_rows == 256) {
-          // both 128-row tiles of the unit in one box (rows past O read as 0)
-          mbar_arrive_expect_tx(fb, 2 * kATileBytes);
-          tma_load_3d(a_dst, &s->tmA, fb, kc, x.blk0 * 128, x.group, pol_w);
+        } else if (R > 1) {
+          // the unit's tile of weight piece pc at k step ks; the token
+          // producer arrives only on a k step's first weight step, so this
+          // thread arrives in its place on the others
+          mbar_arrive_expect_tx(fb, kATileBytes);
+          tma_load_3d(a_dst, &s->tmA, fb, kc + pc * s->a_piece_cols, x.blk0 * 128, x.group,
+                      pol_w);
+          if (pc) mbar_arrive(fb);
         } else {
           mbar_arrive_expect_tx(fb, tx);
           for (int a = 0; a < x.n_a; ++a) {
@@ -532,10 +550,13 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreadsTwo, 1)
       if (kPair || !p.seg[s].b_packed) prefetch_tensormap(&p.seg[s].tmB);
     const uint64_t pol_keep = l2_policy_evict_last();
     const uint64_t pol_normal = l2_policy_evict_normal();
-    int stage = 0, fstage = 0;  // token stage, and the k step's full barrier
-    int estage = 0;             // weight stage of k step issued - Sb
+    int stage = 0;       // token stage
+    int64_t issued = 0;  // token stages issued: stage i goes with weight steps R i .. R i + R - 1
+    int fstage = 0;      // weight stage of weight step R issued (its full barrier)
+    // weight stage and phase of weight step R (issued - Sb) + R - 1, the last
+    // reader of the token stage about to be refilled
+    int estage = R - 1;
     uint32_t ephase = 0;
-    int64_t issued = 0;
     Unit nx = u_first < total ? decode_unit(p, u_first, units0, units1, rank) : Unit{};
     for (int u = u_first; u < total; u += u_step) {
       // the next unit's tile-table loads overlap this unit's work
@@ -560,47 +581,49 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreadsTwo, 1)
                                         : static_cast<uint32_t>(nbox * br) * 128u;
       bool ok = true;
       for (int ks = x.k0; ks < x.k1; ++ks) {
-        if (issued >= sb_n) {  // token stage free once k step issued - Sb was consumed
+        if (issued >= sb_n) {
+          // the token stage is free once the last weight step that read it
+          // (that of token stage issued - Sb) was consumed
           if (!mbar_wait_bounded(a_empty(estage), ephase, abort_flag, p.status)) {
             ok = false;
             break;
           }
-          if (++estage == sa_n) {
-            estage = 0;
+          if ((estage += R) >= sa_n) {
+            estage -= sa_n;
             ephase ^= 1u;
           }
         }
         const uint32_t fb = a_full(fstage);
         if (!kPair || rank == 0) mbar_arrive_expect_tx(fb, tx);
         const uint32_t b_dst = b_base + stage * b_stage_bytes;
-        const int kstep = s->b_k_period ? ks % s->b_k_period : ks;
         if (kPair) {
           for (int bx = 0; bx < nbox; ++bx) {
             if (s->b_packed)
               tma_load_3d_pair(b_dst + bx * kBBoxBytes, &s->tmB, lead(fb), 0,
-                               b_row + bx * kBBoxRows, kstep, pol_b);
+                               b_row + bx * kBBoxRows, ks, pol_b);
             else
-              tma_load_2d_pair(b_dst + bx * kBBoxBytes, &s->tmB, lead(fb), kstep * kBK,
+              tma_load_2d_pair(b_dst + bx * kBBoxBytes, &s->tmB, lead(fb), ks * kBK,
                                b_row + bx * kBBoxRows, pol_b);
           }
         } else if (s->b_packed) {
           const uint8_t* src =
-              s->b_packed + (static_cast<int64_t>(kstep) * s->b_plane_rows + b_row) * 128;
+              s->b_packed + (static_cast<int64_t>(ks) * s->b_plane_rows + b_row) * 128;
           bulk_load(b_dst, src, tx, fb, pol_b);
         } else {
           for (int bx = 0; bx < nbox; ++bx)
-            tma_load_2d(b_dst + bx * br * 128u, &s->tmB, fb, kstep * kBK, b_row + bx * br, pol_b);
+            tma_load_2d(b_dst + bx * br * 128u, &s->tmB, fb, ks * kBK, b_row + bx * br, pol_b);
         }
         ++issued;
-        if (++fstage == sa_n) fstage = 0;
+        if ((fstage += R) >= sa_n) fstage -= sa_n;
         if (++stage == sb_n) stage = 0;
       }
       if (!ok) break;
     }
     const int64_t first = issued > sb_n ? issued - sb_n : 0;
     for (int64_t q = first; q < issued; ++q) {
-      const int st = static_cast<int>(q % sa_n);
-      const uint32_t par = static_cast<uint32_t>((q / sa_n) & 1);
+      const int64_t last = R * q + R - 1;
+      const int st = static_cast<int>(last % sa_n);
+      const uint32_t par = static_cast<uint32_t>((last / sa_n) & 1);
       if (!drain_wait(a_empty(st), par, p.status)) break;
     }
   } else if ((warp == 1 || (two_issuers && warp == 3 + kEpiWarps)) && lane == 0 && rank == 0) {
@@ -639,24 +662,36 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreadsTwo, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t idesc = idesc_bf16_f32(kPair ? 256 : 128, n);
-      for (int ks = x.k0; ks < x.k1; ++ks) {
+      for (int t = x.k0 * R, pc = 0; t < x.k1 * R; ++t) {
         if (!mbar_wait_bounded<kPair>(a_full(sa), pa, abort_flag, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint64_t bdesc = smem_desc_sw128(b_base + sb * b_stage_bytes);
-        // accumulators of this CTA (of each CTA of a pair): its weight tiles
-        const int n_acc = (kPair && p.a_per_unit == 1) ? 1 : x.n_a;
-        const int a_lo = two_issuers ? my_acc : 0;
-        const int a_hi = two_issuers ? min(my_acc + 1, n_acc) : n_acc;
-        for (int a = a_lo; a < a_hi; ++a) {
-          const uint64_t adesc = smem_desc_sw128(a_base + sa * a_stage_bytes + a * kATileBytes);
-          const uint32_t d = tmem_base + acc_column(rg, a);
+        if (R > 1) {
+          // weight piece pc against the k step's token stage, into the
+          // unit's one accumulator
+          const uint64_t adesc = smem_desc_sw128(a_base + sa * a_stage_bytes);
+          const uint32_t d = tmem_base + acc_column(rg, 0);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
             tc_mma_bf16<kPair>(d, adesc + 2u * kk, bdesc + 2u * kk, idesc,
-                               ((ks - x.k0) | kk) != 0);
+                               ((t - x.k0 * R) | kk) != 0);
+        } else {
+          // accumulators of this CTA (of each CTA of a pair): its weight tiles
+          const int n_acc = (kPair && p.a_per_unit == 1) ? 1 : x.n_a;
+          const int a_lo = two_issuers ? my_acc : 0;
+          const int a_hi = two_issuers ? min(my_acc + 1, n_acc) : n_acc;
+          for (int a = a_lo; a < a_hi; ++a) {
+            const uint64_t adesc =
+                smem_desc_sw128(a_base + sa * a_stage_bytes + a * kATileBytes);
+            const uint32_t d = tmem_base + acc_column(rg, a);
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              tc_mma_bf16<kPair>(d, adesc + 2u * kk, bdesc + 2u * kk, idesc,
+                                 ((t - x.k0) | kk) != 0);
+          }
         }
         if (kPair)  // release the stages of both CTAs
           tc_commit_pair(a_empty(sa), kPairMask);
@@ -666,7 +701,10 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreadsTwo, 1)
           sa = 0;
           pa ^= 1u;
         }
-        if (++sb == sb_n) sb = 0;
+        if (++pc == R) {  // the k step's last weight step: next token stage
+          pc = 0;
+          if (++sb == sb_n) sb = 0;
+        }
       }
       if (!ok) break;
       if (kPair) {  // both CTAs' accumulators are ready
@@ -1042,7 +1080,7 @@ CUresult encode_tmap_gate_up_5d(CUtensorMap* map, const void* base, int64_t grou
   return encode(map, base, 5, dims, strides, box);
 }
 
-GemmPlan plan_gemm(int nt, int a_per_unit, bool pair) {
+GemmPlan plan_gemm(int nt, int a_per_unit, bool pair, int pieces) {
   // token ring: 3 stages; weight ring: the rest of the budget
   static const int forced_b = [] {  // tuning override of the token ring depth
     const char* v = getenv("FGS_B_STAGES");
@@ -1067,6 +1105,16 @@ GemmPlan plan_gemm(int nt, int a_per_unit, bool pair) {
     g.b_stages = static_cast<int>((kSmemBudget - 2 * a_stage) / b_stage);
   }
   if (g.b_stages > sa) g.b_stages = sa;  // see the barrier layout in the kernel
+  // R = pieces weight steps per token stage: a token copy reaches the full
+  // barrier of weight step R i while the last weight step of token stage
+  // i - Sb has been consumed, so weight step R i - Sa must precede it:
+  // Sa >= R (Sb - 1) + 1 (R = 1: Sa >= Sb)
+  while (pieces > 1 && g.b_stages > 1 && sa < pieces * (g.b_stages - 1) + 1) {
+    --g.b_stages;
+    const size_t left = kSmemBudget - g.b_stages * b_stage;
+    sa = static_cast<int>(left / a_stage);
+    if (sa > kMaxStages) sa = kMaxStages;
+  }
   g.a_stages = sa;
   g.f8_stages = 0;
   g.smem_bytes = 1024 + a_stage * sa + b_stage * g.b_stages + 8 * (2 * sa + 5) + 16;
@@ -1149,7 +1197,7 @@ CUresult encode_pair_maps(GemmSegment& s, int a_per_unit) {
 bool pair_capable(const GemmParams& p) {
   for (int i = 0; i < p.nseg; ++i) {
     const GemmSegment& s = p.seg[i];
-    if (!s.a_packed || s.a_fp8 || s.a_groups < 1 || s.a128 % 2 || s.ksplit > 1 || s.b_k_period)
+    if (!s.a_packed || s.a_fp8 || s.a_groups < 1 || s.a128 % 2 || s.ksplit > 1)
       return false;
   }
   return p.nseg > 0;
@@ -1177,14 +1225,22 @@ cudaError_t launch_tc_gemm(const GemmParams& params, int num_sms, cudaStream_t s
   for (int i = 0; i < p.nseg; ++i)
     if (p.seg[i].a128 % 4) pair_two = false;
   p.a_per_unit = p.fp8 ? 2 : p.pair ? (pair_two ? 2 : 1) : (params.a_per_unit == 1 ? 1 : 2);
-  const GemmPlan plan = p.fp8 ? plan_gemm_fp8(p.nt) : plan_gemm(p.nt, p.a_per_unit, p.pair != 0);
+  if (p.pieces > 1) {  // single-CTA bf16 store mode, one weight tile per unit
+    if (p.fp8 || p.pair || p.pieces > 4) return cudaErrorInvalidValue;
+    for (int i = 0; i < p.nseg; ++i)
+      if ((p.seg[i].own_mode ? p.seg[i].mode : p.mode) != kModeStore || p.seg[i].a_packed)
+        return cudaErrorInvalidValue;
+    p.a_per_unit = 1;
+  }
+  const GemmPlan plan = p.fp8 ? plan_gemm_fp8(p.nt)
+                              : plan_gemm(p.nt, p.a_per_unit, p.pair != 0, p.pieces);
   if (p.fp8 && plan.f8_stages < 2) return cudaErrorInvalidValue;
   p.a_stages = plan.a_stages;
   p.b_stages = plan.b_stages;
   // two MMA issuers where token tiles are large enough for the single
   // issuer's per-k-step cost to show (with 32-token tiles the weight stream
   // sets the pace and the second commit per stage only delays its release)
-  p.two = (!p.fp8 && p.nt >= 128) ? 1 : 0;
+  p.two = (!p.fp8 && p.pieces <= 1 && p.nt >= 128) ? 1 : 0;
   p.f8_stages = plan.f8_stages;
   if (p.pair)
     for (int i = 0; i < p.nseg; ++i)

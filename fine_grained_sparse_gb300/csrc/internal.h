@@ -133,16 +133,16 @@ struct GemmSegment {
   int b_box_rows;   // rows of one tmB box: a whole token tile in one copy
   const void* b_src;   // the rows tmB maps (re-encoded with 32-row boxes for
   int64_t b_src_rows;  // CTA pairs, which load half tiles)
-  int a_box_rows;   // store-mode weights read through tmA: 128 (a box per
-                    // tile) or 256 (both tiles of a unit in one copy)
   int k_steps;      // A's K / 64
-  int b_k_period;   // B's k coordinate wraps every b_k_period steps (0: never)
   int a128;         // 128-row A tiles along O (SwiGLU: F/64, store: O/128)
   int a_boxes;      // SwiGLU A tile: 1 = one 5-D box, 8 = eight 16-row boxes
   int a_rows;       // SwiGLU: F (row offset of the up half)
   int o_limit;      // store mode: columns o >= o_limit are not written
-  int ksplit;       // K split into ksplit equal parts (0 or 1: none); part j
-                    // writes out_f32 + j * out_split_stride (fp32 store only)
+  int ksplit;       // K split into ksplit parts (0 or 1: none) of k_steps
+                    // j / ksplit .. (j + 1) k_steps / ksplit; part j writes
+                    // out_f32 + j * out_split_stride (fp32 store only)
+  int a_piece_cols;  // GemmParams::pieces > 1: A column offset of piece p is
+                     // p * a_piece_cols
   int64_t out_split_stride;
   // packed weights (one contiguous bulk copy per stage) instead of tmA
   const uint8_t* a_packed;
@@ -208,6 +208,12 @@ struct GemmParams {
   // 1: the MMAs of the two accumulators are issued by two threads, each
   // committing its own (set by launch_tc_gemm for large token tiles)
   int two;
+  // > 1 (single-CTA bf16 store mode, one weight tile per unit): the weights
+  // are the sum of `pieces` matrices side by side along A's columns (the
+  // split router weight); each k step of B is matched by `pieces` weight
+  // stages, one per piece, all accumulated into the unit's accumulator, so
+  // a token stage is read by pieces x 4 MMAs
+  int pieces;
   int* status;
 };
 
@@ -215,7 +221,7 @@ struct GemmPlan {
   int nt, a_stages, b_stages, f8_stages;
   size_t smem_bytes;
 };
-GemmPlan plan_gemm(int nt, int a_per_unit, bool pair);
+GemmPlan plan_gemm(int nt, int a_per_unit, bool pair, int pieces = 1);
 GemmPlan plan_gemm_fp8(int nt);
 // Whether a launch can run on CTA pairs (packed weights with an even number
 // of 128-row tiles in every segment, no K split).

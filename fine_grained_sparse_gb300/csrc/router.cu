@@ -19,7 +19,11 @@
 //    after a cluster barrier every CTA selects for a share of the 64 tokens by
 //    reading the whole 64 x E logit row set through distributed shared memory.
 // Selection is one warp per token: sigmoid + bias per lane, group top-2 sums
-// by warp shuffles, then K rounds of a warp arg-max.
+// by warp shuffles, then the K (+1) best in one pass (a warp sort of the
+// lanes' bests, then of the candidates they bound) or K rounds of a warp
+// arg-max.  router_logits_kernel holds each lane's experts as one run of
+// consecutive indices (a K2 group of 48 is 4 lanes of 12); the other kernels
+// stride them across the warp.
 #include <cooperative_groups.h>
 #include <math_constants.h>
 
@@ -84,7 +88,15 @@ __device__ __forceinline__ void warp_top2(float& m1, float& m2) {
   }
 }
 
-template <int PM>
+// The expert a lane holds in its slot j: strided (lane + 32 j: a warp's
+// loads of one slot are 128 consecutive bytes) or blocked (PM consecutive
+// experts per lane: a group of E / G experts spans few lanes).
+template <int PM, bool kBlocked>
+__device__ __forceinline__ int expert_of(int lane, int j) {
+  return kBlocked ? lane * PM + j : lane + 32 * j;
+}
+
+template <int PM, bool kBlocked>
 __device__ __forceinline__ void group_top2(const float (&c)[PM], int lane, int E, int gsize, int g,
                                           float& m1, float& m2) {
   m1 = -CUDART_INF_F;
@@ -92,7 +104,7 @@ __device__ __forceinline__ void group_top2(const float (&c)[PM], int lane, int E
   const int lo = g * gsize, hi = lo + gsize;
 #pragma unroll
   for (int j = 0; j < PM; ++j) {
-    const int e = lane + 32 * j;
+    const int e = expert_of<PM, kBlocked>(lane, j);
     if (e >= lo && e < hi && e < E) {
       const float v = c[j];
       if (v > m1) {
@@ -164,8 +176,10 @@ __device__ __forceinline__ void warp_sort_desc(uint64_t& key, float& z, int lane
 }
 
 // Selection for one token by one warp.  Lane `lane` holds the logits of
-// experts e = lane + 32 j, j < PM.  Writes topk_idx[0..K) and topk_w[0..K).
-template <int PM>
+// experts expert_of(lane, j), j < PM.  Writes topk_idx[0..K) and
+// topk_w[0..K).  Every decision uses the (value, index) order alone, so the
+// result does not depend on the layout.
+template <int PM, bool kBlocked = false>
 __device__ __forceinline__ void select_token(const float (&z)[PM], int lane, int E,
                                              const float* __restrict__ bias, int K, int G,
                                              int Gk, float scale, int norm,
@@ -178,7 +192,7 @@ __device__ __forceinline__ void select_token(const float (&z)[PM], int lane, int
   unsigned exact = 0u;  // bit j: c[j] holds the exact value
 #pragma unroll
   for (int j = 0; j < PM; ++j) {
-    const int e = lane + 32 * j;
+    const int e = expert_of<PM, kBlocked>(lane, j);
     if (e < E) {
       const float b = __ldg(bias + e);
       if (fabsf(z[j]) <= kFastRange) {
@@ -196,7 +210,7 @@ __device__ __forceinline__ void select_token(const float (&z)[PM], int lane, int
   auto refine_above = [&](float threshold, int lo, int hi) {
 #pragma unroll
     for (int j = 0; j < PM; ++j) {
-      const int e = lane + 32 * j;
+      const int e = expert_of<PM, kBlocked>(lane, j);
       if (!((exact >> j) & 1u) && c[j] >= threshold && e >= lo && e < hi) {
         c[j] = exact_c(z[j], __ldg(bias + e));
         exact |= 1u << j;
@@ -207,11 +221,47 @@ __device__ __forceinline__ void select_token(const float (&z)[PM], int lane, int
   if (G > 1) {
     // group score = sum of the two largest biased scores in the group
     const int gsize = E / G;
+    // blocked layout with whole groups of a power-of-two count of lanes
+    // each (K2: 48 experts = 4 lanes of 12): every lane's experts lie in one
+    // group, so the top-2 is lane-local and then merged over the group's lanes
+    const int lpg = kBlocked ? gsize / PM : 0;
+    const bool lane_groups = kBlocked && gsize % PM == 0 && lpg > 0 && lpg <= 32 &&
+                             (lpg & (lpg - 1)) == 0 && G * gsize == E;
     auto group_scores = [&]() {
       float mine = -CUDART_INF_F;
+      if (lane_groups) {
+        float m1 = -CUDART_INF_F, m2 = -CUDART_INF_F;
+#pragma unroll
+        for (int j = 0; j < PM; ++j) {
+          if (expert_of<PM, kBlocked>(lane, j) < E) {
+            const float v = c[j];
+            if (v > m1) {
+              m2 = m1;
+              m1 = v;
+            } else if (v > m2) {
+              m2 = v;
+            }
+          }
+        }
+        for (int off = 1; off < lpg; off <<= 1) {
+          const float o1 = __shfl_xor_sync(full, m1, off);
+          const float o2 = __shfl_xor_sync(full, m2, off);
+          if (m1 >= o1) {
+            m2 = fmaxf(m2, o1);
+          } else {
+            m2 = fmaxf(m1, o2);
+            m1 = o1;
+          }
+        }
+        // group g's score sits in its lanes g lpg .. (g + 1) lpg - 1
+        const float sum = __fadd_rn(m1, m2);
+        const float got = __shfl_sync(full, sum, lane < G ? lane * lpg : 0);
+        if (lane < G) mine = got;
+        return mine;
+      }
       for (int g = 0; g < G; ++g) {
         float m1, m2;
-        group_top2(c, lane, E, gsize, g, m1, m2);
+        group_top2<PM, kBlocked>(c, lane, E, gsize, g, m1, m2);
         if (lane == g) mine = __fadd_rn(m1, m2);
       }
       return mine;
@@ -241,7 +291,7 @@ __device__ __forceinline__ void select_token(const float (&z)[PM], int lane, int
       // near-tie between groups: make every possible top-2 member exact
       for (int g = 0; g < G; ++g) {
         float m1, m2;
-        group_top2(c, lane, E, gsize, g, m1, m2);
+        group_top2<PM, kBlocked>(c, lane, E, gsize, g, m1, m2);
         refine_above(m2 - kMargin, g * gsize, (g + 1) * gsize);
       }
       gscore = group_scores();
@@ -249,7 +299,7 @@ __device__ __forceinline__ void select_token(const float (&z)[PM], int lane, int
     }
 #pragma unroll
     for (int j = 0; j < PM; ++j) {
-      const int e = lane + 32 * j;
+      const int e = expert_of<PM, kBlocked>(lane, j);
       if (e < E && !((kept_mask >> (e / gsize)) & 1u)) {
         c[j] = 0.0f;  // literal 0.0 fill
         exact |= 1u << j;
@@ -270,7 +320,7 @@ __device__ __forceinline__ void select_token(const float (&z)[PM], int lane, int
       float bz = 0.0f;
 #pragma unroll
       for (int j = 0; j < PM; ++j) {
-        const int e = lane + 32 * j;
+        const int e = expert_of<PM, kBlocked>(lane, j);
         if (e < E && !((taken >> j) & 1u) && before(c[j], e, bv, bi)) {
           bv = c[j];
           bi = e;
@@ -279,8 +329,8 @@ __device__ __forceinline__ void select_token(const float (&z)[PM], int lane, int
       }
       const int mine = bi;
       warp_best(bv, bi);
-      const int owner = bi & 31;
-      if (lane == owner && mine == bi) taken |= 1u << (bi >> 5);
+      const int owner = kBlocked ? bi / PM : bi & 31;
+      if (lane == owner && mine == bi) taken |= 1u << (kBlocked ? bi - owner * PM : bi >> 5);
       bz = __shfl_sync(full, bz, owner);
       if (lane == k) {
         sel_idx = bi;
@@ -301,7 +351,7 @@ __device__ __forceinline__ void select_token(const float (&z)[PM], int lane, int
     int li = 0x7fffffff;
 #pragma unroll
     for (int j = 0; j < PM; ++j) {
-      const int e = lane + 32 * j;
+      const int e = expert_of<PM, kBlocked>(lane, j);
       if (e < E && before(c[j], e, lv, li)) {
         lv = c[j];
         li = e;
@@ -316,7 +366,7 @@ __device__ __forceinline__ void select_token(const float (&z)[PM], int lane, int
     unsigned mine = 0u;
 #pragma unroll
     for (int j = 0; j < PM; ++j) {
-      const int e = lane + 32 * j;
+      const int e = expert_of<PM, kBlocked>(lane, j);
       if (e < E && order_key(c[j], e) >= floor_key) mine |= 1u << j;
     }
     const int n = __popc(mine);
@@ -332,7 +382,7 @@ __device__ __forceinline__ void select_token(const float (&z)[PM], int lane, int
 #pragma unroll
     for (int j = 0; j < PM; ++j) {
       if ((mine >> j) & 1u) {
-        cand_key[pos] = order_key(c[j], lane + 32 * j);
+        cand_key[pos] = order_key(c[j], expert_of<PM, kBlocked>(lane, j));
         cand_z[pos] = z[j];
         ++pos;
       }
@@ -526,8 +576,32 @@ __global__ void __launch_bounds__(kThreads) router_fused_kernel(
 // ascending part order, so the result does not depend on scheduling.
 constexpr int kSelWarps = 8;  // tokens (warps) per block of router_logits_kernel
 
+// A lane's PM logits of one part in the blocked layout (experts lane PM ..
+// lane PM + PM - 1): 16-byte loads when the lane's run is whole and aligned.
 template <int PM>
-__global__ void __launch_bounds__(kSelWarps * 32) router_logits_kernel(
+__device__ __forceinline__ void load_blocked(const float* __restrict__ row, int lane, int E,
+                                             float (&v)[PM]) {
+  const int e0 = lane * PM;
+  if (PM % 4 == 0 && E % 4 == 0 && e0 + PM <= E) {
+    const float4* p4 = reinterpret_cast<const float4*>(row + e0);
+#pragma unroll
+    for (int i = 0; i < PM / 4; ++i) {
+      const float4 f = __ldg(p4 + i);
+      v[4 * i] = f.x;
+      v[4 * i + 1] = f.y;
+      v[4 * i + 2] = f.z;
+      v[4 * i + 3] = f.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < PM; ++j) v[j] = e0 + j < E ? __ldg(row + e0 + j) : 0.0f;
+  }
+}
+
+// One warp per token, in the blocked layout (each lane PM consecutive
+// experts: whole-lane group scores, 16-byte loads).
+template <int PM>
+__global__ void __launch_bounds__(kSelWarps * 32, PM <= 12 ? 4 : 2) router_logits_kernel(
     const float* __restrict__ logits, int parts, int64_t part_stride,
     const float* __restrict__ bias, int T, int E, int K, int G, int Gk, float scale, int norm,
     int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
@@ -539,9 +613,8 @@ __global__ void __launch_bounds__(kSelWarps * 32) router_logits_kernel(
   // the loads of a batch of parts of all the lane's experts are in flight
   // at once (small batches split the GEMM's K into dozens of parts)
   float z[PM];
-  const float* pz = logits + t * E + lane;
-#pragma unroll
-  for (int j = 0; j < PM; ++j) z[j] = lane + 32 * j < E ? __ldg(pz + 32 * j) : 0.0f;
+  const float* row = logits + t * E;
+  load_blocked<PM>(row, lane, E, z);
   // (two parts at a time for the widest rows, whose registers would
   // otherwise cap the kernel at one block per SM)
   constexpr int kBatch = PM > 16 ? 2 : 4;
@@ -549,24 +622,23 @@ __global__ void __launch_bounds__(kSelWarps * 32) router_logits_kernel(
   for (; q + kBatch <= parts; q += kBatch) {
     float b[kBatch][PM];
 #pragma unroll
-    for (int i = 0; i < kBatch; ++i)
-#pragma unroll
-      for (int j = 0; j < PM; ++j)
-        b[i][j] = lane + 32 * j < E ? __ldg(pz + (q + i) * part_stride + 32 * j) : 0.0f;
+    for (int i = 0; i < kBatch; ++i) load_blocked<PM>(row + (q + i) * part_stride, lane, E, b[i]);
 #pragma unroll
     for (int i = 0; i < kBatch; ++i)
 #pragma unroll
       for (int j = 0; j < PM; ++j) z[j] += b[i][j];
   }
-  for (; q < parts; ++q)
+  for (; q < parts; ++q) {
+    float b[PM];
+    load_blocked<PM>(row + q * part_stride, lane, E, b);
 #pragma unroll
-    for (int j = 0; j < PM; ++j)
-      if (lane + 32 * j < E) z[j] += __ldg(pz + q * part_stride + 32 * j);
+    for (int j = 0; j < PM; ++j) z[j] += b[j];
+  }
   __shared__ uint64_t cand_key[kSelWarps][32];
   __shared__ float cand_z[kSelWarps][32];
   const int w = threadIdx.x / 32;
-  select_token<PM>(z, lane, E, bias, K, G, Gk, scale, norm, topk_idx + t * K, topk_w + t * K,
-                   cand_key[w], cand_z[w]);
+  select_token<PM, true>(z, lane, E, bias, K, G, Gk, scale, norm, topk_idx + t * K,
+                         topk_w + t * K, cand_key[w], cand_z[w]);
 }
 
 // Small batches whose GEMM split K into many parts: one block per token,

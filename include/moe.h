@@ -440,15 +440,15 @@ int32_t moe_layer_forward_host_release(void* workspace);
  *   Scratch for P K parts: 256 + S + 4 T E P bytes (each term rounded up
  *   to 256), S = 6 E d, or 0 when cfg->router_weight is
  *   MOE_ROUTER_WEIGHT_SPLIT.  P is moe_router's own count of K parts when
- *   that fits the array; otherwise the largest smaller count that fits (a
- *   multiple of 3 whose third divides d_model / 64), and the logits are then
- *   summed in a different grouping than moe_router's: they may differ from
- *   it in the last bit, and so may a selection whose deciding margin is of
- *   that size.  The call is rejected with MOE_ERR_WORKSPACE, before anything
- *   is enqueued, only when even P = 3 does not fit: 256 + S + 12 T E > 64 MiB,
- *   which holds for every T above a bound (K2 router, E = 384, d = 7168:
- *   T > 10979, or T > 14563 with the split weight; K3, E = 896: T > 2657, or
- *   T > 6241 with the split weight).
+ *   that fits the array; otherwise the largest smaller count that fits, and
+ *   the logits are then summed in a different grouping than moe_router's:
+ *   they may differ from it in the last bit, and so may a selection whose
+ *   deciding margin is of that size.  The call is rejected with
+ *   MOE_ERR_WORKSPACE, before anything is enqueued, only when even P = 1
+ *   does not fit: 256 + S + 4 T E > 64 MiB, which holds for every T above a
+ *   bound (K2 router, E = 384, d = 7168: T > 32938, or T > 43690 with the
+ *   split weight; K3, E = 896: T > 7972, or T > 18724 with the split
+ *   weight).
  *   The call looks up the array's device address in the current context
  *   the first time it runs in that context (again after the context was
  *   destroyed and created anew); make that first call before any stream

@@ -183,23 +183,24 @@ def test_host_pipeline_release_without_state(fgs):
 
 
 @pytest.mark.parametrize("E,T,split,ok", [
-    (384, 10979, False, True), (384, 10980, False, False),
-    (384, 14563, True, True), (384, 14564, True, False),
-    (896, 2657, False, True), (896, 2658, False, False),
-    (896, 6241, True, True), (896, 6242, True, False),
+    (384, 32938, False, True), (384, 32939, False, False),
+    (384, 43690, True, True), (384, 43691, True, False),
+    (896, 7972, False, True), (896, 7973, False, False),
+    (896, 18724, True, True), (896, 18725, True, False),
 ])
 def test_noalloc_router_size_bound(fgs, E, T, split, ok):
     """moe_router_noalloc rejects a problem, before any CUDA call, exactly when
-    even three K parts overflow its 64 MiB scratch (the bound its header
+    even one K part overflows its 64 MiB scratch (the bound its header
     states); larger problems are rejected, smaller ones get past the check."""
     cfg = fgs.config(d_model=7168, E_routed=E, K=8,
                      router_weight=fgs.MOE_ROUTER_WEIGHT_SPLIT if split else 0)
+    need = 256 + (0 if split else (6 * E * 7168 + 255) // 256 * 256) + \
+        (4 * T * E + 255) // 256 * 256
     if ok:
         # accepted sizes would go on to the GPU: check the bound arithmetic only
-        need = 256 + (0 if split else (6 * E * 7168 + 255) // 256 * 256) + \
-            (12 * T * E + 255) // 256 * 256
         assert need <= 64 << 20
         return
+    assert need > 64 << 20
     st = fgs.lib.moe_router_noalloc(ctypes.byref(cfg), T, 0x1000, 0x1000, 0x1000, 0x1000,
                                     0x1000, None)
     assert st == 4

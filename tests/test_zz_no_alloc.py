@@ -57,7 +57,7 @@ def test_noalloc_router_matches_workspace_router_twice():
         assert rel_max_err(got_w, ref_w) <= TOL_WEIGHTS
 
 
-@pytest.mark.parametrize("name,T", [("k2_router", 800), ("k2_router", 3000), ("k3_latent", 2048)])
+@pytest.mark.parametrize("name,T", [("k2_router", 9000), ("k3_latent", 2048), ("k3_latent", 4096)])
 def test_noalloc_router_with_fewer_k_parts(name, T):
     """Sizes where moe_router's own count of K parts would overflow the
     static scratch: the call runs with fewer parts, so its logits are summed
@@ -95,9 +95,9 @@ def test_noalloc_router_with_fewer_k_parts(name, T):
 def test_noalloc_router_rejects_oversized_problems():
     need_gpu()
     fgs = lib()
-    shape = synth.shape("k3_latent")  # E = 896, T = 4096: above the T <= 2657 bound
+    shape = synth.shape("k3_latent")
     cfg = fgs.config(shape, d_ff=0)
-    T = shape.T
+    T = 8192  # E = 896: above the T <= 7972 bound
     dummy = torch.zeros(16, dtype=torch.uint8, device="cuda")
     st = fgs.lib.moe_router_noalloc(ctypes.byref(cfg), T, dummy.data_ptr(), dummy.data_ptr(),
                                     dummy.data_ptr(), dummy.data_ptr(), dummy.data_ptr(), None)
