@@ -126,7 +126,7 @@ __device__ __forceinline__ int segment_units(const GemmParams& p, const GemmSegm
 // The second segment's units (the shared experts: compute-heavy, their
 // weights shared by all token tiles) come first, the first segment's
 // weight-streaming units after them.
-__device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int units0, int units1,
+__device__ __noinline__ Unit decode_unit(const GemmParams& p, int u, int units0, int units1,
                                             int rank) {
   Unit x;
   x.seg = u < units1 ? 1 : 0;
@@ -184,9 +184,9 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int unit
     x.ntiles = tpg;
   }
   // part j of a split K: k steps [j K / ns, (j + 1) K / ns)
-  if (ns > 1) {
-    x.k0 = static_cast<int>(static_cast<int64_t>(x.split) * s->k_steps / ns);
-    x.k1 = static_cast<int>(static_cast<int64_t>(x.split + 1) * s->k_steps / ns);
+  if (ns > 1) {  // (split + 1) k_steps < 2^31: ns <= 48 parts of at most 2^20 k steps
+    x.k0 = x.split * s->k_steps / ns;
+    x.k1 = (x.split + 1) * s->k_steps / ns;
   } else {
     x.k0 = 0;
     x.k1 = s->k_steps;
@@ -207,71 +207,64 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int unit
   return x;
 }
 
-// Epilogue helpers over one 64-column TMEM load (64 tokens from tok0): the
-// whole chunk is one straight-line block, so the 8 x 8 transposes of its
-// four 16-token groups overlap; tokens past n_rows are computed on the
+// Epilogue helpers over one 16-column TMEM load (16 tokens from tok0).  The
+// epilogue walks a unit's tokens in such blocks in a loop that is not
+// unrolled: the kernel's instruction footprint stays small (unrolled 64-token
+// chunks of every output form made it hundreds of KB, and the epilogue warps
+// then waited on instruction fetch).  Tokens past n_rows are computed on the
 // accumulator's padding columns and not stored.
 
 // SwiGLU: lane l < 16 holds the gate and lane l + 16 the up value of feature
-// blk*64 + 16q + (l & 15); for each 16-token group the gate lane forms h for
-// tokens 0..7 and the up lane for 8..15, each receiving the other half's
-// values for its tokens, and after the transpose within each lane octet
-// lane i holds one token's 8 features: one 16-byte store.  Packed output:
-// plane blk, 8-feature chunk fc swizzled by row % 8.
-__device__ __forceinline__ void swiglu_chunk(const uint32_t (&v)[64], int tok0, int n_rows,
+// blk*64 + 16q + (l & 15); the gate lane forms h for tokens 0..7 of the block
+// and the up lane for 8..15, each receiving the other half's values for its
+// tokens, and after the transpose within each lane octet lane i holds one
+// token's 8 features: one 16-byte store.  Packed output: plane blk, 8-feature
+// chunk fc swizzled by row % 8.
+__device__ __forceinline__ void swiglu_block(const uint32_t (&v)[16], int tok0, int n_rows,
                                              int lane, int q, int blk, __nv_bfloat16* out,
                                              bool out_packed, int64_t plane_rows, int64_t out_row,
                                              int64_t ld) {
   const bool is_gate = lane < 16;
-  uint32_t w[4][4];
+  uint32_t w[4];
 #pragma unroll
-  for (int sub = 0; sub < 4; ++sub) {
+  for (int j = 0; j < 8; j += 2) {
+    float hh[2];
 #pragma unroll
-    for (int j = 0; j < 8; j += 2) {
-      float hh[2];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int a = sub * 16 + j + e, b = sub * 16 + 8 + j + e;
-        const float own = __uint_as_float(is_gate ? v[a] : v[b]);
-        const float send = __uint_as_float(is_gate ? v[b] : v[a]);
-        const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
-        const float g = is_gate ? own : recv;
-        const float u = is_gate ? recv : own;
-        hh[e] = silu_f(g) * u;
-      }
-      w[sub][j >> 1] = pack_bf16x2(hh[0], hh[1]);
+    for (int e = 0; e < 2; ++e) {
+      const int a = j + e, b = 8 + j + e;
+      const float own = __uint_as_float(is_gate ? v[a] : v[b]);
+      const float send = __uint_as_float(is_gate ? v[b] : v[a]);
+      const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+      const float g = is_gate ? own : recv;
+      const float u = is_gate ? recv : own;
+      hh[e] = silu_f(g) * u;
     }
+    w[j >> 1] = pack_bf16x2(hh[0], hh[1]);
   }
-#pragma unroll
-  for (int sub = 0; sub < 4; ++sub) transpose8x8_b16(w[sub], lane);
+  transpose8x8_b16(w, lane);
   const int oct = lane >> 3;
   const int fc = 2 * q + (oct & 1);
-#pragma unroll
-  for (int sub = 0; sub < 4; ++sub) {
-    const int tok = tok0 + sub * 16 + (oct >> 1) * 8 + (lane & 7);
-    if (tok < n_rows) {
-      const int64_t row = out_row + tok;
-      const int64_t off = out_packed ? (((static_cast<int64_t>(blk) * plane_rows + row) << 6) +
-                                        ((fc ^ static_cast<int>(row & 7)) << 3))
-                                     : row * ld + blk * 64 + fc * 8;
-      *reinterpret_cast<uint4*>(out + off) =
-          make_uint4(w[sub][0], w[sub][1], w[sub][2], w[sub][3]);
-    }
+  const int tok = tok0 + (oct >> 1) * 8 + (lane & 7);
+  if (tok < n_rows) {
+    const int64_t row = out_row + tok;
+    const int64_t off = out_packed ? (((static_cast<int64_t>(blk) * plane_rows + row) << 6) +
+                                      ((fc ^ static_cast<int>(row & 7)) << 3))
+                                   : row * ld + blk * 64 + fc * 8;
+    *reinterpret_cast<uint4*>(out + off) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
 // Store mode, bf16 rows of whole 16-byte chunks: v holds this lane's output
-// column for the 64 tokens (scaled by scale[t] when kScale); after the
-// transposes lane i of each octet writes tokens i, 8 + i, ... of its
-// octet's 8 columns, dst being the octet's first column in row tok0's row
-// minus tok0 (the tile's first row).
+// column for the 16 tokens (scaled by scale[t] when kScale); after the
+// transposes lane i of each octet writes tokens i and 8 + i of its octet's 8
+// columns, dst being the octet's first column in the tile's first row.
 template <bool kScale>
-__device__ __forceinline__ void store_rows8_chunk(const uint32_t (&v)[64], const float* scale,
+__device__ __forceinline__ void store_rows8_block(const uint32_t (&v)[16], const float* scale,
                                                   int tok0, int n_rows, __nv_bfloat16* dst,
                                                   int64_t ld, bool col_ok, int lane) {
-  uint32_t w[8][4];
+  uint32_t w[2][4];
 #pragma unroll
-  for (int m = 0; m < 8; ++m) {
+  for (int m = 0; m < 2; ++m) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       float a = __uint_as_float(v[8 * m + 2 * k]), b = __uint_as_float(v[8 * m + 2 * k + 1]);
@@ -283,9 +276,9 @@ __device__ __forceinline__ void store_rows8_chunk(const uint32_t (&v)[64], const
     }
   }
 #pragma unroll
-  for (int m = 0; m < 8; ++m) transpose8x8_b16(w[m], lane);
+  for (int m = 0; m < 2; ++m) transpose8x8_b16(w[m], lane);
 #pragma unroll
-  for (int m = 0; m < 8; ++m) {
+  for (int m = 0; m < 2; ++m) {
     const int tok = tok0 + 8 * m + (lane & 7);
     if (tok < n_rows && col_ok)
       *reinterpret_cast<uint4*>(dst + tok * ld) = make_uint4(w[m][0], w[m][1], w[m][2], w[m][3]);
@@ -817,7 +810,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreadsTwo, 1)
       // accumulator: all warps drain accumulator 0, release its region, then
       // accumulator 1, so a following unit that needs one region starts
       // half an epilogue earlier.  A single-tile unit: all warps, one pass.
-      // In the all-warps passes the warp groups split the 64-column chunks.
+      // In the all-warps passes the warp groups split the 16-token blocks.
       const bool all_warps = single || rg.big;
       const int npass = rg.big ? 2 : 1;
       bool aborted = false;
@@ -834,40 +827,50 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreadsTwo, 1)
         const uint32_t taddr0 =
             tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc_column(rg, acc);
         const int blk = x.blk0 + acc;
-        // 64 columns per TMEM load (one wait each)
-        const int nchunks = (x.n_rows + 63) / 64;
+        // 16 columns (tokens) per TMEM load, one wait each
+        const int nblk = (x.n_rows + 15) / 16;
         const int step = all_warps ? 2 : 1;
-        for (int ch = all_warps ? grp : 0; ch < nchunks; ch += step) {
-          uint32_t v64[64];
-          tmem_ld_x64(taddr0 + static_cast<uint32_t>(ch * 64), v64);
-          tmem_ld_wait(v64);
+#pragma unroll 1
+        for (int bk = all_warps ? grp : 0; bk < nblk; bk += step) {
+          const int tok0 = bk * 16;
+          uint32_t v[16];
+          tmem_ld_x16(taddr0 + static_cast<uint32_t>(tok0), v);
+          tmem_ld_wait(v);
           if (swiglu) {
-            swiglu_chunk(v64, ch * 64, x.n_rows, lane, q, blk, out, out_packed, plane_rows,
+            swiglu_block(v, tok0, x.n_rows, lane, q, blk, out, out_packed, plane_rows,
                          x.out_row, ld);
           } else if (rows8) {
             const int o0 = blk * 128 + q * 32 + (lane & ~7);
             __nv_bfloat16* const dst = out + static_cast<int64_t>(x.out_row) * ld + o0;
             const bool col_ok = o0 < o_limit;
             if (row_scale)
-              store_rows8_chunk<true>(v64, row_scale + x.scale_row, ch * 64, x.n_rows, dst, ld,
+              store_rows8_block<true>(v, row_scale + x.scale_row, tok0, x.n_rows, dst, ld,
                                       col_ok, lane);
             else
-              store_rows8_chunk<false>(v64, nullptr, ch * 64, x.n_rows, dst, ld, col_ok, lane);
+              store_rows8_block<false>(v, nullptr, tok0, x.n_rows, dst, ld, col_ok, lane);
           } else {
             const int o = blk * 128 + q * 32 + lane;
             if (o < o_limit) {
+              if (out_f32 && !row_scale && !add && tok0 + 16 <= x.n_rows) {
+                // fp32 partial sums (the router): one column of 16 rows
+                float* const dst = out_f32 + (x.out_row + tok0) * ld + o;
 #pragma unroll
-              for (int j = 0; j < 64; ++j) {
-                const int tok = ch * 64 + j;
-                if (tok >= x.n_rows) break;
-                const int64_t row = x.out_row + tok;
-                float val = __uint_as_float(v64[j]);
-                if (row_scale) val *= __ldg(row_scale + x.scale_row + tok);
-                if (add) val += __bfloat162float(add[row * add_ld + o]);
-                if (out_f32)
-                  out_f32[row * ld + o] = val;
-                else
-                  out[row * ld + o] = __float2bfloat16_rn(val);
+                for (int j = 0; j < 16; ++j) dst[j * ld] = __uint_as_float(v[j]);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  const int tok = tok0 + j;
+                  if (tok < x.n_rows) {
+                    const int64_t row = x.out_row + tok;
+                    float val = __uint_as_float(v[j]);
+                    if (row_scale) val *= __ldg(row_scale + x.scale_row + tok);
+                    if (add) val += __bfloat162float(add[row * add_ld + o]);
+                    if (out_f32)
+                      out_f32[row * ld + o] = val;
+                    else
+                      out[row * ld + o] = __float2bfloat16_rn(val);
+                  }
+                }
               }
             }
           }
