@@ -49,7 +49,7 @@
 //   bf16 single-CTA form, warp 11 lane 0: with token tiles of 128 rows or
 //   more, the MMA issuer of the second accumulator (warp 1 then issues the
 //   first's only; see the MMA issuers);
-//   FP8 weights only, warps 11..14: converters (FP8 stage -> bf16 stage).
+//   FP8 weights only, warps 11..18: converters (FP8 stage -> bf16 stage).
 // A segment with implicit token tiles whose weights fit in L2 may instead
 // take its units token-tile-major (GemmSegment::b_major).
 // Split weights (GemmParams::pieces = R > 1; the router, whose fp32 weight is
@@ -83,9 +83,10 @@ constexpr int kThreads = 32 * (3 + kEpiWarps);
 // bf16 single-CTA form: a twelfth warp issues the MMAs of the second
 // accumulator (see the kernel's MMA issuers)
 constexpr int kThreadsTwo = kThreads + 32;
-// FP8 weights: four more warps convert each landed FP8 stage into the bf16
-// weight ring (one warp per SM sub-partition)
-constexpr int kConvWarps = 4;
+// FP8 weights: eight more warps convert each landed FP8 stage into the bf16
+// weight ring (two per SM sub-partition; the kernel then has 96 registers a
+// thread)
+constexpr int kConvWarps = 8;
 constexpr int kThreadsFp8 = kThreads + 32 * kConvWarps;
 constexpr uint32_t kF8TileBytes = 128 * 64;  // one 128-row x 64-k FP8 tile
 constexpr int kMaxStages = 12;
@@ -126,8 +127,8 @@ __device__ __forceinline__ int segment_units(const GemmParams& p, const GemmSegm
 // The second segment's units (the shared experts: compute-heavy, their
 // weights shared by all token tiles) come first, the first segment's
 // weight-streaming units after them.
-__device__ __noinline__ Unit decode_unit(const GemmParams& p, int u, int units0, int units1,
-                                            int rank) {
+__device__ __forceinline__ Unit decode_unit_body(const GemmParams& p, int u, int units0,
+                                                 int units1, int rank) {
   Unit x;
   x.seg = u < units1 ? 1 : 0;
   int local = x.seg ? u : u - units1;
@@ -205,6 +206,23 @@ __device__ __noinline__ Unit decode_unit(const GemmParams& p, int u, int units0,
     x.n_a = 1;
   }
   return x;
+}
+
+// Out of line in the bf16 kernels: inlined at each role's two call sites it
+// was a tenth of the kernel's machine code.  The FP8 kernel keeps it inline
+// (measured faster there: K2 decode 5.81 vs 6.22 ms per step).
+__device__ __noinline__ Unit decode_unit_call(const GemmParams& p, int u, int units0, int units1,
+                                              int rank) {
+  return decode_unit_body(p, u, units0, units1, rank);
+}
+
+template <bool kInline>
+__device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int units0, int units1,
+                                            int rank) {
+  if constexpr (kInline)
+    return decode_unit_body(p, u, units0, units1, rank);
+  else
+    return decode_unit_call(p, u, units0, units1, rank);
 }
 
 // Epilogue helpers over one 16-column TMEM load (16 tokens from tok0).  The
@@ -450,11 +468,11 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreadsTwo, 1)
     int stage = 0;
     uint32_t phase = 0;
     int64_t issued = 0;
-    Unit nx = u_first < total ? decode_unit(p, u_first, units0, units1, rank) : Unit{};
+    Unit nx = u_first < total ? decode_unit<kFp8>(p, u_first, units0, units1, rank) : Unit{};
     for (int u = u_first; u < total; u += u_step) {
       // the next unit's tile-table loads overlap this unit's work
       const Unit x = nx;
-      if (u + u_step < total) nx = decode_unit(p, u + u_step, units0, units1, rank);
+      if (u + u_step < total) nx = decode_unit<kFp8>(p, u + u_step, units0, units1, rank);
       const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
       const uint32_t tx = (kFp8 ? kF8TileBytes : kATileBytes) * x.n_a;
       // a weight block read by one token tile is streamed; one shared by
@@ -550,11 +568,11 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreadsTwo, 1)
     // reader of the token stage about to be refilled
     int estage = R - 1;
     uint32_t ephase = 0;
-    Unit nx = u_first < total ? decode_unit(p, u_first, units0, units1, rank) : Unit{};
+    Unit nx = u_first < total ? decode_unit<kFp8>(p, u_first, units0, units1, rank) : Unit{};
     for (int u = u_first; u < total; u += u_step) {
       // the next unit's tile-table loads overlap this unit's work
       const Unit x = nx;
-      if (u + u_step < total) nx = decode_unit(p, u + u_step, units0, units1, rank);
+      if (u + u_step < total) nx = decode_unit<kFp8>(p, u + u_step, units0, units1, rank);
       const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
       // token rows are kept for the units that re-read them, except in a
       // token-tile-major segment, whose readers of a tile run side by side
@@ -633,11 +651,11 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreadsTwo, 1)
     int sa = 0, sb = 0;
     uint32_t pa = 0;
     int c = 0;
-    Unit nx = u_first < total ? decode_unit(p, u_first, units0, units1, rank) : Unit{};
+    Unit nx = u_first < total ? decode_unit<kFp8>(p, u_first, units0, units1, rank) : Unit{};
     for (int u = u_first; u < total; u += u_step) {
       // the next unit's tile-table loads overlap this unit's work
       const Unit x = nx;
-      if (u + u_step < total) nx = decode_unit(p, u + u_step, units0, units1, rank);
+      if (u + u_step < total) nx = decode_unit<kFp8>(p, u + u_step, units0, units1, rank);
       const uint32_t n = static_cast<uint32_t>((x.n_rows + 15) & ~15);
       const Regions rg = regions_of(p, n, c);
       bool ok;
@@ -716,19 +734,19 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreadsTwo, 1)
     drain_wait(drain_bar, 0, p.status);
   } else if (kFp8 && warp >= 3 + kEpiWarps) {
     // ---------------------------------------------- FP8 -> bf16 converters
-    // Thread ct handles the 8-byte FP8 pieces ct + 128 i of a stage: piece
-    // pc is row pc / 8 of the stage's 256 rows (tile pc / 1024), so piece i
-    // of every thread lies in tile i / 8 and in its gate half (rows with bit
-    // 4 clear) for even i, its up half for odd i -- the record's scale
-    // 2 (i / 8) + (i % 2).  A plain store-mode tile has one scale, written
-    // twice in its record.
+    // Thread ct of the kCT converter threads handles the 8-byte FP8 pieces
+    // pc = ct + kCT i of a stage: piece pc is row pc / 8 of the stage's 256
+    // rows, in tile pc / 1024 (the same for every thread at a given i) and
+    // in that tile's gate half (rows with bit 4 clear) or up half -- the
+    // record's scale 2 (pc / 1024) + (pc / 128) % 2.  A plain store-mode tile
+    // has one scale, written twice in its record.
     const int ct = threadIdx.x - 32 * (3 + kEpiWarps);
     int sa = 0, s8 = 0;
     uint32_t pa = 0, p8 = 0;
-    Unit nx = u_first < total ? decode_unit(p, u_first, units0, units1, rank) : Unit{};
+    Unit nx = u_first < total ? decode_unit<kFp8>(p, u_first, units0, units1, rank) : Unit{};
     for (int u = u_first; u < total; u += u_step) {
       const Unit x = nx;
-      if (u + u_step < total) nx = decode_unit(p, u + u_step, units0, units1, rank);
+      if (u + u_step < total) nx = decode_unit<kFp8>(p, u + u_step, units0, units1, rank);
       bool ok = true;
       for (int ks = x.k0; ks < x.k1; ++ks) {
         if (!warp_wait(f8full(s8), p8, abort_flag, p.status) ||
@@ -742,12 +760,14 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreadsTwo, 1)
         for (int j = 0; j < 4; ++j) sc[j] = rec[j];
         const uint8_t* src = smem_f8 + s8 * (2 * kF8TileBytes);
         uint8_t* dst = smem + sa * a_stage_bytes;
-        const int n_i = 8 * x.n_a;
+        constexpr int kCT = 32 * kConvWarps;
+        const int n_i = (1024 / kCT) * x.n_a;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 2048 / kCT; ++i) {
           if (i < n_i) {
-            const int pc = ct + 128 * i;
-            const float scale = sc[2 * (i >> 3) + (i & 1)];
+            const int pc = ct + kCT * i;
+            const int tile = i / (1024 / kCT);
+            const float scale = ((pc >> 7) & 1) ? sc[2 * tile + 1] : sc[2 * tile];
             const uint2 v = *reinterpret_cast<const uint2*>(src + 8 * pc);
             uint4 o;
             o.x = e4m3x2_scaled_bf16x2(v.x & 0xffffu, scale);
@@ -783,11 +803,11 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreadsTwo, 1)
 
     const bool single = p.a_per_unit == 1;
     int c = 0;
-    Unit nx = u_first < total ? decode_unit(p, u_first, units0, units1, rank) : Unit{};
+    Unit nx = u_first < total ? decode_unit<kFp8>(p, u_first, units0, units1, rank) : Unit{};
     for (int u = u_first; u < total; u += u_step) {
       // the next unit's tile-table loads overlap this unit's work
       const Unit x = nx;
-      if (u + u_step < total) nx = decode_unit(p, u + u_step, units0, units1, rank);
+      if (u + u_step < total) nx = decode_unit<kFp8>(p, u + u_step, units0, units1, rank);
       const GemmSegment* s = x.seg ? &p.seg[1] : &p.seg[0];
       const bool swiglu = s->mode == kModeSwiGLU;
       // the segment's output description, once per unit, in registers
