@@ -92,6 +92,25 @@ def test_router_matches_oracle(name, T, tensor_cores):
     _check_router_from_x(shape, g["x"], g["W_r"], g["bias"], tensor_cores)
 
 
+@pytest.mark.parametrize("parts,tile,name,T", [(5, 256, "k2_prefill", 700), (7, 128, "k3_latent", 300),
+                                           (1, 256, "k2_router", 600), (48, 32, "k2_decode", 100)])
+def test_router_uneven_k_parts(parts, tile, name, T):
+    """The tensor-core router with K part counts that split the d / 64 k
+    steps unevenly (112 = 22 + 22 + 23 + 22 + 23 at 5 parts), a single part,
+    and 48 parts of 2-3 k steps, each with its token tile, against the oracle
+    (gap criterion), in a child process: the overrides are read once per
+    process."""
+    need_gpu()
+    import os
+    import subprocess
+    import sys
+    env = dict(os.environ, FGS_ROUTER_KSPLIT=str(parts), FGS_ROUTER_TILE=str(tile))
+    here = os.path.dirname(os.path.abspath(__file__))
+    r = subprocess.run([sys.executable, os.path.join(here, "_router_env_case.py"), name, str(T)],
+                       env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
+
+
 @pytest.mark.parametrize("tensor_cores", [True, False], ids=["split_bf16_tc", "fp32_ffma"])
 def test_router_ragged_tokens_and_small_E(tensor_cores):
     need_gpu()
