@@ -563,7 +563,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreadsTwo, 1)
     const uint64_t pol_normal = l2_policy_evict_normal();
     int stage = 0;       // token stage
     int64_t issued = 0;  // token stages issued: stage i goes with weight steps R i .. R i + R - 1
-    int fstage = 0;      // weight stage of weight step R issued (its full barrier)
+    int fstage = 0;      // weight stage of weight step R * issued (its full barrier)
     // weight stage and phase of weight step R (issued - Sb) + R - 1, the last
     // reader of the token stage about to be refilled
     int estage = R - 1;
