@@ -115,7 +115,7 @@ def test_router_uneven_k_parts(parts, tile, name, T):
 def test_router_ragged_tokens_and_small_E(tensor_cores):
     need_gpu()
     for T, E, K, G, Gk in [(1, 16, 4, 1, 1), (65, 40, 5, 4, 2), (130, 130, 7, 1, 1),
-                           (300, 200, 6, 1, 1)]:
+                           (300, 200, 6, 1, 1), (77, 1024, 32, 8, 4), (513, 1024, 32, 1, 1)]:
         shape = synth.custom(T=T, d_model=256, E_routed=E, K=K, n_group=G, topk_group=Gk,
                              router_only=True)
         g = synth.generate(shape, device="cuda", seed=T + E)
