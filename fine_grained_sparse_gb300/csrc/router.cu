@@ -886,6 +886,7 @@ cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream) {
   if (a.logits) {
     if (a.E <= 128) return launch_logits<4>(a, stream);
     if (a.E <= 384) return launch_logits<12>(a, stream);
+    if (a.E <= 896) return launch_logits<28>(a, stream);  // K3: every lane holds experts
     return launch_logits<32>(a, stream);
   }
   if (a.x_bf16) {
