@@ -12,10 +12,11 @@
 // consecutive pairs (a power of two from 32 to 1024, about 256 chunks):
 //   chunk_count_kernel  per-chunk, per-expert counts (shared-memory atomics;
 //                       integer counts do not depend on their order)
-//   chunk_scan_kernel   one CTA: counts[e] and offsets (exclusive scan over
-//                       experts), and each chunk's start within each expert
-//                       (exclusive scan over chunks)
-//   chunk_scatter_kernel one warp per chunk, its pairs in order, 32 at a
+//   chunk_scan_kernel   a CTA per 32 experts: counts[e], and each chunk's
+//                       start within each expert (exclusive scan over chunks)
+//   chunk_scatter_kernel offsets (exclusive scan of counts over the experts,
+//                       in every CTA; CTA 0 stores them), then one warp per
+//                       chunk, its pairs in order, 32 at a
 //                       time: a pair's slot is its expert's running position
 //                       in the chunk plus its rank among the lanes of the
 //                       same expert (match_any) -> perm / inv
@@ -80,56 +81,101 @@ __global__ void __launch_bounds__(kChunkThreads) chunk_count_kernel(
     ccount[static_cast<int64_t>(blockIdx.x) * E + i] = hist[i];
 }
 
-// One CTA of 1024 threads (E <= 1024): thread e turns ccount[c][e] into the
-// count of e in chunks before c, sums counts[e], and the CTA scans the
-// counts into offsets.
+// A CTA per 32 experts, 1024 threads: lane l serves expert 32 b + l and
+// warp w a contiguous run of the chunks, so every load and store of a warp
+// covers 32 consecutive experts.  Each warp sums its run, the warps' sums
+// are scanned across the CTA, and each warp then rewrites ccount[c][e] as
+// the count of e in the chunks before c; the last warp's total is counts[e].
+// (The exclusive scan of counts over the experts -- the offsets -- is taken
+// by the scatter kernel.)
 __global__ void __launch_bounds__(1024) chunk_scan_kernel(int32_t* __restrict__ ccount,
                                                           int nchunks, int E,
-                                                          int32_t* __restrict__ counts,
-                                                          int32_t* __restrict__ offsets) {
+                                                          int32_t* __restrict__ counts) {
   pdl_wait();
-  __shared__ int scan[1024];
-  const int e = threadIdx.x;
-  int total = 0;
+  __shared__ int part[32][33];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int e = blockIdx.x * 32 + lane;
+  const int per = (nchunks + 31) / 32;
+  const int c0 = min(nchunks, w * per), c1 = min(nchunks, c0 + per);
+  int sum = 0;
   if (e < E) {
-    // 16 independent loads in flight, then their prefix
-    for (int c0 = 0; c0 < nchunks; c0 += 16) {
-      int v[16];
+    int c = c0;
+    for (; c + 8 <= c1; c += 8) {  // eight loads in flight
+      int v[8];
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        v[i] = c0 + i < nchunks ? ccount[static_cast<int64_t>(c0 + i) * E + e] : 0;
+      for (int i = 0; i < 8; ++i) v[i] = ccount[static_cast<int64_t>(c + i) * E + e];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        if (c0 + i < nchunks) ccount[static_cast<int64_t>(c0 + i) * E + e] = total;
-        total += v[i];
-      }
+      for (int i = 0; i < 8; ++i) sum += v[i];
     }
-    counts[e] = total;
+    for (; c < c1; ++c) sum += ccount[static_cast<int64_t>(c) * E + e];
   }
-  scan[e] = total;
+  part[w][lane] = sum;
   __syncthreads();
-  for (int off = 1; off < 1024; off <<= 1) {  // inclusive Hillis-Steele scan
-    const int v = e >= off ? scan[e - off] : 0;
-    __syncthreads();
-    scan[e] += v;
-    __syncthreads();
+  int run = 0;  // this expert's count in the chunks before c0
+  for (int i = 0; i < w; ++i) run += part[i][lane];
+  if (e < E) {
+    for (int c = c0; c < c1; ++c) {
+      const int64_t at = static_cast<int64_t>(c) * E + e;
+      const int v = ccount[at];
+      ccount[at] = run;
+      run += v;
+    }
+    if (w == 31) counts[e] = run;
   }
-  if (e < E) offsets[e] = scan[e] - total;
-  if (e == E - 1) offsets[E] = scan[e];
+}
+
+// offsets = the exclusive scan of counts over the experts (E <= 1024), in
+// shared memory, by the 32 * kScatterWarps threads of a CTA: each thread a
+// run of up to four experts, then a scan of the runs across the warps.
+__device__ __forceinline__ void scan_counts(const int32_t* __restrict__ counts, int E,
+                                            int* off_s, int* warp_s) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int per = (E + 32 * kScatterWarps - 1) / (32 * kScatterWarps);  // <= 4
+  const int e0 = t * per;
+  int v[4], run = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[i] = (i < per && e0 + i < E) ? counts[e0 + i] : 0;
+    run += v[i];
+  }
+  int incl = run;  // inclusive scan of the runs within the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int x = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  if (lane == 31) warp_s[warp] = incl;
+  __syncthreads();
+  int base = 0;
+  for (int i = 0; i < warp; ++i) base += warp_s[i];
+  int acc = base + incl - run;  // exclusive start of this thread's run
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (i < per && e0 + i < E) off_s[e0 + i] = acc;
+    acc += v[i];
+  }
+  if (t == 32 * kScatterWarps - 1) off_s[E] = acc;  // the last run ends the scan
+  __syncthreads();
 }
 
 __global__ void __launch_bounds__(32 * kScatterWarps) chunk_scatter_kernel(
     const int32_t* __restrict__ idx, int64_t n, int chunk, int E,
-    const int32_t* __restrict__ ccount, const int32_t* __restrict__ offsets, int nchunks,
-    int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+    const int32_t* __restrict__ ccount, const int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int nchunks, int32_t* __restrict__ perm,
+    int32_t* __restrict__ inv) {
   pdl_wait();
   extern __shared__ int cnt_all[];
+  int* off_s = cnt_all + kScatterWarps * E;  // E + 1 offsets
+  __shared__ int warp_s[kScatterWarps];
+  scan_counts(counts, E, off_s, warp_s);
+  if (blockIdx.x == 0)
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = off_s[e];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int c = blockIdx.x * kScatterWarps + warp;
   if (c >= nchunks) return;
   int* cnt = cnt_all + warp * E;  // this chunk's next slot per expert
   for (int e = lane; e < E; e += 32)
-    cnt[e] = __ldg(offsets + e) + __ldg(ccount + static_cast<int64_t>(c) * E + e);
+    cnt[e] = off_s[e] + __ldg(ccount + static_cast<int64_t>(c) * E + e);
   __syncwarp();
   const unsigned lt_mask = (1u << lane) - 1u;
   const int64_t j0 = static_cast<int64_t>(c) * chunk;
@@ -465,14 +511,14 @@ cudaError_t launch_permute(const int32_t* topk_idx, int64_t T, int K, int E, int
                                dim3(kChunkThreads), sizeof(int) * E, stream, topk_idx, n, chunk, E,
                                ccount, status);
   if (err != cudaSuccess) return err;
-  err = launch_pdl(chunk_scan_kernel, dim3(1), dim3(1024), 0, stream, ccount,
-                   static_cast<int>(nchunks), E, counts, offsets);
+  err = launch_pdl(chunk_scan_kernel, dim3(static_cast<unsigned>((E + 31) / 32)), dim3(1024), 0,
+                   stream, ccount, static_cast<int>(nchunks), E, counts);
   if (err != cudaSuccess) return err;
   const unsigned blocks = static_cast<unsigned>((nchunks + kScatterWarps - 1) / kScatterWarps);
   return launch_pdl(chunk_scatter_kernel, dim3(blocks), dim3(32 * kScatterWarps),
-                    sizeof(int) * E * kScatterWarps, stream, topk_idx, n, chunk, E,
-                    static_cast<const int32_t*>(ccount), static_cast<const int32_t*>(offsets),
-                    static_cast<int>(nchunks), perm, inv);
+                    sizeof(int) * (E * kScatterWarps + E + 1), stream, topk_idx, n, chunk, E,
+                    static_cast<const int32_t*>(ccount), static_cast<const int32_t*>(counts),
+                    offsets, static_cast<int>(nchunks), perm, inv);
 }
 
 int64_t max_tiles(int64_t rows, int E, int nt) { return rows / nt + E; }
