@@ -72,7 +72,7 @@ def parse_args():
     ap.add_argument("--config", default="k2_prefill", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="own", choices=["own", "reference"])
     ap.add_argument("--cpu-sample-tokens", type=int, default=0,
-                    help="tokens of the CPU oracle sample (default 384, about 10 s on 16 "
+                    help="tokens of the CPU oracle sample (default 1024, about 10 s on 16 "
                          "cores; 48 with FP8 weights, whose per-expert dequantisation "
                          "dominates the oracle's time)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -686,7 +686,7 @@ def run_layer(args, fgs, torch, synth, name, steps, warmup, world, rank, local, 
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_from_device(shape, g, idx.cpu().numpy(),
                                                         args.cpu_sample_tokens or
-                                                        (48 if is_fp8(shape) else 384))
+                                                        (48 if is_fp8(shape) else 1024))
     return line
 
 
