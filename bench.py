@@ -660,27 +660,43 @@ def run_layer(args, fgs, torch, synth, name, steps, warmup, world, rank, local, 
     x_host = g["x"].cpu().pin_memory()
     y_host = torch.empty((T, shape.d_model), dtype=g["x"].dtype).pin_memory()
 
-    def step_host():
-        fgs.moe_layer_forward_host(cfg, T, x_host, gp["W_r"], gp["bias"], gp["W_gate_up"],
-                                   gp["W_down"], gp.get("Ws_gate_up"), gp.get("Ws_down"),
-                                   gp.get("W_lat_down"), gp.get("W_lat_up"), y_host, ws, nws,
-                                   stream=stream)
+    def step_host(fn):
+        fn(cfg, T, x_host, gp["W_r"], gp["bias"], gp["W_gate_up"], gp["W_down"],
+           gp.get("Ws_gate_up"), gp.get("Ws_down"), gp.get("W_lat_down"), gp.get("W_lat_up"),
+           y_host, ws, nws, stream=stream)
 
-    for _ in range(2):
-        step_host()
-    stream.synchronize()
+    def time_host(fn, flush):
+        for _ in range(2):
+            step_host(fn)
+        if flush:
+            fgs.moe_layer_forward_host_flush(ws, stream=stream)
+        stream.synchronize()
+        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        es.record(stream)
+        for _ in range(e_steps):
+            step_host(fn)
+        # every step's y is on the host before the closing event
+        if flush:
+            fgs.moe_layer_forward_host_flush(ws, stream=stream)
+        ee.record(stream)
+        ee.synchronize()
+        return max_over_ranks(torch, es.elapsed_time(ee), world, "cuda")
+
     e_steps = max(3, min(steps, 50))
-    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    es.record(stream)
-    for _ in range(e_steps):
-        step_host()
-    ee.record(stream)
-    ee.synchronize()
-    e_ms = max_over_ranks(torch, es.elapsed_time(ee), world, "cuda")
     nbytes = T * shape.d_model * g["x"].element_size()
+    # batches streamed through the pipelined call: each y leaves the device
+    # while the next batch computes
+    e_ms = time_host(fgs.moe_layer_forward_host_pipelined, True)
     line["e2e"] = {"value": round(job_tokens_per_s(world, T, e_steps, e_ms), 1), "unit": UNIT,
                    "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes, "steps": e_steps,
-                   "api": "moe_layer_forward_host (pinned host x and y)"}
+                   "api": "moe_layer_forward_host_pipelined (pinned host x and y; y of a batch "
+                          "copied out during the next batch's forward; flushed before the "
+                          "closing event)"}
+    # the synchronous call: y valid as soon as the stream has passed the call
+    s_ms = time_host(fgs.moe_layer_forward_host, False)
+    line["e2e_sync"] = {"value": round(job_tokens_per_s(world, T, e_steps, s_ms), 1),
+                        "unit": UNIT, "steps": e_steps,
+                        "api": "moe_layer_forward_host (pinned host x and y)"}
 
     fgs.moe_layer_forward_host_release(ws)
     if rank == 0 and not args.no_cpu_baseline:

@@ -23,7 +23,8 @@ __all__ = [
     "config", "moe_version", "moe_status_string", "moe_validate_config", "moe_workspace_size",
     "moe_get_device_status", "moe_router", "moe_router_from_logits", "moe_permute",
     "moe_grouped_swiglu", "moe_combine", "moe_linear", "moe_layer_forward",
-    "moe_layer_forward_host", "moe_layer_forward_host_release", "moe_last_error_detail",
+    "moe_layer_forward_host", "moe_layer_forward_host_pipelined", "moe_layer_forward_host_flush",
+    "moe_layer_forward_host_release", "moe_last_error_detail",
     "moe_pack_weights", "pack_layer_weights",
     "moe_router_noalloc", "moe_launch_count", "moe_dense_gates", "moe_update_bias",
     "moe_quantile_bias_update",
@@ -101,6 +102,8 @@ _SIGS = {
     "moe_split_router_weight": ([_CFG, _P, _P, _P], _I32),
     "moe_layer_forward": ([_CFG, _I64] + [_P] * 14 + [_SZ, _P, _P], _I32),
     "moe_layer_forward_host": ([_CFG, _I64] + [_P] * 11 + [_SZ, _P], _I32),
+    "moe_layer_forward_host_pipelined": ([_CFG, _I64] + [_P] * 11 + [_SZ, _P], _I32),
+    "moe_layer_forward_host_flush": ([_P, _P], _I32),
     "moe_layer_forward_host_release": ([_P], _I32),
 }
 for _name, (_args, _res) in _SIGS.items():
@@ -280,6 +283,23 @@ def moe_layer_forward_host(cfg, T, x_host, W_r, bias, W_gate_up, W_down, Ws_gate
                                       _ptr(Ws_down), _ptr(W_lat_down), _ptr(W_lat_up),
                                       _ptr(y_host), _ptr(workspace), ws_bytes, _stream(stream)),
            "moe_layer_forward_host")
+
+
+def moe_layer_forward_host_pipelined(cfg, T, x_host, W_r, bias, W_gate_up, W_down, Ws_gate_up,
+                                     Ws_down, W_lat_down, W_lat_up, y_host, workspace, ws_bytes,
+                                     stream=None):
+    """moe_layer_forward_host whose y_host is valid once `stream` has passed
+    the next such call on the workspace, or moe_layer_forward_host_flush."""
+    _check(lib.moe_layer_forward_host_pipelined(
+        ctypes.byref(cfg), T, _ptr(x_host), _ptr(W_r), _ptr(bias), _ptr(W_gate_up), _ptr(W_down),
+        _ptr(Ws_gate_up), _ptr(Ws_down), _ptr(W_lat_down), _ptr(W_lat_up), _ptr(y_host),
+        _ptr(workspace), ws_bytes, _stream(stream)), "moe_layer_forward_host_pipelined")
+
+
+def moe_layer_forward_host_flush(workspace, stream=None):
+    """Make `stream` wait for the latest pipelined call's copy of y."""
+    _check(lib.moe_layer_forward_host_flush(_ptr(workspace), _stream(stream)),
+           "moe_layer_forward_host_flush")
 
 
 def moe_layer_forward_host_release(workspace):

@@ -265,7 +265,7 @@ Layout layout(const moe_config* c, int64_t T) {
   L.x_lat = take(c->d_latent ? static_cast<size_t>(T) * c->d_latent * eb : 0);
   L.r_lat = take(c->d_latent ? static_cast<size_t>(T) * c->d_latent * eb : 0);
   L.x_stage = take(2 * round256(static_cast<size_t>(T) * c->d_model * eb));  // two, alternating
-  L.y_stage = take(static_cast<size_t>(T) * c->d_model * eb);
+  L.y_stage = take(2 * round256(static_cast<size_t>(T) * c->d_model * eb));  // two, alternating
   L.total = o;
   return L;
 }
@@ -1123,21 +1123,26 @@ namespace {
 struct HostPipe {
   cudaEvent_t copied[2] = {nullptr, nullptr};  // x landed in staging buffer b
   cudaEvent_t read[2] = {nullptr, nullptr};    // the forward that read buffer b finished
+  cudaEvent_t landed[2] = {nullptr, nullptr};  // y of buffer b copied out (pipelined calls)
   bool used[2] = {false, false};
+  bool y_out[2] = {false, false};  // a copy-out of y buffer b was enqueued
   int next = 0;
+  int last = -1;  // buffer of the latest pipelined call, until its y is waited for
 };
 
 std::mutex g_pipe_mutex;
 std::unordered_map<void*, HostPipe> g_pipes;
-cudaStream_t g_copy_stream[64] = {nullptr};
+cudaStream_t g_copy_stream[64] = {nullptr};  // x in
+cudaStream_t g_out_stream[64] = {nullptr};   // y out (pipelined calls)
 
-}  // namespace
-
-int32_t moe_layer_forward_host(const moe_config* cfg, int64_t T, const void* x_host,
-                               const float* W_r, const float* bias, const void* W_gate_up,
-                               const void* W_down, const void* Ws_gate_up, const void* Ws_down,
-                               const void* W_lat_down, const void* W_lat_up, void* y_host,
-                               void* workspace, size_t ws_bytes, void* stream) {
+// The host-buffer forward, synchronous (y_host valid once `stream` is
+// synchronised) or pipelined (y_host of this call valid once `stream` has
+// passed the next pipelined call on the workspace, or a flush).
+int32_t forward_host(const moe_config* cfg, int64_t T, const void* x_host, const float* W_r,
+                     const float* bias, const void* W_gate_up, const void* W_down,
+                     const void* Ws_gate_up, const void* Ws_down, const void* W_lat_down,
+                     const void* W_lat_up, void* y_host, void* workspace, size_t ws_bytes,
+                     void* stream, bool pipelined) {
   int32_t st = check_layer_cfg(cfg, T);
   if (st != MOE_OK) return st;
   if (!x_host || !y_host) return fail(MOE_ERR_INVALID_ARG, "null host pointer");
@@ -1149,29 +1154,33 @@ int32_t moe_layer_forward_host(const moe_config* cfg, int64_t T, const void* x_h
   MOE_CUDA(cudaGetDevice(&dev));
   if (dev >= 64) return fail(MOE_ERR_INVALID_ARG, "device index above 63");
   HostPipe* hp;
-  cudaStream_t cs;
+  cudaStream_t cs, os;
   int b;
   {
     std::lock_guard<std::mutex> lock(g_pipe_mutex);
     if (!g_copy_stream[dev])
       MOE_CUDA(cudaStreamCreateWithFlags(&g_copy_stream[dev], cudaStreamNonBlocking));
+    if (!g_out_stream[dev])
+      MOE_CUDA(cudaStreamCreateWithFlags(&g_out_stream[dev], cudaStreamNonBlocking));
     cs = g_copy_stream[dev];
+    os = g_out_stream[dev];
     hp = &g_pipes[workspace];
     for (int i = 0; i < 2; ++i) {
       if (!hp->copied[i]) MOE_CUDA(cudaEventCreateWithFlags(&hp->copied[i], cudaEventDisableTiming));
       if (!hp->read[i]) MOE_CUDA(cudaEventCreateWithFlags(&hp->read[i], cudaEventDisableTiming));
+      if (!hp->landed[i]) MOE_CUDA(cudaEventCreateWithFlags(&hp->landed[i], cudaEventDisableTiming));
     }
     b = hp->next;
     hp->next ^= 1;
   }
   void* xd = at<void>(workspace, L.x_stage + b * round256(bytes));
-  // y_host pinned and mapped into this device's address space: the layer's
-  // last kernel writes y there itself (over the host link), so no staging
-  // copy delays the next call's forward on `stream`
-  void* yd = at<void>(workspace, L.y_stage);
+  void* yd = at<void>(workspace, L.y_stage + b * round256(bytes));
+  // synchronous form: y_host pinned and mapped into this device's address
+  // space is written by the layer's last kernel itself (over the host link),
+  // so no staging copy delays the next call's forward on `stream`
   bool y_direct = false;
   static const int direct_ok = env_int("FGS_Y_DIRECT", 1);  // 0: always stage and copy
-  if (direct_ok) {
+  if (!pipelined && direct_ok) {
     cudaPointerAttributes pa;
     if (cudaPointerGetAttributes(&pa, y_host) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
         pa.devicePointer && aligned16(pa.devicePointer) && pa.device == dev) {
@@ -1186,13 +1195,60 @@ int32_t moe_layer_forward_host(const moe_config* cfg, int64_t T, const void* x_h
   MOE_CUDA(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, cs));
   MOE_CUDA(cudaEventRecord(hp->copied[b], cs));
   MOE_CUDA(cudaStreamWaitEvent(s, hp->copied[b], 0));
+  // y buffer b is free once its last copy-out has finished (two calls ago)
+  if (hp->y_out[b]) MOE_CUDA(cudaStreamWaitEvent(s, hp->landed[b], 0));
   st = moe_layer_forward(cfg, T, xd, W_r, bias, W_gate_up, W_down, Ws_gate_up, Ws_down,
                          W_lat_down, W_lat_up, yd, nullptr, nullptr, nullptr, workspace, ws_bytes,
                          nullptr, stream);
   if (st != MOE_OK) return st;
   MOE_CUDA(cudaEventRecord(hp->read[b], s));
   hp->used[b] = true;
-  if (!y_direct) MOE_CUDA(cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s));
+  if (!pipelined) {
+    if (!y_direct) MOE_CUDA(cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s));
+    return MOE_OK;
+  }
+  // pipelined: y goes out on the output stream while the next call's forward
+  // runs; `stream` waits for the previous pipelined call's copy-out only now,
+  // after this call's forward (by then that copy has long finished)
+  MOE_CUDA(cudaStreamWaitEvent(os, hp->read[b], 0));
+  MOE_CUDA(cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, os));
+  MOE_CUDA(cudaEventRecord(hp->landed[b], os));
+  hp->y_out[b] = true;
+  if (hp->last >= 0 && hp->last != b) MOE_CUDA(cudaStreamWaitEvent(s, hp->landed[hp->last], 0));
+  hp->last = b;
+  return MOE_OK;
+}
+
+}  // namespace
+
+int32_t moe_layer_forward_host(const moe_config* cfg, int64_t T, const void* x_host,
+                               const float* W_r, const float* bias, const void* W_gate_up,
+                               const void* W_down, const void* Ws_gate_up, const void* Ws_down,
+                               const void* W_lat_down, const void* W_lat_up, void* y_host,
+                               void* workspace, size_t ws_bytes, void* stream) {
+  return forward_host(cfg, T, x_host, W_r, bias, W_gate_up, W_down, Ws_gate_up, Ws_down,
+                      W_lat_down, W_lat_up, y_host, workspace, ws_bytes, stream, false);
+}
+
+int32_t moe_layer_forward_host_pipelined(const moe_config* cfg, int64_t T, const void* x_host,
+                                         const float* W_r, const float* bias,
+                                         const void* W_gate_up, const void* W_down,
+                                         const void* Ws_gate_up, const void* Ws_down,
+                                         const void* W_lat_down, const void* W_lat_up,
+                                         void* y_host, void* workspace, size_t ws_bytes,
+                                         void* stream) {
+  return forward_host(cfg, T, x_host, W_r, bias, W_gate_up, W_down, Ws_gate_up, Ws_down,
+                      W_lat_down, W_lat_up, y_host, workspace, ws_bytes, stream, true);
+}
+
+int32_t moe_layer_forward_host_flush(void* workspace, void* stream) {
+  if (!workspace) return fail(MOE_ERR_INVALID_ARG, "workspace is null");
+  std::lock_guard<std::mutex> lock(g_pipe_mutex);
+  auto it = g_pipes.find(workspace);
+  if (it == g_pipes.end() || it->second.last < 0) return MOE_OK;
+  MOE_CUDA(cudaStreamWaitEvent(static_cast<cudaStream_t>(stream),
+                               it->second.landed[it->second.last], 0));
+  it->second.last = -1;
   return MOE_OK;
 }
 
@@ -1205,7 +1261,7 @@ int32_t moe_layer_forward_host_release(void* workspace) {
   // work completes; waits already enqueued on it are unaffected
   cudaError_t first = cudaSuccess;
   for (int i = 0; i < 2; ++i) {
-    for (cudaEvent_t e : {it->second.copied[i], it->second.read[i]}) {
+    for (cudaEvent_t e : {it->second.copied[i], it->second.read[i], it->second.landed[i]}) {
       if (!e) continue;
       const cudaError_t r = cudaEventDestroy(e);
       if (first == cudaSuccess) first = r;

@@ -414,9 +414,40 @@ int32_t moe_layer_forward_host(const moe_config* cfg, int64_t T, const void* x_h
                                void* workspace, size_t ws_bytes, void* stream);
 
 /*
- * Release the library's per-workspace state of moe_layer_forward_host: the
- * four CUDA events that order its staging copies, kept from the first
- * host-buffer call on `workspace` until this call (the paper has no
+ * moe_layer_forward_host for a stream of batches, with the copy of y out of
+ * the device overlapped with the next batch's forward.  Arguments, errors and
+ * the handling of x are those of moe_layer_forward_host; y is always staged
+ * in the workspace (one of two buffers, alternating with x's) and copied to
+ * y_host on a second copy stream of the library once this call's forward has
+ * finished.  y_host of this call is therefore valid once `stream` has passed
+ * the NEXT moe_layer_forward_host_pipelined call on the same workspace (that
+ * call makes `stream` wait for this copy after enqueueing its own forward),
+ * or moe_layer_forward_host_flush(workspace, stream); until then the caller
+ * must neither read nor reuse y_host.  Successive calls may pass the same
+ * y_host: its copies are made in call order.  No counterpart on the pages:
+ * it keeps the host link (about 0.2 TB/s each way on one GB300) off the
+ * critical path of a batch stream. */
+int32_t moe_layer_forward_host_pipelined(const moe_config* cfg, int64_t T, const void* x_host,
+                                         const float* W_r, const float* bias,
+                                         const void* W_gate_up, const void* W_down,
+                                         const void* Ws_gate_up, const void* Ws_down,
+                                         const void* W_lat_down, const void* W_lat_up,
+                                         void* y_host, void* workspace, size_t ws_bytes,
+                                         void* stream);
+
+/*
+ * Make `stream` wait for the copy of y of the latest
+ * moe_layer_forward_host_pipelined call on `workspace` (after this, a
+ * synchronisation of `stream` leaves that y in its y_host).  Nothing pending
+ * (or a workspace never used by that call): no effect.  MOE_ERR_INVALID_ARG
+ * for a NULL workspace; MOE_ERR_CUDA if the wait cannot be enqueued. */
+int32_t moe_layer_forward_host_flush(void* workspace, void* stream);
+
+/*
+ * Release the library's per-workspace state of moe_layer_forward_host and
+ * moe_layer_forward_host_pipelined: the six CUDA events that order their
+ * staging copies, kept from the first host-buffer call on `workspace` until
+ * this call (the paper has no
  * counterpart; it bounds what a caller that cycles through workspaces
  * holds).  Work already enqueued is not waited for.  A later host-buffer
  * call on the same workspace starts afresh; it must not be enqueued before

@@ -180,6 +180,9 @@ def test_host_pipeline_release_without_state(fgs):
     assert lib.moe_layer_forward_host_release(None) == 1
     # a workspace that never went through moe_layer_forward_host: nothing to release
     assert lib.moe_layer_forward_host_release(0x1000) == 0
+    # nothing pending: the flush enqueues nothing (no stream is touched)
+    assert lib.moe_layer_forward_host_flush(None, None) == 1
+    assert lib.moe_layer_forward_host_flush(0x1000, None) == 0
 
 
 @pytest.mark.parametrize("E,T,split,ok", [

@@ -157,6 +157,49 @@ def test_layer_forward_host_pipelined_calls(shape, y_pinned):
         assert torch.equal(yh, y.cpu())
 
 
+@pytest.mark.parametrize("same_y", [False, True], ids=["own_y", "shared_y"])
+@pytest.mark.parametrize("shape", SMALL[1:3], ids=lambda s: s.name)
+def test_layer_host_pipelined(shape, same_y):
+    """moe_layer_forward_host_pipelined: each call's y reaches its y_host by
+    the next call (or the flush) and equals the device-buffer forward's, bit
+    for bit; a y_host shared by all calls ends with the last call's y."""
+    need_gpu()
+    fgs = lib()
+    g = synth.generate(shape, device="cuda")
+    cfg = fgs.config(shape)
+    T = shape.T
+    ws, nws = workspace(cfg, T)
+    xs = [synth.generate(shape, device="cuda", seed=s, weights=False)["x"] for s in (1, 2, 3, 4)]
+    xs_host = [x.cpu().pin_memory() for x in xs]
+    n_y = 1 if same_y else len(xs)
+    ys_host = [torch.full((T, shape.d_model), float("nan"), dtype=xs[0].dtype).pin_memory()
+               for _ in range(n_y)]
+    stream = torch.cuda.Stream()
+    for i, xh in enumerate(xs_host):  # enqueued back to back
+        fgs.moe_layer_forward_host_pipelined(cfg, T, xh, g["W_r"], g["bias"], g["W_gate_up"],
+                                             g["W_down"], g.get("Ws_gate_up"), g.get("Ws_down"),
+                                             g.get("W_lat_down"), g.get("W_lat_up"),
+                                             ys_host[i % n_y], ws, nws, stream=stream)
+    fgs.moe_layer_forward_host_flush(ws, stream=stream)
+    stream.synchronize()
+    assert fgs.moe_get_device_status(ws) == 0
+    want = []
+    for x in xs:
+        ws2, nws2 = workspace(cfg, T)
+        y = torch.empty((T, shape.d_model), dtype=x.dtype, device="cuda")
+        fgs.moe_layer_forward(cfg, T, x, g["W_r"], g["bias"], g["W_gate_up"], g["W_down"],
+                              g.get("Ws_gate_up"), g.get("Ws_down"), g.get("W_lat_down"),
+                              g.get("W_lat_up"), y, None, None, None, ws2, nws2)
+        torch.cuda.synchronize()
+        want.append(y.cpu())
+    if same_y:
+        assert torch.equal(ys_host[0], want[-1])
+    else:
+        for yh, y in zip(ys_host, want):
+            assert torch.equal(yh, y)
+    fgs.moe_layer_forward_host_release(ws)
+
+
 @pytest.mark.parametrize("shape", SMALL[1:3], ids=lambda s: s.name)
 def test_layer_with_presplit_router_weight(shape):
     """The layer forward with the router weight split once
