@@ -62,6 +62,9 @@ _FP8_NOTE = (" -- expert weights FP8 E4M3 with one fp32 scale per 128 x 128 bloc
 for _n in ("k2_decode", "k2_prefill", "k3_latent"):
     WORKLOADS[_n + "_fp8"] = WORKLOADS[_n].replace(", bf16 experts", "") + _FP8_NOTE
 PROFILE_DIR = os.path.join(ROOT, "profiles")
+# the roofline's live gate/up duration: events around that launch in every
+# GU_EVERY-th timed step
+GU_EVERY = 4
 
 
 def parse_args():
@@ -542,12 +545,13 @@ def run_layer(args, fgs, torch, synth, name, steps, warmup, world, rank, local, 
     if status:
         raise RuntimeError("device status after warm-up: " + fgs.moe_status_string(status))
 
-    # inside the timed region only the gate/up launch is bracketed by events
-    # (each recorded event keeps the kernels on its two sides from
-    # overlapping); the other stage times come from an instrumented pass
-    # after it
+    # inside the timed region only the gate/up launch is bracketed by events,
+    # in every GU_EVERY-th step (each recorded event keeps the kernels on its
+    # two sides from overlapping, about 0.03 ms a step at K2 prefill); the
+    # other stage times come from an instrumented pass after it
     gu_events = [[None, None, torch.cuda.Event(enable_timing=True),
-                  torch.cuda.Event(enable_timing=True), None, None] for _ in range(steps)]
+                  torch.cuda.Event(enable_timing=True), None, None]
+                 if i % GU_EVERY == 0 else None for i in range(steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(device_id(torch, local)) if rank == 0 else None
     if sampler:
@@ -585,7 +589,7 @@ def run_layer(args, fgs, torch, synth, name, steps, warmup, world, rank, local, 
     if status:
         raise RuntimeError("device status after the timed steps: " + fgs.moe_status_string(status))
     router_ms = time_router(fgs, torch, cfg, T, gp, ws, nws, stream)
-    gu_live_ms = statistics.mean(ev[2].elapsed_time(ev[3]) for ev in gu_events)
+    gu_live_ms = statistics.mean(ev[2].elapsed_time(ev[3]) for ev in gu_events if ev)
     # stage breakdown: a few steps with every stage boundary recorded
     step_events = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)]
                    for _ in range(min(steps, 10))]
@@ -610,6 +614,8 @@ def run_layer(args, fgs, torch, synth, name, steps, warmup, world, rank, local, 
                 "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
                 "peak_source": peaks["source"],
+                "duration_samples": (f"events around the launch in {sum(1 for e in gu_events if e)}"
+                                     f" of the {steps} timed steps (every {GU_EVERY}th)"),
                 "algorithmic_bytes_per_launch": work["gate_up_bytes"],
                 "tensor_frac_of_sustained": round(work["flops_gate_up"] / (gu_ms / 1e3) / 1e12
                                                   / peaks["bf16_tflops_sustained"], 4)}
