@@ -328,21 +328,32 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, int* s
 // one region per accumulator.  Every unit advances a region counter c by the
 // regions it uses; region use c is region c % 2 in its (c / 2)-th phase --
 // the same sequence in every role.
+// With the weights in TMEM (GemmParams::tmem_a: token tiles of at most 64
+// rows) the regions are columns [0, 128) and [128, 256), each accumulator 64
+// columns, and columns [256, 512) hold the weight stages.
 struct Regions {
-  bool big;  // two accumulators of more than 128 columns: one region each
-  int c;     // first region use of the unit
+  bool big;     // two accumulators of more than 128 columns: one region each
+  bool narrow;  // 128-column regions (weights in TMEM)
+  int c;        // first region use of the unit
 };
 
 __device__ __forceinline__ Regions regions_of(const GemmParams& p, uint32_t n, int c) {
-  return Regions{p.a_per_unit == 2 && n > 128, c};
+  return Regions{p.a_per_unit == 2 && n > 128 && !p.tmem_a, p.tmem_a != 0, c};
 }
 __device__ __forceinline__ int region_of(const Regions& r, int acc) {
   return r.big ? ((r.c + acc) & 1) : (r.c & 1);
 }
 __device__ __forceinline__ uint32_t region_phase(int use) { return static_cast<uint32_t>(use >> 1) & 1u; }
 __device__ __forceinline__ uint32_t acc_column(const Regions& r, int acc) {
+  if (r.narrow) return 128u * static_cast<uint32_t>(r.c & 1) + 64u * static_cast<uint32_t>(acc);
   return r.big ? 256u * static_cast<uint32_t>((r.c + acc) & 1)
                : 256u * static_cast<uint32_t>(r.c & 1) + 128u * static_cast<uint32_t>(acc);
+}
+// TMEM column of weight stage s, tile a (weights in TMEM: 64 columns a
+// stage, the two 128-row tiles side by side, two bf16 of k per column)
+constexpr uint32_t kTmemAStage0 = 256;
+__device__ __forceinline__ uint32_t tmem_a_column(int s, int a) {
+  return kTmemAStage0 + 64u * static_cast<uint32_t>(s) + 32u * static_cast<uint32_t>(a);
 }
 
 // One kernel body, two tensor-core modes:
@@ -379,7 +390,10 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreadsTwo, 1)
   const int nt = p.nt;
   const int R = p.pieces > 1 ? p.pieces : 1;  // weight steps per k step
   const uint32_t b_stage_bytes = b_stage_bytes_of(nt, kPair);
-  const uint32_t a_stage_bytes = kATileBytes * static_cast<uint32_t>(p.a_per_unit);
+  // FP8 weights at small token tiles: the converters write the bf16 weights
+  // into TMEM (no bf16 weight stages in shared memory)
+  const bool tmem_a = kFp8 && p.tmem_a;
+  const uint32_t a_stage_bytes = tmem_a ? 0u : kATileBytes * static_cast<uint32_t>(p.a_per_unit);
   const int s8_n = kFp8 ? p.f8_stages : 0;
   uint8_t* smem_b = smem + sa_n * a_stage_bytes;
   uint8_t* smem_f8 = smem_b + sb_n * b_stage_bytes;          // FP8 ring: s8 x 2 tiles
@@ -695,9 +709,16 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreadsTwo, 1)
           const int a_lo = two_issuers ? my_acc : 0;
           const int a_hi = two_issuers ? min(my_acc + 1, n_acc) : n_acc;
           for (int a = a_lo; a < a_hi; ++a) {
+            const uint32_t d = tmem_base + acc_column(rg, a);
+            if (tmem_a) {  // the converters' bf16 tile in TMEM, 8 columns per 16 k
+              const uint32_t at = tmem_base + tmem_a_column(sa, a);
+#pragma unroll
+              for (int kk = 0; kk < kBK / 16; ++kk)
+                tc_mma_bf16_ta(d, at + 8u * kk, bdesc + 2u * kk, idesc, ((t - x.k0) | kk) != 0);
+              continue;
+            }
             const uint64_t adesc =
                 smem_desc_sw128(a_base + sa * a_stage_bytes + a * kATileBytes);
-            const uint32_t d = tmem_base + acc_column(rg, a);
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk)
               tc_mma_bf16<kPair>(d, adesc + 2u * kk, bdesc + 2u * kk, idesc,
@@ -732,6 +753,84 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreadsTwo, 1)
     else
       tc_commit(drain_bar);
     drain_wait(drain_bar, 0, p.status);
+  } else if (kFp8 && tmem_a && warp >= 3 + kEpiWarps) {
+    // ------------------------------------- FP8 -> bf16 converters, into TMEM
+    // Warp w converts row 32 (w % 4) + lane -- the TMEM lanes it may access
+    // -- of tile (w - 3 - kEpiWarps) / 4 of each stage: the row's 64 codes
+    // (8-byte pieces, logical piece c at (c ^ row % 8) * 8 of its 64 bytes)
+    // into 32 columns, two bf16 of k per column, scaled by the scale of the
+    // row's half (gate or up: row bit 4).  Software-pipelined by one k step:
+    // a step's codes are converted before the previous step's TMEM store is
+    // waited for and that step released (full and FP8-empty barriers), so
+    // the store's latency overlaps the conversion.
+    const int ct = threadIdx.x - 32 * (3 + kEpiWarps);
+    const int tile = (ct >> 5) >> 2;
+    const int row = 32 * (warp & 3) + lane;
+    const int x7 = row & 7;
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    int sa = 0, s8 = 0, pend_sa = -1, pend_s8 = 0;
+    uint32_t pa = 0, p8 = 0;
+    bool ok = true;
+    auto release_pending = [&]() {
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(f8empty(pend_s8));
+        mbar_arrive(a_full(pend_sa));
+      }
+    };
+    Unit nx = u_first < total ? decode_unit<kFp8>(p, u_first, units0, units1, rank) : Unit{};
+    for (int u = u_first; u < total && ok; u += u_step) {
+      const Unit x = nx;
+      if (u + u_step < total) nx = decode_unit<kFp8>(p, u + u_step, units0, units1, rank);
+      const bool mine = tile < x.n_a;
+      for (int ks = x.k0; ks < x.k1; ++ks) {
+        if (!warp_wait(f8full(s8), p8, abort_flag, p.status) ||
+            !warp_wait(a_empty(sa), pa ^ 1u, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        // the MMAs that read this TMEM stage have completed
+        tc_fence_after();
+        uint32_t w[32];
+        if (mine) {
+          const float scale =
+              reinterpret_cast<const float*>(smem_rec + 16 * s8)[2 * tile + ((row >> 4) & 1)];
+          const uint8_t* src = smem_f8 + s8 * (2 * kF8TileBytes) + tile * kF8TileBytes + row * 64;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            // logical pieces 2j and 2j + 1 share a 16-byte pair, swapped
+            // when the row's swizzle is odd
+            const uint4 v = *reinterpret_cast<const uint4*>(src + ((j ^ (x7 >> 1)) << 4));
+            const uint2 lo = (x7 & 1) ? make_uint2(v.z, v.w) : make_uint2(v.x, v.y);
+            const uint2 hi = (x7 & 1) ? make_uint2(v.x, v.y) : make_uint2(v.z, v.w);
+            w[8 * j + 0] = e4m3x2_scaled_bf16x2(lo.x & 0xffffu, scale);
+            w[8 * j + 1] = e4m3x2_scaled_bf16x2(lo.x >> 16, scale);
+            w[8 * j + 2] = e4m3x2_scaled_bf16x2(lo.y & 0xffffu, scale);
+            w[8 * j + 3] = e4m3x2_scaled_bf16x2(lo.y >> 16, scale);
+            w[8 * j + 4] = e4m3x2_scaled_bf16x2(hi.x & 0xffffu, scale);
+            w[8 * j + 5] = e4m3x2_scaled_bf16x2(hi.x >> 16, scale);
+            w[8 * j + 6] = e4m3x2_scaled_bf16x2(hi.y & 0xffffu, scale);
+            w[8 * j + 7] = e4m3x2_scaled_bf16x2(hi.y >> 16, scale);
+          }
+        }
+        if (pend_sa >= 0) release_pending();
+        if (mine) tmem_st_x32(lane_base + tmem_a_column(sa, tile), w);
+        pend_sa = sa;
+        pend_s8 = s8;
+        if (++s8 == s8_n) {
+          s8 = 0;
+          p8 ^= 1u;
+        }
+        if (++sa == sa_n) {
+          sa = 0;
+          pa ^= 1u;
+        }
+      }
+    }
+    if (ok && pend_sa >= 0) release_pending();
+    tmem_st_wait();  // no store of this warp outlives it (TMEM is freed at the end)
   } else if (kFp8 && warp >= 3 + kEpiWarps) {
     // ---------------------------------------------- FP8 -> bf16 converters
     // Thread ct of the kCT converter threads handles the 8-byte FP8 pieces
@@ -1147,7 +1246,7 @@ GemmPlan plan_gemm(int nt, int a_per_unit, bool pair, int pieces) {
 // FP8 weights: two bf16 weight stages (the converters stay one stage ahead
 // of the MMAs), two token stages, and every remaining byte as FP8 stages
 // (the copies in flight from HBM), at most kMaxStages.
-GemmPlan plan_gemm_fp8(int nt) {
+GemmPlan plan_gemm_fp8(int nt, bool tmem_a) {
   static const int forced_a = [] {  // tuning override: bf16 weight stages
     const char* v = getenv("FGS_FP8_A_STAGES");
     return (v && *v) ? atoi(v) : 0;
@@ -1159,9 +1258,16 @@ GemmPlan plan_gemm_fp8(int nt) {
   GemmPlan g;
   g.nt = nt;
   const size_t b_stage = b_stage_bytes_of(nt, false);
-  const size_t a_stage = 2ull * kATileBytes;
-  g.a_stages = (forced_a >= 2 && forced_a <= 4) ? forced_a : 2;
-  g.b_stages = 2;
+  // weights in TMEM: four stages there (columns 256..511), none in shared memory
+  const size_t a_stage = tmem_a ? 0 : 2ull * kATileBytes;
+  g.a_stages = tmem_a ? 4 : (forced_a >= 2 && forced_a <= 4) ? forced_a : 2;
+  // weights in TMEM: the bf16 stages' shared memory goes to the token ring
+  // (at most as deep as the weight ring)
+  static const int forced_b = [] {  // tuning override: token stages with weights in TMEM
+    const char* v = getenv("FGS_FP8_B_STAGES");
+    return (v && *v) ? atoi(v) : 0;
+  }();
+  g.b_stages = tmem_a ? ((forced_b >= 2 && forced_b <= 4) ? forced_b : 4) : 2;
   const size_t f8_stage = 2ull * kF8TileBytes + 16 + 16;  // tiles, record, two barriers
   const size_t fixed = 1024 + a_stage * g.a_stages + b_stage * g.b_stages +
                        8 * (2 * g.a_stages + 5) + 16;
@@ -1226,6 +1332,14 @@ bool pair_capable(const GemmParams& p) {
   return p.nseg > 0;
 }
 
+bool fp8_tmem_enabled() {
+  static const int on = [] {  // tuning override: 0 = bf16 weight stages in shared memory
+    const char* v = getenv("FGS_FP8_TMEM");
+    return (v && *v) ? atoi(v) : 1;
+  }();
+  return on != 0;
+}
+
 cudaError_t launch_tc_gemm(const GemmParams& params, int num_sms, cudaStream_t stream) {
   GemmParams p = params;
   for (int i = 0; i < p.nseg; ++i) {
@@ -1255,7 +1369,10 @@ cudaError_t launch_tc_gemm(const GemmParams& params, int num_sms, cudaStream_t s
         return cudaErrorInvalidValue;
     p.a_per_unit = 1;
   }
-  const GemmPlan plan = p.fp8 ? plan_gemm_fp8(p.nt)
+  // FP8 weights with token tiles of at most 64 rows: the converters write the
+  // weights into TMEM, beside two 128-column accumulator regions
+  p.tmem_a = (p.fp8 && p.nt <= 64 && p.a_per_unit == 2 && fp8_tmem_enabled()) ? 1 : 0;
+  const GemmPlan plan = p.fp8 ? plan_gemm_fp8(p.nt, p.tmem_a != 0)
                               : plan_gemm(p.nt, p.a_per_unit, p.pair != 0, p.pieces);
   if (p.fp8 && plan.f8_stages < 2) return cudaErrorInvalidValue;
   p.a_stages = plan.a_stages;

@@ -214,6 +214,10 @@ struct GemmParams {
   // stages, one per piece, all accumulated into the unit's accumulator, so
   // a token stage is read by pieces x 4 MMAs
   int pieces;
+  // FP8 weights, token tiles of at most 64 rows (set by launch_tc_gemm): the
+  // converter warps write the bf16 weight tiles into TMEM, where the MMAs
+  // read them, instead of into shared-memory stages
+  int tmem_a;
   int* status;
 };
 
@@ -222,7 +226,7 @@ struct GemmPlan {
   size_t smem_bytes;
 };
 GemmPlan plan_gemm(int nt, int a_per_unit, bool pair, int pieces = 1);
-GemmPlan plan_gemm_fp8(int nt);
+GemmPlan plan_gemm_fp8(int nt, bool tmem_a = false);
 // Whether a launch can run on CTA pairs (packed weights with an even number
 // of 128-row tiles in every segment, no K split).
 bool pair_capable(const GemmParams& p);
