@@ -49,7 +49,9 @@
 //   bf16 single-CTA form, warp 11 lane 0: with token tiles of 128 rows or
 //   more, the MMA issuer of the second accumulator (warp 1 then issues the
 //   first's only; see the MMA issuers);
-//   FP8 weights only, warps 11..18: converters (FP8 stage -> bf16 stage).
+//   FP8 weights only, warps 11..18: converters (FP8 stage -> bf16 stage, in
+//   shared memory or, with token tiles of at most 64 rows, in TMEM), and
+//   warp 19 lane 0: the MMA issuer of the second accumulator.
 // A segment with implicit token tiles whose weights fit in L2 may instead
 // take its units token-tile-major (GemmSegment::b_major).
 // Split weights (GemmParams::pieces = R > 1; the router, whose fp32 weight is
@@ -87,7 +89,9 @@ constexpr int kThreadsTwo = kThreads + 32;
 // weight ring (two per SM sub-partition; the kernel then has 96 registers a
 // thread)
 constexpr int kConvWarps = 8;
-constexpr int kThreadsFp8 = kThreads + 32 * kConvWarps;
+// and a twentieth warp issues the MMAs of the second accumulator (see the
+// MMA issuers; weights in TMEM)
+constexpr int kThreadsFp8 = kThreads + 32 * kConvWarps + 32;
 constexpr uint32_t kF8TileBytes = 128 * 64;  // one 128-row x 64-k FP8 tile
 constexpr int kMaxStages = 12;
 constexpr size_t kSmemBudget = 229376;  // pipeline bytes per CTA (224 KB)
@@ -381,7 +385,10 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreadsTwo, 1)
     tc_gemm_kernel(const __grid_constant__ GemmParams p) {
   // two MMA issuers, one per accumulator (bf16 forms, large token tiles:
   // GemmParams::two)
-  const bool two_issuers = !kFp8 && p.two;
+  const bool two_issuers = p.two != 0;
+  // the second issuer: the warp after the epilogue's (bf16), after the
+  // converters' (FP8)
+  const int issuer2_warp = kFp8 ? 3 + kEpiWarps + kConvWarps : 3 + kEpiWarps;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -651,7 +658,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreadsTwo, 1)
       const uint32_t par = static_cast<uint32_t>((last / sa_n) & 1);
       if (!drain_wait(a_empty(st), par, p.status)) break;
     }
-  } else if ((warp == 1 || (two_issuers && warp == 3 + kEpiWarps)) && lane == 0 && rank == 0) {
+  } else if ((warp == 1 || (two_issuers && warp == issuer2_warp)) && lane == 0 && rank == 0) {
     // ------------------------------------------------------- MMA issuers
     // With two_issuers warp 1 issues the MMAs of accumulator 0 and the last
     // warp those of accumulator 1, each followed by its own commit: one
@@ -753,7 +760,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreadsTwo, 1)
     else
       tc_commit(drain_bar);
     drain_wait(drain_bar, 0, p.status);
-  } else if (kFp8 && tmem_a && warp >= 3 + kEpiWarps) {
+  } else if (kFp8 && tmem_a && warp >= 3 + kEpiWarps && warp < 3 + kEpiWarps + kConvWarps) {
     // ------------------------------------- FP8 -> bf16 converters, into TMEM
     // Warp w converts row 32 (w % 4) + lane -- the TMEM lanes it may access
     // -- of tile (w - 3 - kEpiWarps) / 4 of each stage: the row's 64 codes
@@ -831,7 +838,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreadsTwo, 1)
     }
     if (ok && pend_sa >= 0) release_pending();
     tmem_st_wait();  // no store of this warp outlives it (TMEM is freed at the end)
-  } else if (kFp8 && warp >= 3 + kEpiWarps) {
+  } else if (kFp8 && warp >= 3 + kEpiWarps && warp < 3 + kEpiWarps + kConvWarps) {
     // ---------------------------------------------- FP8 -> bf16 converters
     // Thread ct of the kCT converter threads handles the 8-byte FP8 pieces
     // pc = ct + kCT i of a stage: piece pc is row pc / 8 of the stage's 256
@@ -1378,9 +1385,11 @@ cudaError_t launch_tc_gemm(const GemmParams& params, int num_sms, cudaStream_t s
   p.a_stages = plan.a_stages;
   p.b_stages = plan.b_stages;
   // two MMA issuers where token tiles are large enough for the single
-  // issuer's per-k-step cost to show (with 32-token tiles the weight stream
-  // sets the pace and the second commit per stage only delays its release)
-  p.two = (!p.fp8 && p.pieces <= 1 && p.nt >= 128) ? 1 : 0;
+  // issuer's per-k-step cost to show (with 32-token tiles the bf16 weight
+  // stream sets the pace and the second commit per stage only delays its
+  // release), and with the FP8 weights in TMEM, whose k steps come at half
+  // the bytes (one issuer takes about 1000 cycles a k step, two about 500)
+  p.two = (p.pieces <= 1 && (p.nt >= 128 || p.tmem_a)) ? 1 : 0;
   p.f8_stages = plan.f8_stages;
   if (p.pair)
     for (int i = 0; i < p.nseg; ++i)
