@@ -318,6 +318,24 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return ok;
 }
 
+// Two barriers for a whole warp: lane 0 tests both at once (their latencies
+// overlap when both phases have completed, the common case), then waits
+// (bounded) for any that had not.
+__device__ __forceinline__ bool warp_wait2(uint32_t bar1, uint32_t parity1, uint32_t bar2,
+                                           uint32_t parity2, volatile int* abort_flag,
+                                           int* status) {
+  bool ok = false;
+  if ((threadIdx.x & 31) == 0) {
+    const bool d1 = mbar_try_wait(bar1, parity1);
+    const bool d2 = mbar_try_wait(bar2, parity2);
+    ok = (d1 || mbar_wait_bounded(bar1, parity1, abort_flag, status)) &&
+         (d2 || mbar_wait_bounded(bar2, parity2, abort_flag, status));
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok;
+}
+
 // Drain wait: bounded by time only (ignores the abort flag).
 __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, int* status) {
   int local_abort = 0;
@@ -793,8 +811,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreadsTwo, 1)
       if (u + u_step < total) nx = decode_unit<kFp8>(p, u + u_step, units0, units1, rank);
       const bool mine = tile < x.n_a;
       for (int ks = x.k0; ks < x.k1; ++ks) {
-        if (!warp_wait(f8full(s8), p8, abort_flag, p.status) ||
-            !warp_wait(a_empty(sa), pa ^ 1u, abort_flag, p.status)) {
+        if (!warp_wait2(f8full(s8), p8, a_empty(sa), pa ^ 1u, abort_flag, p.status)) {
           ok = false;
           break;
         }
@@ -855,8 +872,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreadsTwo, 1)
       if (u + u_step < total) nx = decode_unit<kFp8>(p, u + u_step, units0, units1, rank);
       bool ok = true;
       for (int ks = x.k0; ks < x.k1; ++ks) {
-        if (!warp_wait(f8full(s8), p8, abort_flag, p.status) ||
-            !warp_wait(a_empty(sa), pa ^ 1u, abort_flag, p.status)) {
+        if (!warp_wait2(f8full(s8), p8, a_empty(sa), pa ^ 1u, abort_flag, p.status)) {
           ok = false;
           break;
         }
