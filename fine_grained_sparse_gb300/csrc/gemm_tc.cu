@@ -829,14 +829,10 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreadsTwo, 1)
             const uint4 v = *reinterpret_cast<const uint4*>(src + ((j ^ (x7 >> 1)) << 4));
             const uint2 lo = (x7 & 1) ? make_uint2(v.z, v.w) : make_uint2(v.x, v.y);
             const uint2 hi = (x7 & 1) ? make_uint2(v.x, v.y) : make_uint2(v.z, v.w);
-            w[8 * j + 0] = e4m3x2_scaled_bf16x2(lo.x & 0xffffu, scale);
-            w[8 * j + 1] = e4m3x2_scaled_bf16x2(lo.x >> 16, scale);
-            w[8 * j + 2] = e4m3x2_scaled_bf16x2(lo.y & 0xffffu, scale);
-            w[8 * j + 3] = e4m3x2_scaled_bf16x2(lo.y >> 16, scale);
-            w[8 * j + 4] = e4m3x2_scaled_bf16x2(hi.x & 0xffffu, scale);
-            w[8 * j + 5] = e4m3x2_scaled_bf16x2(hi.x >> 16, scale);
-            w[8 * j + 6] = e4m3x2_scaled_bf16x2(hi.y & 0xffffu, scale);
-            w[8 * j + 7] = e4m3x2_scaled_bf16x2(hi.y >> 16, scale);
+            e4m3x4_scaled_bf16x2x2(lo.x, scale, w[8 * j + 0], w[8 * j + 1]);
+            e4m3x4_scaled_bf16x2x2(lo.y, scale, w[8 * j + 2], w[8 * j + 3]);
+            e4m3x4_scaled_bf16x2x2(hi.x, scale, w[8 * j + 4], w[8 * j + 5]);
+            e4m3x4_scaled_bf16x2x2(hi.y, scale, w[8 * j + 6], w[8 * j + 7]);
           }
         }
         if (pend_sa >= 0) release_pending();
@@ -892,10 +888,8 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreadsTwo, 1)
             const float scale = ((pc >> 7) & 1) ? sc[2 * tile + 1] : sc[2 * tile];
             const uint2 v = *reinterpret_cast<const uint2*>(src + 8 * pc);
             uint4 o;
-            o.x = e4m3x2_scaled_bf16x2(v.x & 0xffffu, scale);
-            o.y = e4m3x2_scaled_bf16x2(v.x >> 16, scale);
-            o.z = e4m3x2_scaled_bf16x2(v.y & 0xffffu, scale);
-            o.w = e4m3x2_scaled_bf16x2(v.y >> 16, scale);
+            e4m3x4_scaled_bf16x2x2(v.x, scale, o.x, o.y);
+            e4m3x4_scaled_bf16x2x2(v.y, scale, o.z, o.w);
             *reinterpret_cast<uint4*>(dst + 16 * pc) = o;
           }
         }
