@@ -429,33 +429,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&p);
 }
 
-// Two FP8 E4M3 codes (bits 0..7 and 8..15 of `two`) times `scale`, as a
-// bf16 pair (the low code in the low half).  E4M3 -> f16 is exact (one
-// hardware conversion for the pair), f16 -> f32 is exact, the product is
-// rounded to fp32 and then to bf16.
-__device__ __forceinline__ uint32_t e4m3x2_scaled_bf16x2(uint32_t two, float scale) {
-  uint32_t h2;
-  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
-      : "=r"(h2)
-      : "r"(two));
-  float lo, hi;
-  asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
-      : "=f"(lo), "=f"(hi)
-      : "r"(h2));
-  // both products in one paired fp32 multiply (round to nearest, subnormals
-  // kept: the same two products as two multiplies)
-  float plo, phi;
-  asm("{\n\t.reg .b64 x, s, r;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 s, {%4, %4};\n\t"
-      "mul.rn.f32x2 r, x, s;\n\tmov.b64 {%0, %1}, r;\n\t}"
-      : "=f"(plo), "=f"(phi)
-      : "f"(lo), "f"(hi), "f"(scale));
-  return pack_bf16x2(plo, phi);
-}
-
 // Four FP8 E4M3 codes (the bytes of `four`, lowest first) times `scale`, as
-// two bf16 pairs (o0: bytes 0 and 1, o1: bytes 2 and 3): the same arithmetic
-// as e4m3x2_scaled_bf16x2, with the word's halves fed to the conversions
-// directly.
+// two bf16 pairs (o0: bytes 0 and 1, o1: bytes 2 and 3, the lower byte in
+// the low half).  E4M3 -> f16 is exact (one hardware conversion per pair,
+// fed from a half of the word), f16 -> f32 is exact, each product is rounded
+// to fp32 (two per paired multiply, round to nearest, subnormals kept) and
+// then to bf16.
 __device__ __forceinline__ void e4m3x4_scaled_bf16x2x2(uint32_t four, float scale, uint32_t& o0,
                                                        uint32_t& o1) {
   uint32_t h0, h1;
