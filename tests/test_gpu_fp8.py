@@ -153,6 +153,43 @@ SMALL = [
 ]
 
 
+# token tiles of 32 rows (T <= 256): the weights go through TMEM unless
+# FGS_FP8_TMEM=0 keeps them in shared memory
+FP8_ENV_SHAPES = [
+    synth.custom(name="fp8_env_grouped", T=256, d_model=512, E_routed=32, K=4, E_shared=1,
+                 d_ff=256, d_ff_shared=128, n_group=4, topk_group=2, x_dist="clusters32",
+                 weights="fp8"),
+    synth.custom(name="fp8_env_odd_tiles", T=200, d_model=384, E_routed=12, K=3, E_shared=1,
+                 d_ff=256, d_ff_shared=128, weights="fp8"),
+    synth.custom(name="fp8_env_k3", T=128, d_model=512, d_latent=256, E_routed=16, K=4,
+                 E_shared=2, d_ff=128, d_ff_shared=128, weights="fp8"),
+]
+
+
+@pytest.mark.parametrize("case", range(len(FP8_ENV_SHAPES)),
+                         ids=[s.name for s in FP8_ENV_SHAPES])
+def test_fp8_weights_in_tmem_equal_shared_memory_form(case):
+    """The two FP8 forms apply the same arithmetic to each code, so the
+    layer's output bytes are identical whether the converters write the bf16
+    weights into TMEM or into shared memory (each form in its own process:
+    the library reads the override once)."""
+    need_gpu()
+    import os
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    out = {}
+    for tmem in ("1", "0"):
+        env = dict(os.environ, FGS_FP8_TMEM=tmem)
+        r = subprocess.run([sys.executable, os.path.join(here, "_fp8_env_case.py"), str(case)],
+                           env=env, capture_output=True, text=True, timeout=600)
+        assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
+        line = [ln for ln in r.stdout.splitlines() if ln.startswith("digest ")][-1].split()
+        assert line[2] == "1", "non-finite output"
+        out[tmem] = line[1]
+    assert out["1"] == out["0"]
+
+
 @pytest.mark.parametrize("shape", SMALL, ids=lambda s: s.name)
 def test_layer_fp8_small_every_token(shape):
     need_gpu()
